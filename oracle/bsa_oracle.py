@@ -1,0 +1,329 @@
+"""fp64 CPU oracle: radius-rescued block selection + explicit softmax attention.
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.  Only the tests, ``smoke()`` and
+the benchmark's CPU-baseline leg may import or run this module.  It shares no
+code with the CUDA path.
+
+Source: the article "Your 128K Context Is 6x Slower Than It Needs to Be"
+(articles.phantom-byte.com), sections "Why block-sparse attention
+underperforms: the mean-dilution trap" and "The rescue branch: two selection
+paths, one mask", and the FlashAttention description in
+"attention-kernel-optimization" (skill-vault.co.in), section "FlashAttention
+(1 -> 2 -> 3)", which fixes that tiled online softmax equals the explicit
+softmax computed here.
+
+The article gives prose, not formulas.  Each function states the reading it
+implements; the same readings are listed in the design notes of the repository.
+All arithmetic is float64 on the bf16-rounded inputs.
+
+Layouts: q [b, N, Hq, d], k and v [b, N, Hkv, d]; per-block tensors are
+[b, H, nb, ...]; masks are [b, Hkv, nb_q, nb_k] uint8 with bit 0 = forced
+(first or diagonal block), bit 1 = kept by the centroid path, bit 2 = kept by
+the rescue path.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+FORCED, CENTROID, RESCUE = 1, 2, 4
+
+
+# ------------------------------------------------------------ block summaries
+
+def block_meta(k: np.ndarray, block: int):
+    """Centroid and radius of every key block.
+
+    Rescue branch section: "for each key block, compute the centroid, then
+    compute the maximum distance from any key in that block to that centroid".
+    The centroid is the mean of the block's keys (mean-dilution section: "the
+    average of the keys inside it"); the distance is read as plain Euclidean.
+
+    k: [b, N, Hkv, d].  Returns centroid [b, Hkv, nb, d], radius [b, Hkv, nb].
+    """
+    b, n, h, d = k.shape
+    nb = n // block
+    kb = np.asarray(k, dtype=np.float64).reshape(b, nb, block, h, d).transpose(0, 3, 1, 2, 4)
+    centroid = kb.mean(axis=3)
+    dist = np.sqrt(np.sum((kb - centroid[:, :, :, None, :]) ** 2, axis=-1))
+    radius = dist.max(axis=-1)
+    return centroid, radius
+
+
+def nearest_rank(count: int, num: int, den: int) -> int:
+    """1-based nearest rank ceil(num/den * count), at least 1."""
+    return max(1, (num * count + den - 1) // den)
+
+
+def radius_quantiles(radius: np.ndarray):
+    """Median and 90th-percentile radius per (batch, KV head).
+
+    Rescue branch section: the coefficient uses "the median and the 90th
+    percentile as the reference points", computed "separately for each layer
+    and each key-value head" over the prompt's blocks.  Reading: nearest-rank
+    quantiles over all nb blocks, q(p) = r_(ceil(p nb)) of the ascending sort
+    (so the median is the lower median for even nb).
+
+    radius: [b, Hkv, nb].  Returns (med, p90), each [b, Hkv].
+    """
+    nb = radius.shape[-1]
+    srt = np.sort(radius, axis=-1)
+    med = srt[..., nearest_rank(nb, 1, 2) - 1]
+    p90 = srt[..., nearest_rank(nb, 9, 10) - 1]
+    return med, p90
+
+
+def rescue_coefficient(radius: np.ndarray, med: np.ndarray, p90: np.ndarray):
+    """Radius-adaptive rescue coefficient alpha_j in [0, 1].
+
+    Rescue branch section: a coefficient "derived from the distribution of
+    those radii, using the median and the 90th percentile".  Reading: a block
+    no wider than the median gets no bonus, a block at or beyond p90 the full
+    bonus, linear in between:
+        alpha_j = clamp((r_j - med) / (p90 - med), 0, 1),
+    and alpha = 0 for every block when p90 - med <= 1e-12 * p90.
+    """
+    med = np.asarray(med, dtype=np.float64)[..., None]
+    p90 = np.asarray(p90, dtype=np.float64)[..., None]
+    span = p90 - med
+    degenerate = span <= 1e-12 * p90
+    safe = np.where(degenerate, 1.0, span)
+    alpha = np.clip((radius - med) / safe, 0.0, 1.0)
+    return np.where(degenerate, 0.0, alpha)
+
+
+def query_summary(q: np.ndarray, block: int):
+    """Per query block: mean query and mean query norm.
+
+    Rescue branch section: the centroid branch scores each block on "average
+    relevance".  Reading: the query side of a block is summarised by the mean
+    of its queries (qbar) and the mean of their Euclidean norms (nbar).
+
+    q: [b, N, Hq, d].  Returns qbar [b, Hq, nb, d], nbar [b, Hq, nb].
+    """
+    b, n, h, d = q.shape
+    nb = n // block
+    qb = np.asarray(q, dtype=np.float64).reshape(b, nb, block, h, d).transpose(0, 3, 1, 2, 4)
+    qbar = qb.mean(axis=3)
+    nbar = np.sqrt(np.sum(qb * qb, axis=-1)).mean(axis=-1)
+    return qbar, nbar
+
+
+def block_scores(qbar, nbar, centroid, radius, alpha, scale: float, b: int, g: int):
+    """Centroid-path and rescue-path scores for one (batch, KV head).
+
+    Centroid path (rescue branch section, "scores every block on average
+    relevance"):  S_c[i, j] = max over the group's query heads h of
+    scale * (qbar_{h,i} . c_j).
+    Rescue path ("scores rescue candidates against the base path with that
+    coefficient applied"):  R[i, j] = max_h scale * (qbar_{h,i} . c_j +
+    alpha_j * nbar_{h,i} * r_j).  Since |qbar| <= nbar, with alpha_j = 1 the
+    rescue score bounds every key of block j (Cauchy-Schwarz), so a single
+    outlier key cannot be diluted away.  Reading: the group's heads are
+    combined by a max, so one head is not diluted by the others (GQA sharing,
+    32 query heads over 4 KV heads).
+
+    Returns (S_c, R), each [nb, nb] float64 (row i = query block, column j =
+    key block; entries with j > i are meaningless).
+    """
+    hq = qbar.shape[1]
+    hkv = centroid.shape[1]
+    grp = hq // hkv
+    heads = slice(g * grp, (g + 1) * grp)
+    dots = np.einsum("hid,jd->hij", qbar[b, heads], centroid[b, g])
+    s_c = scale * dots.max(axis=0)
+    bonus = nbar[b, heads][:, :, None] * (alpha[b, g] * radius[b, g])[None, None, :]
+    r = scale * (dots + bonus).max(axis=0)
+    return s_c, r
+
+
+# ------------------------------------------------------------ selection
+
+PPM = 1_000_000
+
+
+def ratio_ppm(ratio: float) -> int:
+    """Keep-ratio in parts per million, rounded half up."""
+    return int(math.floor(ratio * PPM + 0.5))
+
+
+def keep_count(ppm: int, i: int) -> int:
+    """ceil(ratio * (i + 1)) in integer arithmetic (ratio = ppm / 1e6).
+
+    Reading of "thresholded independently": each path keeps a fixed fraction
+    of the causal row (i + 1 blocks), rounded up.
+    """
+    return (ppm * (i + 1) + PPM - 1) // PPM
+
+
+def _top(cands: np.ndarray, score: np.ndarray, k: int) -> np.ndarray:
+    """The k best candidates: higher score first, ties to the lower index."""
+    if k <= 0 or cands.size == 0:
+        return cands[:0]
+    s = score[cands]
+    order = np.lexsort((cands, -s))
+    return cands[order[:k]]
+
+
+def select_row(s_c_row, r_row, alpha_row, i: int, ppm_c: int, ppm_r: int):
+    """Blocks kept for query block i (one batch, one KV head).
+
+    * Forced: key block 0 and the diagonal block i are always kept and take
+      part in neither ranking (reading; the article does not say).
+    * Centroid path: the top k_c = min(ceil(rho_c (i+1)), i-1) candidates
+      j in 1..i-1 by S_c.
+    * Rescue path: among the candidates the centroid path dropped and whose
+      radius is above the median (alpha_j > 0), the top
+      k_r = min(ceil(rho_r (i+1)), #eligible) by R ("rescued into the mask
+      even when their average score says otherwise").
+    * The two paths are thresholded independently and combined by OR.
+
+    Returns (centroid_kept, rescue_kept) as ascending int arrays.
+    """
+    cands = np.arange(1, i, dtype=np.int64)
+    kc = min(keep_count(ppm_c, i), cands.size)
+    cent = np.sort(_top(cands, s_c_row, kc))
+    dropped = np.setdiff1d(cands, cent)
+    eligible = dropped[alpha_row[dropped] > 0.0]
+    kr = min(keep_count(ppm_r, i), eligible.size)
+    resc = np.sort(_top(eligible, r_row, kr))
+    return cent, resc
+
+
+def select_blocks(q, k, block: int, centroid_keep: float, rescue_keep: float,
+                  scale: float | None = None, with_scores: bool = False):
+    """Whole mask build for one layer: meta, quantiles, alpha, scores, select.
+
+    Returns a dict with centroid, radius, med, p90, alpha, qbar, nbar and the
+    uint8 mask [b, Hkv, nb, nb] (bits FORCED | CENTROID | RESCUE); with
+    ``with_scores`` also the per-(b, g) score matrices.
+    """
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    nb = n // block
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    centroid, radius = block_meta(k, block)
+    med, p90 = radius_quantiles(radius)
+    alpha = rescue_coefficient(radius, med, p90)
+    qbar, nbar = query_summary(q, block)
+    ppm_c, ppm_r = ratio_ppm(centroid_keep), ratio_ppm(rescue_keep)
+    mask = np.zeros((b, hkv, nb, nb), dtype=np.uint8)
+    scores = {}
+    for bi in range(b):
+        for g in range(hkv):
+            s_c, r = block_scores(qbar, nbar, centroid, radius, alpha, scale, bi, g)
+            if with_scores:
+                scores[(bi, g)] = (s_c, r)
+            for i in range(nb):
+                mask[bi, g, i, 0] |= FORCED
+                mask[bi, g, i, i] |= FORCED
+                cent, resc = select_row(s_c[i], r[i], alpha[bi, g], i, ppm_c, ppm_r)
+                mask[bi, g, i, cent] |= CENTROID
+                mask[bi, g, i, resc] |= RESCUE
+    out = dict(centroid=centroid, radius=radius, med=med, p90=p90, alpha=alpha,
+               qbar=qbar, nbar=nbar, mask=mask, scale=scale)
+    if with_scores:
+        out["scores"] = scores
+    return out
+
+
+def kv_lists(mask: np.ndarray):
+    """Kept key blocks per row, ascending.  Returns (kv_idx, kv_cnt).
+
+    kv_idx is [b, Hkv, nb, nb] int32 with the first kv_cnt entries of a row
+    valid and the rest set to -1.
+    """
+    b, h, nq, nk = mask.shape
+    kv_idx = np.full((b, h, nq, nk), -1, dtype=np.int32)
+    kv_cnt = np.zeros((b, h, nq), dtype=np.int32)
+    for bi in range(b):
+        for g in range(h):
+            for i in range(nq):
+                js = np.nonzero(mask[bi, g, i])[0]
+                kv_idx[bi, g, i, :js.size] = js
+                kv_cnt[bi, g, i] = js.size
+    return kv_idx, kv_cnt
+
+
+# ------------------------------------------------------------ attention
+
+def _attend(qi, keys, vals, qpos, kpos, scale):
+    """Explicit causal softmax attention of queries qi over the given keys."""
+    s = scale * (qi @ keys.T)
+    s = np.where(kpos[None, :] <= qpos[:, None], s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = (p @ vals) / l
+    lse = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def sparse_attention_rows(q, k, v, mask, block: int, rows, scale: float | None = None):
+    """Attention for selected (batch, query head, query block) rows only.
+
+    Rescue branch section: "the combined mask still runs as regular
+    block-sparse FlashAttention".  For each query token t of block i and head
+    h (KV head g = h // (Hq/Hkv)) the keys are the tokens s <= t of the key
+    blocks kept in mask[b, g, i]; the output is the explicit softmax-weighted
+    sum of their values and lse the natural log of the softmax normaliser.
+
+    mask: boolean-like [b, Hkv, nb, nb].  rows: iterable of (b, h, i).
+    Returns {(b, h, i): (o [block, d], lse [block])}.
+    """
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    grp = hq // hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = {}
+    for (bi, h, i) in rows:
+        g = h // grp
+        kept = np.nonzero(mask[bi, g, i])[0]
+        kpos = (kept[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+        qpos = i * block + np.arange(block)
+        qi = np.asarray(q[bi, qpos, h, :], dtype=np.float64)
+        keys = np.asarray(k[bi, kpos, g, :], dtype=np.float64)
+        vals = np.asarray(v[bi, kpos, g, :], dtype=np.float64)
+        out[(bi, h, i)] = _attend(qi, keys, vals, qpos, kpos, scale)
+    return out
+
+
+def sparse_attention(q, k, v, mask, block: int, scale: float | None = None):
+    """Full sparse attention.  Returns o [b, N, Hq, d], lse [b, Hq, N]."""
+    b, n, hq, d = q.shape
+    nb = n // block
+    o = np.zeros((b, n, hq, d), dtype=np.float64)
+    lse = np.zeros((b, hq, n), dtype=np.float64)
+    rows = [(bi, h, i) for bi in range(b) for h in range(hq) for i in range(nb)]
+    res = sparse_attention_rows(q, k, v, mask, block, rows, scale)
+    for (bi, h, i), (oi, li) in res.items():
+        o[bi, i * block:(i + 1) * block, h, :] = oi
+        lse[bi, h, i * block:(i + 1) * block] = li
+    return o, lse
+
+
+def dense_attention(q, k, v, scale: float | None = None):
+    """Dense causal softmax attention with GQA (every key s <= t).
+
+    Returns o [b, N, Hq, d], lse [b, Hq, N].
+    """
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    grp = hq // hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((b, n, hq, d), dtype=np.float64)
+    lse = np.zeros((b, hq, n), dtype=np.float64)
+    pos = np.arange(n)
+    for bi in range(b):
+        for h in range(hq):
+            g = h // grp
+            oi, li = _attend(np.asarray(q[bi, :, h, :], dtype=np.float64),
+                             np.asarray(k[bi, :, g, :], dtype=np.float64),
+                             np.asarray(v[bi, :, g, :], dtype=np.float64), pos, pos, scale)
+            o[bi, :, h, :] = oi
+            lse[bi, h, :] = li
+    return o, lse
