@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark one layer of radius-rescued block-sparse long-context prefill.
+
+A step is one pass of the whole hot path over one layer of seeded synthetic
+input resident in HBM: bsa_block_meta (centroids, radii, quantiles, rescue
+coefficient), bsa_select_mask (query pooling, two-path scores, top-k, kept
+lists) and bsa_prefill_fwd (sparse attention over the kept blocks).  Default
+workload: 131072 tokens, 32 query heads over 4 KV heads, head_dim 128, block
+128, keep-ratios 0.10 / 0.02 (the long-prefill shape of the article "Your 128K
+Context Is 6x Slower Than It Needs to Be").
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill ms/layer & kept-block TFLOPS at 128K GQA 32/4; mask-build HBM GB/s"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa32x4_n131072_d128_b128")
+    ap.add_argument("--layers", type=int, default=2, help="distinct seeded layers rotated per step")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def peak_value(d, *keys):
+    for k in keys:
+        if k in d and isinstance(d[k], (int, float)):
+            return float(d[k])
+    return None
+
+
+def kept_flops(kv_cnt: np.ndarray, block: int, d: int, group: int) -> float:
+    """Kept-block FLOPs: 4 B^2 d per off-diagonal block, 2 B^2 d for the diagonal, per query head."""
+    cnt = kv_cnt.astype(np.int64)
+    per = 4.0 * block * block * d
+    return float(group * (per * (cnt - 1).clip(min=0).sum() + 0.5 * per * (cnt > 0).sum()))
+
+
+def source_sha(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+ATTN_SOURCES = ("block_sparse_long_kv_gb300/csrc/bsa_attn.cu", "block_sparse_long_kv_gb300/csrc/sm103_ptx.cuh")
+
+
+def profiled_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(path):
+        return None, None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_sha") != source_sha(*ATTN_SOURCES):
+        return None, d
+    return d.get("bytes_per_launch_full"), d
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(w, lay, budget_s: float, rng_seed: int = 0):
+    """Time the fp64 oracle on a bounded sample of one layer; extrapolate to ms/layer.
+
+    Sample: key-block meta for a slice of key blocks (scaled by block count),
+    query summary + scores + selection for random rows (scaled by row count),
+    attention for random (head, query block) rows of those (scaled by kept FLOPs).
+    """
+    import oracle as O
+    import synth
+    rng = np.random.default_rng(rng_seed)
+    nb, B, d, G = w.nb, w.block, w.head_dim, w.group
+    scale = 1.0 / math.sqrt(d)
+    t0 = time.perf_counter()
+    # meta on a slice of key blocks of KV head 0
+    nbs = min(nb, 64)
+    kslice = synth.bf16_to_f64(lay["k"][:, :nbs * B, 0:1])
+    O.block_meta(kslice, B)
+    t_meta = (time.perf_counter() - t0) * (nb / nbs) * w.hkv * w.batch
+    # full radii are needed for the quantiles the selection uses
+    k32 = synth.bf16_to_f32(lay["k"])
+    centroid, radius = O.block_meta(k32, B)
+    med, p90 = O.radius_quantiles(radius)
+    alpha = O.rescue_coefficient(radius, med, p90)
+    del k32
+    # selection rows
+    t1 = time.perf_counter()
+    rows = []
+    nsel = 0
+    while time.perf_counter() - t1 < budget_s * 0.3 or nsel < 4:
+        g = int(rng.integers(0, w.hkv))
+        i = int(rng.integers(1, nb))
+        qs = synth.bf16_to_f64(lay["q"][0:1, i * B:(i + 1) * B, g * G:(g + 1) * G])
+        qb, nbar = O.query_summary(qs, B)
+        qfull = np.zeros((1, w.hq, 1, d))
+        nfull = np.zeros((1, w.hq, 1))
+        qfull[0, g * G:(g + 1) * G] = qb[0]
+        nfull[0, g * G:(g + 1) * G] = nbar[0]
+        s_c, r = O.block_scores(qfull, nfull, centroid, radius, alpha, scale, 0, g)
+        cent, resc = O.select_row(s_c[0], r[0], alpha[0, g], i, O.ratio_ppm(w.centroid_keep),
+                                  O.ratio_ppm(w.rescue_keep))
+        rows.append((g, i, np.union1d(np.union1d(cent, resc), [0, i])))
+        nsel += 1
+        if nsel >= 256:
+            break
+    t_sel = (time.perf_counter() - t1) * (nb * w.hkv * w.batch / nsel)
+    # attention rows, FLOP-weighted
+    q32, v32 = synth.bf16_to_f32(lay["q"]), synth.bf16_to_f32(lay["v"])
+    k32 = synth.bf16_to_f32(lay["k"])
+    t2 = time.perf_counter()
+    flops_done = 0.0
+    nat = 0
+    for (g, i, kept) in rows:
+        mask = np.zeros((1, w.hkv, nb, nb), dtype=bool)
+        mask[0, g, i, kept] = True
+        h = g * G + int(rng.integers(0, G))
+        O.sparse_attention_rows(q32, k32, v32, mask, B, [(0, h, i)], scale)
+        flops_done += 4.0 * B * B * d * (len(kept) - 1) + 2.0 * B * B * d
+        nat += 1
+        if time.perf_counter() - t2 > budget_s * 0.6:
+            break
+    t_att_per_flop = (time.perf_counter() - t2) / flops_done
+    return {"t_meta": t_meta, "t_sel": t_sel, "t_att_per_flop": t_att_per_flop,
+            "sample": f"meta over {nbs} of {nb} key blocks (1 KV head), selection for {nsel} "
+                      f"random query-block rows, attention for {nat} random (head, query block) rows; "
+                      f"extrapolated to the whole layer by block count, row count and kept FLOPs"}
+
+
+def threads_used():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [x.get("num_threads", 1) for x in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+    w = synth.workload(args.workload)
+    lay = synth.make_layer(w, layer=0)
+    per_step = max(3.0, min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup)))
+    est = []
+    for s in range(args.warmup + args.steps):
+        r = oracle_sample(w, lay, per_step, rng_seed=s)
+        if s >= args.warmup:
+            est.append(r)
+    # kept FLOPs of the layer from the oracle's expected keep counts (ratios fixed per row)
+    import oracle as O
+    cnt = np.zeros((w.batch, w.hkv, w.nb), dtype=np.int64)
+    for i in range(w.nb):
+        nc = max(i - 1, 0)
+        kc = min(O.keep_count(O.ratio_ppm(w.centroid_keep), i), nc)
+        kr = min(O.keep_count(O.ratio_ppm(w.rescue_keep), i), max(nc - kc, 0))
+        cnt[..., i] = (1 if i == 0 else 2) + kc + kr
+    fl = kept_flops(cnt, w.block, w.head_dim, w.group)
+    ms = [1e3 * (r["t_meta"] + r["t_sel"] + r["t_att_per_flop"] * fl) for r in est]
+    val = float(np.median(ms))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "ms/layer",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": val, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded generator, same workload)",
+        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
+                   "rescue_keep": w.rescue_keep},
+        "cpu_baseline": {"value": val, "unit": "ms/layer", "cores": threads_used(),
+                         "kind": "oracle", "sample": est[0]["sample"]},
+        "e2e": {"value": val, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "fp64 numpy oracle timed on a bounded sample per step, extrapolated (upper bound of "
+                "keep counts used for the FLOP scale)",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import block_sparse_long_kv_gb300 as bsa
+    from block_sparse_long_kv_gb300 import build as bld
+    import synth
+    if rank == 0:
+        bld.build()
+    if world > 1:
+        dist.barrier()
+
+    w = synth.workload(args.workload)
+    s = bsa.make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
+    prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0)
+    scale = 1.0 / math.sqrt(w.head_dim)
+
+    # resident inputs: `layers` distinct seeded layers per rank (replicas process their own layers)
+    host_layers = []
+    dev_layers = []
+    for li in range(args.layers):
+        lay = synth.make_layer(w, layer=rank * args.layers + li)
+        host_layers.append(lay)
+        up = lambda x: torch.from_numpy(lay[x].view(np.int16)).to(dev).view(torch.bfloat16)
+        dev_layers.append({x: up(x) for x in ("q", "k", "v")})
+    meta = bsa.alloc_meta(s, dev)
+    sel = bsa.alloc_select(s, dev, with_mask=False)
+    o = torch.empty_like(dev_layers[0]["q"])
+    lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(L, evs=None):
+        if evs:
+            evs[0].record(stream)
+        bsa.block_meta(s, L["k"], meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], status)
+        if evs:
+            evs[1].record(stream)
+        bsa.select_mask(s, prm, L["q"], meta["centroid"], meta["radius"], meta["alpha"],
+                        sel["kv_idx"], sel["kv_cnt"], None, status)
+        if evs:
+            evs[2].record(stream)
+        bsa.prefill_fwd(s, L["q"], L["k"], L["v"], sel["kv_idx"], sel["kv_cnt"], scale, o, lse, status)
+        if evs:
+            evs[3].record(stream)
+
+    # kept FLOPs and list bytes per layer (exact, from the kernels' own kv_cnt)
+    flops, list_bytes, density = [], [], []
+    for L in dev_layers:
+        step(L)
+        torch.cuda.synchronize(dev)
+        cnt = sel["kv_cnt"].cpu().numpy()
+        flops.append(kept_flops(cnt, w.block, w.head_dim, w.group))
+        list_bytes.append(float(cnt.sum()) * 4 + cnt.size * 4)
+        density.append(float(cnt.sum()) / (w.batch * w.hkv * w.nb * (w.nb + 1) / 2))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    for i in range(args.warmup):
+        step(dev_layers[i % len(dev_layers)])
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        step(dev_layers[i % len(dev_layers)], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    meta_ms = np.array([evs[i][0].elapsed_time(evs[i][1]) for i in range(K)])
+    sel_ms = np.array([evs[i][1].elapsed_time(evs[i][2]) for i in range(K)])
+    att_ms = np.array([evs[i][2].elapsed_time(evs[i][3]) for i in range(K)])
+    fl = np.array([flops[i % len(flops)] for i in range(K)])
+    lb = np.array([list_bytes[i % len(list_bytes)] for i in range(K)])
+    mask_bytes = w.batch * w.seq * (w.hq + w.hkv) * w.head_dim * 2 + lb
+    kept_tflops = float((fl / (att_ms * 1e-3)).mean() / 1e12)
+    mask_ms = meta_ms + sel_ms
+    mask_gbs = float((mask_bytes / (mask_ms * 1e-3)).mean() / 1e9)
+
+    pk, src = peaks()
+    bf16_peak = peak_value(pk, "bf16_tflops", "bf16_tflops_burst")
+    hbm_peak = peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm_gb_s")
+    traffic, _ = profiled_traffic()
+    ms_per_layer = total_ms / (K * world)
+    result = {
+        "metric": METRIC, "value": ms_per_layer, "unit": "ms/layer", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator: clustered keys with log-uniform block spreads, planted needles)",
+        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
+                   "rescue_keep": w.rescue_keep, "layers_rotated": args.layers,
+                   "l2": "inputs larger than L2 (Q alone is 1.07 GB per layer), layers rotated"},
+        "kept_block_tflops": kept_tflops,
+        "attention_ms": float(att_ms.mean()),
+        "mask_build_ms": float(mask_ms.mean()),
+        "mask_build_gbs": mask_gbs,
+        "density": float(np.mean(density)),
+        "roofline": {"kernel": "attn_kernel (bsa_prefill_fwd)", "bound": "tensor",
+                     "achieved": kept_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": kept_tflops / bf16_peak if bf16_peak else None,
+                     "peak_source": f"{src} bf16 burst", "traffic": traffic,
+                     "flops_per_launch": float(np.mean(flops))},
+        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + select_kernel",
+                                "bound": "hbm", "achieved": mask_gbs, "peak": hbm_peak,
+                                "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
+                                "peak_source": f"{src} hbm copy",
+                                "bytes_per_launch": float(np.mean(mask_bytes))},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+
+    # end to end through the C ABI: pinned host -> device, one bsa_prefill_layer call, O -> host
+    if not args.no_e2e:
+        ws = bsa.alloc_layer_workspace(s, dev)
+        hl = host_layers[0]
+        pinned = {x: torch.from_numpy(hl[x].view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for x in ("q", "k", "v")}
+        o_host = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+        dq = {x: torch.empty_like(dev_layers[0][x]) for x in ("q", "k", "v")}
+
+        def e2e_step():
+            for x in ("q", "k", "v"):
+                dq[x].copy_(pinned[x], non_blocking=True)
+            bsa.prefill_layer(s, prm, dq["q"], dq["k"], dq["v"], scale, o, lse, ws, status)
+            o_host.copy_(o, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, args.e2e_steps)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(pinned[x].numel() * 2 for x in pinned)
+        result["e2e"] = {"value": e2e_ms / (n_e2e * world), "unit": "ms/layer",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host.numel() * 2,
+                         "steps": n_e2e, "api": "bsa_prefill_layer (C ABI) + pinned host copies"}
+        result["gpu_launches_e2e_per_step"] = 4
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_sample(w, host_layers[0], args.cpu_budget)
+        cpu_ms = 1e3 * (r["t_meta"] + r["t_sel"] + r["t_att_per_flop"] * float(np.mean(flops)))
+        result["cpu_baseline"] = {"value": cpu_ms, "unit": "ms/layer", "cores": threads_used(),
+                                  "kind": "oracle", "sample": r["sample"]}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

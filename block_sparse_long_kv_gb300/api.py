@@ -1,0 +1,169 @@
+"""Python binding of the libbsa C ABI, on torch CUDA tensors.
+
+The functions carry the C entry points' names without the ``bsa_`` prefix and
+do argument marshalling only (dtype / device / contiguity checks, pointers,
+the current CUDA stream); every step of the path runs in libbsa's kernels.
+PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "Shape", "SelectParams", "make_shape", "block_meta", "select_mask", "prefill_fwd",
+    "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
+    "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
+]
+
+Shape = _lib.Shape
+SelectParams = _lib.SelectParams
+
+
+def make_shape(batch: int, seq: int, hq: int, hkv: int, head_dim: int, block: int) -> Shape:
+    return Shape(batch, seq, hq, hkv, head_dim, block)
+
+
+def _ptr(t, name, dtype=None, numel=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims(s: Shape):
+    nb = s.seq // s.block
+    return s.batch, s.seq, s.hq, s.hkv, s.head_dim, nb
+
+
+def block_meta(shape: Shape, k, centroid, radius, quant, alpha, dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_block_meta", lib.bsa_block_meta(
+        ctypes.byref(shape), _ptr(k, "k", torch.bfloat16, b * n * hkv * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
+        _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(quant, "quant", torch.float32, b * hkv * 2),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def select_mask(shape: Shape, params: SelectParams, q, centroid, radius, alpha, kv_idx, kv_cnt,
+                mask=None, dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_select_mask", lib.bsa_select_mask(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
+        _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb),
+        _ptr(mask, "mask", torch.uint8, b * hkv * nb * nb),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def prefill_fwd(shape: Shape, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse=None,
+                dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_prefill_fwd", lib.bsa_prefill_fwd(
+        ctypes.byref(shape), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
+        _ptr(k, "k", torch.bfloat16, b * n * hkv * d), _ptr(v, "v", torch.bfloat16, b * n * hkv * d),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb), ctypes.c_float(softmax_scale),
+        _ptr(o, "o", torch.bfloat16, b * n * hq * d), _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def prefill_dense_fwd(shape: Shape, q, k, v, softmax_scale, o, lse=None, dev_status=None,
+                      stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_prefill_dense_fwd", lib.bsa_prefill_dense_fwd(
+        ctypes.byref(shape), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
+        _ptr(k, "k", torch.bfloat16, b * n * hkv * d), _ptr(v, "v", torch.bfloat16, b * n * hkv * d),
+        ctypes.c_float(softmax_scale), _ptr(o, "o", torch.bfloat16, b * n * hq * d),
+        _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def prefill_layer_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.load().bsa_prefill_layer_workspace_bytes(ctypes.byref(shape)))
+
+
+def prefill_layer(shape: Shape, params: SelectParams, q, k, v, softmax_scale, o, lse, workspace,
+                  dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_prefill_layer", lib.bsa_prefill_layer(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
+        _ptr(k, "k", torch.bfloat16, b * n * hkv * d), _ptr(v, "v", torch.bfloat16, b * n * hkv * d),
+        ctypes.c_float(softmax_scale), _ptr(o, "o", torch.bfloat16, b * n * hq * d),
+        _ptr(lse, "lse", torch.float32, b * hq * n), _ptr(workspace, "workspace", torch.uint8),
+        ctypes.c_size_t(workspace.numel()), _ptr(dev_status, "dev_status", torch.int32),
+        _stream(stream)))
+
+
+def layer_views(shape: Shape, workspace: torch.Tensor) -> dict:
+    """Tensor views of the intermediates bsa_prefill_layer leaves in its workspace."""
+    b, n, hq, hkv, d, nb = _dims(shape)
+    offs = (ctypes.c_size_t * 6)()
+    _lib.check("bsa_prefill_layer_views", _lib.load().bsa_prefill_layer_views(ctypes.byref(shape), offs))
+
+    def view(i, dtype, shp):
+        cnt = math.prod(shp)
+        return workspace[offs[i]:offs[i] + cnt * 4].view(dtype).view(*shp)
+
+    return {
+        "centroid": view(0, torch.float32, (b, hkv, d, nb)),
+        "radius": view(1, torch.float32, (b, hkv, nb)),
+        "quant": view(2, torch.float32, (b, hkv, 2)),
+        "alpha": view(3, torch.float32, (b, hkv, nb)),
+        "kv_idx": view(4, torch.int32, (b, hkv, nb, nb)),
+        "kv_cnt": view(5, torch.int32, (b, hkv, nb)),
+    }
+
+
+def alloc_meta(shape: Shape, device="cuda") -> dict:
+    b, n, hq, hkv, d, nb = _dims(shape)
+    f32 = dict(dtype=torch.float32, device=device)
+    return {"centroid": torch.empty(b, hkv, d, nb, **f32), "radius": torch.empty(b, hkv, nb, **f32),
+            "quant": torch.empty(b, hkv, 2, **f32), "alpha": torch.empty(b, hkv, nb, **f32)}
+
+
+def alloc_select(shape: Shape, device="cuda", with_mask: bool = True) -> dict:
+    b, n, hq, hkv, d, nb = _dims(shape)
+    out = {"kv_idx": torch.empty(b, hkv, nb, nb, dtype=torch.int32, device=device),
+           "kv_cnt": torch.empty(b, hkv, nb, dtype=torch.int32, device=device)}
+    out["mask"] = torch.empty(b, hkv, nb, nb, dtype=torch.uint8, device=device) if with_mask else None
+    return out
+
+
+def alloc_layer_workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    return torch.empty(prefill_layer_workspace_bytes(shape), dtype=torch.uint8, device=device)
+
+
+def status_string(code: int) -> str:
+    return _lib.load().bsa_status_string(code).decode()
+
+
+def version() -> int:
+    return int(_lib.load().bsa_version())

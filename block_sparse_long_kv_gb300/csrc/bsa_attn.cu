@@ -1,0 +1,508 @@
+// Block-sparse causal prefill attention on tcgen05 tensor cores (sm_103a).
+//
+// Source: "Your 128K Context Is 6x Slower Than It Needs to Be"
+// (articles.phantom-byte.com), section "The rescue branch": the combined mask
+// runs as regular block-sparse FlashAttention; and "attention-kernel-
+// optimization" (skill-vault.co.in), section "FlashAttention (1 -> 2 -> 3)":
+// Q/K/V tiles streamed through on-chip memory with online-softmax rescaling,
+// so the N x N score matrix never reaches HBM.
+//
+// One CTA owns NT query tiles of 128 rows that share one kept-block list: the
+// rows are 128 tokens of one head (block 128 / 256) or 64 tokens x 2 heads of
+// the same KV group (block 64), so K and V tiles are loaded once per CTA for
+// NT tiles (GQA sharing).  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K and V tiles of every kept
+//               block through a 2-stage mbarrier ring
+//   warp 1      TMEM owner and single-thread MMA issuer:
+//                 S_t = Q_t K^T   (SS form, both operands in shared memory)
+//                 O_t += P_t V    (TS form, P read from TMEM)
+//   warps 4..   NT softmax warpgroups, one thread per query row: read S_t
+//               from TMEM, causal mask on the diagonal tile only, online
+//               softmax in registers (exp2), P_t as bf16 back into TMEM over
+//               S_t, rare O_t rescale, then the epilogue (O / l, LSE)
+// TMEM columns: S_t at t*KT, O_t at NT*KT + t*D (fp32 accumulators, one TMEM
+// lane per query row).  Every mbarrier wait is bounded: on timeout the kernel
+// records BSA_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs, frees
+// TMEM and returns.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "bsa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;   // 4 s: no legitimate wait comes close
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 0.2 s per in-flight copy on abort
+
+struct AttnParams {
+  const int32_t *kv_idx;  // [b, hkv, nb, nb] (sparse) or null (dense)
+  const int32_t *kv_cnt;  // [b, hkv, nb]
+  uint16_t *o;            // bf16 [b, seq, hq, d]
+  float *lse;             // [b, hq, seq] or null
+  int32_t *dev_status;    // nullable
+  int batch, seq, hq, hkv, nb, group;
+  float scale_log2;       // softmax scale * log2(e)
+};
+
+template <int D, int BLK, int NT>
+struct Cfg {
+  static constexpr int KT = BLK < 128 ? BLK : 128;  // key-tile rows
+  static constexpr int QH = BLK == 64 ? 2 : 1;      // heads stacked in one 128-row Q tile
+  static constexpr int QTOK = 128 / QH;             // tokens per Q tile
+  static constexpr int NQS = BLK == 256 ? 2 : 1;    // Q tiles along one query block
+  static constexpr int SUB = BLK / KT;              // key tiles per key block
+  static constexpr int NCH = D / 64;                // 128-byte swizzle chunks per row
+  static constexpr int NS = 2;                      // K/V pipeline stages
+  static constexpr uint32_t Q_TILE = 128u * D * 2;
+  static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;
+  static constexpr uint32_t Q_CHUNK = 128u * 128;
+  static constexpr uint32_t KV_CHUNK = static_cast<uint32_t>(KT) * 128;
+  static constexpr int TM_O = NT * KT;
+  static constexpr int TM_NEED = NT * (KT + D);
+  static constexpr uint32_t TM_COLS =
+      TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128 : TM_NEED <= 256 ? 256 : 512;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + NT * Q_TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NS * KV_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + NS * KV_TILE;
+  // barriers: Q, K full[NS], V full[NS], K empty[NS], V empty[NS], S full[NT],
+  // P ready[NT], O done[NT], final drain
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NS, B_KE = B_VF + NS, B_VE = B_KE + NS,
+                       B_SF = B_VE + NS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
+                       NBARS = B_FIN + 1;
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;  // + 1 KB alignment slack
+  static constexpr int THREADS = 128 + 128 * NT;
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, KT, false);
+  static constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(128, D, true);
+  static_assert(TM_NEED <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
+};
+
+struct Ctl {
+  volatile int *abort_flag;
+  int32_t *dev_status;
+};
+
+__device__ __forceinline__ void report(const Ctl &c, int code) {
+  *c.abort_flag = 1;
+  if (c.dev_status != nullptr) atomicCAS(c.dev_status, 0, code);
+}
+
+// Bounded wait for phase `parity` of `bar`; false if this CTA is aborting.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*c.abort_flag) return false;
+      // another CTA already gave up: stop at once instead of waiting out our own limit
+      if (c.dev_status != nullptr && *reinterpret_cast<volatile int32_t *>(c.dev_status) != 0) {
+        *c.abort_flag = 1;
+        return false;
+      }
+      if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        report(c, BSA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait that ignores the abort flag (used to drain in-flight work on abort).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kDrainTimeoutNs) return;
+  }
+}
+
+template <int D, int BLK, int NT, bool DENSE>
+__global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using C = Cfg<D, BLK, NT>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char *sb = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  auto bar = [&](int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::OFF_BAR + C::NBARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const Ctl ctl{abort_flag, p.dev_status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: heavy rows first (i descending), head tiles of one row adjacent
+  const int nhp = p.group / C::QH / NT;
+  int item = blockIdx.x;
+  const int hp = item % nhp;
+  item /= nhp;
+  const int g = item % p.hkv;
+  item /= p.hkv;
+  const int b = item % p.batch;
+  item /= p.batch;
+  const int qs = item % C::NQS;
+  const int i = p.nb - 1 - item / C::NQS;
+  const int qtok0 = i * BLK + qs * 128;  // first query token of the CTA's tiles
+  const size_t row = (static_cast<size_t>(b) * p.hkv + g) * p.nb + i;
+  int cnt;
+  if constexpr (DENSE) {
+    cnt = i + 1;
+  } else {
+    cnt = p.kv_cnt[row];
+    cnt = cnt < 0 ? 0 : (cnt > i + 1 ? i + 1 : cnt);
+  }
+  const int32_t *kvrow = DENSE ? nullptr : p.kv_idx + row * p.nb;
+  // the diagonal block of the first half of a 256-row block has an all-masked second key tile
+  const int T = cnt * C::SUB - ((C::NQS == 2 && qs == 0 && cnt > 0) ? 1 : 0);
+  auto key_block = [&](int n) -> int { return DENSE ? n / C::SUB : __ldg(kvrow + n / C::SUB); };
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < C::NBARS; ++x) {
+      uint32_t count = 1;
+      if (x >= C::B_PR && x < C::B_PR + NT) count = 4;  // one arrive per softmax warp
+      ptx::mbar_init(bar(x), count);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0 && T > 0) {
+      ptx::tma_prefetch_desc(&tm_q);
+      ptx::tma_prefetch_desc(&tm_k);
+      ptx::tma_prefetch_desc(&tm_v);
+      ptx::mbar_arrive_expect_tx(bar(C::B_Q), NT * C::Q_TILE);
+      for (int t = 0; t < NT; ++t) {
+        const int h0 = g * p.group + (hp * NT + t) * C::QH;
+        for (int c = 0; c < C::NCH; ++c)
+          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * 64, h0, qtok0, b);
+      }
+      int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
+      for (int n = 0; n < T; ++n) {
+        const int st = n % C::NS, use = n / C::NS;
+        const int ktok0 = key_block(n) * BLK + (n % C::SUB) * C::KT;
+        if (use > 0 && !wait_bar(bar(C::B_KE + st), (use - 1) & 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_KF + st), C::KV_TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          ptx::tma_load_4d(sK + st * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + st), c * 64, g, ktok0, b);
+        k_issued = n + 1;
+        if (use > 0 && !wait_bar(bar(C::B_VE + st), (use - 1) & 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_VF + st), C::KV_TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          ptx::tma_load_4d(sV + st * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + st), c * 64, g, ktok0, b);
+        v_issued = n + 1;
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the CTA's shared memory is released
+        drain_bar(bar(C::B_Q), 0);
+        for (int n = k_issued - C::NS > 0 ? k_issued - C::NS : 0; n < k_issued; ++n) {
+          const int st = n % C::NS, ph = (n / C::NS) & 1;
+          drain_bar(bar(C::B_KF + st), ph);
+          if (n < v_issued) drain_bar(bar(C::B_VF + st), ph);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && T > 0) {
+      bool ok = wait_bar(bar(C::B_Q), 0, ctl);
+      ptx::tc_fence_after();
+      for (int n = 0; ok && n < T; ++n) {
+        const int st = n % C::NS, ph = (n / C::NS) & 1;
+        if (!(ok = wait_bar(bar(C::B_KF + st), ph, ctl))) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < NT && ok; ++t) {
+          if (n > 0) {
+            if (!(ok = wait_bar(bar(C::B_OD + t), (n - 1) & 1, ctl))) break;
+            ptx::tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = ptx::sdesc_sw128(sQ + t * C::Q_TILE + (kk / 4) * C::Q_CHUNK + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(sK + st * C::KV_TILE + (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, 16, 1024);
+            ptx::mma_ss(tmem + t * C::KT, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(C::B_SF + t));
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(C::B_KE + st));
+        if (!(ok = wait_bar(bar(C::B_VF + st), ph, ctl))) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!(ok = wait_bar(bar(C::B_PR + t), n & 1, ctl))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::KT / 16; ++kk) {
+            const uint64_t bd = ptx::sdesc_sw128(sV + st * C::KV_TILE + kk * 2048, C::KV_CHUNK, 1024);
+            ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * C::KT + kk * 8, bd, C::IDESC_O,
+                        (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(C::B_OD + t));
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(C::B_VE + st));
+      }
+      if (!ok) {
+        // every MMA issued so far must finish before TMEM is released
+        ptx::mma_commit(bar(C::B_FIN));
+        drain_bar(bar(C::B_FIN), 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================================================================ softmax + epilogue
+    const int t = (warp - 4) >> 2;             // query tile of this warpgroup
+    const int r = ((warp & 3) << 5) + lane;     // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off + t * C::KT;
+    const uint32_t tO = tmem + lane_off + C::TM_O + t * D;
+    const int tok = r / C::QH;
+    const int head = g * p.group + (hp * NT + t) * C::QH + (r % C::QH);
+    const int qtok = qtok0 + tok;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int n = 0; n < T; ++n) {
+      if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
+      ptx::tc_fence_after();
+      const int j = key_block(n);
+      const int ktok0 = j * BLK + (n % C::SUB) * C::KT;
+      uint32_t sr[C::KT];
+#pragma unroll
+      for (int c = 0; c < C::KT / 32; ++c)
+        ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      ptx::tmem_wait_ld();
+      float mx = -INFINITY;
+      if (ktok0 + C::KT - 1 > qtok0) {
+        // tile overlaps the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok
+        const int lim = qtok - ktok0;
+#pragma unroll
+        for (int c = 0; c < C::KT; ++c) {
+          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sr[c]));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::KT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      }
+      const float mt = mx * sl2;
+      float factor = 1.f;
+      bool resc = false;
+      if (mt > m + 8.f) {  // rescale only when the running max grows by more than 2^8
+        factor = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - mt);
+        resc = n > 0;
+        m = mt;
+      }
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+#pragma unroll
+      for (int c16 = 0; c16 < C::KT / 32; ++c16) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e]), sl2, -mb));
+          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e + 1]), sl2, -mb));
+          rs += p0 + p1;
+          pk[e] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16(tS + c16 * 16, pk);
+      }
+      l = l * factor + rs;
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          ptx::tmem_ld32(tO + c * 32, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+          ptx::tmem_st32(tO + c * 32, ov);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::B_PR + t));
+    }
+
+    if (ok && T > 0) ok = wait_bar(bar(C::B_OD + t), (T - 1) & 1, ctl);
+    ptx::tc_fence_after();
+    const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
+    uint16_t *orow = p.o + ((static_cast<size_t>(b) * p.seq + qtok) * p.hq + head) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      if (T > 0) {
+        ptx::tmem_ld32(tO + c * 32, ov);
+        ptx::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = ptx::pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+      uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+    if (p.lse != nullptr) {
+      const float lse = (ok && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      p.lse[(static_cast<size_t>(b) * p.hq + head) * p.seq + qtok] = lse;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(cudaError_t *err) {
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  *err = status;
+  return fn;
+}
+
+// [batch, seq, heads, d] bf16 viewed as a 4-D tensor (d innermost), tile box
+// {64, box_heads, box_tokens, 1} with 128-byte swizzling.
+bool make_map(EncodeTiledFn fn, CUtensorMap *map, const void *ptr, int batch, int seq, int heads,
+              int d, int box_heads, int box_tokens) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(seq), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2,
+                                 static_cast<cuuint64_t>(seq) * heads * d * 2};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_heads),
+                             static_cast<cuuint32_t>(box_tokens), 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int BLK, int NT, bool DENSE>
+bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void *v,
+                    const AttnParams &prm, cudaStream_t stream, cudaError_t *cerr) {
+  using C = Cfg<D, BLK, NT>;
+  cudaError_t e = cudaSuccess;
+  EncodeTiledFn fn = encode_fn(&e);
+  if (fn == nullptr || e != cudaSuccess) {
+    *cerr = e == cudaSuccess ? cudaErrorNotSupported : e;
+    return BSA_ERR_CUDA;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!make_map(fn, &mq, q, s.batch, s.seq, s.hq, D, C::QH, C::QTOK) ||
+      !make_map(fn, &mk, k, s.batch, s.seq, s.hkv, D, 1, C::KT) ||
+      !make_map(fn, &mv, v, s.batch, s.seq, s.hkv, D, 1, C::KT)) {
+    *cerr = cudaErrorInvalidValue;
+    return BSA_ERR_CUDA;
+  }
+  auto kern = attn_kernel<D, BLK, NT, DENSE>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) {
+    *cerr = e;
+    return BSA_ERR_CUDA;
+  }
+  const long long nitems = static_cast<long long>(s.nb) * C::NQS * s.batch * s.hkv * (s.group / C::QH / NT);
+  kern<<<static_cast<unsigned>(nitems), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *cerr = e;
+    return BSA_ERR_CUDA;
+  }
+  return BSA_OK;
+}
+
+template <int D, int BLK, bool DENSE>
+bsa_status launch_nt(const AttnShape &s, const void *q, const void *k, const void *v,
+                     const AttnParams &prm, cudaStream_t st, cudaError_t *cerr) {
+  constexpr int QH = BLK == 64 ? 2 : 1;
+  if ((s.group / QH) % 2 == 0) return launch_t<D, BLK, 2, DENSE>(s, q, k, v, prm, st, cerr);
+  return launch_t<D, BLK, 1, DENSE>(s, q, k, v, prm, st, cerr);
+}
+
+template <int D, bool DENSE>
+bsa_status launch_blk(const AttnShape &s, const void *q, const void *k, const void *v,
+                      const AttnParams &prm, cudaStream_t st, cudaError_t *cerr) {
+  switch (s.block) {
+    case 64: return launch_nt<D, 64, DENSE>(s, q, k, v, prm, st, cerr);
+    case 128: return launch_nt<D, 128, DENSE>(s, q, k, v, prm, st, cerr);
+    case 256: return launch_nt<D, 256, DENSE>(s, q, k, v, prm, st, cerr);
+    default: return BSA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+bsa_status launch_attention(const AttnShape &s, const void *q, const void *k, const void *v,
+                            const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o,
+                            float *lse, int32_t *dev_status, cudaStream_t stream,
+                            cudaError_t *cuda_err) {
+  *cuda_err = cudaSuccess;
+  AttnParams prm{};
+  prm.kv_idx = kv_idx;
+  prm.kv_cnt = kv_cnt;
+  prm.o = static_cast<uint16_t *>(o);
+  prm.lse = lse;
+  prm.dev_status = dev_status;
+  prm.batch = s.batch;
+  prm.seq = s.seq;
+  prm.hq = s.hq;
+  prm.hkv = s.hkv;
+  prm.nb = s.nb;
+  prm.group = s.group;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const bool dense = kv_idx == nullptr;
+  if (s.d == 64)
+    return dense ? launch_blk<64, true>(s, q, k, v, prm, stream, cuda_err)
+                 : launch_blk<64, false>(s, q, k, v, prm, stream, cuda_err);
+  if (s.d == 128)
+    return dense ? launch_blk<128, true>(s, q, k, v, prm, stream, cuda_err)
+                 : launch_blk<128, false>(s, q, k, v, prm, stream, cuda_err);
+  return BSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace bsa

@@ -1,0 +1,40 @@
+// Internal declarations shared by the libbsa translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bsa.h"
+
+namespace bsa {
+
+constexpr int kMaxBlocks = 4096;  // nb limit (select kernel keeps one score row in smem)
+
+struct MaskShape {
+  int batch, seq, hq, hkv, d, block, nb, group;
+};
+
+// Block meta: centroid [b, hkv, d, nb], radius [b, hkv, nb].
+cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
+                              cudaStream_t stream);
+// Quantiles [b, hkv, 2] and alpha [b, hkv, nb] from radius.
+cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
+                             cudaStream_t stream);
+// Fused query pooling + centroid/rescue scores + top-k + list emission.
+cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
+                          const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
+                          float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
+                          cudaStream_t stream);
+
+struct AttnShape {
+  int batch, seq, hq, hkv, d, block, nb, group;
+};
+
+// Sparse (kv_idx != nullptr) or dense (kv_idx == nullptr) causal attention.
+// Returns BSA_OK or an error code; `cuda_err` receives the CUDA error if any.
+bsa_status launch_attention(const AttnShape &s, const void *q, const void *k, const void *v,
+                            const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o,
+                            float *lse, int32_t *dev_status, cudaStream_t stream,
+                            cudaError_t *cuda_err);
+
+}  // namespace bsa

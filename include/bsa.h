@@ -1,0 +1,186 @@
+/*
+ * bsa.h - C ABI of libbsa: radius-rescued block-sparse causal prefill
+ * attention for GB300 (sm_103a).
+ *
+ * The method follows the article "Your 128K Context Is 6x Slower Than It
+ * Needs to Be" (articles.phantom-byte.com), sections "Why block-sparse
+ * attention underperforms: the mean-dilution trap" and "The rescue branch:
+ * two selection paths, one mask".  Per (layer, KV head) a linear-time mask
+ * build summarises every key block by its centroid and radius, derives a
+ * radius-adaptive rescue coefficient from the median and 90th-percentile
+ * radius, thresholds a centroid path and a rescue path independently and ORs
+ * the two masks; FlashAttention-style attention with online softmax then runs
+ * over the kept blocks only ("attention-kernel-optimization",
+ * skill-vault.co.in, section "FlashAttention (1 -> 2 -> 3)").
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers into memory the caller owns; the
+ *     library never allocates, frees or synchronises.  Every call is
+ *     asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Tensors are dense, contiguous, row-major.  Q is [batch, seq, hq, d],
+ *     K and V are [batch, seq, hkv, d], O is [batch, seq, hq, d], all bf16.
+ *     Device pointers must be 16-byte aligned.
+ *   - Notation: nb = seq / block key (and query) blocks; G = hq / hkv query
+ *     heads per KV head; query head h reads KV head g = h / G.
+ *   - Host-side argument errors are returned before anything is launched.
+ *     A failed launch returns BSA_ERR_CUDA.
+ *   - `dev_status` (nullable) is a device int32 the kernels set to a nonzero
+ *     bsa_status when a bounded device-side wait gives up (the kernel then
+ *     returns without hanging the GPU).  The caller zeroes it and reads it
+ *     after its own synchronisation.
+ *   - NaN or Inf inputs give undefined (but memory-safe) results.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *bsa_stream_t;
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = 1,    /* null pointer, misaligned pointer, bad ratio */
+  BSA_ERR_SHAPE = 2,          /* inconsistent shape (seq % block, hq % hkv, ...) */
+  BSA_ERR_UNSUPPORTED = 3,    /* consistent but not implemented (head_dim, block, ...) */
+  BSA_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+  BSA_ERR_CUDA = 5,           /* a CUDA runtime or driver call failed */
+  BSA_ERR_DEVICE_TIMEOUT = 6  /* written to *dev_status by a kernel whose wait gave up */
+} bsa_status;
+
+/*
+ * Problem shape.  Supported: head_dim in {64, 128}; block in {64, 128, 256};
+ * seq % block == 0; nb % 4 == 0; 1 <= nb <= 4096; hq % hkv == 0; for block 64
+ * the group size G must be even (two heads share one 128-row query tile).
+ */
+typedef struct {
+  int32_t batch, seq, hq, hkv, head_dim, block;
+} bsa_shape;
+
+/*
+ * Selection parameters (rescue branch section: "the two branches are then
+ * thresholded independently").  Each path keeps a fraction of the causal row:
+ * query block i keeps ceil(ratio * (i + 1)) candidates on each path, computed
+ * as (ppm * (i + 1) + 999999) / 1000000 with ppm = floor(ratio * 1e6 + 0.5),
+ * clipped to the available candidates.  Ratios must lie in [0, 1].
+ * flags: reserved, must be 0.
+ */
+typedef struct {
+  float centroid_keep;
+  float rescue_keep;
+  int32_t flags;
+} bsa_select_params;
+
+/* Bits of the optional mask written by bsa_select_mask. */
+#define BSA_MASK_FORCED 1u    /* key block 0 or the diagonal block */
+#define BSA_MASK_CENTROID 2u  /* kept by the centroid path */
+#define BSA_MASK_RESCUE 4u    /* kept by the rescue path */
+
+/*
+ * bsa_block_meta - key-block summaries and the rescue coefficient.
+ *
+ * Rescue branch section: "for each key block, compute the centroid, then
+ * compute the maximum distance from any key in that block to that centroid";
+ * the coefficient is "derived from the distribution of those radii, using the
+ * median and the 90th percentile as the reference points", computed "for each
+ * layer and each key-value head".
+ *
+ *   centroid[b][g][x][j]  (fp32, [batch, hkv, head_dim, nb], dimension-major so
+ *                         that the scoring kernel reads it coalesced)
+ *                         = mean over the block's keys of k[x]
+ *   radius[b][g][j]       = max over the block's keys of |k - centroid|_2
+ *   quant[b][g][0..1]     = median and 90th percentile of radius[b][g][:],
+ *                           nearest rank: r_(ceil(p * nb)) of the ascending sort
+ *   alpha[b][g][j]        = clamp((r_j - med) / (p90 - med), 0, 1), or 0 for
+ *                           all j when p90 - med <= 1e-12 * p90
+ * All outputs fp32, caller-allocated.  k: bf16 [batch, seq, hkv, head_dim].
+ */
+bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid, float *radius,
+                          float *quant, float *alpha, int32_t *dev_status, bsa_stream_t stream);
+
+/*
+ * bsa_select_mask - score every causal key block and emit the kept lists.
+ *
+ * Rescue branch section: the centroid branch scores every block on average
+ * relevance and keeps the high ones; the rescue branch rescues wide-radius
+ * blocks "even when their average score says otherwise"; the two masks are
+ * combined.  With s = 1/sqrt(head_dim), qbar_{h,i} the mean query of block i
+ * for head h and nbar_{h,i} the mean of those queries' L2 norms:
+ *   S_c[i][j] = max over the G heads of KV head g of s * qbar_{h,i}.c_j
+ *   R[i][j]   = max over those heads of s * (qbar_{h,i}.c_j + alpha_j * nbar_{h,i} * r_j)
+ * Row i keeps blocks 0 and i (forced, outside both rankings), the top
+ * ceil(centroid_keep * (i+1)) of 1..i-1 by S_c, and the top
+ * ceil(rescue_keep * (i+1)) by R of the candidates the centroid path dropped
+ * whose alpha_j > 0.  Ties go to the lower block index.
+ *
+ * Outputs: kv_idx[b][g][i][0..kv_cnt-1] (int32, [batch, hkv, nb, nb]) holds the
+ * kept key blocks of row i in ascending order; entries past kv_cnt are left
+ * unspecified.  kv_cnt[b][g][i] (int32, [batch, hkv, nb]).  mask (nullable,
+ * uint8 [batch, hkv, nb, nb]) receives the BSA_MASK_* bits of every (i, j).
+ * q: bf16 [batch, seq, hq, head_dim]; centroid, radius, alpha as written by
+ * bsa_block_meta.  Needs no workspace.
+ */
+bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *params, const void *q,
+                           const float *centroid, const float *radius, const float *alpha,
+                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, int32_t *dev_status,
+                           bsa_stream_t stream);
+
+/*
+ * bsa_prefill_fwd - causal attention over the kept key blocks.
+ *
+ * Rescue branch section: "the combined mask still runs as regular
+ * block-sparse FlashAttention".  For every query token t of block i and head h:
+ *   O[t][h] = sum_s softmax_s(scale * q_t . k_s) v_s,  over the tokens s <= t
+ *             of the key blocks kv_idx[b][g][i][0..kv_cnt-1], g = h / G;
+ *   lse[b][h][t] = natural log of that softmax's normaliser (fp32, nullable).
+ * kv_idx rows must be strictly ascending, in [0, i], and contain i; block 0
+ * need not be present.  Tiled online softmax gives the explicit softmax's
+ * result up to rounding.  o: bf16 [batch, seq, hq, head_dim].
+ */
+bsa_status bsa_prefill_fwd(const bsa_shape *shape, const void *q, const void *k, const void *v,
+                           const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale,
+                           void *o, float *lse, int32_t *dev_status, bsa_stream_t stream);
+
+/*
+ * bsa_prefill_dense_fwd - the same kernel with every causal block kept
+ * (the dense baseline every speedup in the article is normalised against).
+ */
+bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const void *k,
+                                 const void *v, float softmax_scale, void *o, float *lse,
+                                 int32_t *dev_status, bsa_stream_t stream);
+
+/*
+ * bsa_prefill_layer - one whole layer of the hot path in one call:
+ * bsa_block_meta, bsa_select_mask, then bsa_prefill_fwd, all on `stream`.
+ * The intermediate tensors live in `workspace` (device, 256-byte aligned, at
+ * least bsa_prefill_layer_workspace_bytes(shape) bytes).  kv_idx/kv_cnt are
+ * also left in the workspace; bsa_prefill_layer_views gives their offsets.
+ */
+size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape);
+bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *params,
+                             const void *q, const void *k, const void *v, float softmax_scale,
+                             void *o, float *lse, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, bsa_stream_t stream);
+
+/*
+ * Byte offsets inside the bsa_prefill_layer workspace of: centroid, radius,
+ * quant, alpha, kv_idx, kv_cnt (in that order, 6 entries written to offsets).
+ */
+bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets);
+
+/* Human-readable name of a status code (static storage). */
+const char *bsa_status_string(bsa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

@@ -1,0 +1,191 @@
+"""Helpers for GPU-vs-oracle parity: run the CUDA path through the C ABI on
+seeded inputs, run the oracle on the same bf16 values, and apply the mask
+comparison protocol.
+
+Mask protocol: masks must agree bit for bit except for excused blocks.  A
+mismatched block is excused when
+  * its oracle score on the path where it differs lies within 1e-4 relative of
+    that row's oracle threshold (the lowest kept score), the denominator being
+    max(|threshold|, 1e-3 * rms of the row's candidate scores);
+  * its radius lies within 1e-4 relative of the median (rescue eligibility flip);
+  * its row holds an excused centroid-path block (the rescue candidate set
+    depends on the centroid path).
+Forced bits must always match.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle as O
+import synth
+
+REL = 1e-4
+
+
+def to_dev(bits: np.ndarray, device="cuda"):
+    return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def shape_of(w):
+    from block_sparse_long_kv_gb300 import make_shape
+    return make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
+
+
+def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda"):
+    """Run bsa_block_meta + bsa_select_mask; return numpy results."""
+    import block_sparse_long_kv_gb300 as bsa
+    s = shape_of(w)
+    q, k = to_dev(lay["q"], device), to_dev(lay["k"], device)
+    meta = bsa.alloc_meta(s, device)
+    sel = bsa.alloc_select(s, device, with_mask=True)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    bsa.block_meta(s, k, meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], status)
+    prm = bsa.SelectParams(w.centroid_keep if centroid_keep is None else centroid_keep,
+                           w.rescue_keep if rescue_keep is None else rescue_keep, 0)
+    bsa.select_mask(s, prm, q, meta["centroid"], meta["radius"], meta["alpha"], sel["kv_idx"],
+                    sel["kv_cnt"], sel["mask"], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    out = {kk: v.cpu().numpy() for kk, v in {**meta, **sel}.items()}
+    return out
+
+
+def check_lists_match_mask(mask, kv_idx, kv_cnt):
+    b, h, nb, _ = mask.shape
+    for bi in range(b):
+        for g in range(h):
+            for i in range(nb):
+                js = np.nonzero(mask[bi, g, i])[0]
+                assert kv_cnt[bi, g, i] == js.size, (bi, g, i)
+                np.testing.assert_array_equal(kv_idx[bi, g, i, :js.size], js)
+
+
+def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None):
+    """Oracle mask rows for selected query blocks only.
+
+    rows_by_bg: {(b, g): [i, ...]}.  Returns dict with per-(b, g, i) mask rows
+    and the row scores, plus the oracle meta (centroid, radius, med, p90, alpha).
+    """
+    rc = w.centroid_keep if centroid_keep is None else centroid_keep
+    rr = w.rescue_keep if rescue_keep is None else rescue_keep
+    k = synth.bf16_to_f64(lay["k"])
+    centroid, radius = O.block_meta(k, w.block)
+    del k
+    med, p90 = O.radius_quantiles(radius)
+    alpha = O.rescue_coefficient(radius, med, p90)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    grp = w.group
+    rows = {}
+    for (b, g), ilist in rows_by_bg.items():
+        ilist = sorted(ilist)
+        # mean query / norm of just these blocks (oracle query_summary on each block's tokens)
+        qbar = np.zeros((grp, len(ilist), w.head_dim))
+        nbar = np.zeros((grp, len(ilist)))
+        for ri, i in enumerate(ilist):
+            qs = synth.bf16_to_f64(lay["q"][b:b + 1, i * w.block:(i + 1) * w.block,
+                                            g * grp:(g + 1) * grp])
+            qb1, nb1 = O.query_summary(qs, w.block)
+            qbar[:, ri] = qb1[0, :, 0]
+            nbar[:, ri] = nb1[0, :, 0]
+        # pad to the oracle's [b, Hq, rows, d] layout with this group's heads at g*grp
+        qb = np.zeros((b + 1, w.hq, len(ilist), w.head_dim))
+        nbb = np.zeros((b + 1, w.hq, len(ilist)))
+        qb[b, g * grp:(g + 1) * grp] = qbar
+        nbb[b, g * grp:(g + 1) * grp] = nbar
+        s_c, r = O.block_scores(qb, nbb, centroid, radius, alpha, scale, b, g)
+        for ri, i in enumerate(ilist):
+            cent, resc = O.select_row(s_c[ri], r[ri], alpha[b, g], i, O.ratio_ppm(rc), O.ratio_ppm(rr))
+            m = np.zeros(w.nb, dtype=np.uint8)
+            m[0] |= O.FORCED
+            m[i] |= O.FORCED
+            m[cent] |= O.CENTROID
+            m[resc] |= O.RESCUE
+            rows[(b, g, i)] = (m, s_c[ri], r[ri])
+    return dict(rows=rows, centroid=centroid, radius=radius, med=med, p90=p90, alpha=alpha)
+
+
+def compare_mask_rows(gpu_mask, orc):
+    """Apply the protocol; returns (n_compared_blocks, n_excused).  Raises on an unexcused mismatch."""
+    excused = 0
+    compared = 0
+    for (b, g, i), (om, s_c, r) in orc["rows"].items():
+        gm = gpu_mask[b, g, i]
+        compared += i + 1
+        diff = np.nonzero(gm != om)[0]
+        if diff.size == 0:
+            continue
+        assert not np.any((gm[diff] ^ om[diff]) & O.FORCED), ("forced bits differ", b, g, i)
+        cands = np.arange(1, i)
+        cent = np.nonzero(om & O.CENTROID)[0]
+        resc = np.nonzero(om & O.RESCUE)[0]
+
+        def near(score, kept, j):
+            if kept.size == 0:
+                return False
+            t = score[kept].min()
+            rms = math.sqrt(float(np.mean(score[cands] ** 2))) if cands.size else 0.0
+            den = max(abs(t), 1e-3 * rms)
+            return abs(score[j] - t) <= REL * den
+
+        med = orc["med"][b, g]
+        cent_excused = False
+        row_ok = []
+        for j in diff:
+            if (gm[j] ^ om[j]) & O.CENTROID:
+                ok = near(s_c, cent, j)
+                cent_excused |= ok
+                row_ok.append((j, ok))
+        for j in diff:
+            if not ((gm[j] ^ om[j]) & O.CENTROID) and ((gm[j] ^ om[j]) & O.RESCUE):
+                ok = (near(r, resc, j) or abs(orc["radius"][b, g, j] - med) <= REL * med
+                      or cent_excused)
+                row_ok.append((j, ok))
+        for j, ok in row_ok:
+            assert ok, f"unexcused mask mismatch at b={b} g={g} i={i} j={j}: gpu={gm[j]} oracle={om[j]}"
+        excused += len(row_ok)
+    return compared, excused
+
+
+def upload_lists(mask_rows_full, device="cuda"):
+    kv_idx, kv_cnt = O.kv_lists(mask_rows_full)
+    return (torch.from_numpy(kv_idx).to(device), torch.from_numpy(kv_cnt).to(device))
+
+
+def gpu_attention(w, lay, kv_idx=None, kv_cnt=None, scale=None, device="cuda"):
+    import block_sparse_long_kv_gb300 as bsa
+    s = shape_of(w)
+    q, k, v = to_dev(lay["q"], device), to_dev(lay["k"], device), to_dev(lay["v"], device)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
+    if kv_idx is None:
+        bsa.prefill_dense_fwd(s, q, k, v, scale, o, lse, status)
+    else:
+        bsa.prefill_fwd(s, q, k, v, kv_idx, kv_cnt, scale, o, lse, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check_attention_rows(w, lay, o_gpu, lse_gpu, keep, rows, scale=None):
+    """Compare GPU rows (b, h, i) against the oracle: max-abs 2e-2, mean-abs 2e-3, LSE 1e-3."""
+    # float32 holds bf16 values exactly; the oracle widens each slice to float64
+    q = synth.bf16_to_f32(lay["q"])
+    k = synth.bf16_to_f32(lay["k"])
+    v = synth.bf16_to_f32(lay["v"])
+    ref = O.sparse_attention_rows(q, k, v, keep, w.block, rows, scale)
+    errs = []
+    lerr = 0.0
+    for (b, h, i), (oi, li) in ref.items():
+        go = o_gpu[b, i * w.block:(i + 1) * w.block, h, :]
+        errs.append(np.abs(go - oi))
+        lerr = max(lerr, float(np.abs(lse_gpu[b, h, i * w.block:(i + 1) * w.block] - li).max()))
+    e = np.concatenate([x.reshape(-1) for x in errs])
+    assert e.max() <= 2e-2, f"max-abs {e.max()}"
+    assert e.mean() <= 2e-3, f"mean-abs {e.mean()}"
+    assert lerr <= 1e-3, f"lse {lerr}"
+    return float(e.max()), float(e.mean()), lerr

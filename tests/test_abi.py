@@ -1,0 +1,118 @@
+"""libbsa loads, exports every symbol include/bsa.h declares, and rejects bad
+arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_long_kv_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from block_sparse_long_kv_gb300 import _lib
+    names = header_functions()
+    assert "bsa_prefill_fwd" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings(lib):
+    from block_sparse_long_kv_gb300 import _lib
+    for code, name in _lib.STATUS.items():
+        assert lib.bsa_status_string(code).decode() == name
+    assert lib.bsa_version() >= 100
+
+
+FAKE = 0x10000          # aligned, never dereferenced: every call below fails validation first
+MIS = 0x10001
+
+
+def shp(**kw):
+    from block_sparse_long_kv_gb300 import _lib
+    base = dict(batch=1, seq=1024, hq=2, hkv=1, head_dim=64, block=64)
+    base.update(kw)
+    return _lib.Shape(**base)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(seq=1000), 2), (dict(hq=3, hkv=2), 2), (dict(batch=0), 2), (dict(seq=0), 2),
+    (dict(head_dim=96), 3), (dict(block=32), 3), (dict(seq=64 * 6), 3),       # nb % 4
+    (dict(seq=64 * 4100), 3), (dict(hq=3, hkv=1, block=64), 3),               # nb > 4096; odd group
+    (dict(hq=24, hkv=1, block=128), 3),                                         # group 24
+])
+def test_shape_validation(lib, kw, code):
+    s = shp(**kw)
+    p = [ctypes.c_void_p(FAKE)] * 6
+    assert lib.bsa_block_meta(ctypes.byref(s), *p[:5], None, None) == code
+    assert lib.bsa_prefill_dense_fwd(ctypes.byref(s), *p[:3], ctypes.c_float(0.1), p[0], None,
+                                     None, None) == code
+    assert lib.bsa_prefill_layer_workspace_bytes(ctypes.byref(s)) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    from block_sparse_long_kv_gb300 import _lib
+    s = shp()
+    f = ctypes.c_void_p(FAKE)
+    assert lib.bsa_block_meta(None, f, f, f, f, f, None, None) == 1
+    assert lib.bsa_block_meta(ctypes.byref(s), None, f, f, f, f, None, None) == 1
+    assert lib.bsa_block_meta(ctypes.byref(s), ctypes.c_void_p(MIS), f, f, f, f, None, None) == 1
+    prm = _lib.SelectParams(0.25, 0.05, 0)
+    args = [f] * 6
+    assert lib.bsa_select_mask(ctypes.byref(s), None, *args, None, None, None) == 1
+    for bad in (_lib.SelectParams(1.5, 0.0, 0), _lib.SelectParams(0.1, -0.1, 0),
+                _lib.SelectParams(float("nan"), 0.0, 0), _lib.SelectParams(0.1, 0.1, 1)):
+        assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(bad), *args, None, None, None) == 1
+    assert lib.bsa_prefill_fwd(ctypes.byref(s), f, f, f, None, f, ctypes.c_float(0.1), f, None,
+                               None, None) == 1
+    assert lib.bsa_prefill_fwd(ctypes.byref(s), f, f, f, f, f, ctypes.c_float(0.0), f, None,
+                               None, None) == 1
+    assert lib.bsa_prefill_fwd(ctypes.byref(s), f, f, f, f, f, ctypes.c_float(float("inf")), f,
+                               None, None, None) == 1
+
+
+def test_layer_workspace_layout(lib):
+    s = shp(batch=2, seq=8192, hq=32, hkv=4, head_dim=128, block=128)
+    total = lib.bsa_prefill_layer_workspace_bytes(ctypes.byref(s))
+    offs = (ctypes.c_size_t * 6)()
+    assert lib.bsa_prefill_layer_views(ctypes.byref(s), offs) == 0
+    nb = 64
+    sizes = [2 * 4 * 128 * nb * 4, 2 * 4 * nb * 4, 2 * 4 * 2 * 4, 2 * 4 * nb * 4,
+             2 * 4 * nb * nb * 4, 2 * 4 * nb * 4]
+    for x in range(6):
+        assert offs[x] % 256 == 0
+        if x:
+            assert offs[x] >= offs[x - 1] + sizes[x - 1]
+    assert total >= offs[5] + sizes[5]
+    f = ctypes.c_void_p(FAKE)
+    from block_sparse_long_kv_gb300 import _lib
+    prm = _lib.SelectParams(0.25, 0.05, 0)
+    assert lib.bsa_prefill_layer(ctypes.byref(s), ctypes.byref(prm), f, f, f, ctypes.c_float(0.1),
+                                 f, None, f, ctypes.c_size_t(total - 1), None, None) == 4
+    assert lib.bsa_prefill_layer(ctypes.byref(s), ctypes.byref(prm), f, f, f, ctypes.c_float(0.1),
+                                 f, None, ctypes.c_void_p(FAKE + 16), ctypes.c_size_t(total),
+                                 None, None) == 4
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    pkg = os.path.join(ROOT, "block_sparse_long_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in src.replace("oracle-free", ""), fn
+                assert "import synth" not in src, fn

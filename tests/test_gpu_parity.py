@@ -1,0 +1,227 @@
+"""GPU-vs-oracle parity through the C ABI (needs a GB300 and the built library).
+
+Masks: bit-exact up to the excuse protocol in parity_util.  Attention: bf16
+output within max-abs 2e-2 and mean-abs 2e-3 of the fp64 oracle, LSE within
+1e-3.  Meta: centroid / radius within 1e-5 relative, quantiles at the same rank.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from parity_util import (check_attention_rows, check_lists_match_mask, compare_mask_rows,
+                         gpu_attention, gpu_mask_build, oracle_rows, shape_of, to_dev,
+                         upload_lists)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_long_kv_gb300 import build
+    build.build()
+
+
+def all_rows(w):
+    return {(b, g): list(range(w.nb)) for b in range(w.batch) for g in range(w.hkv)}
+
+
+def check_meta(w, lay, got, orc):
+    cen = got["centroid"].transpose(0, 1, 3, 2)          # [b, hkv, nb, d]
+    scale = np.abs(orc["centroid"]).max()
+    assert np.abs(cen - orc["centroid"]).max() <= 1e-5 * max(scale, 1.0)
+    np.testing.assert_allclose(got["radius"], orc["radius"], rtol=1e-5)
+    # quantiles: the GPU picks the block the oracle's rank names (up to near-ties)
+    nb = w.nb
+    for b in range(w.batch):
+        for g in range(w.hkv):
+            order = np.lexsort((np.arange(nb), orc["radius"][b, g]))
+            for qi, rank in ((0, O.nearest_rank(nb, 1, 2)), (1, O.nearest_rank(nb, 9, 10))):
+                want = got["radius"][b, g, order[rank - 1]]
+                if got["quant"][b, g, qi] != want:
+                    ref = orc["radius"][b, g, order[rank - 1]]
+                    near = np.abs(orc["radius"][b, g] - ref) <= 1e-4 * ref
+                    assert near.sum() > 1, ("quantile rank differs", b, g, qi)
+    assert np.abs(got["alpha"] - orc["alpha"]).max() <= 1e-3
+
+
+def full_mask_parity(w, lay, rc=None, rr=None, rows=None):
+    got = gpu_mask_build(w, lay, rc, rr)
+    check_lists_match_mask(got["mask"], got["kv_idx"], got["kv_cnt"])
+    orc = oracle_rows(w, lay, rows or all_rows(w), rc, rr)
+    check_meta(w, lay, got, orc)
+    compared, excused = compare_mask_rows(got["mask"], orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)
+    return got, orc, excused
+
+
+def oracle_keep(w, orc):
+    keep = np.zeros((w.batch, w.hkv, w.nb, w.nb), dtype=np.uint8)
+    for (b, g, i), (m, _, _) in orc["rows"].items():
+        keep[b, g, i] = m
+    return keep
+
+
+def sample_rows(w, per_group, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(w.batch):
+        for h in range(w.hq):
+            iss = {0, w.nb - 1, w.nb // 2} | set(rng.integers(0, w.nb, per_group).tolist())
+            rows += [(b, h, int(i)) for i in sorted(iss)]
+    return rows
+
+
+# ------------------------------------------------------------------ tiny, full coverage
+
+def test_tiny_mask_and_attention_full():
+    w = synth.workload("tiny_h2x1_n1024_d64_b64")
+    lay = synth.make_layer(w)
+    got, orc, _ = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    rows = [(0, h, i) for h in range(w.hq) for i in range(w.nb)]
+    check_attention_rows(w, lay, o, lse, keep != 0, rows)
+
+
+def test_tiny_dense_equals_oracle_dense():
+    w = synth.workload("tiny_h2x1_n1024_d64_b64")
+    lay = synth.make_layer(w)
+    o, lse = gpu_attention(w, lay)
+    q, k, v = (synth.bf16_to_f64(lay[x]) for x in ("q", "k", "v"))
+    od, ld = O.dense_attention(q, k, v)
+    assert np.abs(o - od).max() <= 2e-2 and np.abs(o - od).mean() <= 2e-3
+    assert np.abs(lse - ld).max() <= 1e-3
+
+
+def test_tiny_needles_kept():
+    w = synth.workload("tiny_h2x1_n1024_d64_b64")
+    lay = synth.make_layer(w)
+    got = gpu_mask_build(w, lay)
+    hit = tot = 0
+    for (b, g, jb, slot, pos) in lay["needles"]:
+        for i in sorted(set((pos // w.block).tolist())):
+            tot += 1
+            hit += bool(got["mask"][b, g, i, jb])
+    assert tot > 0 and hit / tot >= 0.5
+
+
+# ------------------------------------------------------------------ GQA 32/4, head_dim 128
+
+@pytest.mark.parametrize("name", ["gqa32x4_n8192_d128_b128", "gqa32x4_n32768_d128_b128"])
+def test_gqa_mask_full_attention_sampled(name):
+    w = synth.workload(name)
+    lay = synth.make_layer(w)
+    got, orc, excused = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    check_attention_rows(w, lay, o, lse, keep != 0, sample_rows(w, 3))
+    # end to end through the GPU's own lists on rows whose masks match the oracle's
+    o2, lse2 = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                             torch.from_numpy(got["kv_cnt"]).cuda())
+    rows = [(b, h, i) for (b, h, i) in sample_rows(w, 3, seed=1)
+            if np.array_equal(got["mask"][b, h // w.group, i], keep[b, h // w.group, i])]
+    assert rows
+    check_attention_rows(w, lay, o2, lse2, keep != 0, rows)
+
+
+@pytest.mark.parametrize("block", [64, 256])
+def test_block_size_variants(block):
+    w = synth.Workload(f"gqa_b{block}", 1, 8192, 32, 4, 128, block, 0.1, 0.02, seed_base=4000)
+    lay = synth.make_layer(w)
+    got, orc, _ = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    check_attention_rows(w, lay, o, lse, keep != 0, sample_rows(w, 2))
+
+
+@pytest.mark.parametrize("rc, rr", [(0.0, 0.0), (0.05, 0.0), (0.2, 0.05), (1.0, 0.0)])
+def test_keep_ratio_variants(rc, rr):
+    w = synth.workload("gqa32x4_n8192_d128_b128")
+    lay = synth.make_layer(w, seed=77)
+    got, orc, _ = full_mask_parity(w, lay, rc, rr)
+    if rc == 1.0:
+        # every causal block kept: the sparse path must equal the dense path bit for bit
+        o_s, l_s = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                                 torch.from_numpy(got["kv_cnt"]).cuda())
+        o_d, l_d = gpu_attention(w, lay)
+        np.testing.assert_array_equal(o_s, o_d)
+        np.testing.assert_array_equal(l_s, l_d)
+    if rc == 0.0 and rr == 0.0:
+        assert np.all(got["kv_cnt"][..., 1:] == 2) and np.all(got["kv_cnt"][..., 0] == 1)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(batch=2, seq=2048, hq=8, hkv=8, head_dim=128, block=128),   # G = 1
+    dict(batch=1, seq=4096, hq=16, hkv=1, head_dim=128, block=128),  # G = 16
+    dict(batch=1, seq=2048, hq=8, hkv=2, head_dim=64, block=128),    # d = 64, block 128
+    dict(batch=1, seq=4096, hq=8, hkv=2, head_dim=64, block=256),    # d = 64, block 256
+    dict(batch=2, seq=256, hq=4, hkv=2, head_dim=128, block=64),     # nb = 4, minimum
+])
+def test_shape_variants(cfg):
+    w = synth.Workload("var", cfg["batch"], cfg["seq"], cfg["hq"], cfg["hkv"], cfg["head_dim"],
+                       cfg["block"], 0.25, 0.05, seed_base=99, needles_fixed=1)
+    lay = synth.make_layer(w)
+    got, orc, _ = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    check_attention_rows(w, lay, o, lse, keep != 0, sample_rows(w, 2))
+    o_d, l_d = gpu_attention(w, lay)
+    rows = sample_rows(w, 1, seed=3)
+    check_attention_rows(w, lay, o_d, l_d, np.ones_like(keep, dtype=bool), rows)
+
+
+def test_deterministic_and_layer_entry_point():
+    import block_sparse_long_kv_gb300 as bsa
+    w = synth.workload("gqa32x4_n8192_d128_b128")
+    lay = synth.make_layer(w)
+    s = shape_of(w)
+    q, k, v = (to_dev(lay[x]) for x in ("q", "k", "v"))
+    ws = bsa.alloc_layer_workspace(s)
+    prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0)
+    outs = []
+    for _ in range(2):
+        o = torch.empty_like(q)
+        lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bsa.prefill_layer(s, prm, q, k, v, 1 / math.sqrt(w.head_dim), o, lse, ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append((o.clone(), lse.clone(), bsa.layer_views(s, ws)["kv_cnt"].clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    got = gpu_mask_build(w, lay)
+    np.testing.assert_array_equal(outs[0][2].cpu().numpy(), got["kv_cnt"])
+
+
+# ------------------------------------------------------------------ 128K, sampled rows
+
+def test_long_prefill_128k_sampled():
+    w = synth.workload("gqa32x4_n131072_d128_b128")
+    lay = synth.make_layer(w, layer=0)
+    got = gpu_mask_build(w, lay)
+    rng = np.random.default_rng(5)
+    rows = {(0, g): sorted({0, 1, 2, w.nb - 1, w.nb // 2} | set(rng.integers(0, w.nb, 24).tolist()))
+            for g in range(w.hkv)}
+    orc = oracle_rows(w, lay, rows)
+    check_meta(w, lay, got, orc)
+    compared, excused = compare_mask_rows(got["mask"], orc)
+    assert excused <= max(4, compared // 1000)
+    # kv lists of every row agree with the mask; density is in the expected range
+    check_lists_match_mask(got["mask"][:, :, -8:], got["kv_idx"][:, :, -8:], got["kv_cnt"][:, :, -8:])
+    o, lse = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                           torch.from_numpy(got["kv_cnt"]).cuda())
+    att_rows = []
+    for (b, g), ilist in rows.items():
+        for i in ilist[::3]:
+            if np.array_equal(got["mask"][b, g, i], orc["rows"][(b, g, i)][0]):
+                att_rows += [(b, g * w.group + hh, i) for hh in (0, w.group - 1)]
+    check_attention_rows(w, lay, o, lse, oracle_keep(w, orc) != 0, att_rows)
