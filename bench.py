@@ -303,6 +303,7 @@ def run_ours(args):
         dev_layers.append({x: up(x) for x in ("q", "k", "v")})
     meta = bsa.alloc_meta(s, dev)
     sel = bsa.alloc_select(s, dev, with_mask=False)
+    sel_ws = torch.empty(bsa.select_workspace_bytes(s), dtype=torch.uint8, device=dev)
     o = torch.empty_like(dev_layers[0]["q"])
     lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -315,7 +316,7 @@ def run_ours(args):
         if evs:
             evs[1].record(stream)
         bsa.select_mask(s, prm, L["q"], meta["centroid"], meta["radius"], meta["alpha"],
-                        sel["kv_idx"], sel["kv_cnt"], None, status)
+                        sel["kv_idx"], sel["kv_cnt"], None, sel_ws, status)
         if evs:
             evs[2].record(stream)
         bsa.prefill_fwd(s, L["q"], L["k"], L["v"], sel["kv_idx"], sel["kv_cnt"], scale, o, lse, status)
@@ -398,12 +399,12 @@ def run_ours(args):
                      "frac": kept_tflops / bf16_peak if bf16_peak else None,
                      "peak_source": f"{src} bf16 burst", "traffic": traffic,
                      "flops_per_launch": float(np.mean(flops))},
-        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + select_kernel",
+        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + qpool_kernel + select_kernel",
                                 "bound": "hbm", "achieved": mask_gbs, "peak": hbm_peak,
                                 "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
                                 "peak_source": f"{src} hbm copy",
                                 "bytes_per_launch": float(np.mean(mask_bytes))},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 5 * K,
         "clocks": clk,
     }
 
@@ -444,7 +445,7 @@ def run_ours(args):
         result["e2e"] = {"value": e2e_ms / (n_e2e * world), "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host.numel() * 2,
                          "steps": n_e2e, "api": "bsa_prefill_layer (C ABI) + pinned host copies"}
-        result["gpu_launches_e2e_per_step"] = 4
+        result["gpu_launches_e2e_per_step"] = 5
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = oracle_sample(w, host_layers[0], args.cpu_budget)

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 __all__ = [
-    "Shape", "SelectParams", "make_shape", "block_meta", "select_mask", "prefill_fwd",
+    "Shape", "SelectParams", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
     "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
     "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
 ]
@@ -65,10 +65,18 @@ def block_meta(shape: Shape, k, centroid, radius, quant, alpha, dev_status=None,
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 
+def select_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.load().bsa_select_workspace_bytes(ctypes.byref(shape)))
+
+
 def select_mask(shape: Shape, params: SelectParams, q, centroid, radius, alpha, kv_idx, kv_cnt,
-                mask=None, dev_status=None, stream=None):
+                mask=None, workspace=None, dev_status=None, stream=None):
+    """bsa_select_mask.  ``workspace``: uint8 CUDA tensor of select_workspace_bytes(shape)
+    bytes (allocated here on the current device if None)."""
     b, n, hq, hkv, d, nb = _dims(shape)
     lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(select_workspace_bytes(shape), dtype=torch.uint8, device=q.device)
     _lib.check("bsa_select_mask", lib.bsa_select_mask(
         ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
         _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
@@ -77,6 +85,7 @@ def select_mask(shape: Shape, params: SelectParams, q, centroid, radius, alpha, 
         _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
         _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb),
         _ptr(mask, "mask", torch.uint8, b * hkv * nb * nb),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 

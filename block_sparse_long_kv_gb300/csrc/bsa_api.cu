@@ -48,13 +48,14 @@ int64_t ratio_ppm(float r) { return static_cast<int64_t>(floor(static_cast<doubl
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout of bsa_prefill_layer: centroid, radius, quant, alpha,
-// kv_idx, kv_cnt, each 256-byte aligned.
-void layer_views(const bsa_shape *s, size_t off[6], size_t *total) {
+// kv_idx, kv_cnt, select scratch, each 256-byte aligned.
+void layer_views(const bsa_shape *s, size_t off[7], size_t *total) {
   const size_t b = s->batch, h = s->hkv, d = s->head_dim, nb = s->seq / s->block;
-  const size_t sizes[6] = {b * h * d * nb * 4, b * h * nb * 4, b * h * 2 * 4,
-                           b * h * nb * 4,     b * h * nb * nb * 4, b * h * nb * 4};
+  const size_t sizes[7] = {b * h * d * nb * 4, b * h * nb * 4,      b * h * 2 * 4, b * h * nb * 4,
+                           b * h * nb * nb * 4, b * h * nb * 4,
+                           bsa::select_workspace_bytes(mask_shape(s))};
   size_t cur = 0;
-  for (int x = 0; x < 6; ++x) {
+  for (int x = 0; x < 7; ++x) {
     off[x] = cur;
     cur = round_up(cur + sizes[x], 256);
   }
@@ -96,11 +97,16 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
   return BSA_OK;
 }
 
+size_t bsa_select_workspace_bytes(const bsa_shape *shape) {
+  if (check_shape(shape) != BSA_OK) return 0;
+  return bsa::select_workspace_bytes(mask_shape(shape));
+}
+
 bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *params, const void *q,
                            const float *centroid, const float *radius, const float *alpha,
-                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, int32_t *dev_status,
-                           bsa_stream_t stream) {
-  (void)dev_status;  // the select kernel has no waits
+                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  (void)dev_status;  // the select kernels have no waits
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
   if (!params || !q || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
@@ -110,11 +116,14 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
   if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius) || !aligned16(alpha) ||
       !aligned16(kv_idx) || !aligned16(kv_cnt) || (mask && !aligned16(mask)))
     return BSA_ERR_INVALID_ARG;
+  const bsa::MaskShape ms = mask_shape(shape);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::select_workspace_bytes(ms))
+    return BSA_ERR_WORKSPACE;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(shape->head_dim)));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (bsa::launch_select(mask_shape(shape), q, centroid, radius, alpha,
-                         ratio_ppm(params->centroid_keep), ratio_ppm(params->rescue_keep), scale,
-                         kv_idx, kv_cnt, mask, s) != cudaSuccess)
+  if (bsa::launch_select(ms, q, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
+                         ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, workspace,
+                         s) != cudaSuccess)
     return BSA_ERR_CUDA;
   return BSA_OK;
 }
@@ -152,7 +161,7 @@ bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const vo
 
 size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape) {
   if (check_shape(shape) != BSA_OK) return 0;
-  size_t off[6], total = 0;
+  size_t off[7], total = 0;
   layer_views(shape, off, &total);
   return total;
 }
@@ -161,8 +170,9 @@ bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets) {
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
   if (!offsets) return BSA_ERR_INVALID_ARG;
-  size_t total = 0;
-  layer_views(shape, offsets, &total);
+  size_t off[7], total = 0;
+  layer_views(shape, off, &total);
+  for (int x = 0; x < 6; ++x) offsets[x] = off[x];
   return BSA_OK;
 }
 
@@ -172,7 +182,7 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
                              int32_t *dev_status, bsa_stream_t stream) {
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
-  size_t off[6], total = 0;
+  size_t off[7], total = 0;
   layer_views(shape, off, &total);
   if (!workspace || workspace_bytes < total) return BSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_WORKSPACE;
@@ -186,7 +196,7 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
   bsa_status r = bsa_block_meta(shape, k, centroid, radius, quant, alpha, dev_status, stream);
   if (r != BSA_OK) return r;
   r = bsa_select_mask(shape, params, q, centroid, radius, alpha, kv_idx, kv_cnt, nullptr,
-                      dev_status, stream);
+                      ws + off[6], total - off[6], dev_status, stream);
   if (r != BSA_OK) return r;
   return bsa_prefill_fwd(shape, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status,
                          stream);

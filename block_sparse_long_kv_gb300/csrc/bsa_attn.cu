@@ -12,10 +12,13 @@
 // the same KV group (block 64), so K and V tiles are loaded once per CTA for
 // NT tiles (GQA sharing).  Warp roles:
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of every kept
-//               block through a 2-stage mbarrier ring
+//               block through mbarrier rings (KS K stages, VS V stages)
 //   warp 1      TMEM owner and single-thread MMA issuer:
 //                 S_t = Q_t K^T   (SS form, both operands in shared memory)
 //                 O_t += P_t V    (TS form, P read from TMEM)
+//               in the ping-pong order S_0(n), PV_1(n-1), S_1(n), PV_0(n), so
+//               the tensor core works on one tile while the other tile's
+//               softmax runs
 //   warps 4..   NT softmax warpgroups, one thread per query row: read S_t
 //               from TMEM, causal mask on the diagonal tile only, online
 //               softmax in registers (exp2), P_t as bf16 back into TMEM over
@@ -58,23 +61,24 @@ struct Cfg {
   static constexpr int NQS = BLK == 256 ? 2 : 1;    // Q tiles along one query block
   static constexpr int SUB = BLK / KT;              // key tiles per key block
   static constexpr int NCH = D / 64;                // 128-byte swizzle chunks per row
-  static constexpr int NS = 2;                      // K/V pipeline stages
   static constexpr uint32_t Q_TILE = 128u * D * 2;
   static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;
   static constexpr uint32_t Q_CHUNK = 128u * 128;
   static constexpr uint32_t KV_CHUNK = static_cast<uint32_t>(KT) * 128;
+  static constexpr int KS = 2;  // K stages: K(n+KS) only needs S(n) done
+  // V stages: V(n+VS) needs PV_1(n) done, which comes late; use 3 when they fit
+  static constexpr int VS = (NT * Q_TILE + KS * KV_TILE + 3 * KV_TILE + 2048 <= 227u * 1024) ? 3 : 2;
   static constexpr int TM_O = NT * KT;
   static constexpr int TM_NEED = NT * (KT + D);
   static constexpr uint32_t TM_COLS =
       TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128 : TM_NEED <= 256 ? 256 : 512;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NT * Q_TILE;
-  static constexpr uint32_t OFF_V = OFF_K + NS * KV_TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + NS * KV_TILE;
-  // barriers: Q, K full[NS], V full[NS], K empty[NS], V empty[NS], S full[NT],
-  // P ready[NT], O done[NT], final drain
-  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NS, B_KE = B_VF + NS, B_VE = B_KE + NS,
-                       B_SF = B_VE + NS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
+  static constexpr uint32_t OFF_V = OFF_K + KS * KV_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_TILE;
+  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain
+  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
+                       B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
                        NBARS = B_FIN + 1;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;  // + 1 KB alignment slack
   static constexpr int THREADS = 128 + 128 * NT;
@@ -185,6 +189,10 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  // the producer / MMA warpgroup needs few registers; the softmax warpgroups take the rest:
+  // 72 * 128 + 216 * 256 = 64512 = 168 * 384, exactly the launch allocation
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0 && T > 0) {
@@ -199,69 +207,93 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
       for (int n = 0; n < T; ++n) {
-        const int st = n % C::NS, use = n / C::NS;
         const int ktok0 = key_block(n) * BLK + (n % C::SUB) * C::KT;
-        if (use > 0 && !wait_bar(bar(C::B_KE + st), (use - 1) & 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_KF + st), C::KV_TILE);
+        const int ks = n % C::KS, ku = n / C::KS;
+        if (ku > 0 && !wait_bar(bar(C::B_KE + ks), (ku - 1) & 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sK + st * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + st), c * 64, g, ktok0, b);
+          ptx::tma_load_4d(sK + ks * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * 64, g, ktok0, b);
         k_issued = n + 1;
-        if (use > 0 && !wait_bar(bar(C::B_VE + st), (use - 1) & 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_VF + st), C::KV_TILE);
+        const int vs = n % C::VS, vu = n / C::VS;
+        if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sV + st * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + st), c * 64, g, ktok0, b);
+          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g, ktok0, b);
         v_issued = n + 1;
       }
       if (*abort_flag) {
         // let every copy still in flight land before the CTA's shared memory is released
         drain_bar(bar(C::B_Q), 0);
-        for (int n = k_issued - C::NS > 0 ? k_issued - C::NS : 0; n < k_issued; ++n) {
-          const int st = n % C::NS, ph = (n / C::NS) & 1;
-          drain_bar(bar(C::B_KF + st), ph);
-          if (n < v_issued) drain_bar(bar(C::B_VF + st), ph);
-        }
+        for (int n = k_issued - C::KS > 0 ? k_issued - C::KS : 0; n < k_issued; ++n)
+          drain_bar(bar(C::B_KF + n % C::KS), (n / C::KS) & 1);
+        for (int n = v_issued - C::VS > 0 ? v_issued - C::VS : 0; n < v_issued; ++n)
+          drain_bar(bar(C::B_VF + n % C::VS), (n / C::VS) & 1);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     if (lane == 0 && T > 0) {
+      auto issue_s = [&](int t, int ks) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(sQ + t * C::Q_TILE + (kk / 4) * C::Q_CHUNK + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(sK + ks * C::KV_TILE + (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, 16, 1024);
+          ptx::mma_ss(tmem + t * C::KT, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_SF + t));
+      };
+      auto issue_pv = [&](int t, int vs, int n) {
+#pragma unroll
+        for (int kk = 0; kk < C::KT / 16; ++kk) {
+          const uint64_t bd = ptx::sdesc_sw128(sV + vs * C::KV_TILE + kk * 2048, C::KV_CHUNK, 1024);
+          ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * C::KT + kk * 8, bd, C::IDESC_O,
+                      (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_OD + t));
+      };
       bool ok = wait_bar(bar(C::B_Q), 0, ctl);
       ptx::tc_fence_after();
       for (int n = 0; ok && n < T; ++n) {
-        const int st = n % C::NS, ph = (n / C::NS) & 1;
-        if (!(ok = wait_bar(bar(C::B_KF + st), ph, ctl))) break;
+        const int ks = n % C::KS;
+        if (!(ok = wait_bar(bar(C::B_KF + ks), (n / C::KS) & 1, ctl))) break;
         ptx::tc_fence_after();
-        for (int t = 0; t < NT && ok; ++t) {
+        // S_0(n) once PV_0(n-1) has released the S_0 / P_0 columns
+        if (n > 0) {
+          if (!(ok = wait_bar(bar(C::B_OD + 0), (n - 1) & 1, ctl))) break;
+          ptx::tc_fence_after();
+        }
+        issue_s(0, ks);
+        if constexpr (NT == 2) {
           if (n > 0) {
-            if (!(ok = wait_bar(bar(C::B_OD + t), (n - 1) & 1, ctl))) break;
+            // PV_1(n-1) overlaps softmax_0(n); then S_1(n) once PV_1(n-1) is done
+            const int pv = n - 1, vs = pv % C::VS;
+            if (!(ok = wait_bar(bar(C::B_PR + 1), pv & 1, ctl))) break;
+            ptx::tc_fence_after();
+            issue_pv(1, vs, pv);
+            ptx::mma_commit(bar(C::B_VE + vs));
+            if (!(ok = wait_bar(bar(C::B_OD + 1), pv & 1, ctl))) break;
             ptx::tc_fence_after();
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(sQ + t * C::Q_TILE + (kk / 4) * C::Q_CHUNK + (kk % 4) * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(sK + st * C::KV_TILE + (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, 16, 1024);
-            ptx::mma_ss(tmem + t * C::KT, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(bar(C::B_SF + t));
+          issue_s(1, ks);
         }
-        if (!ok) break;
-        ptx::mma_commit(bar(C::B_KE + st));
-        if (!(ok = wait_bar(bar(C::B_VF + st), ph, ctl))) break;
+        ptx::mma_commit(bar(C::B_KE + ks));
+        const int vs = n % C::VS;
+        if (!(ok = wait_bar(bar(C::B_VF + vs), (n / C::VS) & 1, ctl))) break;
+        if (!(ok = wait_bar(bar(C::B_PR + 0), n & 1, ctl))) break;
         ptx::tc_fence_after();
-        for (int t = 0; t < NT && ok; ++t) {
-          if (!(ok = wait_bar(bar(C::B_PR + t), n & 1, ctl))) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::KT / 16; ++kk) {
-            const uint64_t bd = ptx::sdesc_sw128(sV + st * C::KV_TILE + kk * 2048, C::KV_CHUNK, 1024);
-            ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * C::KT + kk * 8, bd, C::IDESC_O,
-                        (n > 0 || kk > 0) ? 1u : 0u);
+        issue_pv(0, vs, n);
+        if constexpr (NT == 1) ptx::mma_commit(bar(C::B_VE + vs));
+      }
+      if constexpr (NT == 2) {
+        if (ok) {
+          const int pv = T - 1, vs = pv % C::VS;
+          if ((ok = wait_bar(bar(C::B_PR + 1), pv & 1, ctl))) {
+            ptx::tc_fence_after();
+            issue_pv(1, vs, pv);
+            ptx::mma_commit(bar(C::B_VE + vs));
           }
-          ptx::mma_commit(bar(C::B_OD + t));
         }
-        if (!ok) break;
-        ptx::mma_commit(bar(C::B_VE + st));
       }
       if (!ok) {
         // every MMA issued so far must finish before TMEM is released
@@ -270,8 +302,10 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
     // ================================================================ softmax + epilogue
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
     const int t = (warp - 4) >> 2;             // query tile of this warpgroup
     const int r = ((warp & 3) << 5) + lane;     // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
@@ -294,19 +328,23 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       for (int c = 0; c < C::KT / 32; ++c)
         ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       ptx::tmem_wait_ld();
-      float mx = -INFINITY;
       if (ktok0 + C::KT - 1 > qtok0) {
         // tile overlaps the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok
         const int lim = qtok - ktok0;
 #pragma unroll
-        for (int c = 0; c < C::KT; ++c) {
+        for (int c = 0; c < C::KT; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sr[c]));
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < C::KT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
+      // row max as a tree of eight independent chains
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
+#pragma unroll
+      for (int c = 8; c < C::KT; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mt = mx * sl2;
       float factor = 1.f;
       bool resc = false;
@@ -316,7 +354,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         m = mt;
       }
       const float mb = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c16 = 0; c16 < C::KT / 32; ++c16) {
         uint32_t pk[16];
@@ -324,12 +362,12 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e]), sl2, -mb));
           const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e + 1]), sl2, -mb));
-          rs += p0 + p1;
+          rs4[e & 3] += p0 + p1;
           pk[e] = ptx::pack_bf16x2(p0, p1);
         }
         ptx::tmem_st16(tS + c16 * 16, pk);
       }
-      l = l * factor + rs;
+      l = l * factor + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {

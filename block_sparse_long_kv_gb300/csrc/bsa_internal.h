@@ -20,11 +20,13 @@ cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid
 // Quantiles [b, hkv, 2] and alpha [b, hkv, nb] from radius.
 cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
                              cudaStream_t stream);
-// Fused query pooling + centroid/rescue scores + top-k + list emission.
+// Bytes of select workspace: mean query [b, hq, nb, d] and mean query norm [b, hq, nb], fp32.
+size_t select_workspace_bytes(const MaskShape &s);
+// Query pooling into the workspace, then centroid/rescue scores + top-k + list emission.
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
                           float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                          cudaStream_t stream);
+                          void *workspace, cudaStream_t stream);
 
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;

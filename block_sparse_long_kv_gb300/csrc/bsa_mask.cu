@@ -8,14 +8,16 @@
 // selection paths, OR-combined.  The build reads every token a fixed number of
 // times, so it is linear in the sequence length.
 //
-// Three launches:
+// Four launches:
 //   meta_kernel     one CTA per (b, g, j): centroid and radius of key block j
-//   quant_kernel    one CTA per (b, g): nearest-rank median / p90 and alpha
-//   select_kernel   one CTA per (b, g, i): mean query and mean query norm of
-//                   block i for the G heads of group g (the dominant HBM
-//                   stream), then centroid / rescue scores for every causal
-//                   key block, per-path top-k by radix select, OR, emission
-//                   of the ascending kept list.
+//                   (streams K once)
+//   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii,
+//                   nearest-rank median / p90, rescue coefficient alpha
+//   qpool_kernel    one CTA per (b, i, head chunk): mean query and mean query
+//                   norm of block i (streams Q once: the dominant HBM bytes)
+//   select_kernel   one CTA per (b, g, i): centroid / rescue scores for every
+//                   causal key block (FFMA on L2-resident summaries), per-path
+//                   top-k by radix select, OR, ascending kept-list emission
 // Every reduction runs in a fixed order, so results are deterministic.
 
 #include <cuda_bf16.h>
@@ -69,19 +71,37 @@ __global__ void __launch_bounds__(kThreads) meta_kernel(const uint16_t *__restri
       k + (static_cast<size_t>(b) * seq + static_cast<size_t>(j) * block) * tok_stride +
       static_cast<size_t>(g) * D;
 
+  // block * VPR vectors, a multiple of kThreads for every supported (block, D)
   const int nvec = block * VPR;
-  for (int e = tid; e < nvec; e += kThreads) {
-    const int t = e / VPR, v = e - t * VPR;
-    sk[e] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride) + v);
+  for (int e0 = 0; e0 < nvec; e0 += 8 * kThreads) {
+    uint4 u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int e = e0 + r * kThreads + tid;
+      const int t = e / VPR, v = e - t * VPR;
+      if (e < nvec)
+        u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride) + v);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int e = e0 + r * kThreads + tid;
+      if (e < nvec) sk[e] = u[r];
+    }
   }
   __syncthreads();
 
   const uint16_t *skh = reinterpret_cast<const uint16_t *>(sk);
   {
+    // four interleaved partial sums per thread, combined in a fixed order
     const int x = tid % D, p = tid / D;
-    float s = 0.f;
-    for (int t = p; t < block; t += P) s += bf16_at(skh, t * D + x);
-    part[p * D + x] = s;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int t = p; t < block; t += 4 * P) {
+      s0 += bf16_at(skh, t * D + x);
+      s1 += bf16_at(skh, (t + P) * D + x);
+      s2 += bf16_at(skh, (t + 2 * P) * D + x);
+      s3 += bf16_at(skh, (t + 3 * P) * D + x);
+    }
+    part[p * D + x] = (s0 + s1) + (s2 + s3);
   }
   __syncthreads();
   if (tid < D) {
@@ -96,14 +116,22 @@ __global__ void __launch_bounds__(kThreads) meta_kernel(const uint16_t *__restri
 
   const int warp = tid >> 5, lane = tid & 31;
   float best = 0.f;
-  for (int t = warp; t < block; t += kThreads / 32) {
-    float acc = 0.f;
+  for (int t = warp * 4; t < block; t += kThreads / 32 * 4) {  // four rows per warp at a time
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int x = lane; x < D; x += 32) {
-      const float dl = bf16_at(skh, t * D + x) - sc[x];
-      acc = fmaf(dl, dl, acc);
+      const float cx = sc[x];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float dl = bf16_at(skh, (t + r) * D + x) - cx;
+        acc[r] = fmaf(dl, dl, acc[r]);
+      }
     }
-    best = fmaxf(best, warp_sum(acc));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+    best = fmaxf(best, fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])));
   }
   if (lane == 0) wmax[warp] = best;
   __syncthreads();
@@ -117,30 +145,35 @@ __global__ void __launch_bounds__(kThreads) meta_kernel(const uint16_t *__restri
 
 // ---------------------------------------------------------------- quantiles
 
+// Bitonic sort of the nb radii (padded with +inf to a power of two), then
+// nearest-rank median / p90 and alpha.
 __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ radius,
                                                      float *__restrict__ quant,
-                                                     float *__restrict__ alpha, int nb) {
+                                                     float *__restrict__ alpha, int nb, int npow2) {
   extern __shared__ float sr[];
-  __shared__ float s_med, s_p90;
   const int g = blockIdx.x, b = blockIdx.y, hkv = gridDim.x;
   const size_t base = (static_cast<size_t>(b) * hkv + g) * nb;
-  for (int j = threadIdx.x; j < nb; j += blockDim.x) sr[j] = radius[base + j];
+  for (int j = threadIdx.x; j < npow2; j += blockDim.x) sr[j] = j < nb ? radius[base + j] : INFINITY;
   __syncthreads();
-  // nearest rank (1-based): ceil(nb / 2) and ceil(9 nb / 10)
-  const int i_med = (nb + 1) / 2 - 1;
-  const int i_p90 = (9 * nb + 9) / 10 - 1;
-  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
-    const float rj = sr[j];
-    int pos = 0;  // position of j in the (value, index)-ordered ascending sort
-    for (int q = 0; q < nb; ++q) {
-      const float rq = sr[q];
-      pos += (rq < rj) || (rq == rj && q < j);
+  for (int kk = 2; kk <= npow2; kk <<= 1) {
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int idx = threadIdx.x; idx < npow2; idx += blockDim.x) {
+        const int ixj = idx ^ jj;
+        if (ixj > idx) {
+          const bool up = (idx & kk) == 0;
+          const float a = sr[idx], c = sr[ixj];
+          if ((a > c) == up) {
+            sr[idx] = c;
+            sr[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
     }
-    if (pos == i_med) s_med = rj;
-    if (pos == i_p90) s_p90 = rj;
   }
-  __syncthreads();
-  const float med = s_med, p90 = s_p90;
+  // nearest rank (1-based): ceil(nb / 2) and ceil(9 nb / 10)
+  const float med = sr[(nb + 1) / 2 - 1];
+  const float p90 = sr[(9 * nb + 9) / 10 - 1];
   const float span = p90 - med;
   const bool degenerate = span <= 1e-12f * p90;
   if (threadIdx.x == 0) {
@@ -149,26 +182,77 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
   }
   for (int j = threadIdx.x; j < nb; j += blockDim.x) {
     float a = 0.f;
-    if (!degenerate) a = fminf(fmaxf((sr[j] - med) / span, 0.f), 1.f);
+    if (!degenerate) a = fminf(fmaxf((radius[base + j] - med) / span, 0.f), 1.f);
     alpha[base + j] = a;
   }
 }
 
+// ---------------------------------------------------------------- query pooling
+
+// One thread per (head, 8 dimensions); the token loop keeps 8 16-byte loads in
+// flight per thread.  Writes qbar[b][g][i][x][hh] (dimension-major within the
+// group, the layout the scoring loop reads) and nbar[b][g][i][hh].
+template <int D>
+__global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restrict__ q,
+                                                         float *__restrict__ qbar,
+                                                         float *__restrict__ nbar, int seq,
+                                                         int hq, int hkv, int block, int nb,
+                                                         int hpc) {
+  constexpr int VH = D / 8;  // lanes per head
+  const int i = blockIdx.x, hc = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int hl = tid / VH, xv = tid - hl * VH;
+  const int h = hc * hpc + hl;
+  const size_t tok_stride = static_cast<size_t>(hq) * D;
+  const uint16_t *base = q + (static_cast<size_t>(b) * seq + static_cast<size_t>(i) * block) * tok_stride +
+                         static_cast<size_t>(h) * D + xv * 8;
+  // lanes present in this warp (the last warp may be partial); a head's lanes never straddle warps
+  const int present = min(32, static_cast<int>(blockDim.x) - (tid & ~31));
+  const unsigned wmask = present >= 32 ? 0xffffffffu : ((1u << present) - 1u);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  float nsum = 0.f;
+  for (int t0 = 0; t0 < block; t0 += 8) {
+    uint4 u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride));
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float f[8];
+      unpack_bf16x8(u[r], f);
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[e] += f[e];
+        sq = fmaf(f[e], f[e], sq);
+      }
+#pragma unroll
+      for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
+      nsum += sqrtf(sq);
+    }
+  }
+  const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
+  const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
+  float *qb = qbar + (row * D + xv * 8) * grp + hh;
+  const float inv_b = 1.f / static_cast<float>(block);  // exact: block is a power of two
+#pragma unroll
+  for (int e = 0; e < 8; ++e) qb[e * grp] = acc[e] * inv_b;
+  if (xv == 0) nbar[row * grp + hh] = nsum * inv_b;
+}
+
 // ---------------------------------------------------------------- select
 
-// Order-preserving 48-bit key: score bits on top (higher score = larger key),
-// then 0xFFFF - j so that equal scores rank the lower block index first.
-// Keys are unique within a row, so the k-th largest is a single element.
-__device__ __forceinline__ uint64_t rank_key(float s, int j) {
-  uint32_t u = __float_as_uint(s);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(u) << 16) | static_cast<uint64_t>(0xFFFFu - static_cast<uint32_t>(j));
+// Order-preserving key of a float score: a higher score gives a larger key.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 struct SelectSmem {
   unsigned hist[256];
-  unsigned long long bc_digit;
-  unsigned bc_above;
+  unsigned bc_digit, bc_above, bc_count;
   int wsum[kThreads / 32];
   int total;
 };
@@ -185,7 +269,7 @@ __device__ int block_exclusive_scan(int v, SelectSmem &sm, int *total) {
   if (lane == 31) sm.wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kThreads / 32 ? sm.wsum[lane] : 0;
+    const int w = lane < kThreads / 32 ? sm.wsum[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -202,24 +286,24 @@ __device__ int block_exclusive_scan(int v, SelectSmem &sm, int *total) {
   return res;
 }
 
-// Key of the k-th largest (1-based) eligible element of score[jlo, jhi).
-// Requires 1 <= k <= number of eligible elements.  Radix select, 8-bit digits
-// from the most significant end; called by the whole block.
-template <typename Elig>
-__device__ uint64_t radix_kth_largest(const float *score, int jlo, int jhi, Elig elig, int k,
-                                      SelectSmem &sm) {
+// Marks (flags |= bit) the k best eligible entries of score[1, i): higher score
+// first, ties to the lower index.  Requires 1 <= k < number eligible.  Radix
+// select over the 32-bit score key, 8-bit digits from the top; the rare case of
+// several entries sharing the threshold key is settled by index order.
+__device__ void mark_top_k(const float *score, const uint8_t *flags_in, uint8_t elig_bit,
+                           uint8_t *flags, uint8_t bit, int i, int k, SelectSmem &sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint64_t prefix = 0, pmask = 0;
-  unsigned krem = static_cast<unsigned>(k);
-  for (int shift = 40; shift >= 0; shift -= 8) {
+  uint32_t prefix = 0, pmask = 0;
+  unsigned krem = static_cast<unsigned>(k), n_eq = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
     sm.hist[tid] = 0;  // kThreads == 256 bins
     __syncthreads();
-    for (int base = jlo; base < jhi; base += kThreads) {
+    for (int base = 1; base < i; base += kThreads) {
       const int j = base + tid;
-      bool ok = j < jhi && elig(j);
-      const uint64_t key = ok ? rank_key(score[j], j) : 0ull;
+      bool ok = j < i && (flags_in[j] & elig_bit);
+      const uint32_t key = ok ? score_key(score[j]) : 0u;
       ok = ok && ((key & pmask) == prefix);
-      const unsigned digit = static_cast<unsigned>(key >> shift) & 255u;
+      const unsigned digit = (key >> shift) & 255u;
       const unsigned peers = __match_any_sync(0xffffffffu, ok ? digit : 256u);
       if (ok && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
     }
@@ -232,7 +316,7 @@ __device__ uint64_t radix_kth_largest(const float *score, int jlo, int jhi, Elig
         c[e] = sm.hist[8 * lane + e];
         s += c[e];
       }
-      unsigned suf = s;  // sum over lanes >= this lane
+      unsigned suf = s;  // elements in the bins of lanes >= this lane
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
@@ -242,145 +326,177 @@ __device__ uint64_t radix_kth_largest(const float *score, int jlo, int jhi, Elig
 #pragma unroll
       for (int e = 7; e >= 0; --e) {
         if (acc < krem && krem <= acc + c[e]) {
-          sm.bc_digit = static_cast<unsigned long long>(8 * lane + e);
+          sm.bc_digit = 8 * lane + e;
           sm.bc_above = acc;
+          sm.bc_count = c[e];
         }
         acc += c[e];
       }
     }
     __syncthreads();
     krem -= sm.bc_above;
-    prefix |= static_cast<uint64_t>(sm.bc_digit) << shift;
-    pmask |= 0xFFull << shift;
+    n_eq = sm.bc_count;
+    prefix |= sm.bc_digit << shift;
+    pmask |= 0xFFu << shift;
     __syncthreads();
   }
-  return prefix;
+  // keys above the threshold are in; krem of the n_eq keys equal to it are in
+  if (n_eq == krem) {
+    for (int j = 1 + tid; j < i; j += kThreads)
+      if ((flags_in[j] & elig_bit) && score_key(score[j]) >= prefix) flags[j] |= bit;
+  } else {
+    for (int j = 1 + tid; j < i; j += kThreads)
+      if ((flags_in[j] & elig_bit) && score_key(score[j]) > prefix) flags[j] |= bit;
+    const int n = i - 1;
+    const int chunk = (n + kThreads - 1) / kThreads;
+    const int lo = 1 + min(tid * chunk, n), hi = min(lo + chunk, i);
+    int cnt = 0;
+    for (int j = lo; j < hi; ++j) cnt += (flags_in[j] & elig_bit) && score_key(score[j]) == prefix;
+    int total = 0;
+    int rank = block_exclusive_scan(cnt, sm, &total);
+    for (int j = lo; j < hi; ++j)
+      if ((flags_in[j] & elig_bit) && score_key(score[j]) == prefix) {
+        if (rank < static_cast<int>(krem)) flags[j] |= bit;
+        ++rank;
+      }
+  }
+  __syncthreads();
+}
+
+constexpr uint8_t kCand = 0x40;  // candidate of the centroid path (1 <= j < i)
+constexpr uint8_t kElig = 0x20;  // candidate of the rescue path
+
+constexpr int kPassCols = kThreads / 32 * 128;  // key blocks scored per pass (4 per thread)
+constexpr int kStageFloats = 4096;              // 16 KB per pipeline stage
+constexpr int kStages = 3;
+
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads) select_kernel(
-    const uint16_t *__restrict__ q, const float *__restrict__ centroid,
-    const float *__restrict__ radius, const float *__restrict__ alpha, int32_t *__restrict__ kv_idx,
-    int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask, int seq, int hq, int hkv, int block,
-    int nb, long long ppm_c, long long ppm_r, float scale) {
-  constexpr int VH = D / 8;    // 16-byte vectors per head row
-  constexpr int VR = G * VH;   // vectors per token row of the group
-  static_assert(VR <= kThreads && kThreads % VR == 0, "group row must fit the block");
-  constexpr int RPP = kThreads / VR;  // token rows per pass
-
+    const float *__restrict__ qbar, const float *__restrict__ nbar,
+    const float *__restrict__ centroid, const float *__restrict__ radius,
+    const float *__restrict__ alpha, int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt,
+    uint8_t *__restrict__ mask, int hkv, int nb, long long ppm_c, long long ppm_r, float scale) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float *psum = reinterpret_cast<float *>(smem);   // [RPP][G*D]
-  float *pn = psum + RPP * G * D;                   // [RPP][G]
-  float *qbt = pn + ((RPP * G + 3) & ~3);           // [D][G]  mean query, dimension-major
-  float *nbar = qbt + D * G;                        // [G]
-  float *sS = nbar + ((G + 3) & ~3);                // [nb] centroid-path score
-  float *sR = sS + nb;                              // [nb] rescue-path score
+  float *stage = reinterpret_cast<float *>(smem);  // [kStages][kStageFloats] centroid chunks
+  float *qbt = stage + kStages * kStageFloats;     // [D][G] mean query, dimension-major
+  float *nbs = qbt + D * G;                         // [G]
+  float *sS = nbs + ((G + 3) & ~3);               // [nb] centroid-path score
+  float *sR = sS + nb;                            // [nb] rescue-path score
   uint8_t *flags = reinterpret_cast<uint8_t *>(sR + nb);  // [nb]
   __shared__ SelectSmem sm;
 
   const int i = nb - 1 - static_cast<int>(blockIdx.x);  // longest rows first
   const int g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // ---- query pooling: block i, heads g*G .. g*G+G-1 (G*D contiguous bf16 per token)
-  {
-    const int v = tid % VR, r0 = tid / VR, hh = v / VH;
-    const size_t tok_stride = static_cast<size_t>(hq) * D;
-    const uint16_t *base = q + (static_cast<size_t>(b) * seq + static_cast<size_t>(i) * block) * tok_stride +
-                           static_cast<size_t>(g) * G * D + static_cast<size_t>(v) * 8;
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    float nsum = 0.f;
-    const int nrow = block / RPP;
-#pragma unroll 4
-    for (int it = 0; it < nrow; ++it) {
-      const int t = r0 + it * RPP;
-      const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride));
-      float f[8];
-      unpack_bf16x8(u, f);
-      float sq = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[e] += f[e];
-        sq = fmaf(f[e], f[e], sq);
-      }
-#pragma unroll
-      for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-      nsum += sqrtf(sq);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) psum[r0 * G * D + v * 8 + e] = acc[e];
-    if (v % VH == 0) pn[r0 * G + hh] = nsum;
-  }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += kThreads) {
-    float s = 0.f;
-    for (int r = 0; r < RPP; ++r) s += psum[r * G * D + e];
-    const int hh = e / D, x = e - hh * D;
-    qbt[x * G + hh] = s / static_cast<float>(block);
-  }
-  if (tid < G) {
-    float s = 0.f;
-    for (int r = 0; r < RPP; ++r) s += pn[r * G + tid];
-    nbar[tid] = s / static_cast<float>(block);
-  }
-  for (int j = tid; j < nb; j += kThreads) flags[j] = 0;
-  __syncthreads();
-
-  // ---- scores for candidates j in [1, i-1]; thread tile = 4 key blocks x G heads
   const size_t gb = static_cast<size_t>(b) * hkv + g;
+  const size_t row = gb * nb + i;
+
+  {
+    const float4 *src = reinterpret_cast<const float4 *>(qbar + row * D * G);
+    for (int e = tid; e < D * G / 4; e += kThreads) reinterpret_cast<float4 *>(qbt)[e] = __ldg(src + e);
+    if (tid < G) nbs[tid] = __ldg(nbar + row * G + tid);
+  }
+  for (int j = tid; j < nb; j += kThreads) flags[j] = (j >= 1 && j < i) ? kCand : 0;
+  __syncthreads();
+
+  // ---- scores for candidates j in [1, i-1]; thread tile = 4 key blocks x G heads.
+  // Centroid rows centroid[x][p0, p0 + 1024) are staged through shared memory
+  // in chunks of xc rows by a kStages-deep cp.async pipeline.
   const float *cbase = centroid + gb * D * nb;
   const float *rb = radius + gb * nb;
   const float *ab = alpha + gb * nb;
-  for (int j0 = warp * 128; j0 < i; j0 += kThreads / 32 * 128) {
-    const int jq = j0 + lane * 4;
-    if (jq < i) {
-      float acc[G][4];
+  const int jend = (i + 3) & ~3;
+  for (int p0 = 0; p0 < i; p0 += kPassCols) {  // block-uniform
+    const int cols = min(kPassCols, jend - p0);  // multiple of 4
+    const int vpr = cols / 4;
+    int xc = kStageFloats / cols;
+    xc = xc > D ? D : xc;
+    while (xc & (xc - 1)) xc &= xc - 1;  // power of two, divides D
+    const int nch = D / xc;
+    auto issue = [&](int c) {
+      float *dst = stage + (c % kStages) * kStageFloats;
+      const int nv = xc * vpr;
+      for (int e = tid; e < nv; e += kThreads) {
+        const int xx = e / vpr, v = e - xx * vpr;
+        cp_async16(dst + xx * cols + v * 4, cbase + static_cast<size_t>(c * xc + xx) * nb + p0 + v * 4);
+      }
+      cp_async_commit();
+    };
+    for (int c = 0; c < kStages - 1; ++c) {
+      if (c < nch) issue(c);
+      else cp_async_commit();
+    }
+    float acc[G][4];
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
+    for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
-      const float *cp = cbase + jq;
-#pragma unroll 4
-      for (int x = 0; x < D; ++x) {
-        const float4 c4 = __ldg(reinterpret_cast<const float4 *>(cp + static_cast<size_t>(x) * nb));
-        float qv[G];
-        if constexpr (G % 4 == 0) {
+      for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
+    const int jl = warp * 128 + lane * 4;  // this thread's first column within the pass
+    const bool act = p0 + jl < i;
+    for (int c = 0; c < nch; ++c) {
+      if (c + kStages - 1 < nch) issue(c + kStages - 1);
+      else cp_async_commit();
+      cp_async_wait<kStages - 1>();
+      __syncthreads();
+      if (act) {
+        const float *buf = stage + (c % kStages) * kStageFloats + jl;
+        const float *qrow = qbt + c * xc * G;
+        for (int xx = 0; xx < xc; ++xx) {
+          const float4 c4 = *reinterpret_cast<const float4 *>(buf + xx * cols);
+          float qv[G];
+          if constexpr (G % 4 == 0) {
 #pragma unroll
-          for (int h4 = 0; h4 < G / 4; ++h4) {
-            const float4 t = reinterpret_cast<const float4 *>(qbt + x * G)[h4];
-            qv[4 * h4] = t.x;
-            qv[4 * h4 + 1] = t.y;
-            qv[4 * h4 + 2] = t.z;
-            qv[4 * h4 + 3] = t.w;
+            for (int h4 = 0; h4 < G / 4; ++h4) {
+              const float4 t = reinterpret_cast<const float4 *>(qrow + xx * G)[h4];
+              qv[4 * h4] = t.x;
+              qv[4 * h4 + 1] = t.y;
+              qv[4 * h4 + 2] = t.z;
+              qv[4 * h4 + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) qv[hh] = qrow[xx * G + hh];
           }
-        } else {
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) qv[hh] = qbt[x * G + hh];
-        }
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          acc[hh][0] = fmaf(qv[hh], c4.x, acc[hh][0]);
-          acc[hh][1] = fmaf(qv[hh], c4.y, acc[hh][1]);
-          acc[hh][2] = fmaf(qv[hh], c4.z, acc[hh][2]);
-          acc[hh][3] = fmaf(qv[hh], c4.w, acc[hh][3]);
+          for (int hh = 0; hh < G; ++hh) {
+            acc[hh][0] = fmaf(qv[hh], c4.x, acc[hh][0]);
+            acc[hh][1] = fmaf(qv[hh], c4.y, acc[hh][1]);
+            acc[hh][2] = fmaf(qv[hh], c4.z, acc[hh][2]);
+            acc[hh][3] = fmaf(qv[hh], c4.w, acc[hh][3]);
+          }
         }
       }
+      __syncthreads();
+    }
+    if (act) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int j = jq + c;
+        const int j = p0 + jl + c;
         if (j >= 1 && j < i) {
-          const float bonus = ab[j] * rb[j];
+          const float a = ab[j];
+          const float bonus = a * rb[j];
           float dm = acc[0][c];
-          float rm = fmaf(nbar[0], bonus, acc[0][c]);
+          float rm = fmaf(nbs[0], bonus, acc[0][c]);
 #pragma unroll
           for (int hh = 1; hh < G; ++hh) {
             dm = fmaxf(dm, acc[hh][c]);
-            rm = fmaxf(rm, fmaf(nbar[hh], bonus, acc[hh][c]));
+            rm = fmaxf(rm, fmaf(nbs[hh], bonus, acc[hh][c]));
           }
           sS[j] = dm * scale;
           sR[j] = rm * scale;
+          if (a > 0.f) flags[j] |= kElig;  // provisional: cleared below if the centroid path keeps j
         }
       }
     }
@@ -395,86 +511,83 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   const int ncand = i > 1 ? i - 1 : 0;
   const long long kc_full = (ppm_c * (i + 1) + 999999LL) / 1000000LL;
   const int kc = static_cast<int>(kc_full < ncand ? kc_full : ncand);
-  if (kc > 0) {
-    uint64_t thr = 0;
-    if (kc < ncand) thr = radix_kth_largest(sS, 1, i, [](int) { return true; }, kc, sm);
-    for (int j = 1 + tid; j < i; j += kThreads)
-      if (kc == ncand || rank_key(sS[j], j) >= thr) flags[j] |= BSA_MASK_CENTROID;
+  if (kc == ncand) {
+    for (int j = 1 + tid; j < i; j += kThreads) flags[j] |= BSA_MASK_CENTROID;
+    __syncthreads();
+  } else if (kc > 0) {
+    mark_top_k(sS, flags, kCand, flags, BSA_MASK_CENTROID, i, kc, sm);
   }
-  __syncthreads();
 
   // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
-  auto eligible = [&](int j) { return !(flags[j] & BSA_MASK_CENTROID) && ab[j] > 0.f; };
   int my = 0;
-  for (int j = 1 + tid; j < i; j += kThreads) my += eligible(j) ? 1 : 0;
+  for (int j = 1 + tid; j < i; j += kThreads) {
+    if (flags[j] & BSA_MASK_CENTROID) flags[j] &= static_cast<uint8_t>(~kElig);
+    my += (flags[j] & kElig) ? 1 : 0;
+  }
   int nelig = 0;
   (void)block_exclusive_scan(my, sm, &nelig);
   const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
   const int kr = static_cast<int>(kr_full < nelig ? kr_full : nelig);
-  if (kr > 0) {
-    uint64_t thr = 0;
-    if (kr < nelig) thr = radix_kth_largest(sR, 1, i, eligible, kr, sm);
-    __syncthreads();  // every thread has evaluated eligible() before flags change
+  if (kr == nelig && kr > 0) {
     for (int j = 1 + tid; j < i; j += kThreads)
-      if (eligible(j) && (kr == nelig || rank_key(sR[j], j) >= thr)) flags[j] |= 0x80;
+      if (flags[j] & kElig) flags[j] |= BSA_MASK_RESCUE;
     __syncthreads();
-    for (int j = 1 + tid; j < i; j += kThreads)
-      if (flags[j] & 0x80) flags[j] = static_cast<uint8_t>((flags[j] & 0x7F) | BSA_MASK_RESCUE);
+  } else if (kr > 0) {
+    mark_top_k(sR, flags, kElig, flags, BSA_MASK_RESCUE, i, kr, sm);
   }
-  __syncthreads();
 
   // ---- emit the ascending kept list of row i and the optional mask row
+  constexpr uint8_t kKeep = BSA_MASK_FORCED | BSA_MASK_CENTROID | BSA_MASK_RESCUE;
   const int n = i + 1;
   const int chunk = (n + kThreads - 1) / kThreads;
   const int lo = min(tid * chunk, n), hi = min(lo + chunk, n);
   int cnt = 0;
-  for (int j = lo; j < hi; ++j) cnt += flags[j] != 0;
+  for (int j = lo; j < hi; ++j) cnt += (flags[j] & kKeep) != 0;
   int total = 0;
   int off = block_exclusive_scan(cnt, sm, &total);
-  int32_t *row = kv_idx + (gb * nb + i) * static_cast<size_t>(nb);
+  int32_t *dst = kv_idx + row * static_cast<size_t>(nb);
   for (int j = lo; j < hi; ++j)
-    if (flags[j]) row[off++] = j;
-  if (tid == 0) kv_cnt[gb * nb + i] = total;
+    if (flags[j] & kKeep) dst[off++] = j;
+  if (tid == 0) kv_cnt[row] = total;
   if (mask != nullptr) {
-    uint8_t *mrow = mask + (gb * nb + i) * static_cast<size_t>(nb);
-    for (int j = tid; j < nb; j += kThreads) mrow[j] = j <= i ? flags[j] : 0;
+    uint8_t *mrow = mask + row * static_cast<size_t>(nb);
+    for (int j = tid; j < nb; j += kThreads) mrow[j] = j <= i ? (flags[j] & kKeep) : 0;
   }
 }
 
 template <int D, int G>
 size_t select_smem_bytes(int nb) {
-  constexpr int RPP = kThreads / (G * D / 8);
-  size_t floats = static_cast<size_t>(RPP) * G * D + ((RPP * G + 3) & ~3) + D * G + ((G + 3) & ~3) +
-                  2 * static_cast<size_t>(nb);
-  return floats * 4 + static_cast<size_t>(nb);
+  return (static_cast<size_t>(kStages) * kStageFloats + static_cast<size_t>(D) * G + ((G + 3) & ~3) +
+          2 * static_cast<size_t>(nb)) * 4 + static_cast<size_t>(nb);
 }
 
 template <int D, int G>
-cudaError_t launch_select_t(const MaskShape &s, const void *q, const float *centroid,
-                            const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                            float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                            cudaStream_t stream) {
+cudaError_t launch_select_t(const MaskShape &s, const float *qbar, const float *nbar,
+                            const float *centroid, const float *radius, const float *alpha,
+                            int64_t ppm_c, int64_t ppm_r, float scale, int32_t *kv_idx,
+                            int32_t *kv_cnt, uint8_t *mask, cudaStream_t stream) {
   const size_t smem = select_smem_bytes<D, G>(s.nb);
   cudaError_t e = cudaFuncSetAttribute(select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(s.nb, s.hkv, s.batch);
-  select_kernel<D, G><<<grid, kThreads, smem, stream>>>(
-      static_cast<const uint16_t *>(q), centroid, radius, alpha, kv_idx, kv_cnt, mask, s.seq, s.hq,
-      s.hkv, s.block, s.nb, static_cast<long long>(ppm_c), static_cast<long long>(ppm_r), scale);
+  select_kernel<D, G><<<grid, kThreads, smem, stream>>>(qbar, nbar, centroid, radius, alpha, kv_idx,
+                                                       kv_cnt, mask, s.hkv, s.nb,
+                                                       static_cast<long long>(ppm_c),
+                                                       static_cast<long long>(ppm_r), scale);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_select_d(const MaskShape &s, const void *q, const float *c, const float *r,
-                            const float *a, int64_t pc, int64_t pr, float scale, int32_t *idx,
-                            int32_t *cnt, uint8_t *mask, cudaStream_t st) {
+cudaError_t launch_select_d(const MaskShape &s, const float *qb, const float *nbr, const float *c,
+                            const float *r, const float *a, int64_t pc, int64_t pr, float scale,
+                            int32_t *idx, int32_t *cnt, uint8_t *mask, cudaStream_t st) {
   switch (s.group) {
-    case 1: return launch_select_t<D, 1>(s, q, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 2: return launch_select_t<D, 2>(s, q, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 4: return launch_select_t<D, 4>(s, q, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 8: return launch_select_t<D, 8>(s, q, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 16: return launch_select_t<D, 16>(s, q, c, r, a, pc, pr, scale, idx, cnt, mask, st);
+    case 1: return launch_select_t<D, 1>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
+    case 2: return launch_select_t<D, 2>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
+    case 4: return launch_select_t<D, 4>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
+    case 8: return launch_select_t<D, 8>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
+    case 16: return launch_select_t<D, 16>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -492,7 +605,31 @@ cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, fl
   return cudaGetLastError();
 }
 
+// Heads per query-pooling CTA: the largest divisor of hq with <= 256 threads.
+int qpool_heads(int hq, int d) {
+  int best = 1;
+  for (int h = 1; h <= hq; ++h)
+    if (hq % h == 0 && h * (d / 8) <= kThreads) best = h;
+  return best;
+}
+
+template <int D>
+cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *qbar, float *nbar,
+                           cudaStream_t stream) {
+  const int hpc = qpool_heads(s.hq, D);
+  dim3 grid(s.nb, s.hq / hpc, s.batch);
+  qpool_kernel<D><<<grid, hpc * (D / 8), 0, stream>>>(static_cast<const uint16_t *>(q), qbar, nbar,
+                                                      s.seq, s.hq, s.hkv, s.block, s.nb, hpc);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+size_t select_workspace_bytes(const MaskShape &s) {
+  const size_t qb = static_cast<size_t>(s.batch) * s.hq * s.nb * s.d * 4;
+  const size_t nbr = static_cast<size_t>(s.batch) * s.hq * s.nb * 4;
+  return (qb + 255) / 256 * 256 + (nbr + 255) / 256 * 256;
+}
 
 cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
                               cudaStream_t stream) {
@@ -503,21 +640,34 @@ cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid
 
 cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
                              cudaStream_t stream) {
+  int npow2 = 1;
+  while (npow2 < s.nb) npow2 <<= 1;
   dim3 grid(s.hkv, s.batch);
-  quant_kernel<<<grid, 1024, static_cast<size_t>(s.nb) * 4, stream>>>(radius, quant, alpha, s.nb);
+  const int threads = npow2 < 1024 ? (npow2 < 32 ? 32 : npow2) : 1024;
+  quant_kernel<<<grid, threads, static_cast<size_t>(npow2) * 4, stream>>>(radius, quant, alpha, s.nb, npow2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
                           float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                          cudaStream_t stream) {
-  if (s.d == 64)
-    return launch_select_d<64>(s, q, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx, kv_cnt,
-                               mask, stream);
-  if (s.d == 128)
-    return launch_select_d<128>(s, q, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx, kv_cnt,
-                                mask, stream);
+                          void *workspace, cudaStream_t stream) {
+  const size_t qb_bytes = (static_cast<size_t>(s.batch) * s.hq * s.nb * s.d * 4 + 255) / 256 * 256;
+  float *qbar = static_cast<float *>(workspace);
+  float *nbar = reinterpret_cast<float *>(static_cast<char *>(workspace) + qb_bytes);
+  cudaError_t e;
+  if (s.d == 64) {
+    e = launch_qpool_d<64>(s, q, qbar, nbar, stream);
+    if (e != cudaSuccess) return e;
+    return launch_select_d<64>(s, qbar, nbar, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx,
+                               kv_cnt, mask, stream);
+  }
+  if (s.d == 128) {
+    e = launch_qpool_d<128>(s, q, qbar, nbar, stream);
+    if (e != cudaSuccess) return e;
+    return launch_select_d<128>(s, qbar, nbar, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx,
+                                kv_cnt, mask, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -123,12 +123,16 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
  * unspecified.  kv_cnt[b][g][i] (int32, [batch, hkv, nb]).  mask (nullable,
  * uint8 [batch, hkv, nb, nb]) receives the BSA_MASK_* bits of every (i, j).
  * q: bf16 [batch, seq, hq, head_dim]; centroid, radius, alpha as written by
- * bsa_block_meta.  Needs no workspace.
+ * bsa_block_meta.  workspace: device scratch of at least
+ * bsa_select_workspace_bytes(shape) bytes, 16-byte aligned, owned by the
+ * caller (it holds the per-block mean queries and mean query norms; its
+ * contents need no initialisation and are dead after the call's kernels finish).
  */
+size_t bsa_select_workspace_bytes(const bsa_shape *shape);
 bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *params, const void *q,
                            const float *centroid, const float *radius, const float *alpha,
-                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, int32_t *dev_status,
-                           bsa_stream_t stream);
+                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream);
 
 /*
  * bsa_prefill_fwd - causal attention over the kept key blocks.
@@ -158,8 +162,9 @@ bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const vo
  * bsa_prefill_layer - one whole layer of the hot path in one call:
  * bsa_block_meta, bsa_select_mask, then bsa_prefill_fwd, all on `stream`.
  * The intermediate tensors live in `workspace` (device, 256-byte aligned, at
- * least bsa_prefill_layer_workspace_bytes(shape) bytes).  kv_idx/kv_cnt are
- * also left in the workspace; bsa_prefill_layer_views gives their offsets.
+ * least bsa_prefill_layer_workspace_bytes(shape) bytes): centroid, radius,
+ * quant, alpha, kv_idx, kv_cnt and the select scratch.  bsa_prefill_layer_views
+ * gives the offsets of the first six.
  */
 size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape);
 bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *params,

@@ -46,7 +46,7 @@ def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda"):
     prm = bsa.SelectParams(w.centroid_keep if centroid_keep is None else centroid_keep,
                            w.rescue_keep if rescue_keep is None else rescue_keep, 0)
     bsa.select_mask(s, prm, q, meta["centroid"], meta["radius"], meta["alpha"], sel["kv_idx"],
-                    sel["kv_cnt"], sel["mask"], status)
+                    sel["kv_cnt"], sel["mask"], dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     out = {kk: v.cpu().numpy() for kk, v in {**meta, **sel}.items()}

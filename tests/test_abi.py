@@ -73,10 +73,18 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.bsa_block_meta(ctypes.byref(s), ctypes.c_void_p(MIS), f, f, f, f, None, None) == 1
     prm = _lib.SelectParams(0.25, 0.05, 0)
     args = [f] * 6
-    assert lib.bsa_select_mask(ctypes.byref(s), None, *args, None, None, None) == 1
+    big = ctypes.c_size_t(1 << 40)
+    assert lib.bsa_select_mask(ctypes.byref(s), None, *args, None, f, big, None, None) == 1
     for bad in (_lib.SelectParams(1.5, 0.0, 0), _lib.SelectParams(0.1, -0.1, 0),
                 _lib.SelectParams(float("nan"), 0.0, 0), _lib.SelectParams(0.1, 0.1, 1)):
-        assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(bad), *args, None, None, None) == 1
+        assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(bad), *args, None, f, big,
+                                   None, None) == 1
+    need = lib.bsa_select_workspace_bytes(ctypes.byref(s))
+    assert need == 2 * 16 * 64 * 4 + 256        # qbar (8192 B) + nbar (128 B), each 256-aligned
+    assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(prm), *args, None, None, big,
+                               None, None) == 4
+    assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(prm), *args, None, f,
+                               ctypes.c_size_t(need - 1), None, None) == 4
     assert lib.bsa_prefill_fwd(ctypes.byref(s), f, f, f, None, f, ctypes.c_float(0.1), f, None,
                                None, None) == 1
     assert lib.bsa_prefill_fwd(ctypes.byref(s), f, f, f, f, f, ctypes.c_float(0.0), f, None,
