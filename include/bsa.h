@@ -135,6 +135,34 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
                            size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream);
 
 /*
+ * bsa_select_mask_noalloc - bsa_select_mask without a caller-provided workspace.
+ *
+ * The article has no counterpart to this call; it is a library convenience for
+ * callers that cannot allocate device memory, such as a host framework that
+ * owns the whole device pool and forbids allocations outside it, or a
+ * latency-critical caller that must not call cudaMalloc because it can
+ * synchronise the device.  The call computes exactly what bsa_select_mask
+ * computes (same kernels, same outputs), with its scratch in a fixed 12 MiB
+ * array inside the library's device image, so it allocates nothing.
+ *   - Every GPU that loads libbsa keeps those 12 MiB until the process exits.
+ *   - Shapes needing more than 12 MiB of select scratch
+ *     (bsa_select_workspace_bytes(shape) > 12 MiB: at 32 query heads,
+ *     head_dim 128 and block 128 that is beyond about 96K tokens, so the
+ *     131072-token layer, which needs 16.9 MB, is refused) return
+ *     BSA_ERR_WORKSPACE.
+ *   - All calls on one device share that array: calls whose kernels overlap on
+ *     the GPU (unordered streams) race and give wrong results.  Calls ordered
+ *     on one stream are safe.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ * Arguments and errors otherwise as bsa_select_mask.
+ */
+bsa_status bsa_select_mask_noalloc(const bsa_shape *shape, const bsa_select_params *params,
+                                   const void *q, const float *centroid, const float *radius,
+                                   const float *alpha, int32_t *kv_idx, int32_t *kv_cnt,
+                                   uint8_t *mask, int32_t *dev_status, bsa_stream_t stream);
+
+/*
  * bsa_prefill_fwd - causal attention over the kept key blocks.
  *
  * Rescue branch section: "the combined mask still runs as regular
