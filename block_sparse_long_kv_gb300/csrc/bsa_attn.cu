@@ -19,10 +19,15 @@
 //               in the ping-pong order S_0(n), PV_1(n-1), S_1(n), PV_0(n), so
 //               the tensor core works on one tile while the other tile's
 //               softmax runs
-//   warps 4..   NT softmax warpgroups, one thread per query row: read S_t
-//               from TMEM, causal mask on the diagonal tile only, online
-//               softmax in registers (exp2), P_t as bf16 back into TMEM over
-//               S_t, rare O_t rescale, then the epilogue (O / l, LSE)
+//   warps 4..   softmax warps: for 128-column key tiles two warps per 32-row
+//               TMEM sub-partition, each thread owning half of a query row's
+//               columns (the halves exchange partial maxima through shared
+//               memory); read S_t from TMEM, causal mask on the diagonal tile
+//               only, online softmax in registers (exp2), P_t as bf16 back into
+//               TMEM over S_t, rare O_t rescale, then the epilogue (O / l, LSE)
+// setmaxnreg moves registers from the producer / MMA warpgroup to the softmax
+// warps; the host refuses to launch if the compiled register count differs
+// from the budget the split assumes.
 // TMEM columns: S_t at t*KT, O_t at NT*KT + t*D (fp32 accumulators, one TMEM
 // lane per query row).  Every mbarrier wait is bounded: on timeout the kernel
 // records BSA_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs, frees
@@ -65,9 +70,16 @@ struct Cfg {
   static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;
   static constexpr uint32_t Q_CHUNK = 128u * 128;
   static constexpr uint32_t KV_CHUNK = static_cast<uint32_t>(KT) * 128;
+  // Softmax threads per query row: with 128-column key tiles two warps share each
+  // 32-row TMEM sub-partition, one per 64-column half, so a tile's softmax takes
+  // half as long; they exchange partial row maxima through shared memory.
+  static constexpr int CH = KT == 128 ? 2 : 1;
+  static constexpr int CW = KT / CH;                 // S columns per softmax thread
+  static constexpr uint32_t RED_BYTES = NT * CH * 128 * 2;  // bf16 partial maxima
   static constexpr int KS = 2;  // K stages: K(n+KS) only needs S(n) done
   // V stages: V(n+VS) needs PV_1(n) done, which comes late; use 3 when they fit
-  static constexpr int VS = (NT * Q_TILE + KS * KV_TILE + 3 * KV_TILE + 2048 <= 227u * 1024) ? 3 : 2;
+  static constexpr int VS =
+      (NT * Q_TILE + KS * KV_TILE + 3 * KV_TILE + RED_BYTES + 1024 + 512 <= 227u * 1024) ? 3 : 2;
   static constexpr int TM_O = NT * KT;
   static constexpr int TM_NEED = NT * (KT + D);
   static constexpr uint32_t TM_COLS =
@@ -80,8 +92,17 @@ struct Cfg {
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
                        B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
                        NBARS = B_FIN + 1;
-  static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;  // + 1 KB alignment slack
-  static constexpr int THREADS = 128 + 128 * NT;
+  static constexpr uint32_t OFF_RED = (OFF_BAR + NBARS * 8 + 16 + 15) / 16 * 16;
+  static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;  // + 1 KB alignment slack
+  static constexpr int THREADS = 128 + 128 * NT * CH;
+  // setmaxnreg split between the producer / MMA warpgroup and the softmax
+  // warpgroups; each sum equals the launch allocation (threads x registers):
+  //   640 threads x 96 = 128 x 56 + 512 x 104,  384 threads x 168 = 128 x 72 + 256 x 216
+  static constexpr int REG_LAUNCH = THREADS == 640 ? 96 : THREADS == 384 ? 168 : 0;
+  static constexpr int REG_LOW = THREADS == 640 ? 56 : 72;
+  static constexpr int REG_HIGH = THREADS == 640 ? 104 : 216;
+  static_assert(REG_LAUNCH == 0 || 128 * REG_LOW + (THREADS - 128) * REG_HIGH <= THREADS * REG_LAUNCH,
+                "register split exceeds the launch allocation");
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, KT, false);
   static constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(128, D, true);
   static_assert(TM_NEED <= 512, "TMEM budget");
@@ -173,7 +194,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int x = 0; x < C::NBARS; ++x) {
       uint32_t count = 1;
-      if (x >= C::B_PR && x < C::B_PR + NT) count = 4;  // one arrive per softmax warp
+      if (x >= C::B_PR && x < C::B_PR + NT) count = 4 * C::CH;  // one arrive per softmax warp
       ptx::mbar_init(bar(x), count);
     }
     *abort_flag = 0;
@@ -190,9 +211,8 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  // the producer / MMA warpgroup needs few registers; the softmax warpgroups take the rest:
-  // 72 * 128 + 216 * 256 = 64512 = 168 * 384, exactly the launch allocation
-  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+  // the producer / MMA warpgroup needs few registers; the softmax warpgroups take the rest
+  if constexpr (C::REG_LAUNCH != 0) ptx::setmaxnreg_dec<C::REG_LOW>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0 && T > 0) {
@@ -234,22 +254,29 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     if (lane == 0 && T > 0) {
+      // descriptors are linear in the start address (14-bit field, shared addresses
+      // < 256 KB): each MMA adds a constant to a base built once here
+      const uint64_t dq0 = ptx::sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = ptx::sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = ptx::sdesc_sw128(sV, C::KV_CHUNK, 1024);
       auto issue_s = [&](int t, int ks) {
+        const uint64_t dq = dq0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
+        const uint64_t dk = dk0 + static_cast<uint64_t>(ks) * (C::KV_TILE >> 4);
+        const uint32_t dst = tmem + t * C::KT;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(sQ + t * C::Q_TILE + (kk / 4) * C::Q_CHUNK + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(sK + ks * C::KV_TILE + (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, 16, 1024);
-          ptx::mma_ss(tmem + t * C::KT, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          const uint64_t qo = ((kk / 4) * C::Q_CHUNK + (kk % 4) * 32) >> 4;
+          const uint64_t ko = ((kk / 4) * C::KV_CHUNK + (kk % 4) * 32) >> 4;
+          ptx::mma_ss(dst, dq + qo, dk + ko, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(C::B_SF + t));
       };
       auto issue_pv = [&](int t, int vs, int n) {
+        const uint64_t dv = dv0 + static_cast<uint64_t>(vs) * (C::KV_TILE >> 4);
+        const uint32_t dst = tmem + C::TM_O + t * D, src = tmem + t * C::KT;
 #pragma unroll
-        for (int kk = 0; kk < C::KT / 16; ++kk) {
-          const uint64_t bd = ptx::sdesc_sw128(sV + vs * C::KV_TILE + kk * 2048, C::KV_CHUNK, 1024);
-          ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * C::KT + kk * 8, bd, C::IDESC_O,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::KT / 16; ++kk)
+          ptx::mma_ts(dst, src + kk * 8, dv + ((kk * 2048) >> 4), C::IDESC_O, (n > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(C::B_OD + t));
       };
       bool ok = wait_bar(bar(C::B_Q), 0, ctl);
@@ -258,22 +285,18 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         const int ks = n % C::KS;
         if (!(ok = wait_bar(bar(C::B_KF + ks), (n / C::KS) & 1, ctl))) break;
         ptx::tc_fence_after();
-        // S_0(n) once PV_0(n-1) has released the S_0 / P_0 columns
-        if (n > 0) {
-          if (!(ok = wait_bar(bar(C::B_OD + 0), (n - 1) & 1, ctl))) break;
-          ptx::tc_fence_after();
-        }
+        // S_0(n) overwrites the columns PV_0(n-1) reads P_0 from.  tcgen05.mma
+        // operations issued by one thread execute in issue order, so S_0(n) is
+        // queued right behind PV_0(n-1) without waiting for it to complete.
         issue_s(0, ks);
         if constexpr (NT == 2) {
           if (n > 0) {
-            // PV_1(n-1) overlaps softmax_0(n); then S_1(n) once PV_1(n-1) is done
+            // PV_1(n-1) overlaps softmax_0(n); S_1(n) follows it in issue order
             const int pv = n - 1, vs = pv % C::VS;
             if (!(ok = wait_bar(bar(C::B_PR + 1), pv & 1, ctl))) break;
             ptx::tc_fence_after();
             issue_pv(1, vs, pv);
             ptx::mma_commit(bar(C::B_VE + vs));
-            if (!(ok = wait_bar(bar(C::B_OD + 1), pv & 1, ctl))) break;
-            ptx::tc_fence_after();
           }
           issue_s(1, ks);
         }
@@ -305,34 +328,41 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   }
   } else {
     // ================================================================ softmax + epilogue
-    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
-    const int t = (warp - 4) >> 2;             // query tile of this warpgroup
-    const int r = ((warp & 3) << 5) + lane;     // query row = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
-    const uint32_t tS = tmem + lane_off + t * C::KT;
-    const uint32_t tO = tmem + lane_off + C::TM_O + t * D;
+    if constexpr (C::REG_LAUNCH != 0) ptx::setmaxnreg_inc<C::REG_HIGH>();
+    const int sw = warp - 4;
+    const int t = sw / (4 * C::CH);             // query tile of this warp
+    const int hf = (sw >> 2) % C::CH;           // column half of the key tile
+    const int sub = warp & 3;                   // TMEM sub-partition: rows 32*sub .. 32*sub+31
+    const int r = (sub << 5) + lane;            // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(sub << 5) << 16;
+    const uint32_t tS = tmem + lane_off + t * C::KT + hf * C::CW;         // this thread's S columns
+    const uint32_t tP = tmem + lane_off + t * C::KT + hf * (C::CW / 2);   // its P columns (bf16 pairs)
+    constexpr int OD_COLS = D / C::CH;                                    // O columns it rescales / writes
+    const uint32_t tO = tmem + lane_off + C::TM_O + t * D + hf * OD_COLS;
+    uint16_t *red = reinterpret_cast<uint16_t *>(sb + C::OFF_RED) + (t * C::CH) * 128;
+    const int pair_bar = 1 + t * 4 + sub;       // the two warps that share rows 32*sub ..
     const int tok = r / C::QH;
     const int head = g * p.group + (hp * NT + t) * C::QH + (r % C::QH);
     const int qtok = qtok0 + tok;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;               // l: this thread's share of the normaliser
     bool ok = true;
 
     for (int n = 0; n < T; ++n) {
       if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
       ptx::tc_fence_after();
       const int j = key_block(n);
-      const int ktok0 = j * BLK + (n % C::SUB) * C::KT;
-      uint32_t sr[C::KT];
+      const int ktok0 = j * BLK + (n % C::SUB) * C::KT + hf * C::CW;  // key of this thread's column 0
+      uint32_t sr[C::CW];
 #pragma unroll
-      for (int c = 0; c < C::KT / 32; ++c)
+      for (int c = 0; c < C::CW / 32; ++c)
         ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       ptx::tmem_wait_ld();
-      if (ktok0 + C::KT - 1 > qtok0) {
-        // tile overlaps the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok
+      if (ktok0 + C::CW - 1 > qtok0) {
+        // columns that overlap the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok
         const int lim = qtok - ktok0;
 #pragma unroll
-        for (int c = 0; c < C::KT; ++c)
+        for (int c = 0; c < C::CW; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
       // row max as a tree of eight independent chains
@@ -340,11 +370,25 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
 #pragma unroll
-      for (int c = 8; c < C::KT; c += 8)
+      for (int c = 8; c < C::CW; c += 8)
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if constexpr (C::CH == 2) {
+        // exchange partial maxima with the other half of the row, rounded up to bf16: any
+        // upper bound of the row max is a valid reference, and both halves then hold the
+        // same value.  The slot is rewritten only after the partner has arrived on P ready,
+        // which the next S tile waits for.
+        uint32_t u = __float_as_uint(mx);
+        if ((u & 0xFFFFu) != 0u && !(u >> 31)) u += 0x10000u;
+        const uint16_t mine = static_cast<uint16_t>(u >> 16);
+        red[hf * 128 + r] = mine;
+        ptx::named_barrier(pair_bar, 64);
+        const uint16_t other = red[(1 - hf) * 128 + r];
+        mx = fmaxf(__uint_as_float(static_cast<uint32_t>(mine) << 16),
+                   __uint_as_float(static_cast<uint32_t>(other) << 16));
+      }
       const float mt = mx * sl2;
       float factor = 1.f;
       bool resc = false;
@@ -356,7 +400,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       const float mb = (m == -INFINITY) ? 0.f : m;
       float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c16 = 0; c16 < C::KT / 32; ++c16) {
+      for (int c16 = 0; c16 < C::CW / 32; ++c16) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -365,12 +409,12 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
           rs4[e & 3] += p0 + p1;
           pk[e] = ptx::pack_bf16x2(p0, p1);
         }
-        ptx::tmem_st16(tS + c16 * 16, pk);
+        ptx::tmem_st16(tP + c16 * 16, pk);
       }
       l = l * factor + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < OD_COLS / 32; ++c) {
           uint32_t ov[32];
           ptx::tmem_ld32(tO + c * 32, ov);
           ptx::tmem_wait_ld();
@@ -387,10 +431,18 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
 
     if (ok && T > 0) ok = wait_bar(bar(C::B_OD + t), (T - 1) & 1, ctl);
     ptx::tc_fence_after();
+    if constexpr (C::CH == 2) {
+      // full normaliser = the two halves' shares, added in a fixed order; the Q tiles'
+      // shared memory is free once every MMA has completed
+      float *lsh = reinterpret_cast<float *>(sb + C::OFF_Q) + (t * C::CH) * 128;
+      lsh[hf * 128 + r] = l;
+      ptx::named_barrier(pair_bar, 64);
+      l = lsh[r] + lsh[128 + r];
+    }
     const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-    uint16_t *orow = p.o + ((static_cast<size_t>(b) * p.seq + qtok) * p.hq + head) * D;
+    uint16_t *orow = p.o + ((static_cast<size_t>(b) * p.seq + qtok) * p.hq + head) * D + hf * OD_COLS;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < OD_COLS / 32; ++c) {
       uint32_t ov[32];
       if (T > 0) {
         ptx::tmem_ld32(tO + c * 32, ov);
@@ -407,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
 #pragma unroll
       for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     }
-    if (p.lse != nullptr) {
+    if (p.lse != nullptr && hf == 0) {
       const float lse = (ok && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       p.lse[(static_cast<size_t>(b) * p.hq + head) * p.seq + qtok] = lse;
     }
@@ -479,6 +531,17 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
     return BSA_ERR_CUDA;
   }
   auto kern = attn_kernel<D, BLK, NT, DENSE>;
+  if constexpr (C::REG_LAUNCH != 0) {
+    // setmaxnreg.inc waits until the registers it asks for are free: the split is only
+    // safe if the kernel really launches with REG_LAUNCH registers per thread
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) {
+      *cerr = e;
+      return BSA_ERR_CUDA;
+    }
+    if (fa.numRegs != C::REG_LAUNCH) return BSA_ERR_UNSUPPORTED;
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) {
     *cerr = e;

@@ -194,6 +194,24 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- registers
+
+// Warpgroup-wide register budget changes (all four warps of the warpgroup execute
+// them).  The budgets of all warpgroups must fit the block's launch allocation.
+template <int R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R) : "memory");
+}
+template <int R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R) : "memory");
+}
+
+// Named barrier over `count` threads (whole warps).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2_approx(float x) {
