@@ -142,7 +142,7 @@ def layer_views(shape: Shape, workspace: torch.Tensor) -> dict:
         return workspace[offs[i]:offs[i] + cnt * 4].view(dtype).view(*shp)
 
     return {
-        "centroid": view(0, torch.float32, (b, hkv, d, nb)),
+        "centroid": view(0, torch.float32, (b, hkv, nb, d)),
         "radius": view(1, torch.float32, (b, hkv, nb)),
         "quant": view(2, torch.float32, (b, hkv, 2)),
         "alpha": view(3, torch.float32, (b, hkv, nb)),
@@ -154,7 +154,7 @@ def layer_views(shape: Shape, workspace: torch.Tensor) -> dict:
 def alloc_meta(shape: Shape, device="cuda") -> dict:
     b, n, hq, hkv, d, nb = _dims(shape)
     f32 = dict(dtype=torch.float32, device=device)
-    return {"centroid": torch.empty(b, hkv, d, nb, **f32), "radius": torch.empty(b, hkv, nb, **f32),
+    return {"centroid": torch.empty(b, hkv, nb, d, **f32), "radius": torch.empty(b, hkv, nb, **f32),
             "quant": torch.empty(b, hkv, 2, **f32), "alpha": torch.empty(b, hkv, nb, **f32)}
 
 

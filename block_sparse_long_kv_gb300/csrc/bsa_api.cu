@@ -106,7 +106,6 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
                            const float *centroid, const float *radius, const float *alpha,
                            int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
                            size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
-  (void)dev_status;  // the select kernels have no waits
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
   if (!params || !q || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
@@ -123,7 +122,7 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (bsa::launch_select(ms, q, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
                          ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, workspace,
-                         s) != cudaSuccess)
+                         dev_status, s) != cudaSuccess)
     return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -475,27 +475,6 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn(cudaError_t *err) {
-  static EncodeTiledFn fn = nullptr;
-  static cudaError_t status = cudaSuccess;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                              cudaEnableDefault, &q);
-    if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
-    fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  *err = status;
-  return fn;
-}
-
 // [batch, seq, heads, d] bf16 viewed as a 4-D tensor (d innermost), tile box
 // {64, box_heads, box_tokens, 1} with 128-byte swizzling.
 bool make_map(EncodeTiledFn fn, CUtensorMap *map, const void *ptr, int batch, int seq, int heads,
@@ -518,7 +497,7 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
                     const AttnParams &prm, cudaStream_t stream, cudaError_t *cerr) {
   using C = Cfg<D, BLK, NT>;
   cudaError_t e = cudaSuccess;
-  EncodeTiledFn fn = encode_fn(&e);
+  EncodeTiledFn fn = tensor_map_encoder(&e);
   if (fn == nullptr || e != cudaSuccess) {
     *cerr = e == cudaSuccess ? cudaErrorNotSupported : e;
     return BSA_ERR_CUDA;
@@ -577,6 +556,22 @@ bsa_status launch_blk(const AttnShape &s, const void *q, const void *k, const vo
 }
 
 }  // namespace
+
+EncodeTiledFn tensor_map_encoder(cudaError_t *err) {
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  *err = status;
+  return fn;
+}
 
 bsa_status launch_attention(const AttnShape &s, const void *q, const void *k, const void *v,
                             const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o,

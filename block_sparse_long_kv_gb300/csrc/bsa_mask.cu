@@ -8,16 +8,17 @@
 // selection paths, OR-combined.  The build reads every token a fixed number of
 // times, so it is linear in the sequence length.
 //
-// Four launches:
+// Five launches:
 //   meta_kernel     one CTA per (b, g, j): centroid and radius of key block j
 //                   (streams K once)
 //   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii,
 //                   nearest-rank median / p90, rescue coefficient alpha
 //   qpool_kernel    one CTA per (b, i, head chunk): mean query and mean query
 //                   norm of block i (streams Q once: the dominant HBM bytes)
-//   select_kernel   one CTA per (b, g, i): centroid / rescue scores for every
-//                   causal key block (FFMA on L2-resident summaries), per-path
-//                   top-k by radix select, OR, ascending kept-list emission
+//   score_kernel    (bsa_score.cu) centroid / rescue scores of every causal key
+//                   block on tensor cores
+//   select_kernel   one CTA per (b, g, i): per-path top-k by radix select, OR,
+//                   ascending kept-list emission
 // Every reduction runs in a fixed order, so results are deterministic.
 
 #include <cuda_bf16.h>
@@ -41,12 +42,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float f[8]) {
 
 __device__ __forceinline__ float bf16_at(const uint16_t *p, int idx) {
   return __uint_as_float(static_cast<uint32_t>(p[idx]) << 16);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
 }
 
 // ---------------------------------------------------------------- block meta
@@ -110,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) meta_kernel(const uint16_t *__restri
     for (int p = 0; p < P; ++p) s += part[p * D + tid];
     const float c = s / static_cast<float>(block);
     sc[tid] = c;
-    centroid[((static_cast<size_t>(b) * hkv + g) * D + tid) * nb + j] = c;
+    centroid[((static_cast<size_t>(b) * hkv + g) * nb + j) * D + tid] = c;
   }
   __syncthreads();
 
@@ -190,8 +185,8 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
 // ---------------------------------------------------------------- query pooling
 
 // One thread per (head, 8 dimensions); the token loop keeps 8 16-byte loads in
-// flight per thread.  Writes qbar[b][g][i][x][hh] (dimension-major within the
-// group, the layout the scoring loop reads) and nbar[b][g][i][hh].
+// flight per thread.  Writes qbar[b][g][i][hh][x] (one K-major row per (query
+// block, head), the A operand of the score GEMM) and nbar[b][g][i][hh].
 template <int D>
 __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restrict__ q,
                                                          float *__restrict__ qbar,
@@ -235,10 +230,10 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
   }
   const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
   const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
-  float *qb = qbar + (row * D + xv * 8) * grp + hh;
+  float4 *qb = reinterpret_cast<float4 *>(qbar + ((row * grp + hh) * D + xv * 8));
   const float inv_b = 1.f / static_cast<float>(block);  // exact: block is a power of two
-#pragma unroll
-  for (int e = 0; e < 8; ++e) qb[e * grp] = acc[e] * inv_b;
+  qb[0] = make_float4(acc[0] * inv_b, acc[1] * inv_b, acc[2] * inv_b, acc[3] * inv_b);
+  qb[1] = make_float4(acc[4] * inv_b, acc[5] * inv_b, acc[6] * inv_b, acc[7] * inv_b);
   if (xv == 0) nbar[row * grp + hh] = nsum * inv_b;
 }
 
@@ -366,144 +361,34 @@ __device__ void mark_top_k(const float *score, const uint8_t *flags_in, uint8_t 
 constexpr uint8_t kCand = 0x40;  // candidate of the centroid path (1 <= j < i)
 constexpr uint8_t kElig = 0x20;  // candidate of the rescue path
 
-constexpr int kPassCols = kThreads / 32 * 128;  // key blocks scored per pass (4 per thread)
-constexpr int kStageFloats = 4096;              // 16 KB per pipeline stage
-constexpr int kStages = 3;
-
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-template <int D, int G>
+// One CTA per (b, g, i), longest rows first: load the row's scores (computed on
+// tensor cores by the score kernel), rank each path, OR, emit the kept list.
 __global__ void __launch_bounds__(kThreads) select_kernel(
-    const float *__restrict__ qbar, const float *__restrict__ nbar,
-    const float *__restrict__ centroid, const float *__restrict__ radius,
-    const float *__restrict__ alpha, int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt,
-    uint8_t *__restrict__ mask, int hkv, int nb, long long ppm_c, long long ppm_r, float scale) {
+    const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
+    int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask, int hkv,
+    int nb, long long ppm_c, long long ppm_r) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float *stage = reinterpret_cast<float *>(smem);  // [kStages][kStageFloats] centroid chunks
-  float *qbt = stage + kStages * kStageFloats;     // [D][G] mean query, dimension-major
-  float *nbs = qbt + D * G;                         // [G]
-  float *sS = nbs + ((G + 3) & ~3);               // [nb] centroid-path score
-  float *sR = sS + nb;                            // [nb] rescue-path score
+  float *sS = reinterpret_cast<float *>(smem);           // [nb] centroid-path score
+  float *sR = sS + nb;                                   // [nb] rescue-path score
   uint8_t *flags = reinterpret_cast<uint8_t *>(sR + nb);  // [nb]
   __shared__ SelectSmem sm;
 
-  const int i = nb - 1 - static_cast<int>(blockIdx.x);  // longest rows first
+  const int i = nb - 1 - static_cast<int>(blockIdx.x);
   const int g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const size_t gb = static_cast<size_t>(b) * hkv + g;
   const size_t row = gb * nb + i;
-
-  {
-    const float4 *src = reinterpret_cast<const float4 *>(qbar + row * D * G);
-    for (int e = tid; e < D * G / 4; e += kThreads) reinterpret_cast<float4 *>(qbt)[e] = __ldg(src + e);
-    if (tid < G) nbs[tid] = __ldg(nbar + row * G + tid);
-  }
-  for (int j = tid; j < nb; j += kThreads) flags[j] = (j >= 1 && j < i) ? kCand : 0;
-  __syncthreads();
-
-  // ---- scores for candidates j in [1, i-1]; thread tile = 4 key blocks x G heads.
-  // Centroid rows centroid[x][p0, p0 + 1024) are staged through shared memory
-  // in chunks of xc rows by a kStages-deep cp.async pipeline.
-  const float *cbase = centroid + gb * D * nb;
-  const float *rb = radius + gb * nb;
   const float *ab = alpha + gb * nb;
-  const int jend = (i + 3) & ~3;
-  for (int p0 = 0; p0 < i; p0 += kPassCols) {  // block-uniform
-    const int cols = min(kPassCols, jend - p0);  // multiple of 4
-    const int vpr = cols / 4;
-    int xc = kStageFloats / cols;
-    xc = xc > D ? D : xc;
-    while (xc & (xc - 1)) xc &= xc - 1;  // power of two, divides D
-    const int nch = D / xc;
-    auto issue = [&](int c) {
-      float *dst = stage + (c % kStages) * kStageFloats;
-      const int nv = xc * vpr;
-      for (int e = tid; e < nv; e += kThreads) {
-        const int xx = e / vpr, v = e - xx * vpr;
-        cp_async16(dst + xx * cols + v * 4, cbase + static_cast<size_t>(c * xc + xx) * nb + p0 + v * 4);
-      }
-      cp_async_commit();
-    };
-    for (int c = 0; c < kStages - 1; ++c) {
-      if (c < nch) issue(c);
-      else cp_async_commit();
+  const float *rc = s_c + row * nb, *rr = s_r + row * nb;
+  for (int j = tid; j < nb; j += kThreads) {
+    uint8_t f = 0;
+    if (j >= 1 && j < i) {
+      sS[j] = rc[j];
+      sR[j] = rr[j];
+      f = kCand | (ab[j] > 0.f ? kElig : 0);  // eligibility is provisional: cleared if the centroid path keeps j
     }
-    float acc[G][4];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
-    const int jl = warp * 128 + lane * 4;  // this thread's first column within the pass
-    const bool act = p0 + jl < i;
-    for (int c = 0; c < nch; ++c) {
-      if (c + kStages - 1 < nch) issue(c + kStages - 1);
-      else cp_async_commit();
-      cp_async_wait<kStages - 1>();
-      __syncthreads();
-      if (act) {
-        const float *buf = stage + (c % kStages) * kStageFloats + jl;
-        const float *qrow = qbt + c * xc * G;
-        for (int xx = 0; xx < xc; ++xx) {
-          const float4 c4 = *reinterpret_cast<const float4 *>(buf + xx * cols);
-          float qv[G];
-          if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int h4 = 0; h4 < G / 4; ++h4) {
-              const float4 t = reinterpret_cast<const float4 *>(qrow + xx * G)[h4];
-              qv[4 * h4] = t.x;
-              qv[4 * h4 + 1] = t.y;
-              qv[4 * h4 + 2] = t.z;
-              qv[4 * h4 + 3] = t.w;
-            }
-          } else {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) qv[hh] = qrow[xx * G + hh];
-          }
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            acc[hh][0] = fmaf(qv[hh], c4.x, acc[hh][0]);
-            acc[hh][1] = fmaf(qv[hh], c4.y, acc[hh][1]);
-            acc[hh][2] = fmaf(qv[hh], c4.z, acc[hh][2]);
-            acc[hh][3] = fmaf(qv[hh], c4.w, acc[hh][3]);
-          }
-        }
-      }
-      __syncthreads();
-    }
-    if (act) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int j = p0 + jl + c;
-        if (j >= 1 && j < i) {
-          const float a = ab[j];
-          const float bonus = a * rb[j];
-          float dm = acc[0][c];
-          float rm = fmaf(nbs[0], bonus, acc[0][c]);
-#pragma unroll
-          for (int hh = 1; hh < G; ++hh) {
-            dm = fmaxf(dm, acc[hh][c]);
-            rm = fmaxf(rm, fmaf(nbs[hh], bonus, acc[hh][c]));
-          }
-          sS[j] = dm * scale;
-          sR[j] = rm * scale;
-          if (a > 0.f) flags[j] |= kElig;  // provisional: cleared below if the centroid path keeps j
-        }
-      }
-    }
-  }
-  if (tid == 0) {
-    flags[0] |= BSA_MASK_FORCED;
-    flags[i] |= BSA_MASK_FORCED;
+    if (j == 0 || j == i) f |= BSA_MASK_FORCED;
+    flags[j] = f;
   }
   __syncthreads();
 
@@ -555,43 +440,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   }
 }
 
-template <int D, int G>
-size_t select_smem_bytes(int nb) {
-  return (static_cast<size_t>(kStages) * kStageFloats + static_cast<size_t>(D) * G + ((G + 3) & ~3) +
-          2 * static_cast<size_t>(nb)) * 4 + static_cast<size_t>(nb);
-}
-
-template <int D, int G>
-cudaError_t launch_select_t(const MaskShape &s, const float *qbar, const float *nbar,
-                            const float *centroid, const float *radius, const float *alpha,
-                            int64_t ppm_c, int64_t ppm_r, float scale, int32_t *kv_idx,
-                            int32_t *kv_cnt, uint8_t *mask, cudaStream_t stream) {
-  const size_t smem = select_smem_bytes<D, G>(s.nb);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  dim3 grid(s.nb, s.hkv, s.batch);
-  select_kernel<D, G><<<grid, kThreads, smem, stream>>>(qbar, nbar, centroid, radius, alpha, kv_idx,
-                                                       kv_cnt, mask, s.hkv, s.nb,
-                                                       static_cast<long long>(ppm_c),
-                                                       static_cast<long long>(ppm_r), scale);
-  return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t launch_select_d(const MaskShape &s, const float *qb, const float *nbr, const float *c,
-                            const float *r, const float *a, int64_t pc, int64_t pr, float scale,
-                            int32_t *idx, int32_t *cnt, uint8_t *mask, cudaStream_t st) {
-  switch (s.group) {
-    case 1: return launch_select_t<D, 1>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 2: return launch_select_t<D, 2>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 4: return launch_select_t<D, 4>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 8: return launch_select_t<D, 8>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    case 16: return launch_select_t<D, 16>(s, qb, nbr, c, r, a, pc, pr, scale, idx, cnt, mask, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 template <int D>
 cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, float *radius,
                           cudaStream_t stream) {
@@ -604,6 +452,7 @@ cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, fl
                                                    s.seq, s.hkv, s.block, s.nb);
   return cudaGetLastError();
 }
+
 
 // Heads per query-pooling CTA: the largest divisor of hq with <= 256 threads.
 int qpool_heads(int hq, int d) {
@@ -623,12 +472,14 @@ cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *qbar, float
   return cudaGetLastError();
 }
 
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
 }  // namespace
 
 size_t select_workspace_bytes(const MaskShape &s) {
-  const size_t qb = static_cast<size_t>(s.batch) * s.hq * s.nb * s.d * 4;
-  const size_t nbr = static_cast<size_t>(s.batch) * s.hq * s.nb * 4;
-  return (qb + 255) / 256 * 256 + (nbr + 255) / 256 * 256;
+  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;  // (b, g, i, h) rows
+  const size_t scores = static_cast<size_t>(s.batch) * s.hkv * s.nb * s.nb;
+  return round256(rows * s.d * 4) + round256(rows * 4) + 2 * round256(scores * 4);
 }
 
 cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
@@ -651,24 +502,29 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
                           float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                          void *workspace, cudaStream_t stream) {
-  const size_t qb_bytes = (static_cast<size_t>(s.batch) * s.hq * s.nb * s.d * 4 + 255) / 256 * 256;
-  float *qbar = static_cast<float *>(workspace);
-  float *nbar = reinterpret_cast<float *>(static_cast<char *>(workspace) + qb_bytes);
+                          void *workspace, int32_t *status, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;
+  const size_t scores = static_cast<size_t>(s.batch) * s.hkv * s.nb * s.nb;
+  char *ws = static_cast<char *>(workspace);
+  float *qbar = reinterpret_cast<float *>(ws);
+  float *nbar = reinterpret_cast<float *>(ws + round256(rows * s.d * 4));
+  float *s_c = reinterpret_cast<float *>(ws + round256(rows * s.d * 4) + round256(rows * 4));
+  float *s_r = reinterpret_cast<float *>(reinterpret_cast<char *>(s_c) + round256(scores * 4));
   cudaError_t e;
-  if (s.d == 64) {
-    e = launch_qpool_d<64>(s, q, qbar, nbar, stream);
-    if (e != cudaSuccess) return e;
-    return launch_select_d<64>(s, qbar, nbar, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx,
-                               kv_cnt, mask, stream);
-  }
-  if (s.d == 128) {
-    e = launch_qpool_d<128>(s, q, qbar, nbar, stream);
-    if (e != cudaSuccess) return e;
-    return launch_select_d<128>(s, qbar, nbar, centroid, radius, alpha, ppm_c, ppm_r, scale, kv_idx,
-                                kv_cnt, mask, stream);
-  }
-  return cudaErrorInvalidValue;
+  if (s.d == 64) e = launch_qpool_d<64>(s, q, qbar, nbar, stream);
+  else if (s.d == 128) e = launch_qpool_d<128>(s, q, qbar, nbar, stream);
+  else return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  e = launch_scores(s, qbar, nbar, centroid, radius, alpha, scale, s_c, s_r, status, stream);
+  if (e != cudaSuccess) return e;
+  const size_t smem = static_cast<size_t>(s.nb) * 9;
+  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(s.nb, s.hkv, s.batch);
+  select_kernel<<<grid, kThreads, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.hkv, s.nb,
+                                                  static_cast<long long>(ppm_c),
+                                                  static_cast<long long>(ppm_r));
+  return cudaGetLastError();
 }
 
 }  // namespace bsa

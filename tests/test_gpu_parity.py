@@ -32,7 +32,7 @@ def all_rows(w):
 
 
 def check_meta(w, lay, got, orc):
-    cen = got["centroid"].transpose(0, 1, 3, 2)          # [b, hkv, nb, d]
+    cen = got["centroid"]                                 # [b, hkv, nb, d]
     scale = np.abs(orc["centroid"]).max()
     assert np.abs(cen - orc["centroid"]).max() <= 1e-5 * max(scale, 1.0)
     np.testing.assert_allclose(got["radius"], orc["radius"], rtol=1e-5)
