@@ -399,12 +399,12 @@ def run_ours(args):
                      "frac": kept_tflops / bf16_peak if bf16_peak else None,
                      "peak_source": f"{src} bf16 burst", "traffic": traffic,
                      "flops_per_launch": float(np.mean(flops))},
-        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + qpool_kernel + select_kernel",
+        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + qpool_kernel + score_kernel + select_kernel",
                                 "bound": "hbm", "achieved": mask_gbs, "peak": hbm_peak,
                                 "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
                                 "peak_source": f"{src} hbm copy",
                                 "bytes_per_launch": float(np.mean(mask_bytes))},
-        "gpu_launches": 5 * K,
+        "gpu_launches": 6 * K,       # meta, quant, qpool, score, select, attention
         "clocks": clk,
     }
 
@@ -445,7 +445,7 @@ def run_ours(args):
         result["e2e"] = {"value": e2e_ms / (n_e2e * world), "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host.numel() * 2,
                          "steps": n_e2e, "api": "bsa_prefill_layer (C ABI) + pinned host copies"}
-        result["gpu_launches_e2e_per_step"] = 5
+        result["gpu_launches_e2e_per_step"] = 6
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = oracle_sample(w, host_layers[0], args.cpu_budget)

@@ -37,10 +37,14 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder(cudaError_t *err);
 
+// Operands of the score GEMM: tf32 hi / lo splits of the centroids [b, hkv, nb, d] and of
+// the mean queries [b, hkv, nb, G, d], mean query norms [b, hkv, nb, G], radius, alpha.
+struct ScoreOperands {
+  const float *c_hi, *c_lo, *q_hi, *q_lo, *nbar, *radius, *alpha;
+};
 // Block scores S_c and R ([b, hkv, nb, nb] fp32, rows i, columns j < i) on tensor cores.
-cudaError_t launch_scores(const MaskShape &s, const float *qbar, const float *nbar,
-                          const float *centroid, const float *radius, const float *alpha,
-                          float scale, float *s_c, float *s_r, int32_t *status, cudaStream_t stream);
+cudaError_t launch_scores(const MaskShape &s, const ScoreOperands &op, float scale, float *s_c,
+                          float *s_r, int32_t *status, cudaStream_t stream);
 
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;

@@ -10,14 +10,16 @@
 //
 // Five launches:
 //   meta_kernel     one CTA per (b, g, j): centroid and radius of key block j
-//                   (streams K once)
+//                   (streams K once, the block held in registers)
 //   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii,
 //                   nearest-rank median / p90, rescue coefficient alpha
 //   qpool_kernel    one CTA per (b, i, head chunk): mean query and mean query
-//                   norm of block i (streams Q once: the dominant HBM bytes)
+//                   norm of block i (streams Q once: the dominant HBM bytes),
+//                   written as tf32 hi / lo splits; one more CTA row splits the
+//                   centroids the same way
 //   score_kernel    (bsa_score.cu) centroid / rescue scores of every causal key
 //                   block on tensor cores
-//   select_kernel   one CTA per (b, g, i): per-path top-k by radix select, OR,
+//   select_kernel   one warp per (b, g, i): per-path top-k by radix select, OR,
 //                   ascending kept-list emission
 // Every reduction runs in a fixed order, so results are deterministic.
 
@@ -46,94 +48,99 @@ __device__ __forceinline__ float bf16_at(const uint16_t *p, int idx) {
 
 // ---------------------------------------------------------------- block meta
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) meta_kernel(const uint16_t *__restrict__ k,
+// One CTA per (b, g, j), the key block held in registers: thread t owns the
+// 8 dimensions v = t % (D/8) of the tokens u, u + TL, u + 2 TL, ... with
+// u = t / (D/8) and TL = 256 / (D/8) token lanes.  Pass 1 sums the tokens into
+// the centroid (lane shuffles, then 8 warp partials in a fixed order); pass 2
+// takes each token's squared distance to it from the same registers, so K is
+// read from HBM once and never staged in shared memory.
+template <int D, int BLK>
+__global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_kernel(const uint16_t *__restrict__ k,
                                                         float *__restrict__ centroid,
                                                         float *__restrict__ radius, int seq,
-                                                        int hkv, int block, int nb) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int VPR = D / 8;       // 16-byte vectors per key row
-  constexpr int P = kThreads / D;  // partial sums per centroid coordinate
-  uint4 *sk = reinterpret_cast<uint4 *>(smem);
-  float *part = reinterpret_cast<float *>(smem + static_cast<size_t>(block) * D * 2);
-  __shared__ float sc[D];
-  __shared__ float wmax[kThreads / 32];
+                                                        int hkv, int nb) {
+  constexpr int VPR = D / 8;          // 16-byte vectors per key row
+  constexpr int TL = kThreads / VPR;  // token lanes
+  constexpr int TPT = BLK / TL;       // tokens per thread
+  constexpr int NW = kThreads / 32;
+  static_assert(TPT >= 1 && TPT * TL == BLK, "block must be a multiple of the token lanes");
+  __shared__ __align__(16) float part[NW][D];
+  __shared__ __align__(16) float sc[D];
+  __shared__ float wmax[NW];
 
   const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int v = tid % VPR, u = tid / VPR;
   const size_t tok_stride = static_cast<size_t>(hkv) * D;
-  const uint16_t *base =
-      k + (static_cast<size_t>(b) * seq + static_cast<size_t>(j) * block) * tok_stride +
-      static_cast<size_t>(g) * D;
+  const uint16_t *base = k + (static_cast<size_t>(b) * seq + static_cast<size_t>(j) * BLK + u) * tok_stride +
+                         static_cast<size_t>(g) * D + v * 8;
+  uint4 raw[TPT];
+#pragma unroll
+  for (int r = 0; r < TPT; ++r)
+    raw[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride));
 
-  // block * VPR vectors, a multiple of kThreads for every supported (block, D)
-  const int nvec = block * VPR;
-  for (int e0 = 0; e0 < nvec; e0 += 8 * kThreads) {
-    uint4 u[8];
+  // ---- pass 1: centroid
+  float s[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int e = e0 + r * kThreads + tid;
-      const int t = e / VPR, v = e - t * VPR;
-      if (e < nvec)
-        u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride) + v);
-    }
+  for (int e = 0; e < 8; ++e) s[e] = 0.f;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int e = e0 + r * kThreads + tid;
-      if (e < nvec) sk[e] = u[r];
-    }
+  for (int r = 0; r < TPT; ++r) {
+    float f[8];
+    unpack_bf16x8(raw[r], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] += f[e];
   }
-  __syncthreads();
-
-  const uint16_t *skh = reinterpret_cast<const uint16_t *>(sk);
-  {
-    // four interleaved partial sums per thread, combined in a fixed order
-    const int x = tid % D, p = tid / D;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    for (int t = p; t < block; t += 4 * P) {
-      s0 += bf16_at(skh, t * D + x);
-      s1 += bf16_at(skh, (t + P) * D + x);
-      s2 += bf16_at(skh, (t + 2 * P) * D + x);
-      s3 += bf16_at(skh, (t + 3 * P) * D + x);
-    }
-    part[p * D + x] = (s0 + s1) + (s2 + s3);
+#pragma unroll
+  for (int off = VPR; off < 32; off <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] += __shfl_xor_sync(0xffffffffu, s[e], off);
+  if (lane < VPR) {
+    float4 *pp = reinterpret_cast<float4 *>(&part[warp][v * 8]);
+    pp[0] = make_float4(s[0], s[1], s[2], s[3]);
+    pp[1] = make_float4(s[4], s[5], s[6], s[7]);
   }
   __syncthreads();
   if (tid < D) {
-    float s = 0.f;
+    float c = 0.f;
 #pragma unroll
-    for (int p = 0; p < P; ++p) s += part[p * D + tid];
-    const float c = s / static_cast<float>(block);
+    for (int w = 0; w < NW; ++w) c += part[w][tid];
+    c *= 1.f / static_cast<float>(BLK);  // exact: BLK is a power of two
     sc[tid] = c;
     centroid[((static_cast<size_t>(b) * hkv + g) * nb + j) * D + tid] = c;
   }
   __syncthreads();
 
-  const int warp = tid >> 5, lane = tid & 31;
+  // ---- pass 2: max squared distance to the centroid
+  float c[8];
+  {
+    const float4 c0 = reinterpret_cast<const float4 *>(sc)[2 * v];
+    const float4 c1 = reinterpret_cast<const float4 *>(sc)[2 * v + 1];
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+    c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+  }
   float best = 0.f;
-  for (int t = warp * 4; t < block; t += kThreads / 32 * 4) {  // four rows per warp at a time
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int x = lane; x < D; x += 32) {
-      const float cx = sc[x];
+  for (int r = 0; r < TPT; ++r) {
+    float f[8];
+    unpack_bf16x8(raw[r], f);
+    float acc = 0.f;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float dl = bf16_at(skh, (t + r) * D + x) - cx;
-        acc[r] = fmaf(dl, dl, acc[r]);
-      }
+    for (int e = 0; e < 8; ++e) {
+      const float dl = f[e] - c[e];
+      acc = fmaf(dl, dl, acc);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
-    best = fmaxf(best, fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])));
+    for (int off = 1; off < VPR; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    best = fmaxf(best, acc);
   }
+#pragma unroll
+  for (int off = VPR; off < 32; off <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
   if (lane == 0) wmax[warp] = best;
   __syncthreads();
   if (tid == 0) {
     float m = wmax[0];
 #pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, wmax[w]);
+    for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
     radius[(static_cast<size_t>(b) * hkv + g) * nb + j] = sqrtf(m);
   }
 }
@@ -184,18 +191,39 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
 
 // ---------------------------------------------------------------- query pooling
 
+// tf32 split of an fp32 value: hi keeps the top 10 mantissa bits (exact in
+// tf32), lo = x - hi is exact in fp32.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
 // One thread per (head, 8 dimensions); the token loop keeps 8 16-byte loads in
-// flight per thread.  Writes qbar[b][g][i][hh][x] (one K-major row per (query
-// block, head), the A operand of the score GEMM) and nbar[b][g][i][hh].
+// flight per thread.  Writes the mean query as tf32 hi / lo splits,
+// q_hi/q_lo[b][g][i][hh][x] (one K-major row per (query block, head): the B
+// operand of the score GEMM), and nbar[b][g][i][hh].  The extra row of CTAs
+// (blockIdx.y == nhc) splits the centroids of key block blockIdx.x of every KV
+// head into c_hi / c_lo, the GEMM's A operand.
 template <int D>
 __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restrict__ q,
-                                                         float *__restrict__ qbar,
-                                                         float *__restrict__ nbar, int seq,
+                                                         float *__restrict__ q_hi,
+                                                         float *__restrict__ q_lo,
+                                                         float *__restrict__ nbar,
+                                                         const float *__restrict__ centroid,
+                                                         float *__restrict__ c_hi,
+                                                         float *__restrict__ c_lo, int seq,
                                                          int hq, int hkv, int block, int nb,
-                                                         int hpc) {
+                                                         int hpc, int nhc) {
   constexpr int VH = D / 8;  // lanes per head
   const int i = blockIdx.x, hc = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
+  if (hc == nhc) {
+    for (int e = tid; e < hkv * D; e += blockDim.x) {
+      const int g = e / D, x = e - g * D;
+      const size_t o = ((static_cast<size_t>(b) * hkv + g) * nb + i) * D + x;
+      const float v = centroid[o], h = tf32_hi(v);
+      c_hi[o] = h;
+      c_lo[o] = v - h;
+    }
+    return;
+  }
   const int hl = tid / VH, xv = tid - hl * VH;
   const int h = hc * hpc + hl;
   const size_t tok_stride = static_cast<size_t>(hq) * D;
@@ -230,229 +258,261 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
   }
   const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
   const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
-  float4 *qb = reinterpret_cast<float4 *>(qbar + ((row * grp + hh) * D + xv * 8));
+  const size_t qo = (row * grp + hh) * D + xv * 8;
   const float inv_b = 1.f / static_cast<float>(block);  // exact: block is a power of two
-  qb[0] = make_float4(acc[0] * inv_b, acc[1] * inv_b, acc[2] * inv_b, acc[3] * inv_b);
-  qb[1] = make_float4(acc[4] * inv_b, acc[5] * inv_b, acc[6] * inv_b, acc[7] * inv_b);
+  float m[8], hi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    m[e] = acc[e] * inv_b;
+    hi[e] = tf32_hi(m[e]);
+  }
+  float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
+  float4 *ql = reinterpret_cast<float4 *>(q_lo + qo);
+  qh[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
+  qh[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+  ql[0] = make_float4(m[0] - hi[0], m[1] - hi[1], m[2] - hi[2], m[3] - hi[3]);
+  ql[1] = make_float4(m[4] - hi[4], m[5] - hi[5], m[6] - hi[6], m[7] - hi[7]);
   if (xv == 0) nbar[row * grp + hh] = nsum * inv_b;
 }
 
 // ---------------------------------------------------------------- select
 
 // Order-preserving key of a float score: a higher score gives a larger key.
+// Every non-NaN score maps to a key >= 1, so key 0 marks "not a candidate".
 __device__ __forceinline__ uint32_t score_key(float s) {
   const uint32_t u = __float_as_uint(s);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-struct SelectSmem {
-  unsigned hist[256];
-  unsigned bc_digit, bc_above, bc_count;
-  int wsum[kThreads / 32];
-  int total;
+constexpr int kSelWarps = 8;  // rows per select CTA, one warp each
+
+__host__ __device__ constexpr size_t select_warp_bytes(int nb) {
+  return static_cast<size_t>(nb) * 4 + 1024 + ((static_cast<size_t>(nb) + 15) & ~static_cast<size_t>(15));
+}
+
+// Radix threshold of the k largest nonzero keys of keys[0, n) (1 <= k < number
+// of nonzero keys), one warp, 8-bit digits from the top.  On return the
+// selection is: every key with (key & pmask) > prefix, plus the first `take`
+// in index order of the `n_eq` nonzero keys with (key & pmask) == prefix.
+struct Threshold {
+  uint32_t prefix, pmask;
+  unsigned take, n_eq;
 };
 
-// Exclusive prefix sum over the block; every thread passes its count.
-__device__ int block_exclusive_scan(int v, SelectSmem &sm, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  if (lane == 31) sm.wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < kThreads / 32 ? sm.wsum[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, wi, off);
-      if (lane >= off) wi += o;
-    }
-    if (lane < kThreads / 32) sm.wsum[lane] = wi - w;
-    if (lane == kThreads / 32 - 1) sm.total = wi;
-  }
-  __syncthreads();
-  const int res = sm.wsum[warp] + incl - v;
-  *total = sm.total;
-  __syncthreads();
-  return res;
-}
-
-// Marks (flags |= bit) the k best eligible entries of score[1, i): higher score
-// first, ties to the lower index.  Requires 1 <= k < number eligible.  Radix
-// select over the 32-bit score key, 8-bit digits from the top; the rare case of
-// several entries sharing the threshold key is settled by index order.
-__device__ void mark_top_k(const float *score, const uint8_t *flags_in, uint8_t elig_bit,
-                           uint8_t *flags, uint8_t bit, int i, int k, SelectSmem &sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, pmask = 0;
-  unsigned krem = static_cast<unsigned>(k), n_eq = 0;
+__device__ Threshold warp_radix_threshold(const uint32_t *keys, int n, unsigned k, unsigned *hist) {
+  const int lane = threadIdx.x & 31;
+  Threshold t{0u, 0u, k, 0u};
   for (int shift = 24; shift >= 0; shift -= 8) {
-    sm.hist[tid] = 0;  // kThreads == 256 bins
-    __syncthreads();
-    for (int base = 1; base < i; base += kThreads) {
-      const int j = base + tid;
-      bool ok = j < i && (flags_in[j] & elig_bit);
-      const uint32_t key = ok ? score_key(score[j]) : 0u;
-      ok = ok && ((key & pmask) == prefix);
+    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    for (int j0 = 0; j0 < n; j0 += 32) {  // warp-uniform trip count: every lane reaches the match
+      const int j = j0 + lane;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      const bool ok = key != 0u && (key & t.pmask) == t.prefix;
       const unsigned digit = (key >> shift) & 255u;
       const unsigned peers = __match_any_sync(0xffffffffu, ok ? digit : 256u);
-      if (ok && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
+      if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
     }
-    __syncthreads();
-    if (warp == 0) {
-      unsigned c[8];
-      unsigned s = 0;
+    __syncwarp();
+    // lane l owns bins 8l .. 8l+7; find the bin holding the take-th largest key
+    unsigned c[8], s = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        c[e] = sm.hist[8 * lane + e];
-        s += c[e];
-      }
-      unsigned suf = s;  // elements in the bins of lanes >= this lane
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
-        if (lane + off < 32) suf += o;
-      }
-      unsigned acc = suf - s;  // elements in bins above this lane's bins
-#pragma unroll
-      for (int e = 7; e >= 0; --e) {
-        if (acc < krem && krem <= acc + c[e]) {
-          sm.bc_digit = 8 * lane + e;
-          sm.bc_above = acc;
-          sm.bc_count = c[e];
-        }
-        acc += c[e];
-      }
+    for (int e = 0; e < 8; ++e) {
+      c[e] = hist[8 * lane + e];
+      s += c[e];
     }
-    __syncthreads();
-    krem -= sm.bc_above;
-    n_eq = sm.bc_count;
-    prefix |= sm.bc_digit << shift;
-    pmask |= 0xFFu << shift;
-    __syncthreads();
-  }
-  // keys above the threshold are in; krem of the n_eq keys equal to it are in
-  if (n_eq == krem) {
-    for (int j = 1 + tid; j < i; j += kThreads)
-      if ((flags_in[j] & elig_bit) && score_key(score[j]) >= prefix) flags[j] |= bit;
-  } else {
-    for (int j = 1 + tid; j < i; j += kThreads)
-      if ((flags_in[j] & elig_bit) && score_key(score[j]) > prefix) flags[j] |= bit;
-    const int n = i - 1;
-    const int chunk = (n + kThreads - 1) / kThreads;
-    const int lo = 1 + min(tid * chunk, n), hi = min(lo + chunk, i);
-    int cnt = 0;
-    for (int j = lo; j < hi; ++j) cnt += (flags_in[j] & elig_bit) && score_key(score[j]) == prefix;
-    int total = 0;
-    int rank = block_exclusive_scan(cnt, sm, &total);
-    for (int j = lo; j < hi; ++j)
-      if ((flags_in[j] & elig_bit) && score_key(score[j]) == prefix) {
-        if (rank < static_cast<int>(krem)) flags[j] |= bit;
-        ++rank;
+    unsigned suf = s;  // keys in the bins of lanes >= this lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
+      if (lane + off < 32) suf += o;
+    }
+    unsigned acc = suf - s, my_digit = 0, my_above = 0, my_count = 0;
+    bool hit = false;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+      if (!hit && acc < t.take && t.take <= acc + c[e]) {
+        hit = true;
+        my_digit = 8 * lane + e;
+        my_above = acc;
+        my_count = c[e];
       }
+      acc += c[e];
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+    const unsigned digit = __shfl_sync(0xffffffffu, my_digit, src);
+    t.take -= __shfl_sync(0xffffffffu, my_above, src);
+    t.n_eq = __shfl_sync(0xffffffffu, my_count, src);
+    t.prefix |= digit << shift;
+    t.pmask |= 0xFFu << shift;
+    __syncwarp();  // hist is rewritten by the next pass
+    if (t.n_eq == t.take) break;  // the whole bin is in: no finer digit needed
   }
-  __syncthreads();
+  return t;
 }
 
-constexpr uint8_t kCand = 0x40;  // candidate of the centroid path (1 <= j < i)
-constexpr uint8_t kElig = 0x20;  // candidate of the rescue path
+// flags[j] |= bit for the keys Threshold t selects among keys[0, n).
+__device__ void warp_mark(const uint32_t *keys, int n, const Threshold &t, uint8_t *flags, uint8_t bit) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const bool all_eq = t.n_eq == t.take;
+  unsigned taken = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t key = j < n ? keys[j] : 0u;
+    const uint32_t top = key & t.pmask;
+    const bool eq = key != 0u && top == t.prefix;
+    bool in = top > t.prefix;
+    if (all_eq) {
+      in = in || eq;
+    } else {
+      const unsigned b = __ballot_sync(0xffffffffu, eq);
+      in = in || (eq && taken + __popc(b & lt) < t.take);
+      taken += __popc(b);
+    }
+    if (in) flags[j] |= bit;
+  }
+}
 
-// One CTA per (b, g, i), longest rows first: load the row's scores (computed on
-// tensor cores by the score kernel), rank each path, OR, emit the kept list.
-__global__ void __launch_bounds__(kThreads) select_kernel(
+// One warp per (b, g, i) row, longest rows first; kSelWarps rows per CTA.
+// Loads the row's centroid-path keys (scores from the tensor-core score
+// kernel), selects the top kc, then the rescue-path keys of the candidates the
+// centroid path dropped and whose alpha is positive, selects the top kr, ORs in
+// the forced sink and diagonal blocks and writes the ascending kept list.
+__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
     const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
     int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask, int hkv,
     int nb, long long ppm_c, long long ppm_r) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float *sS = reinterpret_cast<float *>(smem);           // [nb] centroid-path score
-  float *sR = sS + nb;                                   // [nb] rescue-path score
-  uint8_t *flags = reinterpret_cast<uint8_t *>(sR + nb);  // [nb]
-  __shared__ SelectSmem sm;
-
-  const int i = nb - 1 - static_cast<int>(blockIdx.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = nb - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
+  if (i < 0) return;
   const int g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  // per warp: keys [nb] u32, hist [256] u32, flags [nb] u8 (nb % 4 == 0 keeps each 16-aligned)
+  unsigned char *wbase = smem + static_cast<size_t>(warp) * select_warp_bytes(nb);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(wbase);
+  unsigned *hist = reinterpret_cast<unsigned *>(wbase + static_cast<size_t>(nb) * 4);
+  uint8_t *flags = wbase + static_cast<size_t>(nb) * 4 + 1024;
+
   const size_t gb = static_cast<size_t>(b) * hkv + g;
   const size_t row = gb * nb + i;
   const float *ab = alpha + gb * nb;
-  const float *rc = s_c + row * nb, *rr = s_r + row * nb;
-  for (int j = tid; j < nb; j += kThreads) {
-    uint8_t f = 0;
-    if (j >= 1 && j < i) {
-      sS[j] = rc[j];
-      sR[j] = rr[j];
-      f = kCand | (ab[j] > 0.f ? kElig : 0);  // eligibility is provisional: cleared if the centroid path keeps j
-    }
-    if (j == 0 || j == i) f |= BSA_MASK_FORCED;
-    flags[j] = f;
-  }
-  __syncthreads();
+  const int n4 = (i + 4) & ~3;  // keys / flags [0, n4) cover 0..i; entries j >= i are never candidates
 
   // ---- centroid path: top kc of candidates 1..i-1 by S_c
+  {
+    const float4 *rc = reinterpret_cast<const float4 *>(s_c + row * nb);
+    for (int j4 = lane * 4; j4 < n4; j4 += 128) {
+      const float4 v = rc[j4 >> 2];
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      uint4 kk;
+      uint32_t *kp = reinterpret_cast<uint32_t *>(&kk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j4 + e;
+        kp[e] = (j >= 1 && j < i) ? score_key(x[e]) : 0u;
+      }
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = kk;
+      reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
+    }
+  }
+  __syncwarp();
   const int ncand = i > 1 ? i - 1 : 0;
   const long long kc_full = (ppm_c * (i + 1) + 999999LL) / 1000000LL;
   const int kc = static_cast<int>(kc_full < ncand ? kc_full : ncand);
   if (kc == ncand) {
-    for (int j = 1 + tid; j < i; j += kThreads) flags[j] |= BSA_MASK_CENTROID;
-    __syncthreads();
+    for (int j = 1 + lane; j < i; j += 32) flags[j] = BSA_MASK_CENTROID;
   } else if (kc > 0) {
-    mark_top_k(sS, flags, kCand, flags, BSA_MASK_CENTROID, i, kc, sm);
+    const Threshold t = warp_radix_threshold(keys, i, static_cast<unsigned>(kc), hist);
+    warp_mark(keys, i, t, flags, BSA_MASK_CENTROID);
   }
+  __syncwarp();
 
   // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
-  int my = 0;
-  for (int j = 1 + tid; j < i; j += kThreads) {
-    if (flags[j] & BSA_MASK_CENTROID) flags[j] &= static_cast<uint8_t>(~kElig);
-    my += (flags[j] & kElig) ? 1 : 0;
-  }
   int nelig = 0;
-  (void)block_exclusive_scan(my, sm, &nelig);
+  {
+    const float4 *rr = reinterpret_cast<const float4 *>(s_r + row * nb);
+    for (int j4 = lane * 4; j4 < n4; j4 += 128) {
+      const float4 v = rr[j4 >> 2];
+      const float4 a = *reinterpret_cast<const float4 *>(ab + j4);
+      const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
+      const float x[4] = {v.x, v.y, v.z, v.w}, al[4] = {a.x, a.y, a.z, a.w};
+      uint4 kk;
+      uint32_t *kp = reinterpret_cast<uint32_t *>(&kk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j4 + e;
+        const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
+        kp[e] = elig ? score_key(x[e]) : 0u;
+        nelig += elig ? 1 : 0;
+      }
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = kk;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) nelig += __shfl_xor_sync(0xffffffffu, nelig, off);
+  __syncwarp();
   const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
   const int kr = static_cast<int>(kr_full < nelig ? kr_full : nelig);
-  if (kr == nelig && kr > 0) {
-    for (int j = 1 + tid; j < i; j += kThreads)
-      if (flags[j] & kElig) flags[j] |= BSA_MASK_RESCUE;
-    __syncthreads();
+  if (kr > 0 && kr == nelig) {
+    for (int j = lane; j < i; j += 32)
+      if (keys[j] != 0u) flags[j] |= BSA_MASK_RESCUE;
   } else if (kr > 0) {
-    mark_top_k(sR, flags, kElig, flags, BSA_MASK_RESCUE, i, kr, sm);
+    const Threshold t = warp_radix_threshold(keys, i, static_cast<unsigned>(kr), hist);
+    warp_mark(keys, i, t, flags, BSA_MASK_RESCUE);
   }
+  __syncwarp();
+  if (lane == 0) {
+    flags[0] |= BSA_MASK_FORCED;
+    flags[i] |= BSA_MASK_FORCED;
+  }
+  __syncwarp();
 
   // ---- emit the ascending kept list of row i and the optional mask row
-  constexpr uint8_t kKeep = BSA_MASK_FORCED | BSA_MASK_CENTROID | BSA_MASK_RESCUE;
-  const int n = i + 1;
-  const int chunk = (n + kThreads - 1) / kThreads;
-  const int lo = min(tid * chunk, n), hi = min(lo + chunk, n);
-  int cnt = 0;
-  for (int j = lo; j < hi; ++j) cnt += (flags[j] & kKeep) != 0;
-  int total = 0;
-  int off = block_exclusive_scan(cnt, sm, &total);
   int32_t *dst = kv_idx + row * static_cast<size_t>(nb);
-  for (int j = lo; j < hi; ++j)
-    if (flags[j] & kKeep) dst[off++] = j;
-  if (tid == 0) kv_cnt[row] = total;
-  if (mask != nullptr) {
-    uint8_t *mrow = mask + row * static_cast<size_t>(nb);
-    for (int j = tid; j < nb; j += kThreads) mrow[j] = j <= i ? (flags[j] & kKeep) : 0;
+  const unsigned lt = (1u << lane) - 1u;
+  int total = 0;
+  for (int j0 = 0; j0 <= i; j0 += 32) {
+    const int j = j0 + lane;
+    const bool keep = j <= i && flags[j] != 0;
+    const unsigned bl = __ballot_sync(0xffffffffu, keep);
+    if (keep) dst[total + __popc(bl & lt)] = j;
+    total += __popc(bl);
   }
+  if (lane == 0) kv_cnt[row] = total;
+  if (mask != nullptr) {
+    uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nb));
+    for (int j4 = lane * 4; j4 < nb; j4 += 128) {
+      uint32_t m = 0;
+      if (j4 <= i) {
+        m = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
+        if (j4 + 3 > i) m &= 0xFFFFFFFFu >> (8 * (j4 + 3 - i));  // zero the bytes past i
+      }
+      mrow[j4 >> 2] = m;
+    }
+  }
+}
+
+template <int D, int BLK>
+cudaError_t launch_meta_t(const MaskShape &s, const void *k, float *centroid, float *radius,
+                          cudaStream_t stream) {
+  dim3 grid(s.nb, s.hkv, s.batch);
+  meta_kernel<D, BLK><<<grid, kThreads, 0, stream>>>(static_cast<const uint16_t *>(k), centroid, radius,
+                                                     s.seq, s.hkv, s.nb);
+  return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, float *radius,
                           cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(s.block) * D * 2 + static_cast<size_t>(kThreads / D) * D * 4;
-  cudaError_t e = cudaFuncSetAttribute(meta_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  dim3 grid(s.nb, s.hkv, s.batch);
-  meta_kernel<D><<<grid, kThreads, smem, stream>>>(static_cast<const uint16_t *>(k), centroid, radius,
-                                                   s.seq, s.hkv, s.block, s.nb);
-  return cudaGetLastError();
+  switch (s.block) {
+    case 64: return launch_meta_t<D, 64>(s, k, centroid, radius, stream);
+    case 128: return launch_meta_t<D, 128>(s, k, centroid, radius, stream);
+    case 256: return launch_meta_t<D, 256>(s, k, centroid, radius, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
-
 
 // Heads per query-pooling CTA: the largest divisor of hq with <= 256 threads.
 int qpool_heads(int hq, int d) {
@@ -463,24 +523,45 @@ int qpool_heads(int hq, int d) {
 }
 
 template <int D>
-cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *qbar, float *nbar,
-                           cudaStream_t stream) {
+cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *q_hi, float *q_lo, float *nbar,
+                           const float *centroid, float *c_hi, float *c_lo, cudaStream_t stream) {
   const int hpc = qpool_heads(s.hq, D);
-  dim3 grid(s.nb, s.hq / hpc, s.batch);
-  qpool_kernel<D><<<grid, hpc * (D / 8), 0, stream>>>(static_cast<const uint16_t *>(q), qbar, nbar,
-                                                      s.seq, s.hq, s.hkv, s.block, s.nb, hpc);
+  const int nhc = s.hq / hpc;
+  dim3 grid(s.nb, nhc + 1, s.batch);
+  qpool_kernel<D><<<grid, hpc * (D / 8), 0, stream>>>(static_cast<const uint16_t *>(q), q_hi, q_lo,
+                                                      nbar, centroid, c_hi, c_lo, s.seq, s.hq, s.hkv,
+                                                      s.block, s.nb, hpc, nhc);
   return cudaGetLastError();
 }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+
+// Select workspace regions, each 256-byte aligned: q_hi, q_lo [b, hkv, nb, G, d],
+// nbar [b, hkv, nb, G], c_hi, c_lo [b, hkv, nb, d], S_c, R [b, hkv, nb, nb], all fp32.
+struct SelectRegions {
+  size_t off[7];
+  size_t total;
+};
+
+SelectRegions select_regions(const MaskShape &s) {
+  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;  // (b, g, i, h) rows
+  const size_t blocks = static_cast<size_t>(s.batch) * s.hkv * s.nb;
+  const size_t sizes[7] = {rows * s.d * 4, rows * s.d * 4, rows * 4, blocks * s.d * 4, blocks * s.d * 4,
+                           blocks * s.nb * 4, blocks * s.nb * 4};
+  SelectRegions r{};
+  size_t at = 0;
+  for (int x = 0; x < 7; ++x) {
+    r.off[x] = at;
+    at += round256(sizes[x]);
+  }
+  r.total = at;
+  return r;
+}
+
 }  // namespace
 
-size_t select_workspace_bytes(const MaskShape &s) {
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;  // (b, g, i, h) rows
-  const size_t scores = static_cast<size_t>(s.batch) * s.hkv * s.nb * s.nb;
-  return round256(rows * s.d * 4) + round256(rows * 4) + 2 * round256(scores * 4);
-}
+size_t select_workspace_bytes(const MaskShape &s) { return select_regions(s).total; }
 
 cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
                               cudaStream_t stream) {
@@ -503,27 +584,27 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
                           float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
                           void *workspace, int32_t *status, cudaStream_t stream) {
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;
-  const size_t scores = static_cast<size_t>(s.batch) * s.hkv * s.nb * s.nb;
+  const SelectRegions r = select_regions(s);
   char *ws = static_cast<char *>(workspace);
-  float *qbar = reinterpret_cast<float *>(ws);
-  float *nbar = reinterpret_cast<float *>(ws + round256(rows * s.d * 4));
-  float *s_c = reinterpret_cast<float *>(ws + round256(rows * s.d * 4) + round256(rows * 4));
-  float *s_r = reinterpret_cast<float *>(reinterpret_cast<char *>(s_c) + round256(scores * 4));
+  float *reg[7];
+  for (int x = 0; x < 7; ++x) reg[x] = reinterpret_cast<float *>(ws + r.off[x]);
+  float *q_hi = reg[0], *q_lo = reg[1], *nbar = reg[2], *c_hi = reg[3], *c_lo = reg[4];
+  float *s_c = reg[5], *s_r = reg[6];
   cudaError_t e;
-  if (s.d == 64) e = launch_qpool_d<64>(s, q, qbar, nbar, stream);
-  else if (s.d == 128) e = launch_qpool_d<128>(s, q, qbar, nbar, stream);
+  if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, stream);
+  else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, stream);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
-  e = launch_scores(s, qbar, nbar, centroid, radius, alpha, scale, s_c, s_r, status, stream);
+  e = launch_scores(s, ScoreOperands{c_hi, c_lo, q_hi, q_lo, nbar, radius, alpha}, scale, s_c, s_r,
+                    status, stream);
   if (e != cudaSuccess) return e;
-  const size_t smem = static_cast<size_t>(s.nb) * 9;
+  const size_t smem = kSelWarps * select_warp_bytes(s.nb);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(s.nb, s.hkv, s.batch);
-  select_kernel<<<grid, kThreads, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.hkv, s.nb,
-                                                  static_cast<long long>(ppm_c),
-                                                  static_cast<long long>(ppm_r));
+  dim3 grid((s.nb + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);
+  select_kernel<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.hkv,
+                                                        s.nb, static_cast<long long>(ppm_c),
+                                                        static_cast<long long>(ppm_r));
   return cudaGetLastError();
 }
 

@@ -6,19 +6,22 @@
 // key block j are
 //   S_c[i][j] = s * max_h qbar_{h,i} . c_j
 //   R[i][j]   = s * max_h (qbar_{h,i} . c_j + nbar_{h,i} * alpha_j * r_j)
-// over the G query heads h of group g.  The dot products form the dense
-// product [nb*G x d] x [d x nb]: one CTA computes a 128-row tile (IB query
-// blocks x G heads) against 256 key blocks with fp32 precision recovered from
-// tf32 tensor-core MMAs: each operand is split into hi = tf32(x) (mantissa
-// truncated) and lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi (the
-// dropped A_lo B_lo term and the truncation of lo are below 2^-20 relative).
+// over the G query heads h of group g.  The dot products are a dense product;
+// one CTA computes D = C Qbar^T for 128 key blocks (rows j, the TMEM lanes)
+// against 256 (query block, head) columns, so each thread holds every head of
+// a (j, i) pair in its own registers: the max over heads needs no shuffles and
+// the stores of consecutive j coalesce.  fp32 precision comes from tf32 MMAs
+// on hi / lo splits: x = hi + lo with hi = x with its low 13 mantissa bits
+// cleared (exact in tf32) and lo = x - hi, and
+//   D = A_hi B_hi + A_hi B_lo + A_lo B_hi,
+// whose error (the dropped A_lo B_lo term and lo's own rounding) stays below
+// 2^-20 of |a||b| per product.  The splits are written by the query-pooling
+// launch, so this kernel is TMA loads plus MMAs plus the epilogue.
 //
-// Warp roles: warp 0 issues TMA loads of fp32 K-chunks (32 dims = one 128-byte
-// swizzle row) of both operands; warps 4..7 split each chunk into hi / lo in
-// place in shared memory (elementwise, so the swizzled layout is kept); warp 1
-// owns 256 TMEM columns and issues the MMAs; warps 4..7 then read the
-// accumulator (one TMEM lane per row), take the max over each block's G heads
-// with shuffles, and write S_c and R.  Every wait is bounded.
+// Warp roles: warp 0 issues TMA loads of 32-dimension chunks (one 128-byte
+// swizzle row) of the four operands; warp 1 owns 256 TMEM columns and issues
+// the MMAs; warps 4..7 read the accumulator (one TMEM lane per key block) and
+// write S_c and R.  Every wait is bounded.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,19 +37,20 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: no legitimate wait comes cl
 
 template <int D, int G>
 struct ScoreCfg {
-  static constexpr int ROWS = 128;     // (query block, head) rows per tile
-  static constexpr int IB = ROWS / G;  // query blocks per tile
-  static constexpr int COLS = 256;     // key blocks per tile
+  static constexpr int ROWS = 128;     // key blocks per tile (TMEM lanes)
+  static constexpr int COLS = 256;     // (query block, head) columns per tile
+  static constexpr int NI = COLS / G;  // query blocks per tile
   static constexpr int KC = 32;        // fp32 elements per K-chunk
   static constexpr int NKC = D / KC;
   static constexpr int NS = 2;
   static constexpr uint32_t A_BYTES = ROWS * KC * 4;  // 16 KB
   static constexpr uint32_t B_BYTES = COLS * KC * 4;  // 32 KB
+  // stage layout: A_hi, A_lo, B_hi, B_lo
   static constexpr uint32_t STAGE = 2 * (A_BYTES + B_BYTES);
-  static constexpr uint32_t OFF_BONUS = NS * STAGE;
-  static constexpr uint32_t OFF_BAR = OFF_BONUS + COLS * 4;
-  // barriers: full[NS] (TMA), split[NS] (hi / lo written), empty[NS] (MMAs done), done
-  static constexpr int B_FULL = 0, B_SPLIT = NS, B_EMPTY = 2 * NS, B_DONE = 3 * NS, NBARS = 3 * NS + 1;
+  static constexpr uint32_t OFF_NBAR = NS * STAGE;
+  static constexpr uint32_t OFF_BAR = OFF_NBAR + COLS * 4;
+  // barriers: full[NS] (TMA), empty[NS] (MMAs done with the stage), done
+  static constexpr int B_FULL = 0, B_EMPTY = NS, B_DONE = 2 * NS, NBARS = 2 * NS + 1;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
   static constexpr int THREADS = 256;
   // kind::tf32: D f32, A and B tf32, both K-major, M = 128, N = 256
@@ -79,30 +83,34 @@ __device__ __forceinline__ bool wait_b(uint32_t bar, uint32_t parity, int32_t *s
   return true;
 }
 
+struct ScoreMaps {
+  CUtensorMap c_hi, c_lo, q_hi, q_lo;
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(256, 1)
-    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-                 const float *__restrict__ nbar, const float *__restrict__ radius,
-                 const float *__restrict__ alpha, float *__restrict__ s_c, float *__restrict__ s_r,
-                 int nb, float scale, int32_t *status) {
+    score_kernel(const __grid_constant__ ScoreMaps maps, const float *__restrict__ nbar,
+                 const float *__restrict__ radius, const float *__restrict__ alpha,
+                 float *__restrict__ s_c, float *__restrict__ s_r, int nb, float scale,
+                 int32_t *status) {
   using C = ScoreCfg<D, G>;
-  const int ct = blockIdx.x, rt = blockIdx.y, gb = blockIdx.z;  // gb = b * hkv + g
-  const int i0 = rt * C::IB, j0 = ct * C::COLS;
-  // only tiles with some key block j < i below the diagonal carry work
-  if (j0 >= i0 + C::IB - 1 || i0 >= nb) return;
+  const int jt = blockIdx.x, it = blockIdx.y, gb = blockIdx.z;  // gb = b * hkv + g
+  const int j0 = jt * C::ROWS, i0 = it * C::NI;
+  // only tiles with some key block j below some query block i carry work
+  if (j0 >= i0 + C::NI - 1 || j0 >= nb || i0 >= nb) return;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char *sb = smem_raw + (base - raw);
-  float *bonus = reinterpret_cast<float *>(sb + C::OFF_BONUS);
+  float *snbar = reinterpret_cast<float *>(sb + C::OFF_NBAR);
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int x) { return bar0 + 8u * static_cast<uint32_t>(x); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::OFF_BAR + C::NBARS * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int x = 0; x < C::NBARS; ++x) ptx::mbar_init(bar(x), (x >= C::B_SPLIT && x < C::B_EMPTY) ? 4 : 1);
+    for (int x = 0; x < C::NBARS; ++x) ptx::mbar_init(bar(x), 1);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -111,28 +119,32 @@ __global__ void __launch_bounds__(256, 1)
     ptx::tmem_relinquish();
   }
   for (int c = threadIdx.x; c < C::COLS; c += C::THREADS) {
-    const int j = j0 + c;
-    bonus[c] = j < nb ? alpha[static_cast<size_t>(gb) * nb + j] * radius[static_cast<size_t>(gb) * nb + j] : 0.f;
+    const int i = i0 + c / G;
+    snbar[c] = i < nb ? nbar[(static_cast<size_t>(gb) * nb + i0) * G + c] : 0.f;
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int row0 = (gb * nb + i0) * G;  // first (query block, head) row of the tile
   bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
-      ptx::tma_prefetch_desc(&tm_q);
-      ptx::tma_prefetch_desc(&tm_c);
+      ptx::tma_prefetch_desc(&maps.c_hi);
+      ptx::tma_prefetch_desc(&maps.c_lo);
+      ptx::tma_prefetch_desc(&maps.q_hi);
+      ptx::tma_prefetch_desc(&maps.q_lo);
+      const int arow = gb * nb + j0, brow = (gb * nb + i0) * G;
       int issued = 0;
       for (int kc = 0; kc < C::NKC; ++kc) {
         const int s = kc % C::NS;
         if (kc >= C::NS && !wait_b(bar(C::B_EMPTY + s), (kc / C::NS - 1) & 1, status, ok)) break;
         const uint32_t st = base + s * C::STAGE;
-        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::A_BYTES + C::B_BYTES);
-        ptx::tma_load_2d(st, &tm_q, bar(C::B_FULL + s), kc * C::KC, row0);
-        ptx::tma_load_2d(st + 2 * C::A_BYTES, &tm_c, bar(C::B_FULL + s), kc * C::KC, gb * nb + j0);
+        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * (C::A_BYTES + C::B_BYTES));
+        ptx::tma_load_2d(st, &maps.c_hi, bar(C::B_FULL + s), kc * C::KC, arow);
+        ptx::tma_load_2d(st + C::A_BYTES, &maps.c_lo, bar(C::B_FULL + s), kc * C::KC, arow);
+        ptx::tma_load_2d(st + 2 * C::A_BYTES, &maps.q_hi, bar(C::B_FULL + s), kc * C::KC, brow);
+        ptx::tma_load_2d(st + 2 * C::A_BYTES + C::B_BYTES, &maps.q_lo, bar(C::B_FULL + s), kc * C::KC, brow);
         issued = kc + 1;
       }
       if (!ok) {  // let the copies in flight land before shared memory is released
@@ -147,104 +159,54 @@ __global__ void __launch_bounds__(256, 1)
       const uint64_t da = ptx::sdesc_sw128(base, 16, 1024);
       const uint64_t db = ptx::sdesc_sw128(base + 2 * C::A_BYTES, 16, 1024);
       constexpr uint64_t LO_A = C::A_BYTES >> 4, LO_B = C::B_BYTES >> 4, STG = C::STAGE >> 4;
-      int issued = 0;
       for (int kc = 0; kc < C::NKC; ++kc) {
         const int s = kc % C::NS;
-        if (!wait_b(bar(C::B_SPLIT + s), (kc / C::NS) & 1, status, ok)) break;
+        if (!wait_b(bar(C::B_FULL + s), (kc / C::NS) & 1, status, ok)) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < C::KC / 8; ++ks) {
           const uint64_t a = da + s * STG + ((ks * 32) >> 4), b = db + s * STG + ((ks * 32) >> 4);
-          const uint32_t acc0 = (kc > 0 || ks > 0) ? 1u : 0u;
-          mma_tf32(tmem, a, b, C::IDESC, acc0);                 // hi * hi
-          mma_tf32(tmem, a, b + LO_B, C::IDESC, 1u);            // hi * lo
-          mma_tf32(tmem, a + LO_A, b, C::IDESC, 1u);            // lo * hi
+          mma_tf32(tmem, a, b, C::IDESC, (kc > 0 || ks > 0) ? 1u : 0u);  // hi * hi
+          mma_tf32(tmem, a, b + LO_B, C::IDESC, 1u);                       // hi * lo
+          mma_tf32(tmem, a + LO_A, b, C::IDESC, 1u);                       // lo * hi
         }
         ptx::mma_commit(bar(C::B_EMPTY + s));
-        issued = kc + 1;
       }
-      (void)issued;
       ptx::mma_commit(bar(C::B_DONE));  // also on abort: every issued MMA completes first
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int t4 = threadIdx.x - 128;
-    // ---- split each landed chunk into hi = tf32(x) and lo = x - hi, in place
-    for (int kc = 0; kc < C::NKC; ++kc) {
-      const int s = kc % C::NS;
-      if (!wait_b(bar(C::B_FULL + s), (kc / C::NS) & 1, status, ok)) break;
-      uint32_t *a_hi = reinterpret_cast<uint32_t *>(sb + s * C::STAGE);
-      uint32_t *a_lo = a_hi + C::A_BYTES / 4;
-      uint32_t *b_hi = a_lo + C::A_BYTES / 4;
-      uint32_t *b_lo = b_hi + C::B_BYTES / 4;
-      for (int e = t4 * 4; e < static_cast<int>(C::A_BYTES / 4); e += 128 * 4) {
-        uint4 x = *reinterpret_cast<uint4 *>(a_hi + e);
-        uint4 h = make_uint4(x.x & 0xFFFFE000u, x.y & 0xFFFFE000u, x.z & 0xFFFFE000u, x.w & 0xFFFFE000u);
-        uint4 l = make_uint4(__float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x)),
-                             __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y)),
-                             __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z)),
-                             __float_as_uint(__uint_as_float(x.w) - __uint_as_float(h.w)));
-        *reinterpret_cast<uint4 *>(a_hi + e) = h;
-        *reinterpret_cast<uint4 *>(a_lo + e) = l;
-      }
-      for (int e = t4 * 4; e < static_cast<int>(C::B_BYTES / 4); e += 128 * 4) {
-        uint4 x = *reinterpret_cast<uint4 *>(b_hi + e);
-        uint4 h = make_uint4(x.x & 0xFFFFE000u, x.y & 0xFFFFE000u, x.z & 0xFFFFE000u, x.w & 0xFFFFE000u);
-        uint4 l = make_uint4(__float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x)),
-                             __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y)),
-                             __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z)),
-                             __float_as_uint(__uint_as_float(x.w) - __uint_as_float(h.w)));
-        *reinterpret_cast<uint4 *>(b_hi + e) = h;
-        *reinterpret_cast<uint4 *>(b_lo + e) = l;
-      }
-      ptx::fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::B_SPLIT + s));
-    }
-    // ---- epilogue: max over each query block's G heads, scale, store
     bool dok = true;
     wait_b(bar(C::B_DONE), 0, status, dok);
     ptx::tc_fence_after();
-    const int r = ((warp & 3) << 5) + lane;  // TMEM lane = tile row
-    const int il = r / G, h = r - il * G;
-    const int i = i0 + il;
-    const bool row_ok = ok && dok && i < nb;
-    const float nv = row_ok ? nbar[static_cast<size_t>(gb * nb + i) * G + h] : 0.f;
+    const int r = ((warp & 3) << 5) + lane;  // TMEM lane = key block row
+    const int j = j0 + r;
+    const bool row_ok = dok && j < nb;
+    const float bonus = row_ok ? alpha[static_cast<size_t>(gb) * nb + j] * radius[static_cast<size_t>(gb) * nb + j] : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
-    float *out_c = s_c + (static_cast<size_t>(gb) * nb + (i < nb ? i : 0)) * nb;
-    float *out_r = s_r + (static_cast<size_t>(gb) * nb + (i < nb ? i : 0)) * nb;
 #pragma unroll 1
     for (int cc = 0; cc < C::COLS / 32; ++cc) {
       uint32_t v[32];
       ptx::tmem_ld32(tmem + lane_off + cc * 32, v);
       ptx::tmem_wait_ld();
-      float dm[32], rm[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        dm[e] = __uint_as_float(v[e]);
-        rm[e] = fmaf(nv, bonus[cc * 32 + e], dm[e]);
-      }
+      for (int q = 0; q < 32 / G; ++q) {
+        // columns cc*32 + q*G .. + G-1 hold the G heads of one query block
+        const int c0 = q * G;
+        const int col = cc * 32 + c0;
+        const int i = i0 + col / G;
+        float dm = __uint_as_float(v[c0]);
+        float rm = fmaf(snbar[col], bonus, dm);
 #pragma unroll
-      for (int off = G / 2; off > 0; off >>= 1)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          dm[e] = fmaxf(dm[e], __shfl_xor_sync(0xffffffffu, dm[e], off));
-          rm[e] = fmaxf(rm[e], __shfl_xor_sync(0xffffffffu, rm[e], off));
+        for (int h = 1; h < G; ++h) {
+          const float x = __uint_as_float(v[c0 + h]);
+          dm = fmaxf(dm, x);
+          rm = fmaxf(rm, fmaf(snbar[col + h], bonus, x));
         }
-      // the G lanes of a query block hold the same maxima: lane h stores columns h, h+G, ...
-#pragma unroll
-      for (int e = 0; e < 32; e += G) {
-        float dv = dm[0], rv = rm[0];
-#pragma unroll
-        for (int q = 0; q < G; ++q)
-          if (q == h) {
-            dv = dm[e + q];
-            rv = rm[e + q];
-          }
-        const int j = j0 + cc * 32 + e + h;
-        if (row_ok && j < nb) {
-          out_c[j] = dv * scale;
-          out_r[j] = rv * scale;
+        if (row_ok && j < i && i < nb) {
+          const size_t o = (static_cast<size_t>(gb) * nb + i) * nb + j;
+          s_c[o] = dm * scale;
+          s_r[o] = rm * scale;
         }
       }
     }
@@ -272,45 +234,44 @@ bool make_map_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t row
 }
 
 template <int D, int G>
-cudaError_t launch_t(const MaskShape &s, const float *qbar, const float *nbar, const float *centroid,
-                     const float *radius, const float *alpha, float scale, float *s_c, float *s_r,
+cudaError_t launch_t(const MaskShape &s, const ScoreOperands &op, float scale, float *s_c, float *s_r,
                      int32_t *status, cudaStream_t stream) {
   using C = ScoreCfg<D, G>;
-  CUtensorMap mq, mc;
+  ScoreMaps maps;
   const uint64_t groups = static_cast<uint64_t>(s.batch) * s.hkv;
-  if (!make_map_2d(&mq, qbar, D, groups * s.nb * G, C::ROWS) ||
-      !make_map_2d(&mc, centroid, D, groups * s.nb, C::COLS))
+  if (!make_map_2d(&maps.c_hi, op.c_hi, D, groups * s.nb, C::ROWS) ||
+      !make_map_2d(&maps.c_lo, op.c_lo, D, groups * s.nb, C::ROWS) ||
+      !make_map_2d(&maps.q_hi, op.q_hi, D, groups * s.nb * G, C::COLS) ||
+      !make_map_2d(&maps.q_lo, op.q_lo, D, groups * s.nb * G, C::COLS))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((s.nb + C::COLS - 1) / C::COLS, (s.nb + C::IB - 1) / C::IB, static_cast<unsigned>(groups));
-  score_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mc, nbar, radius, alpha, s_c, s_r,
-                                                                  s.nb, scale, status);
+  dim3 grid((s.nb + C::ROWS - 1) / C::ROWS, (s.nb + C::NI - 1) / C::NI, static_cast<unsigned>(groups));
+  score_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps, op.nbar, op.radius, op.alpha,
+                                                                  s_c, s_r, s.nb, scale, status);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const MaskShape &s, const float *qb, const float *nbr, const float *c,
-                     const float *r, const float *a, float scale, float *sc, float *sr, int32_t *st,
-                     cudaStream_t stream) {
+cudaError_t launch_d(const MaskShape &s, const ScoreOperands &op, float scale, float *sc, float *sr,
+                     int32_t *st, cudaStream_t stream) {
   switch (s.group) {
-    case 1: return launch_t<D, 1>(s, qb, nbr, c, r, a, scale, sc, sr, st, stream);
-    case 2: return launch_t<D, 2>(s, qb, nbr, c, r, a, scale, sc, sr, st, stream);
-    case 4: return launch_t<D, 4>(s, qb, nbr, c, r, a, scale, sc, sr, st, stream);
-    case 8: return launch_t<D, 8>(s, qb, nbr, c, r, a, scale, sc, sr, st, stream);
-    case 16: return launch_t<D, 16>(s, qb, nbr, c, r, a, scale, sc, sr, st, stream);
+    case 1: return launch_t<D, 1>(s, op, scale, sc, sr, st, stream);
+    case 2: return launch_t<D, 2>(s, op, scale, sc, sr, st, stream);
+    case 4: return launch_t<D, 4>(s, op, scale, sc, sr, st, stream);
+    case 8: return launch_t<D, 8>(s, op, scale, sc, sr, st, stream);
+    case 16: return launch_t<D, 16>(s, op, scale, sc, sr, st, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_scores(const MaskShape &s, const float *qbar, const float *nbar,
-                          const float *centroid, const float *radius, const float *alpha,
-                          float scale, float *s_c, float *s_r, int32_t *status, cudaStream_t stream) {
-  if (s.d == 64) return launch_d<64>(s, qbar, nbar, centroid, radius, alpha, scale, s_c, s_r, status, stream);
-  if (s.d == 128) return launch_d<128>(s, qbar, nbar, centroid, radius, alpha, scale, s_c, s_r, status, stream);
+cudaError_t launch_scores(const MaskShape &s, const ScoreOperands &op, float scale, float *s_c,
+                          float *s_r, int32_t *status, cudaStream_t stream) {
+  if (s.d == 64) return launch_d<64>(s, op, scale, s_c, s_r, status, stream);
+  if (s.d == 128) return launch_d<128>(s, op, scale, s_c, s_r, status, stream);
   return cudaErrorInvalidValue;
 }
 

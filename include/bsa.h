@@ -124,9 +124,10 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
  * q: bf16 [batch, seq, hq, head_dim]; centroid, radius, alpha as written by
  * bsa_block_meta.  workspace: device scratch of at least
  * bsa_select_workspace_bytes(shape) bytes, 16-byte aligned, owned by the
- * caller (it holds the per-block mean queries and mean query norms and the two
- * block-score matrices; its contents need no initialisation and are dead after
- * the call's kernels finish).  dev_status (nullable) receives
+ * caller (it holds the per-block mean queries and mean query norms, tf32
+ * hi / lo splits of the mean queries and centroids, and the two block-score
+ * matrices; its contents need no initialisation and are dead after the call's
+ * kernels finish).  dev_status (nullable) receives
  * BSA_ERR_DEVICE_TIMEOUT if the score kernel's bounded waits give up.
  */
 size_t bsa_select_workspace_bytes(const bsa_shape *shape);
@@ -148,8 +149,8 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
  *   - Every GPU that loads libbsa keeps those 12 MiB until the process exits.
  *   - Shapes needing more than 12 MiB of select scratch
  *     (bsa_select_workspace_bytes(shape) > 12 MiB: at 32 query heads,
- *     head_dim 128 and block 128 that is beyond about 52K tokens; the 65536-
- *     and 131072-token layers need 16.9 MB and 50.5 MB) return
+ *     4 KV heads, head_dim 128 and block 128 that is beyond 34816 tokens;
+ *     the 65536- and 131072-token layers need 27.3 MB and 71.4 MB) return
  *     BSA_ERR_WORKSPACE.
  *   - All calls on one device share that array: calls whose kernels overlap on
  *     the GPU (unordered streams) race and give wrong results.  Calls ordered

@@ -80,8 +80,9 @@ def test_null_and_misaligned_pointers(lib):
         assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(bad), *args, None, f, big,
                                    None, None) == 1
     need = lib.bsa_select_workspace_bytes(ctypes.byref(s))
-    # qbar (8192 B) + nbar (128 B) + two 16 x 16 score matrices (1 KB each), each 256-aligned
-    assert need == 2 * 16 * 64 * 4 + 256 + 2 * 1024
+    # q_hi, q_lo (8192 B each) + nbar (128 B) + c_hi, c_lo (4096 B each) + two 16 x 16
+    # score matrices (1 KB each), each region 256-aligned
+    assert need == 2 * 8192 + 256 + 2 * 4096 + 2 * 1024
     assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(prm), *args, None, None, big,
                                None, None) == 4
     assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(prm), *args, None, f,
