@@ -11,16 +11,17 @@
 // Five launches:
 //   meta_kernel     one CTA per (b, g, j): centroid and radius of key block j
 //                   (streams K once, the block held in registers)
-//   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii,
-//                   nearest-rank median / p90, rescue coefficient alpha
+//   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii in
+//                   registers, nearest-rank median / p90, rescue coefficient alpha
 //   qpool_kernel    one CTA per (b, i, head chunk): mean query and mean query
 //                   norm of block i (streams Q once: the dominant HBM bytes),
 //                   written as tf32 hi / lo splits; one more CTA row splits the
 //                   centroids the same way
 //   score_kernel    (bsa_score.cu) centroid / rescue scores of every causal key
 //                   block on tensor cores
-//   select_kernel   one warp per (b, g, i): per-path top-k by radix select, OR,
-//                   ascending kept-list emission
+//   select_kernel   one warp per (b, g, i): per-path exact top-k (a linear
+//                   value histogram, then a radix threshold inside its
+//                   threshold bin), OR, ascending kept-list emission
 // Every reduction runs in a fixed order, so results are deterministic.
 
 #include <cuda_bf16.h>
@@ -40,10 +41,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float f[8]) {
     f[2 * e] = __uint_as_float(w[e] << 16);
     f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
   }
-}
-
-__device__ __forceinline__ float bf16_at(const uint16_t *p, int idx) {
-  return __uint_as_float(static_cast<uint32_t>(p[idx]) << 16);
 }
 
 // ---------------------------------------------------------------- block meta
@@ -147,42 +144,82 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
 
 // ---------------------------------------------------------------- quantiles
 
-// Bitonic sort of the nb radii (padded with +inf to a power of two), then
-// nearest-rank median / p90 and alpha.
+// Bitonic sort of the nb radii (padded with +inf to npow2 >= 32 E entries),
+// then nearest-rank median / p90 and alpha.  Thread t holds entries
+// t E .. t E + E - 1 in registers: exchange distances below E stay in the
+// thread, those below 32 E go through warp shuffles, and only the longer ones
+// through shared memory.
+template <int E>
 __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ radius,
                                                      float *__restrict__ quant,
                                                      float *__restrict__ alpha, int nb, int npow2) {
   extern __shared__ float sr[];
+  __shared__ float sq[2];
   const int g = blockIdx.x, b = blockIdx.y, hkv = gridDim.x;
+  const int tid = threadIdx.x;
   const size_t base = (static_cast<size_t>(b) * hkv + g) * nb;
-  for (int j = threadIdx.x; j < npow2; j += blockDim.x) sr[j] = j < nb ? radius[base + j] : INFINITY;
-  __syncthreads();
+  float x[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int idx = tid * E + e;
+    x[e] = idx < nb ? radius[base + idx] : INFINITY;
+  }
   for (int kk = 2; kk <= npow2; kk <<= 1) {
     for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      for (int idx = threadIdx.x; idx < npow2; idx += blockDim.x) {
-        const int ixj = idx ^ jj;
-        if (ixj > idx) {
-          const bool up = (idx & kk) == 0;
-          const float a = sr[idx], c = sr[ixj];
-          if ((a > c) == up) {
-            sr[idx] = c;
-            sr[ixj] = a;
+      if (jj >= 32 * E) {
+        // partner in another warp: exchange through shared memory
+#pragma unroll
+        for (int e = 0; e < E; ++e) sr[tid * E + e] = x[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int idx = tid * E + e;
+          const float p = sr[idx ^ jj];
+          const bool up = (idx & kk) == 0, lower = (idx & jj) == 0;
+          x[e] = (lower == up) ? fminf(x[e], p) : fmaxf(x[e], p);
+        }
+        __syncthreads();
+      } else if (jj >= E) {
+        const int lj = jj / E;  // partner lane distance
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int idx = tid * E + e;
+          const float p = __shfl_xor_sync(0xffffffffu, x[e], lj);
+          const bool up = (idx & kk) == 0, lower = (idx & jj) == 0;
+          x[e] = (lower == up) ? fminf(x[e], p) : fmaxf(x[e], p);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int pe = e ^ jj;
+          if (pe > e) {
+            const int idx = tid * E + e;
+            const bool up = (idx & kk) == 0;
+            const float a = x[e], c = x[pe];
+            x[e] = up ? fminf(a, c) : fmaxf(a, c);
+            x[pe] = up ? fmaxf(a, c) : fminf(a, c);
           }
         }
       }
-      __syncthreads();
     }
   }
   // nearest rank (1-based): ceil(nb / 2) and ceil(9 nb / 10)
-  const float med = sr[(nb + 1) / 2 - 1];
-  const float p90 = sr[(9 * nb + 9) / 10 - 1];
+  const int r_med = (nb + 1) / 2 - 1, r_p90 = (9 * nb + 9) / 10 - 1;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int idx = tid * E + e;
+    if (idx == r_med) sq[0] = x[e];
+    if (idx == r_p90) sq[1] = x[e];
+  }
+  __syncthreads();
+  const float med = sq[0], p90 = sq[1];
   const float span = p90 - med;
   const bool degenerate = span <= 1e-12f * p90;
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     quant[(static_cast<size_t>(b) * hkv + g) * 2 + 0] = med;
     quant[(static_cast<size_t>(b) * hkv + g) * 2 + 1] = p90;
   }
-  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+  for (int j = tid; j < nb; j += blockDim.x) {
     float a = 0.f;
     if (!degenerate) a = fminf(fmaxf((radius[base + j] - med) / span, 0.f), 1.f);
     alpha[base + j] = a;
@@ -284,16 +321,73 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kSelWarps = 8;  // rows per select CTA, one warp each
+constexpr int kSelWarps = 8;   // rows per select CTA, one warp each
+constexpr int kCompact = 256;  // capacity of the per-warp list of threshold-bin keys
 
 __host__ __device__ constexpr size_t select_warp_bytes(int nb) {
-  return static_cast<size_t>(nb) * 4 + 1024 + ((static_cast<size_t>(nb) + 15) & ~static_cast<size_t>(15));
+  return static_cast<size_t>(nb) * 4 + 1024 + kCompact * 4 +
+         ((static_cast<size_t>(nb) + 15) & ~static_cast<size_t>(15));
+}
+
+// Inverse of score_key for a nonzero key.
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Exclusive prefix sum of c over the lanes of a warp; *total receives the sum.
+__device__ __forceinline__ unsigned warp_exclusive_scan(unsigned c, unsigned *total) {
+  const int lane = threadIdx.x & 31;
+  unsigned incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - c;
+}
+
+// In a 256-bin histogram (lane l reads bins 8l .. 8l+7), the bin holding the
+// take-th largest entry counting down from the top bin, the number of entries
+// in the bins above it, and its own count.  Requires 1 <= take <= total.
+__device__ __forceinline__ void warp_find_bin(const unsigned *hist, unsigned take, unsigned *bin,
+                                              unsigned *above, unsigned *count) {
+  const int lane = threadIdx.x & 31;
+  const uint4 h0 = reinterpret_cast<const uint4 *>(hist)[2 * lane];
+  const uint4 h1 = reinterpret_cast<const uint4 *>(hist)[2 * lane + 1];
+  const unsigned c[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  unsigned s = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s += c[e];
+  unsigned suf = s;  // entries in the bins of lanes >= this lane
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
+    if (lane + off < 32) suf += o;
+  }
+  unsigned acc = suf - s, my_bin = 0, my_above = 0, my_count = 0;
+  bool hit = false;
+#pragma unroll
+  for (int e = 7; e >= 0; --e) {
+    if (!hit && acc < take && take <= acc + c[e]) {
+      hit = true;
+      my_bin = 8 * lane + e;
+      my_above = acc;
+      my_count = c[e];
+    }
+    acc += c[e];
+  }
+  const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+  *bin = __shfl_sync(0xffffffffu, my_bin, src);
+  *above = __shfl_sync(0xffffffffu, my_above, src);
+  *count = __shfl_sync(0xffffffffu, my_count, src);
+  __syncwarp();
 }
 
 // Radix threshold of the k largest nonzero keys of keys[0, n) (1 <= k < number
-// of nonzero keys), one warp, 8-bit digits from the top.  On return the
-// selection is: every key with (key & pmask) > prefix, plus the first `take`
-// in index order of the `n_eq` nonzero keys with (key & pmask) == prefix.
+// of nonzero keys), one warp, 8-bit digits from the top.  The selection is:
+// every key with (key & pmask) > prefix, plus the first `take` in index order
+// of the `n_eq` nonzero keys with (key & pmask) == prefix.
 struct Threshold {
   uint32_t prefix, pmask;
   unsigned take, n_eq;
@@ -315,63 +409,155 @@ __device__ Threshold warp_radix_threshold(const uint32_t *keys, int n, unsigned 
       if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
     }
     __syncwarp();
-    // lane l owns bins 8l .. 8l+7; find the bin holding the take-th largest key
-    unsigned c[8], s = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      c[e] = hist[8 * lane + e];
-      s += c[e];
-    }
-    unsigned suf = s;  // keys in the bins of lanes >= this lane
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
-      if (lane + off < 32) suf += o;
-    }
-    unsigned acc = suf - s, my_digit = 0, my_above = 0, my_count = 0;
-    bool hit = false;
-#pragma unroll
-    for (int e = 7; e >= 0; --e) {
-      if (!hit && acc < t.take && t.take <= acc + c[e]) {
-        hit = true;
-        my_digit = 8 * lane + e;
-        my_above = acc;
-        my_count = c[e];
-      }
-      acc += c[e];
-    }
-    const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-    const unsigned digit = __shfl_sync(0xffffffffu, my_digit, src);
-    t.take -= __shfl_sync(0xffffffffu, my_above, src);
-    t.n_eq = __shfl_sync(0xffffffffu, my_count, src);
+    unsigned digit, above, count;
+    warp_find_bin(hist, t.take, &digit, &above, &count);
+    t.take -= above;
+    t.n_eq = count;
     t.prefix |= digit << shift;
     t.pmask |= 0xFFu << shift;
-    __syncwarp();  // hist is rewritten by the next pass
     if (t.n_eq == t.take) break;  // the whole bin is in: no finer digit needed
   }
   return t;
 }
 
-// flags[j] |= bit for the keys Threshold t selects among keys[0, n).
-__device__ void warp_mark(const uint32_t *keys, int n, const Threshold &t, uint8_t *flags, uint8_t bit) {
+// The k best candidates of a row.  A linear 256-bin histogram of the
+// candidates' values over [lo, hi] finds the bin holding the threshold; bins
+// above it are in, and inside it the radix threshold t over the bin's keys
+// (gathered into a short list) decides, unless the whole bin is in.  The bin
+// map is monotone in the value, so this is the exact top-k of the keys.  With
+// no usable value range, or a threshold bin too crowded for the list, every
+// candidate falls in bin 0 and t is taken over the whole row.
+struct RowSelect {
+  float lo, inv;  // bin(v) = min(255, trunc((v - lo) * inv)); inv == 0 maps everything to bin 0
+  int bstar;
+  bool whole;
+  Threshold t;
+};
+
+__device__ __forceinline__ int value_bin(uint32_t key, float lo, float inv) {
+  return min(255, static_cast<int>((key_value(key) - lo) * inv));
+}
+
+// keys[0, n) are readable 4 at a time: the entries from n up to the next
+// multiple of 4 are zero.
+__device__ RowSelect warp_select(const uint32_t *keys, int n, unsigned k, float lo, float hi,
+                                 unsigned *hist, uint32_t *ckeys) {
   const int lane = threadIdx.x & 31;
-  const unsigned lt = (1u << lane) - 1u;
-  const bool all_eq = t.n_eq == t.take;
-  unsigned taken = 0;
-  for (int j0 = 0; j0 < n; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t key = j < n ? keys[j] : 0u;
-    const uint32_t top = key & t.pmask;
-    const bool eq = key != 0u && top == t.prefix;
-    bool in = top > t.prefix;
-    if (all_eq) {
-      in = in || eq;
-    } else {
-      const unsigned b = __ballot_sync(0xffffffffu, eq);
-      in = in || (eq && taken + __popc(b & lt) < t.take);
-      taken += __popc(b);
+  RowSelect r;
+  r.lo = lo;
+  r.inv = 0.f;
+  r.bstar = 0;
+  r.whole = false;
+  if (hi > lo) {
+    const float inv = 256.f / (hi - lo);
+    if (inv <= 1.0e38f) r.inv = inv;
+  }
+  if (r.inv > 0.f) {
+    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    for (int j = 4 * lane; j < n; j += 128) {
+      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
+      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kv[e] != 0u) atomicAdd(&hist[value_bin(kv[e], r.lo, r.inv)], 1u);
     }
-    if (in) flags[j] |= bit;
+    __syncwarp();
+    unsigned bstar, above, count;
+    warp_find_bin(hist, k, &bstar, &above, &count);
+    r.bstar = static_cast<int>(bstar);
+    const unsigned take = k - above;
+    if (count == take) {
+      r.whole = true;
+      return r;
+    }
+    if (count <= static_cast<unsigned>(kCompact)) {
+      unsigned base = 0;
+      for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
+        const int j = j0 + 4 * lane;
+        uint32_t kv[4] = {0u, 0u, 0u, 0u};
+        unsigned m = 0;
+        if (j < n) {
+          const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
+          kv[0] = kk.x; kv[1] = kk.y; kv[2] = kk.z; kv[3] = kk.w;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (kv[e] != 0u && value_bin(kv[e], r.lo, r.inv) == r.bstar) m |= 1u << e;
+        }
+        unsigned tot;
+        unsigned pos = base + warp_exclusive_scan(__popc(m), &tot);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((m >> e) & 1u) ckeys[pos++] = kv[e];
+        base += tot;
+      }
+      __syncwarp();
+      r.t = warp_radix_threshold(ckeys, static_cast<int>(count), take, hist);
+      return r;
+    }
+  }
+  r.inv = 0.f;
+  r.bstar = 0;
+  r.t = warp_radix_threshold(keys, n, k, hist);
+  return r;
+}
+
+// flags[j] |= bit for the candidates RowSelect r keeps among keys[0, n).  Each
+// lane owns 4 consecutive entries (one flags word); equal keys at the
+// threshold are ranked in index order.
+__device__ void warp_mark(const uint32_t *keys, int n, const RowSelect &r, uint8_t *flags, uint8_t bit) {
+  const int lane = threadIdx.x & 31;
+  const bool ranked = !r.whole && r.t.n_eq != r.t.take;
+  unsigned taken = 0;
+  for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
+    const int j = j0 + 4 * lane;
+    unsigned in = 0, eq = 0;  // bit e: entry j + e
+    if (j < n) {
+      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
+      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (kv[e] == 0u) continue;
+        const int bn = value_bin(kv[e], r.lo, r.inv);
+        if (bn > r.bstar || (bn == r.bstar && r.whole)) {
+          in |= 1u << e;
+        } else if (bn == r.bstar) {
+          const uint32_t top = kv[e] & r.t.pmask;
+          if (top > r.t.prefix) in |= 1u << e;
+          else if (top == r.t.prefix) eq |= 1u << e;
+        }
+      }
+    }
+    if (ranked) {
+      unsigned tot;
+      unsigned rank = taken + warp_exclusive_scan(__popc(eq), &tot);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((eq >> e) & 1u) {
+          if (rank < r.t.take) in |= 1u << e;
+          ++rank;
+        }
+      taken += tot;
+    } else {
+      in |= eq;
+    }
+    if (in != 0u) {
+      uint32_t *fw = reinterpret_cast<uint32_t *>(flags) + (j >> 2);
+      uint32_t w = *fw;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((in >> e) & 1u) w |= static_cast<uint32_t>(bit) << (8 * e);
+      *fw = w;
+    }
+  }
+}
+
+__device__ __forceinline__ void warp_minmax(float &lo, float &hi) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
   }
 }
 
@@ -389,11 +575,13 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
   const int i = nb - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
   if (i < 0) return;
   const int g = blockIdx.y, b = blockIdx.z;
-  // per warp: keys [nb] u32, hist [256] u32, flags [nb] u8 (nb % 4 == 0 keeps each 16-aligned)
+  // per warp: keys [nb] u32, hist [256] u32, ckeys [kCompact] u32, flags [nb] u8
+  // (nb % 4 == 0 keeps each 16-byte aligned)
   unsigned char *wbase = smem + static_cast<size_t>(warp) * select_warp_bytes(nb);
   uint32_t *keys = reinterpret_cast<uint32_t *>(wbase);
   unsigned *hist = reinterpret_cast<unsigned *>(wbase + static_cast<size_t>(nb) * 4);
-  uint8_t *flags = wbase + static_cast<size_t>(nb) * 4 + 1024;
+  uint32_t *ckeys = reinterpret_cast<uint32_t *>(wbase + static_cast<size_t>(nb) * 4 + 1024);
+  uint8_t *flags = wbase + static_cast<size_t>(nb) * 4 + 1024 + kCompact * 4;
 
   const size_t gb = static_cast<size_t>(b) * hkv + g;
   const size_t row = gb * nb + i;
@@ -401,22 +589,28 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
   const int n4 = (i + 4) & ~3;  // keys / flags [0, n4) cover 0..i; entries j >= i are never candidates
 
   // ---- centroid path: top kc of candidates 1..i-1 by S_c
+  float lo = INFINITY, hi = -INFINITY;
   {
     const float4 *rc = reinterpret_cast<const float4 *>(s_c + row * nb);
     for (int j4 = lane * 4; j4 < n4; j4 += 128) {
       const float4 v = rc[j4 >> 2];
       const float x[4] = {v.x, v.y, v.z, v.w};
-      uint4 kk;
-      uint32_t *kp = reinterpret_cast<uint32_t *>(&kk);
+      uint32_t kp[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = j4 + e;
-        kp[e] = (j >= 1 && j < i) ? score_key(x[e]) : 0u;
+        const bool cand = j >= 1 && j < i;
+        kp[e] = cand ? score_key(x[e]) : 0u;
+        if (cand) {
+          lo = fminf(lo, x[e]);
+          hi = fmaxf(hi, x[e]);
+        }
       }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = kk;
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
       reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
     }
   }
+  warp_minmax(lo, hi);
   __syncwarp();
   const int ncand = i > 1 ? i - 1 : 0;
   const long long kc_full = (ppm_c * (i + 1) + 999999LL) / 1000000LL;
@@ -424,13 +618,15 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
   if (kc == ncand) {
     for (int j = 1 + lane; j < i; j += 32) flags[j] = BSA_MASK_CENTROID;
   } else if (kc > 0) {
-    const Threshold t = warp_radix_threshold(keys, i, static_cast<unsigned>(kc), hist);
-    warp_mark(keys, i, t, flags, BSA_MASK_CENTROID);
+    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kc), lo, hi, hist, ckeys);
+    warp_mark(keys, i, r, flags, BSA_MASK_CENTROID);
   }
   __syncwarp();
 
   // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
   int nelig = 0;
+  lo = INFINITY;
+  hi = -INFINITY;
   {
     const float4 *rr = reinterpret_cast<const float4 *>(s_r + row * nb);
     for (int j4 = lane * 4; j4 < n4; j4 += 128) {
@@ -438,20 +634,24 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
       const float4 a = *reinterpret_cast<const float4 *>(ab + j4);
       const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
       const float x[4] = {v.x, v.y, v.z, v.w}, al[4] = {a.x, a.y, a.z, a.w};
-      uint4 kk;
-      uint32_t *kp = reinterpret_cast<uint32_t *>(&kk);
+      uint32_t kp[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = j4 + e;
         const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
         kp[e] = elig ? score_key(x[e]) : 0u;
         nelig += elig ? 1 : 0;
+        if (elig) {
+          lo = fminf(lo, x[e]);
+          hi = fmaxf(hi, x[e]);
+        }
       }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = kk;
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
     }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) nelig += __shfl_xor_sync(0xffffffffu, nelig, off);
+  warp_minmax(lo, hi);
   __syncwarp();
   const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
   const int kr = static_cast<int>(kr_full < nelig ? kr_full : nelig);
@@ -459,8 +659,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
     for (int j = lane; j < i; j += 32)
       if (keys[j] != 0u) flags[j] |= BSA_MASK_RESCUE;
   } else if (kr > 0) {
-    const Threshold t = warp_radix_threshold(keys, i, static_cast<unsigned>(kr), hist);
-    warp_mark(keys, i, t, flags, BSA_MASK_RESCUE);
+    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kr), lo, hi, hist, ckeys);
+    warp_mark(keys, i, r, flags, BSA_MASK_RESCUE);
   }
   __syncwarp();
   if (lane == 0) {
@@ -572,11 +772,16 @@ cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid
 
 cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
                              cudaStream_t stream) {
-  int npow2 = 1;
+  // E entries per thread, at most 1024 threads, and at least one full warp
+  const int e = s.nb > 2048 ? 4 : (s.nb > 1024 ? 2 : 1);
+  int npow2 = 32 * e;
   while (npow2 < s.nb) npow2 <<= 1;
+  const int threads = npow2 / e;
   dim3 grid(s.hkv, s.batch);
-  const int threads = npow2 < 1024 ? (npow2 < 32 ? 32 : npow2) : 1024;
-  quant_kernel<<<grid, threads, static_cast<size_t>(npow2) * 4, stream>>>(radius, quant, alpha, s.nb, npow2);
+  const size_t smem = static_cast<size_t>(npow2) * 4;
+  if (e == 4) quant_kernel<4><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
+  else if (e == 2) quant_kernel<2><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
+  else quant_kernel<1><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
   return cudaGetLastError();
 }
 
