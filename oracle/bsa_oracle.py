@@ -19,7 +19,12 @@ All arithmetic is float64 on the bf16-rounded inputs.
 Layouts: q [b, N, Hq, d], k and v [b, N, Hkv, d]; per-block tensors are
 [b, H, nb, ...]; masks are [b, Hkv, nb_q, nb_k] uint8 with bit 0 = forced
 (first or diagonal block), bit 1 = kept by the centroid path, bit 2 = kept by
-the rescue path.
+the rescue path.  N need not be a multiple of the block size: nb = ceil(N / B)
+and the last block holds the N - (nb - 1) B remaining tokens (reading: a
+partial block is summarised, ranked and attended over its own tokens only).
+Packed ragged batches ("varlen") hold sequence b in tokens
+cu_seqlens[b] .. cu_seqlens[b+1] - 1 of q [T, Hq, d], k and v [T, Hkv, d];
+each sequence is processed on its own, exactly like a batch of one.
 """
 from __future__ import annotations
 
@@ -43,11 +48,19 @@ def block_meta(k: np.ndarray, block: int):
     k: [b, N, Hkv, d].  Returns centroid [b, Hkv, nb, d], radius [b, Hkv, nb].
     """
     b, n, h, d = k.shape
-    nb = n // block
-    kb = np.asarray(k, dtype=np.float64).reshape(b, nb, block, h, d).transpose(0, 3, 1, 2, 4)
+    nfull = n // block
+    kf = np.asarray(k, dtype=np.float64)
+    kb = kf[:, :nfull * block].reshape(b, nfull, block, h, d).transpose(0, 3, 1, 2, 4)
     centroid = kb.mean(axis=3)
     dist = np.sqrt(np.sum((kb - centroid[:, :, :, None, :]) ** 2, axis=-1))
     radius = dist.max(axis=-1)
+    if n % block:
+        # partial last block: its own n - nfull * block keys
+        kt = kf[:, nfull * block:].transpose(0, 2, 1, 3)          # [b, Hkv, rest, d]
+        ct = kt.mean(axis=2)
+        rt = np.sqrt(np.sum((kt - ct[:, :, None, :]) ** 2, axis=-1)).max(axis=-1)
+        centroid = np.concatenate([centroid, ct[:, :, None, :]], axis=2)
+        radius = np.concatenate([radius, rt[:, :, None]], axis=2)
     return centroid, radius
 
 
@@ -103,10 +116,16 @@ def query_summary(q: np.ndarray, block: int):
     q: [b, N, Hq, d].  Returns qbar [b, Hq, nb, d], nbar [b, Hq, nb].
     """
     b, n, h, d = q.shape
-    nb = n // block
-    qb = np.asarray(q, dtype=np.float64).reshape(b, nb, block, h, d).transpose(0, 3, 1, 2, 4)
+    nfull = n // block
+    qf = np.asarray(q, dtype=np.float64)
+    qb = qf[:, :nfull * block].reshape(b, nfull, block, h, d).transpose(0, 3, 1, 2, 4)
     qbar = qb.mean(axis=3)
     nbar = np.sqrt(np.sum(qb * qb, axis=-1)).mean(axis=-1)
+    if n % block:
+        qt = qf[:, nfull * block:].transpose(0, 2, 1, 3)          # [b, Hq, rest, d]
+        qbar = np.concatenate([qbar, qt.mean(axis=2)[:, :, None, :]], axis=2)
+        nbar = np.concatenate([nbar, np.sqrt(np.sum(qt * qt, axis=-1)).mean(axis=-1)[:, :, None]],
+                              axis=2)
     return qbar, nbar
 
 
@@ -201,9 +220,15 @@ def select_blocks(q, k, block: int, centroid_keep: float, rescue_keep: float,
     """
     b, n, hq, d = q.shape
     hkv = k.shape[2]
-    nb = n // block
+    nb = -(-n // block)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if nb == 0:
+        z = np.zeros
+        return dict(centroid=z((b, hkv, 0, d)), radius=z((b, hkv, 0)), med=z((b, hkv)),
+                    p90=z((b, hkv)), alpha=z((b, hkv, 0)), qbar=z((b, hq, 0, d)),
+                    nbar=z((b, hq, 0)), mask=np.zeros((b, hkv, 0, 0), dtype=np.uint8), scale=scale,
+                    **({"scores": {}} if with_scores else {}))
     centroid, radius = block_meta(k, block)
     med, p90 = radius_quantiles(radius)
     alpha = rescue_coefficient(radius, med, p90)
@@ -283,7 +308,9 @@ def sparse_attention_rows(q, k, v, mask, block: int, rows, scale: float | None =
         g = h // grp
         kept = np.nonzero(mask[bi, g, i])[0]
         kpos = (kept[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+        kpos = kpos[kpos < n]                      # a partial last block has fewer keys
         qpos = i * block + np.arange(block)
+        qpos = qpos[qpos < n]
         qi = np.asarray(q[bi, qpos, h, :], dtype=np.float64)
         keys = np.asarray(k[bi, kpos, g, :], dtype=np.float64)
         vals = np.asarray(v[bi, kpos, g, :], dtype=np.float64)
@@ -294,7 +321,7 @@ def sparse_attention_rows(q, k, v, mask, block: int, rows, scale: float | None =
 def sparse_attention(q, k, v, mask, block: int, scale: float | None = None):
     """Full sparse attention.  Returns o [b, N, Hq, d], lse [b, Hq, N]."""
     b, n, hq, d = q.shape
-    nb = n // block
+    nb = -(-n // block)
     o = np.zeros((b, n, hq, d), dtype=np.float64)
     lse = np.zeros((b, hq, n), dtype=np.float64)
     rows = [(bi, h, i) for bi in range(b) for h in range(hq) for i in range(nb)]
@@ -326,4 +353,59 @@ def dense_attention(q, k, v, scale: float | None = None):
                              np.asarray(v[bi, :, g, :], dtype=np.float64), pos, pos, scale)
             o[bi, :, h, :] = oi
             lse[bi, h, :] = li
+    return o, lse
+
+
+# ------------------------------------------------------------ packed ragged batches
+
+def seq_bounds(cu_seqlens, b: int):
+    """Token range [start, end) of sequence b of a packed batch."""
+    return int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+
+
+def varlen_select_blocks(q, k, cu_seqlens, block: int, centroid_keep: float, rescue_keep: float,
+                         scale: float | None = None, with_scores: bool = False):
+    """Mask build of every sequence of a packed batch, each as a batch of one.
+
+    q: [T, Hq, d], k: [T, Hkv, d].  Returns a list with one ``select_blocks``
+    result per sequence (its arrays keep a leading batch dimension of 1).
+    """
+    out = []
+    for b in range(len(cu_seqlens) - 1):
+        s0, s1 = seq_bounds(cu_seqlens, b)
+        out.append(select_blocks(q[None, s0:s1], k[None, s0:s1], block, centroid_keep, rescue_keep,
+                                 scale, with_scores))
+    return out
+
+
+def varlen_attention_rows(q, k, v, cu_seqlens, masks, block: int, rows, scale: float | None = None):
+    """Sparse attention rows of a packed batch.
+
+    masks[b]: boolean-like [1, Hkv, nb_b, nb_b] for sequence b.  rows: iterable
+    of (b, h, i).  Returns {(b, h, i): (o [tokens of block i, d], lse)}.
+    """
+    out = {}
+    for (b, h, i) in rows:
+        s0, s1 = seq_bounds(cu_seqlens, b)
+        res = sparse_attention_rows(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], masks[b], block,
+                                    [(0, h, i)], scale)
+        out[(b, h, i)] = res[(0, h, i)]
+    return out
+
+
+def varlen_dense_attention(q, k, v, cu_seqlens, scale: float | None = None):
+    """Dense causal attention of every sequence of a packed batch.
+
+    Returns o [T, Hq, d] and lse [Hq, T].
+    """
+    t, hq, d = q.shape
+    o = np.zeros((t, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, t), dtype=np.float64)
+    for b in range(len(cu_seqlens) - 1):
+        s0, s1 = seq_bounds(cu_seqlens, b)
+        if s1 == s0:
+            continue
+        ob, lb = dense_attention(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], scale)
+        o[s0:s1] = ob[0]
+        lse[:, s0:s1] = lb[0]
     return o, lse

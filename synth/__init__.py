@@ -33,6 +33,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "workload", "sweep_workloads", "make_layer",
+    "VarlenWorkload", "VARLEN_WORKLOADS", "make_varlen_layer",
     "bf16_bits", "bf16_to_f64", "bf16_to_f32",
 ]
 
@@ -202,3 +203,84 @@ def make_layer(w: Workload, layer: int = 0, seed: int | None = None,
         "q": bf16_bits(q), "k": bf16_bits(k), "v": bf16_bits(v),
         "needles": needles, "seed": seed, "workload": w,
     }
+
+
+# ---------------------------------------------------------------- packed ragged batches
+
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of sequences of mixed lengths (any length, not only
+    multiples of the block), one shape of heads, block and ratios."""
+    name: str
+    lengths: tuple
+    hq: int
+    hkv: int
+    head_dim: int
+    block: int
+    centroid_keep: float
+    rescue_keep: float
+    seed_base: int = 0
+    needles_fixed: int | None = None
+
+    @property
+    def batch(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def total(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.lengths))
+
+    @property
+    def group(self) -> int:
+        return self.hq // self.hkv
+
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lengths)]).astype(np.int32)
+
+
+VARLEN_WORKLOADS = {
+    w.name: w for w in [
+        VarlenWorkload("varlen_h2x1_d64_b64", (1000, 64, 1, 130, 513, 0, 257), 2, 1, 64, 64,
+                       0.25, 0.05, seed_base=5000, needles_fixed=2),
+        VarlenWorkload("varlen_gqa32x4_d128_b128", (8192, 3000, 12345, 128, 700, 20001, 1),
+                       32, 4, 128, 128, 0.15, 0.03, seed_base=6000),
+        VarlenWorkload("varlen_gqa32x4_d128_b64", (4000, 2113, 65, 6000), 32, 4, 128, 64,
+                       0.15, 0.03, seed_base=7000),
+    ]
+}
+
+
+def make_varlen_layer(vw: VarlenWorkload, layer: int = 0, threads: int | None = None) -> dict:
+    """Draw one layer of a packed ragged batch.
+
+    Sequence b is drawn with the single-sequence recipe above at its length
+    rounded up to whole blocks (seed ``seed_base + 1000 * layer + b``), then
+    cut to its length; needle query positions past the cut are dropped.
+    Returns ``q``, ``k``, ``v`` (uint16 bf16 bits, [T, H, d]), ``cu_seqlens``
+    (int32 [batch + 1]) and ``needles`` as (b, g, key_block, key_slot, query
+    positions within the sequence).
+    """
+    qs, ks, vs, needles = [], [], [], []
+    for b, n in enumerate(vw.lengths):
+        if n == 0:
+            continue
+        padded = -(-n // vw.block) * vw.block
+        w = Workload(f"{vw.name}_seq{b}", 1, padded, vw.hq, vw.hkv, vw.head_dim, vw.block,
+                     vw.centroid_keep, vw.rescue_keep, needles_fixed=vw.needles_fixed)
+        lay = make_layer(w, seed=vw.seed_base + 1000 * layer + b, threads=threads)
+        qs.append(lay["q"][0, :n])
+        ks.append(lay["k"][0, :n])
+        vs.append(lay["v"][0, :n])
+        for (_, g, jb, slot, pos) in lay["needles"]:
+            pos = pos[pos < n]
+            if pos.size:
+                needles.append((b, g, jb, slot, pos))
+    d = vw.head_dim
+    cat = lambda xs, h: (np.ascontiguousarray(np.concatenate(xs, axis=0)) if xs
+                         else np.zeros((0, h, d), dtype=np.uint16))
+    return {"q": cat(qs, vw.hq), "k": cat(ks, vw.hkv), "v": cat(vs, vw.hkv),
+            "cu_seqlens": vw.cu_seqlens(), "needles": needles, "workload": vw}

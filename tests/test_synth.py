@@ -41,3 +41,21 @@ def test_named_workloads():
     assert (w.seq, w.hq, w.hkv, w.head_dim, w.block, w.nb, w.layers) == (131072, 32, 4, 128, 128, 1024, 48)
     assert w.needles_per_group() == 20
     assert len(synth.sweep_workloads()) == 27
+
+
+def test_varlen_layer_packs_truncated_sequences():
+    vw = synth.VARLEN_WORKLOADS["varlen_h2x1_d64_b64"]
+    lay = synth.make_varlen_layer(vw)
+    cu = lay["cu_seqlens"]
+    assert cu[0] == 0 and cu[-1] == vw.total == lay["q"].shape[0]
+    assert np.all(np.diff(cu) == np.array(vw.lengths))
+    again = synth.make_varlen_layer(vw, threads=1)
+    for x in ("q", "k", "v"):
+        np.testing.assert_array_equal(lay[x], again[x])
+    # sequence 4 (513 tokens) is the single-sequence draw at 576 tokens, cut to 513
+    w = synth.Workload("x", 1, 576, vw.hq, vw.hkv, vw.head_dim, vw.block, 0.25, 0.05,
+                       needles_fixed=vw.needles_fixed)
+    ref = synth.make_layer(w, seed=vw.seed_base + 4)
+    np.testing.assert_array_equal(lay["k"][cu[4]:cu[5]], ref["k"][0, :513])
+    for (b, g, jb, slot, pos) in lay["needles"]:
+        assert np.all(pos < vw.lengths[b]) and jb * vw.block + slot < vw.lengths[b]
