@@ -31,7 +31,14 @@ class SelectParams(ctypes.Structure):
                 ("flags", ctypes.c_int32)]
 
 
+class VarlenShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("max_seqlen", ctypes.c_int32), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block", ctypes.c_int32)]
+
+
 _SP = ctypes.POINTER(Shape)
+_VP = ctypes.POINTER(VarlenShape)
 _PP = ctypes.POINTER(SelectParams)
 
 SIGNATURES = {
@@ -46,6 +53,15 @@ SIGNATURES = {
     "bsa_prefill_layer": (ctypes.c_int, [_SP, _PP, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                          ctypes.c_size_t, _P, _P]),
     "bsa_prefill_layer_views": (ctypes.c_int, [_SP, ctypes.POINTER(ctypes.c_size_t)]),
+    "bsa_varlen_block_stride": (ctypes.c_int32, [_VP]),
+    "bsa_varlen_block_meta": (ctypes.c_int, [_VP, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "bsa_varlen_select_workspace_bytes": (ctypes.c_size_t, [_VP]),
+    "bsa_varlen_select_mask": (ctypes.c_int, [_VP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              ctypes.c_size_t, _P, _P]),
+    "bsa_varlen_prefill_fwd": (ctypes.c_int, [_VP, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                              _P, _P]),
+    "bsa_varlen_prefill_dense_fwd": (ctypes.c_int, [_VP, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                                    _P, _P]),
     "bsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bsa_version": (ctypes.c_int32, []),
 }

@@ -18,10 +18,14 @@ __all__ = [
     "Shape", "SelectParams", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
     "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
     "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
+    "VarlenShape", "make_varlen_shape", "varlen_block_stride", "varlen_block_meta",
+    "varlen_select_workspace_bytes", "varlen_select_mask", "varlen_prefill_fwd",
+    "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
 ]
 
 Shape = _lib.Shape
 SelectParams = _lib.SelectParams
+VarlenShape = _lib.VarlenShape
 
 
 def make_shape(batch: int, seq: int, hq: int, hkv: int, head_dim: int, block: int) -> Shape:
@@ -168,6 +172,108 @@ def alloc_select(shape: Shape, device="cuda", with_mask: bool = True) -> dict:
 
 def alloc_layer_workspace(shape: Shape, device="cuda") -> torch.Tensor:
     return torch.empty(prefill_layer_workspace_bytes(shape), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- packed ragged batches
+
+def make_varlen_shape(batch: int, total_tokens: int, max_seqlen: int, hq: int, hkv: int,
+                      head_dim: int, block: int) -> VarlenShape:
+    return VarlenShape(batch, total_tokens, max_seqlen, hq, hkv, head_dim, block)
+
+
+def varlen_block_stride(shape: VarlenShape) -> int:
+    """nbs: per-sequence stride of every per-block array (0 for an invalid shape)."""
+    return int(_lib.load().bsa_varlen_block_stride(ctypes.byref(shape)))
+
+
+def _vdims(s: VarlenShape):
+    nbs = varlen_block_stride(s)
+    if nbs == 0:
+        raise _lib.BsaError("bsa_varlen_block_stride", 2)
+    return s.batch, s.total_tokens, s.hq, s.hkv, s.head_dim, nbs
+
+
+def _cu(cu_seqlens, batch):
+    return _ptr(cu_seqlens, "cu_seqlens", torch.int32, batch + 1)
+
+
+def varlen_block_meta(shape: VarlenShape, cu_seqlens, k, centroid, radius, quant, alpha,
+                      dev_status=None, stream=None):
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_varlen_block_meta", lib.bsa_varlen_block_meta(
+        ctypes.byref(shape), _cu(cu_seqlens, b), _ptr(k, "k", torch.bfloat16, t * hkv * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * nbs * d),
+        _ptr(radius, "radius", torch.float32, b * hkv * nbs),
+        _ptr(quant, "quant", torch.float32, b * hkv * 2),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nbs),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def varlen_select_workspace_bytes(shape: VarlenShape) -> int:
+    return int(_lib.load().bsa_varlen_select_workspace_bytes(ctypes.byref(shape)))
+
+
+def varlen_select_mask(shape: VarlenShape, params: SelectParams, cu_seqlens, q, centroid, radius,
+                       alpha, kv_idx, kv_cnt, mask=None, workspace=None, dev_status=None,
+                       stream=None):
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(varlen_select_workspace_bytes(shape), dtype=torch.uint8,
+                                device=q.device)
+    _lib.check("bsa_varlen_select_mask", lib.bsa_varlen_select_mask(
+        ctypes.byref(shape), ctypes.byref(params), _cu(cu_seqlens, b),
+        _ptr(q, "q", torch.bfloat16, t * hq * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * nbs * d),
+        _ptr(radius, "radius", torch.float32, b * hkv * nbs),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nbs),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs * nbs),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nbs),
+        _ptr(mask, "mask", torch.uint8, b * hkv * nbs * nbs),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def varlen_prefill_fwd(shape: VarlenShape, cu_seqlens, q, k, v, kv_idx, kv_cnt, softmax_scale, o,
+                       lse=None, dev_status=None, stream=None):
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_varlen_prefill_fwd", lib.bsa_varlen_prefill_fwd(
+        ctypes.byref(shape), _cu(cu_seqlens, b), _ptr(q, "q", torch.bfloat16, t * hq * d),
+        _ptr(k, "k", torch.bfloat16, t * hkv * d), _ptr(v, "v", torch.bfloat16, t * hkv * d),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs * nbs),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nbs), ctypes.c_float(softmax_scale),
+        _ptr(o, "o", torch.bfloat16, t * hq * d), _ptr(lse, "lse", torch.float32, hq * t),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def varlen_prefill_dense_fwd(shape: VarlenShape, cu_seqlens, q, k, v, softmax_scale, o, lse=None,
+                             dev_status=None, stream=None):
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_varlen_prefill_dense_fwd", lib.bsa_varlen_prefill_dense_fwd(
+        ctypes.byref(shape), _cu(cu_seqlens, b), _ptr(q, "q", torch.bfloat16, t * hq * d),
+        _ptr(k, "k", torch.bfloat16, t * hkv * d), _ptr(v, "v", torch.bfloat16, t * hkv * d),
+        ctypes.c_float(softmax_scale), _ptr(o, "o", torch.bfloat16, t * hq * d),
+        _ptr(lse, "lse", torch.float32, hq * t),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def alloc_varlen_meta(shape: VarlenShape, device="cuda") -> dict:
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    f32 = dict(dtype=torch.float32, device=device)
+    return {"centroid": torch.empty(b, hkv, nbs, d, **f32), "radius": torch.empty(b, hkv, nbs, **f32),
+            "quant": torch.empty(b, hkv, 2, **f32), "alpha": torch.empty(b, hkv, nbs, **f32)}
+
+
+def alloc_varlen_select(shape: VarlenShape, device="cuda", with_mask: bool = True) -> dict:
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    out = {"kv_idx": torch.empty(b, hkv, nbs, nbs, dtype=torch.int32, device=device),
+           "kv_cnt": torch.empty(b, hkv, nbs, dtype=torch.int32, device=device)}
+    out["mask"] = (torch.empty(b, hkv, nbs, nbs, dtype=torch.uint8, device=device)
+                   if with_mask else None)
+    return out
 
 
 def status_string(code: int) -> str:

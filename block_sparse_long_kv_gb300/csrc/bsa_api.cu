@@ -12,33 +12,62 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shape checks shared by every entry point.
-bsa_status check_shape(const bsa_shape *s) {
-  if (s == nullptr) return BSA_ERR_INVALID_ARG;
-  if (s->batch < 1 || s->seq < 1 || s->hq < 1 || s->hkv < 1 || s->head_dim < 1 || s->block < 1)
-    return BSA_ERR_SHAPE;
-  if (s->seq % s->block != 0 || s->hq % s->hkv != 0) return BSA_ERR_SHAPE;
-  if (s->head_dim != 64 && s->head_dim != 128) return BSA_ERR_UNSUPPORTED;
-  if (s->block != 64 && s->block != 128 && s->block != 256) return BSA_ERR_UNSUPPORTED;
-  const int nb = s->seq / s->block;
-  if (nb % 4 != 0 || nb > bsa::kMaxBlocks) return BSA_ERR_UNSUPPORTED;
-  const long long grp = s->hq / s->hkv;
+// Checks shared by the fixed-length and the packed ragged shapes; nb is the
+// largest number of blocks of one sequence.
+bsa_status check_common(int batch, int hq, int hkv, int head_dim, int block, int nb) {
+  if (hq % hkv != 0) return BSA_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return BSA_ERR_UNSUPPORTED;
+  if (block != 64 && block != 128 && block != 256) return BSA_ERR_UNSUPPORTED;
+  if (nb > bsa::kMaxBlocks) return BSA_ERR_UNSUPPORTED;
+  const long long grp = hq / hkv;
   if (grp != 1 && grp != 2 && grp != 4 && grp != 8 && grp != 16) return BSA_ERR_UNSUPPORTED;
-  if (s->block == 64 && grp % 2 != 0) return BSA_ERR_UNSUPPORTED;
+  if (block == 64 && grp % 2 != 0) return BSA_ERR_UNSUPPORTED;
   // grid extents of the widest launch (attention: one CTA per query tile pair)
-  const long long items = static_cast<long long>(nb) * s->batch * s->hq;
+  const long long items = static_cast<long long>(nb) * batch * hq;
   if (items > (1ll << 30)) return BSA_ERR_UNSUPPORTED;
   return BSA_OK;
 }
 
-bsa::MaskShape mask_shape(const bsa_shape *s) {
-  return bsa::MaskShape{s->batch, s->seq, s->hq, s->hkv, s->head_dim, s->block,
-                        s->seq / s->block, s->hq / s->hkv};
+bsa_status check_shape(const bsa_shape *s) {
+  if (s == nullptr) return BSA_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->seq < 1 || s->hq < 1 || s->hkv < 1 || s->head_dim < 1 || s->block < 1)
+    return BSA_ERR_SHAPE;
+  if (s->seq % s->block != 0) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(s->batch) * s->seq > INT32_MAX) return BSA_ERR_UNSUPPORTED;
+  const int nb = s->seq / s->block;
+  if (nb % 4 != 0) return BSA_ERR_UNSUPPORTED;
+  return check_common(s->batch, s->hq, s->hkv, s->head_dim, s->block, nb);
 }
 
-bsa::AttnShape attn_shape(const bsa_shape *s) {
-  return bsa::AttnShape{s->batch, s->seq, s->hq, s->hkv, s->head_dim, s->block,
-                        s->seq / s->block, s->hq / s->hkv};
+bsa_status check_varlen(const bsa_varlen_shape *s, const int32_t *cu_seqlens) {
+  if (s == nullptr || cu_seqlens == nullptr) return BSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return BSA_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->total_tokens < 1 || s->max_seqlen < 1 || s->hq < 1 || s->hkv < 1 ||
+      s->head_dim < 1 || s->block < 1)
+    return BSA_ERR_SHAPE;
+  if (s->max_seqlen > s->total_tokens) return BSA_ERR_SHAPE;
+  const long long nb = (static_cast<long long>(s->max_seqlen) + s->block - 1) / s->block;
+  if (nb > bsa::kMaxBlocks) return BSA_ERR_UNSUPPORTED;
+  return check_common(s->batch, s->hq, s->hkv, s->head_dim, s->block, static_cast<int>(nb));
+}
+
+bsa::MaskShape mask_shape(const bsa_shape *s) {
+  const int nb = s->seq / s->block;
+  return bsa::MaskShape{s->batch, s->seq, s->hq, s->hkv, s->head_dim, s->block,
+                        nb, s->hq / s->hkv, nullptr, s->batch * s->seq, nb};
+}
+
+int varlen_blocks(const bsa_varlen_shape *s) { return (s->max_seqlen + s->block - 1) / s->block; }
+
+int varlen_stride(const bsa_varlen_shape *s) { return (varlen_blocks(s) + 3) / 4 * 4; }
+
+bsa::MaskShape mask_shape(const bsa_varlen_shape *s, const int32_t *cu) {
+  return bsa::MaskShape{s->batch, s->max_seqlen, s->hq, s->hkv, s->head_dim, s->block,
+                        varlen_blocks(s), s->hq / s->hkv, cu, s->total_tokens, varlen_stride(s)};
+}
+
+bsa::AttnShape attn_shape(const bsa::MaskShape &m) {
+  return bsa::AttnShape{m.batch, m.seq, m.hq, m.hkv, m.d, m.block, m.nb, m.group, m.cu, m.total, m.nbs};
 }
 
 bool ratio_ok(float r) { return r >= 0.f && r <= 1.f; }  // false for NaN
@@ -49,17 +78,88 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout of bsa_prefill_layer: centroid, radius, quant, alpha,
 // kv_idx, kv_cnt, select scratch, each 256-byte aligned.
-void layer_views(const bsa_shape *s, size_t off[7], size_t *total) {
-  const size_t b = s->batch, h = s->hkv, d = s->head_dim, nb = s->seq / s->block;
+void layer_views(const bsa::MaskShape &m, size_t off[7], size_t *total) {
+  const size_t b = m.batch, h = m.hkv, d = m.d, nb = m.nbs;
   const size_t sizes[7] = {b * h * d * nb * 4, b * h * nb * 4,      b * h * 2 * 4, b * h * nb * 4,
                            b * h * nb * nb * 4, b * h * nb * 4,
-                           bsa::select_workspace_bytes(mask_shape(s))};
+                           bsa::select_workspace_bytes(m)};
   size_t cur = 0;
   for (int x = 0; x < 7; ++x) {
     off[x] = cur;
     cur = round_up(cur + sizes[x], 256);
   }
   *total = cur;
+}
+
+bsa_status meta_impl(const bsa::MaskShape &ms, const void *k, float *centroid, float *radius,
+                     float *quant, float *alpha, int32_t *dev_status, bsa_stream_t stream) {
+  if (!k || !centroid || !radius || !quant || !alpha) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(centroid) || !aligned16(radius) || !aligned16(quant) ||
+      !aligned16(alpha))
+    return BSA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (bsa::launch_block_meta(ms, k, centroid, radius, dev_status, s) != cudaSuccess) return BSA_ERR_CUDA;
+  if (bsa::launch_quantiles(ms, radius, quant, alpha, dev_status, s) != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status select_impl(const bsa::MaskShape &ms, const bsa_select_params *params, const void *q,
+                       const float *centroid, const float *radius, const float *alpha,
+                       int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                       size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  if (!params || !q || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
+    return BSA_ERR_INVALID_ARG;
+  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
+    return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius) || !aligned16(alpha) ||
+      !aligned16(kv_idx) || !aligned16(kv_cnt) || (mask && !aligned16(mask)))
+    return BSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::select_workspace_bytes(ms))
+    return BSA_ERR_WORKSPACE;
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (bsa::launch_select(ms, q, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
+                         ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, workspace,
+                         dev_status, s) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status prefill_impl(const bsa::MaskShape &ms, const void *q, const void *k, const void *v,
+                        const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale, void *o,
+                        float *lse, int32_t *dev_status, bsa_stream_t stream) {
+  if (!q || !k || !v || !o) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && !aligned16(lse)) || (kv_idx && !aligned16(kv_idx)) ||
+      (kv_cnt && !aligned16(kv_cnt)))
+    return BSA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  cudaError_t ce = cudaSuccess;
+  return bsa::launch_attention(attn_shape(ms), q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse,
+                               dev_status, reinterpret_cast<cudaStream_t>(stream), &ce);
+}
+
+bsa_status layer_impl(const bsa::MaskShape &ms, const bsa_select_params *params, const void *q,
+                      const void *k, const void *v, float softmax_scale, void *o, float *lse,
+                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      bsa_stream_t stream) {
+  size_t off[7], total = 0;
+  layer_views(ms, off, &total);
+  if (!workspace || workspace_bytes < total) return BSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  float *centroid = reinterpret_cast<float *>(ws + off[0]);
+  float *radius = reinterpret_cast<float *>(ws + off[1]);
+  float *quant = reinterpret_cast<float *>(ws + off[2]);
+  float *alpha = reinterpret_cast<float *>(ws + off[3]);
+  int32_t *kv_idx = reinterpret_cast<int32_t *>(ws + off[4]);
+  int32_t *kv_cnt = reinterpret_cast<int32_t *>(ws + off[5]);
+  bsa_status r = meta_impl(ms, k, centroid, radius, quant, alpha, dev_status, stream);
+  if (r != BSA_OK) return r;
+  r = select_impl(ms, params, q, centroid, radius, alpha, kv_idx, kv_cnt, nullptr, ws + off[6],
+                  total - off[6], dev_status, stream);
+  if (r != BSA_OK) return r;
+  return prefill_impl(ms, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status, stream);
 }
 
 }  // namespace
@@ -83,18 +183,9 @@ int32_t bsa_version(void) { return 100; }
 
 bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid, float *radius,
                           float *quant, float *alpha, int32_t *dev_status, bsa_stream_t stream) {
-  (void)dev_status;  // the meta kernels have no waits
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
-  if (!k || !centroid || !radius || !quant || !alpha) return BSA_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(centroid) || !aligned16(radius) || !aligned16(quant) ||
-      !aligned16(alpha))
-    return BSA_ERR_INVALID_ARG;
-  const bsa::MaskShape ms = mask_shape(shape);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (bsa::launch_block_meta(ms, k, centroid, radius, s) != cudaSuccess) return BSA_ERR_CUDA;
-  if (bsa::launch_quantiles(ms, radius, quant, alpha, s) != cudaSuccess) return BSA_ERR_CUDA;
-  return BSA_OK;
+  return meta_impl(mask_shape(shape), k, centroid, radius, quant, alpha, dev_status, stream);
 }
 
 size_t bsa_select_workspace_bytes(const bsa_shape *shape) {
@@ -108,60 +199,33 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
                            size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
-  if (!params || !q || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
-    return BSA_ERR_INVALID_ARG;
-  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
-    return BSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius) || !aligned16(alpha) ||
-      !aligned16(kv_idx) || !aligned16(kv_cnt) || (mask && !aligned16(mask)))
-    return BSA_ERR_INVALID_ARG;
-  const bsa::MaskShape ms = mask_shape(shape);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::select_workspace_bytes(ms))
-    return BSA_ERR_WORKSPACE;
-  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(shape->head_dim)));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (bsa::launch_select(ms, q, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
-                         ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, workspace,
-                         dev_status, s) != cudaSuccess)
-    return BSA_ERR_CUDA;
-  return BSA_OK;
-}
-
-static bsa_status prefill_common(const bsa_shape *shape, const void *q, const void *k,
-                                 const void *v, const int32_t *kv_idx, const int32_t *kv_cnt,
-                                 float softmax_scale, void *o, float *lse, int32_t *dev_status,
-                                 bsa_stream_t stream) {
-  const bsa_status st = check_shape(shape);
-  if (st != BSA_OK) return st;
-  if (!q || !k || !v || !o) return BSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      (lse && !aligned16(lse)) || (kv_idx && !aligned16(kv_idx)) ||
-      (kv_cnt && !aligned16(kv_cnt)))
-    return BSA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BSA_ERR_INVALID_ARG;
-  cudaError_t ce = cudaSuccess;
-  return bsa::launch_attention(attn_shape(shape), q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse,
-                               dev_status, reinterpret_cast<cudaStream_t>(stream), &ce);
+  return select_impl(mask_shape(shape), params, q, centroid, radius, alpha, kv_idx, kv_cnt, mask,
+                     workspace, workspace_bytes, dev_status, stream);
 }
 
 bsa_status bsa_prefill_fwd(const bsa_shape *shape, const void *q, const void *k, const void *v,
                            const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale,
                            void *o, float *lse, int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
   if (!kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
-  return prefill_common(shape, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status, stream);
+  return prefill_impl(mask_shape(shape), q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status,
+                      stream);
 }
 
 bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const void *k,
                                  const void *v, float softmax_scale, void *o, float *lse,
                                  int32_t *dev_status, bsa_stream_t stream) {
-  return prefill_common(shape, q, k, v, nullptr, nullptr, softmax_scale, o, lse, dev_status,
-                        stream);
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  return prefill_impl(mask_shape(shape), q, k, v, nullptr, nullptr, softmax_scale, o, lse,
+                      dev_status, stream);
 }
 
 size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape) {
   if (check_shape(shape) != BSA_OK) return 0;
   size_t off[7], total = 0;
-  layer_views(shape, off, &total);
+  layer_views(mask_shape(shape), off, &total);
   return total;
 }
 
@@ -170,7 +234,7 @@ bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets) {
   if (st != BSA_OK) return st;
   if (!offsets) return BSA_ERR_INVALID_ARG;
   size_t off[7], total = 0;
-  layer_views(shape, off, &total);
+  layer_views(mask_shape(shape), off, &total);
   for (int x = 0; x < 6; ++x) offsets[x] = off[x];
   return BSA_OK;
 }
@@ -181,24 +245,66 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
                              int32_t *dev_status, bsa_stream_t stream) {
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
-  size_t off[7], total = 0;
-  layer_views(shape, off, &total);
-  if (!workspace || workspace_bytes < total) return BSA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_WORKSPACE;
-  char *ws = static_cast<char *>(workspace);
-  float *centroid = reinterpret_cast<float *>(ws + off[0]);
-  float *radius = reinterpret_cast<float *>(ws + off[1]);
-  float *quant = reinterpret_cast<float *>(ws + off[2]);
-  float *alpha = reinterpret_cast<float *>(ws + off[3]);
-  int32_t *kv_idx = reinterpret_cast<int32_t *>(ws + off[4]);
-  int32_t *kv_cnt = reinterpret_cast<int32_t *>(ws + off[5]);
-  bsa_status r = bsa_block_meta(shape, k, centroid, radius, quant, alpha, dev_status, stream);
-  if (r != BSA_OK) return r;
-  r = bsa_select_mask(shape, params, q, centroid, radius, alpha, kv_idx, kv_cnt, nullptr,
-                      ws + off[6], total - off[6], dev_status, stream);
-  if (r != BSA_OK) return r;
-  return bsa_prefill_fwd(shape, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status,
-                         stream);
+  return layer_impl(mask_shape(shape), params, q, k, v, softmax_scale, o, lse, workspace,
+                    workspace_bytes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------- packed ragged batches
+
+int32_t bsa_varlen_block_stride(const bsa_varlen_shape *shape) {
+  if (shape == nullptr) return 0;
+  static const int32_t probe = 0;  // any aligned non-null pointer: only the shape is checked
+  if (check_varlen(shape, &probe) != BSA_OK) return 0;
+  return varlen_stride(shape);
+}
+
+bsa_status bsa_varlen_block_meta(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                 const void *k, float *centroid, float *radius, float *quant,
+                                 float *alpha, int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  return meta_impl(mask_shape(shape, cu_seqlens), k, centroid, radius, quant, alpha, dev_status,
+                   stream);
+}
+
+size_t bsa_varlen_select_workspace_bytes(const bsa_varlen_shape *shape) {
+  static const int32_t probe = 0;
+  if (check_varlen(shape, &probe) != BSA_OK) return 0;
+  return bsa::select_workspace_bytes(mask_shape(shape, &probe));
+}
+
+bsa_status bsa_varlen_select_mask(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                                  const int32_t *cu_seqlens, const void *q, const float *centroid,
+                                  const float *radius, const float *alpha, int32_t *kv_idx,
+                                  int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status,
+                                  bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  return select_impl(mask_shape(shape, cu_seqlens), params, q, centroid, radius, alpha, kv_idx,
+                     kv_cnt, mask, workspace, workspace_bytes, dev_status, stream);
+}
+
+bsa_status bsa_varlen_prefill_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                  const void *q, const void *k, const void *v,
+                                  const int32_t *kv_idx, const int32_t *kv_cnt,
+                                  float softmax_scale, void *o, float *lse, int32_t *dev_status,
+                                  bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  if (!kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
+  return prefill_impl(mask_shape(shape, cu_seqlens), q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse,
+                      dev_status, stream);
+}
+
+bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                        const void *q, const void *k, const void *v,
+                                        float softmax_scale, void *o, float *lse,
+                                        int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  return prefill_impl(mask_shape(shape, cu_seqlens), q, k, v, nullptr, nullptr, softmax_scale, o,
+                      lse, dev_status, stream);
 }
 
 }  // extern "C"

@@ -49,12 +49,14 @@ constexpr uint64_t kWaitTimeoutNs = 4000000000ull;   // 4 s: no legitimate wait 
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 0.2 s per in-flight copy on abort
 
 struct AttnParams {
-  const int32_t *kv_idx;  // [b, hkv, nb, nb] (sparse) or null (dense)
-  const int32_t *kv_cnt;  // [b, hkv, nb]
-  uint16_t *o;            // bf16 [b, seq, hq, d]
-  float *lse;             // [b, hq, seq] or null
+  const int32_t *kv_idx;  // [b, hkv, nbs, nbs] (sparse) or null (dense)
+  const int32_t *kv_cnt;  // [b, hkv, nbs]
+  uint16_t *o;            // bf16 [total, hq, d] (= [b, seq, hq, d] when fixed-length)
+  float *lse;             // [b, hq, seq] (fixed-length) or [hq, total] (packed), or null
   int32_t *dev_status;    // nullable
-  int batch, seq, hq, hkv, nb, group;
+  const int32_t *cu;      // packed ragged batch: sequence b is tokens cu[b] .. cu[b+1]-1; or null
+  int batch, seq, hq, hkv, nb, group;  // seq: fixed length, or max_seqlen when packed
+  int total, nbs;         // tokens in q / k / v / o; per-sequence stride of per-block arrays
   float scale_log2;       // softmax scale * log2(e)
 };
 
@@ -177,8 +179,10 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
   item /= p.batch;
   const int qs = item % C::NQS;
   const int i = p.nb - 1 - item / C::NQS;
-  const int qtok0 = i * BLK + qs * 128;  // first query token of the CTA's tiles
-  const size_t row = (static_cast<size_t>(b) * p.hkv + g) * p.nb + i;
+  const int qtok0 = i * BLK + qs * 128;  // first query token of the CTA's tiles (in its sequence)
+  const SeqSpan sp = seq_span(p.cu, b, p.seq, p.total, p.dev_status);
+  if (qtok0 >= sp.len) return;           // past the end of a shorter sequence: no rows
+  const size_t row = (static_cast<size_t>(b) * p.hkv + g) * p.nbs + i;
   int cnt;
   if constexpr (DENSE) {
     cnt = i + 1;
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
     cnt = p.kv_cnt[row];
     cnt = cnt < 0 ? 0 : (cnt > i + 1 ? i + 1 : cnt);
   }
-  const int32_t *kvrow = DENSE ? nullptr : p.kv_idx + row * p.nb;
+  const int32_t *kvrow = DENSE ? nullptr : p.kv_idx + row * p.nbs;
   // the diagonal block of the first half of a 256-row block has an all-masked second key tile
   const int T = cnt * C::SUB - ((C::NQS == 2 && qs == 0 && cnt > 0) ? 1 : 0);
   auto key_block = [&](int n) -> int { return DENSE ? n / C::SUB : __ldg(kvrow + n / C::SUB); };
@@ -223,22 +227,23 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       for (int t = 0; t < NT; ++t) {
         const int h0 = g * p.group + (hp * NT + t) * C::QH;
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * 64, h0, qtok0, b);
+          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * 64, h0,
+                           sp.start + qtok0, 0);
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
       for (int n = 0; n < T; ++n) {
-        const int ktok0 = key_block(n) * BLK + (n % C::SUB) * C::KT;
+        const int ktok0 = sp.start + key_block(n) * BLK + (n % C::SUB) * C::KT;
         const int ks = n % C::KS, ku = n / C::KS;
         if (ku > 0 && !wait_bar(bar(C::B_KE + ks), (ku - 1) & 1, ctl)) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sK + ks * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * 64, g, ktok0, b);
+          ptx::tma_load_4d(sK + ks * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * 64, g, ktok0, 0);
         k_issued = n + 1;
         const int vs = n % C::VS, vu = n / C::VS;
         if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g, ktok0, b);
+          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g, ktok0, 0);
         v_issued = n + 1;
       }
       if (*abort_flag) {
@@ -440,7 +445,8 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       l = lsh[r] + lsh[128 + r];
     }
     const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-    uint16_t *orow = p.o + ((static_cast<size_t>(b) * p.seq + qtok) * p.hq + head) * D + hf * OD_COLS;
+    const bool row_valid = qtok < sp.len;  // a partial last block's tile rows past the sequence end
+    uint16_t *orow = p.o + ((static_cast<size_t>(sp.start) + qtok) * p.hq + head) * D + hf * OD_COLS;
 #pragma unroll
     for (int c = 0; c < OD_COLS / 32; ++c) {
       uint32_t ov[32];
@@ -456,12 +462,17 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       for (int e = 0; e < 16; ++e)
         pk[e] = ptx::pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
       uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+      if (row_valid) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
     }
-    if (p.lse != nullptr && hf == 0) {
+    if (p.lse != nullptr && hf == 0 && row_valid) {
       const float lse = (ok && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      p.lse[(static_cast<size_t>(b) * p.hq + head) * p.seq + qtok] = lse;
+      const size_t at = p.cu == nullptr
+                            ? (static_cast<size_t>(b) * p.hq + head) * p.seq + qtok
+                            : static_cast<size_t>(head) * p.total + sp.start + qtok;
+      p.lse[at] = lse;
     }
   }
 
@@ -502,10 +513,11 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
     *cerr = e == cudaSuccess ? cudaErrorNotSupported : e;
     return BSA_ERR_CUDA;
   }
+  // one token axis over the whole batch: sequence b starts at token b * seq, or at cu[b] when packed
   CUtensorMap mq, mk, mv;
-  if (!make_map(fn, &mq, q, s.batch, s.seq, s.hq, D, C::QH, C::QTOK) ||
-      !make_map(fn, &mk, k, s.batch, s.seq, s.hkv, D, 1, C::KT) ||
-      !make_map(fn, &mv, v, s.batch, s.seq, s.hkv, D, 1, C::KT)) {
+  if (!make_map(fn, &mq, q, 1, s.total, s.hq, D, C::QH, C::QTOK) ||
+      !make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KT) ||
+      !make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT)) {
     *cerr = cudaErrorInvalidValue;
     return BSA_ERR_CUDA;
   }
@@ -584,12 +596,15 @@ bsa_status launch_attention(const AttnShape &s, const void *q, const void *k, co
   prm.o = static_cast<uint16_t *>(o);
   prm.lse = lse;
   prm.dev_status = dev_status;
+  prm.cu = s.cu;
   prm.batch = s.batch;
   prm.seq = s.seq;
   prm.hq = s.hq;
   prm.hkv = s.hkv;
   prm.nb = s.nb;
   prm.group = s.group;
+  prm.total = s.total;
+  prm.nbs = s.nbs;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   const bool dense = kv_idx == nullptr;
   if (s.d == 64)

@@ -11,18 +11,45 @@ namespace bsa {
 
 constexpr int kMaxBlocks = 4096;  // nb limit (select kernel keeps one score row in smem)
 
+// A batch is either fixed-length (cu == nullptr: sequence b is tokens
+// b*seq .. b*seq+seq-1) or packed ragged (sequence b is tokens cu[b] ..
+// cu[b+1]-1 of `total`, each at most `seq` = max_seqlen long).  nb is the
+// largest block count of a sequence, nbs the per-sequence stride of every
+// per-block array (nb rounded up to a multiple of 4; equal to nb when fixed).
 struct MaskShape {
   int batch, seq, hq, hkv, d, block, nb, group;
+  const int32_t *cu;
+  int total, nbs;
 };
 
-// Block meta: centroid [b, hkv, nb, d], radius [b, hkv, nb].
+// Token span of sequence b.  Packed entries are checked against total and
+// max_seqlen: an inconsistent one records BSA_ERR_INVALID_ARG (if status is
+// set) and reads as an empty sequence, so no kernel touches memory outside
+// the caller's buffers.
+struct SeqSpan {
+  int start, len;
+};
+
+__device__ __forceinline__ SeqSpan seq_span(const int32_t *cu, int b, int seq, int total,
+                                            int32_t *status) {
+  if (cu == nullptr) return SeqSpan{b * seq, seq};
+  const int s0 = __ldg(cu + b), s1 = __ldg(cu + b + 1);
+  if (s0 < 0 || s1 < s0 || s1 > total || s1 - s0 > seq) {
+    if (status != nullptr) atomicCAS(status, 0, static_cast<int32_t>(BSA_ERR_INVALID_ARG));
+    return SeqSpan{0, 0};
+  }
+  return SeqSpan{s0, s1 - s0};
+}
+
+// Block meta: centroid [b, hkv, nbs, d], radius [b, hkv, nbs] (zero past a sequence's blocks).
 cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
-                              cudaStream_t stream);
-// Quantiles [b, hkv, 2] and alpha [b, hkv, nb] from radius.
+                              int32_t *status, cudaStream_t stream);
+// Quantiles [b, hkv, 2] and alpha [b, hkv, nbs] from radius.
 cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
-                             cudaStream_t stream);
-// Bytes of select workspace: mean query [b, hkv, nb, G, d], mean query norm [b, hkv, nb, G]
-// and the two score matrices [b, hkv, nb, nb], all fp32.
+                             int32_t *status, cudaStream_t stream);
+// Bytes of select workspace: tf32 splits of the mean queries [b, hkv, nbs, G, d] and of the
+// centroids [b, hkv, nbs, d], mean query norms [b, hkv, nbs, G] and the two score matrices
+// [b, hkv, nbs, nbs], all fp32.
 size_t select_workspace_bytes(const MaskShape &s);
 // Query pooling into the workspace, tensor-core block scores, then top-k + list emission.
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
@@ -48,6 +75,8 @@ cudaError_t launch_scores(const MaskShape &s, const ScoreOperands &op, float sca
 
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;
+  const int32_t *cu;  // packed ragged batch (o [total, hq, d], lse [hq, total]) or null
+  int total, nbs;
 };
 
 // Sparse (kv_idx != nullptr) or dense (kv_idx == nullptr) causal attention.

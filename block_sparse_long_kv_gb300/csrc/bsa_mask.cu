@@ -51,11 +51,16 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float f[8]) {
 // the centroid (lane shuffles, then 8 warp partials in a fixed order); pass 2
 // takes each token's squared distance to it from the same registers, so K is
 // read from HBM once and never staged in shared memory.
+// A partial last block (a packed sequence whose length is not a multiple of
+// BLK) averages over its own tokens; CTAs past a sequence's last block write
+// zeros.
 template <int D, int BLK>
 __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_kernel(const uint16_t *__restrict__ k,
                                                         float *__restrict__ centroid,
-                                                        float *__restrict__ radius, int seq,
-                                                        int hkv, int nb) {
+                                                        float *__restrict__ radius,
+                                                        const int32_t *__restrict__ cu, int seq,
+                                                        int total, int hkv, int nbs,
+                                                        int32_t *status) {
   constexpr int VPR = D / 8;          // 16-byte vectors per key row
   constexpr int TL = kThreads / VPR;  // token lanes
   constexpr int TPT = BLK / TL;       // tokens per thread
@@ -68,13 +73,23 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
   const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int v = tid % VPR, u = tid / VPR;
+  const SeqSpan sp = seq_span(cu, b, seq, total, status);
+  const size_t ob = (static_cast<size_t>(b) * hkv + g) * nbs + j;
+  const int cnt = min(BLK, sp.len - j * BLK);  // keys in this block
+  if (cnt <= 0) {
+    if (tid < D) centroid[ob * D + tid] = 0.f;
+    if (tid == 0) radius[ob] = 0.f;
+    return;
+  }
   const size_t tok_stride = static_cast<size_t>(hkv) * D;
-  const uint16_t *base = k + (static_cast<size_t>(b) * seq + static_cast<size_t>(j) * BLK + u) * tok_stride +
+  const uint16_t *base = k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * BLK + u) * tok_stride +
                          static_cast<size_t>(g) * D + v * 8;
   uint4 raw[TPT];
 #pragma unroll
   for (int r = 0; r < TPT; ++r)
-    raw[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride));
+    raw[r] = (r * TL + u < cnt)
+                 ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride))
+                 : make_uint4(0u, 0u, 0u, 0u);
 
   // ---- pass 1: centroid
   float s[8];
@@ -101,9 +116,9 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     float c = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) c += part[w][tid];
-    c *= 1.f / static_cast<float>(BLK);  // exact: BLK is a power of two
+    c /= static_cast<float>(cnt);
     sc[tid] = c;
-    centroid[((static_cast<size_t>(b) * hkv + g) * nb + j) * D + tid] = c;
+    centroid[ob * D + tid] = c;
   }
   __syncthreads();
 
@@ -128,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     }
 #pragma unroll
     for (int off = 1; off < VPR; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    best = fmaxf(best, acc);
+    if (r * TL + u < cnt) best = fmaxf(best, acc);
   }
 #pragma unroll
   for (int off = VPR; off < 32; off <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
@@ -138,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     float m = wmax[0];
 #pragma unroll
     for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
-    radius[(static_cast<size_t>(b) * hkv + g) * nb + j] = sqrtf(m);
+    radius[ob] = sqrtf(m);
   }
 }
 
@@ -152,12 +167,25 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
 template <int E>
 __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ radius,
                                                      float *__restrict__ quant,
-                                                     float *__restrict__ alpha, int nb, int npow2) {
+                                                     float *__restrict__ alpha,
+                                                     const int32_t *__restrict__ cu, int seq,
+                                                     int total, int block, int nbs, int npow2,
+                                                     int32_t *status) {
   extern __shared__ float sr[];
   __shared__ float sq[2];
   const int g = blockIdx.x, b = blockIdx.y, hkv = gridDim.x;
   const int tid = threadIdx.x;
-  const size_t base = (static_cast<size_t>(b) * hkv + g) * nb;
+  const size_t base = (static_cast<size_t>(b) * hkv + g) * nbs;
+  const SeqSpan sp = seq_span(cu, b, seq, total, status);
+  const int nb = (sp.len + block - 1) / block;  // this sequence's blocks
+  for (int j = nb + tid; j < nbs; j += blockDim.x) alpha[base + j] = 0.f;
+  if (nb == 0) {
+    if (tid == 0) {
+      quant[(static_cast<size_t>(b) * hkv + g) * 2 + 0] = 0.f;
+      quant[(static_cast<size_t>(b) * hkv + g) * 2 + 1] = 0.f;
+    }
+    return;
+  }
   float x[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -245,16 +273,18 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
                                                          float *__restrict__ nbar,
                                                          const float *__restrict__ centroid,
                                                          float *__restrict__ c_hi,
-                                                         float *__restrict__ c_lo, int seq,
-                                                         int hq, int hkv, int block, int nb,
-                                                         int hpc, int nhc) {
+                                                         float *__restrict__ c_lo,
+                                                         const int32_t *__restrict__ cu, int seq,
+                                                         int total, int hq, int hkv, int block,
+                                                         int nbs, int hpc, int nhc,
+                                                         int32_t *status) {
   constexpr int VH = D / 8;  // lanes per head
   const int i = blockIdx.x, hc = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   if (hc == nhc) {
     for (int e = tid; e < hkv * D; e += blockDim.x) {
       const int g = e / D, x = e - g * D;
-      const size_t o = ((static_cast<size_t>(b) * hkv + g) * nb + i) * D + x;
+      const size_t o = ((static_cast<size_t>(b) * hkv + g) * nbs + i) * D + x;
       const float v = centroid[o], h = tf32_hi(v);
       c_hi[o] = h;
       c_lo[o] = v - h;
@@ -263,8 +293,20 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
   }
   const int hl = tid / VH, xv = tid - hl * VH;
   const int h = hc * hpc + hl;
+  const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
+  const size_t row = (static_cast<size_t>(b) * hkv + g) * nbs + i;
+  const size_t qo = (row * grp + hh) * D + xv * 8;
+  const SeqSpan sp = seq_span(cu, b, seq, total, status);
+  const int cnt = min(block, sp.len - i * block);  // queries in this block
+  if (cnt <= 0) {  // past the sequence's last block: zero rows
+    float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
+    float4 *ql = reinterpret_cast<float4 *>(q_lo + qo);
+    qh[0] = qh[1] = ql[0] = ql[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (xv == 0) nbar[row * grp + hh] = 0.f;
+    return;
+  }
   const size_t tok_stride = static_cast<size_t>(hq) * D;
-  const uint16_t *base = q + (static_cast<size_t>(b) * seq + static_cast<size_t>(i) * block) * tok_stride +
+  const uint16_t *base = q + (static_cast<size_t>(sp.start) + static_cast<size_t>(i) * block) * tok_stride +
                          static_cast<size_t>(h) * D + xv * 8;
   // lanes present in this warp (the last warp may be partial); a head's lanes never straddle warps
   const int present = min(32, static_cast<int>(blockDim.x) - (tid & ~31));
@@ -273,11 +315,13 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   float nsum = 0.f;
-  for (int t0 = 0; t0 < block; t0 += 8) {
+  for (int t0 = 0; t0 < cnt; t0 += 8) {
     uint4 u[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
-      u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride));
+      u[r] = (t0 + r < cnt)
+                 ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride))
+                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       float f[8];
@@ -293,14 +337,11 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
       nsum += sqrtf(sq);
     }
   }
-  const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
-  const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
-  const size_t qo = (row * grp + hh) * D + xv * 8;
-  const float inv_b = 1.f / static_cast<float>(block);  // exact: block is a power of two
+  const float fc = static_cast<float>(cnt);
   float m[8], hi[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    m[e] = acc[e] * inv_b;
+    m[e] = acc[e] / fc;
     hi[e] = tf32_hi(m[e]);
   }
   float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
@@ -309,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
   qh[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
   ql[0] = make_float4(m[0] - hi[0], m[1] - hi[1], m[2] - hi[2], m[3] - hi[3]);
   ql[1] = make_float4(m[4] - hi[4], m[5] - hi[5], m[6] - hi[6], m[7] - hi[7]);
-  if (xv == 0) nbar[row * grp + hh] = nsum * inv_b;
+  if (xv == 0) nbar[row * grp + hh] = nsum / fc;
 }
 
 // ---------------------------------------------------------------- select
@@ -568,13 +609,27 @@ __device__ __forceinline__ void warp_minmax(float &lo, float &hi) {
 // the forced sink and diagonal blocks and writes the ascending kept list.
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
     const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
-    int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask, int hkv,
-    int nb, long long ppm_c, long long ppm_r) {
+    int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask,
+    const int32_t *__restrict__ cu, int seq, int total, int block, int hkv, int nb,
+    long long ppm_c, long long ppm_r, int32_t *status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = nb - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
   if (i < 0) return;
   const int g = blockIdx.y, b = blockIdx.z;
+  {
+    // rows past the sequence's last block: empty list, zero mask row
+    const SeqSpan sp = seq_span(cu, b, seq, total, status);
+    if (i >= (sp.len + block - 1) / block) {
+      const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
+      if (lane == 0) kv_cnt[row] = 0;
+      if (mask != nullptr) {
+        uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nb));
+        for (int j4 = lane * 4; j4 < nb; j4 += 128) mrow[j4 >> 2] = 0u;
+      }
+      return;
+    }
+  }
   // per warp: keys [nb] u32, hist [256] u32, ckeys [kCompact] u32, flags [nb] u8
   // (nb % 4 == 0 keeps each 16-byte aligned)
   unsigned char *wbase = smem + static_cast<size_t>(warp) * select_warp_bytes(nb);
@@ -672,15 +727,15 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
   // ---- emit the ascending kept list of row i and the optional mask row
   int32_t *dst = kv_idx + row * static_cast<size_t>(nb);
   const unsigned lt = (1u << lane) - 1u;
-  int total = 0;
+  int kept = 0;
   for (int j0 = 0; j0 <= i; j0 += 32) {
     const int j = j0 + lane;
     const bool keep = j <= i && flags[j] != 0;
     const unsigned bl = __ballot_sync(0xffffffffu, keep);
-    if (keep) dst[total + __popc(bl & lt)] = j;
-    total += __popc(bl);
+    if (keep) dst[kept + __popc(bl & lt)] = j;
+    kept += __popc(bl);
   }
-  if (lane == 0) kv_cnt[row] = total;
+  if (lane == 0) kv_cnt[row] = kept;
   if (mask != nullptr) {
     uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nb));
     for (int j4 = lane * 4; j4 < nb; j4 += 128) {
@@ -696,20 +751,20 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
 
 template <int D, int BLK>
 cudaError_t launch_meta_t(const MaskShape &s, const void *k, float *centroid, float *radius,
-                          cudaStream_t stream) {
-  dim3 grid(s.nb, s.hkv, s.batch);
+                          int32_t *status, cudaStream_t stream) {
+  dim3 grid(s.nbs, s.hkv, s.batch);
   meta_kernel<D, BLK><<<grid, kThreads, 0, stream>>>(static_cast<const uint16_t *>(k), centroid, radius,
-                                                     s.seq, s.hkv, s.nb);
+                                                     s.cu, s.seq, s.total, s.hkv, s.nbs, status);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, float *radius,
-                          cudaStream_t stream) {
+                          int32_t *status, cudaStream_t stream) {
   switch (s.block) {
-    case 64: return launch_meta_t<D, 64>(s, k, centroid, radius, stream);
-    case 128: return launch_meta_t<D, 128>(s, k, centroid, radius, stream);
-    case 256: return launch_meta_t<D, 256>(s, k, centroid, radius, stream);
+    case 64: return launch_meta_t<D, 64>(s, k, centroid, radius, status, stream);
+    case 128: return launch_meta_t<D, 128>(s, k, centroid, radius, status, stream);
+    case 256: return launch_meta_t<D, 256>(s, k, centroid, radius, status, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -724,13 +779,14 @@ int qpool_heads(int hq, int d) {
 
 template <int D>
 cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *q_hi, float *q_lo, float *nbar,
-                           const float *centroid, float *c_hi, float *c_lo, cudaStream_t stream) {
+                           const float *centroid, float *c_hi, float *c_lo, int32_t *status,
+                           cudaStream_t stream) {
   const int hpc = qpool_heads(s.hq, D);
   const int nhc = s.hq / hpc;
-  dim3 grid(s.nb, nhc + 1, s.batch);
+  dim3 grid(s.nbs, nhc + 1, s.batch);
   qpool_kernel<D><<<grid, hpc * (D / 8), 0, stream>>>(static_cast<const uint16_t *>(q), q_hi, q_lo,
-                                                      nbar, centroid, c_hi, c_lo, s.seq, s.hq, s.hkv,
-                                                      s.block, s.nb, hpc, nhc);
+                                                      nbar, centroid, c_hi, c_lo, s.cu, s.seq, s.total,
+                                                      s.hq, s.hkv, s.block, s.nbs, hpc, nhc, status);
   return cudaGetLastError();
 }
 
@@ -745,10 +801,10 @@ struct SelectRegions {
 };
 
 SelectRegions select_regions(const MaskShape &s) {
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nb;  // (b, g, i, h) rows
-  const size_t blocks = static_cast<size_t>(s.batch) * s.hkv * s.nb;
+  const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nbs;  // (b, g, i, h) rows
+  const size_t blocks = static_cast<size_t>(s.batch) * s.hkv * s.nbs;
   const size_t sizes[7] = {rows * s.d * 4, rows * s.d * 4, rows * 4, blocks * s.d * 4, blocks * s.d * 4,
-                           blocks * s.nb * 4, blocks * s.nb * 4};
+                           blocks * s.nbs * 4, blocks * s.nbs * 4};
   SelectRegions r{};
   size_t at = 0;
   for (int x = 0; x < 7; ++x) {
@@ -764,14 +820,14 @@ SelectRegions select_regions(const MaskShape &s) {
 size_t select_workspace_bytes(const MaskShape &s) { return select_regions(s).total; }
 
 cudaError_t launch_block_meta(const MaskShape &s, const void *k, float *centroid, float *radius,
-                              cudaStream_t stream) {
-  if (s.d == 64) return launch_meta_d<64>(s, k, centroid, radius, stream);
-  if (s.d == 128) return launch_meta_d<128>(s, k, centroid, radius, stream);
+                              int32_t *status, cudaStream_t stream) {
+  if (s.d == 64) return launch_meta_d<64>(s, k, centroid, radius, status, stream);
+  if (s.d == 128) return launch_meta_d<128>(s, k, centroid, radius, status, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *quant, float *alpha,
-                             cudaStream_t stream) {
+                             int32_t *status, cudaStream_t stream) {
   // E entries per thread, at most 1024 threads, and at least one full warp
   const int e = s.nb > 2048 ? 4 : (s.nb > 1024 ? 2 : 1);
   int npow2 = 32 * e;
@@ -779,9 +835,15 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
   const int threads = npow2 / e;
   dim3 grid(s.hkv, s.batch);
   const size_t smem = static_cast<size_t>(npow2) * 4;
-  if (e == 4) quant_kernel<4><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
-  else if (e == 2) quant_kernel<2><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
-  else quant_kernel<1><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.nb, npow2);
+  if (e == 4)
+    quant_kernel<4><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.cu, s.seq, s.total, s.block,
+                                                     s.nbs, npow2, status);
+  else if (e == 2)
+    quant_kernel<2><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.cu, s.seq, s.total, s.block,
+                                                     s.nbs, npow2, status);
+  else
+    quant_kernel<1><<<grid, threads, smem, stream>>>(radius, quant, alpha, s.cu, s.seq, s.total, s.block,
+                                                     s.nbs, npow2, status);
   return cudaGetLastError();
 }
 
@@ -796,20 +858,21 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
   float *q_hi = reg[0], *q_lo = reg[1], *nbar = reg[2], *c_hi = reg[3], *c_lo = reg[4];
   float *s_c = reg[5], *s_r = reg[6];
   cudaError_t e;
-  if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, stream);
-  else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, stream);
+  if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
+  else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   e = launch_scores(s, ScoreOperands{c_hi, c_lo, q_hi, q_lo, nbar, radius, alpha}, scale, s_c, s_r,
                     status, stream);
   if (e != cudaSuccess) return e;
-  const size_t smem = kSelWarps * select_warp_bytes(s.nb);
+  const size_t smem = kSelWarps * select_warp_bytes(s.nbs);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid((s.nb + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);
-  select_kernel<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.hkv,
-                                                        s.nb, static_cast<long long>(ppm_c),
-                                                        static_cast<long long>(ppm_r));
+  dim3 grid((s.nbs + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);
+  select_kernel<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq,
+                                                        s.total, s.block, s.hkv, s.nbs,
+                                                        static_cast<long long>(ppm_c),
+                                                        static_cast<long long>(ppm_r), status);
   return cudaGetLastError();
 }
 

@@ -87,17 +87,25 @@ struct ScoreMaps {
   CUtensorMap c_hi, c_lo, q_hi, q_lo;
 };
 
+struct ScoreSeq {
+  const int32_t *cu;  // packed ragged batch, or null
+  int seq, total, block, hkv;
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(256, 1)
     score_kernel(const __grid_constant__ ScoreMaps maps, const float *__restrict__ nbar,
                  const float *__restrict__ radius, const float *__restrict__ alpha,
-                 float *__restrict__ s_c, float *__restrict__ s_r, int nb, float scale,
-                 int32_t *status) {
+                 float *__restrict__ s_c, float *__restrict__ s_r, int nb, const ScoreSeq sq,
+                 float scale, int32_t *status) {
   using C = ScoreCfg<D, G>;
   const int jt = blockIdx.x, it = blockIdx.y, gb = blockIdx.z;  // gb = b * hkv + g
   const int j0 = jt * C::ROWS, i0 = it * C::NI;
-  // only tiles with some key block j below some query block i carry work
-  if (j0 >= i0 + C::NI - 1 || j0 >= nb || i0 >= nb) return;
+  // this sequence's blocks (nb is the per-sequence stride of every per-block array)
+  const SeqSpan sp = seq_span(sq.cu, gb / sq.hkv, sq.seq, sq.total, status);
+  const int nbb = (sp.len + sq.block - 1) / sq.block;
+  // only tiles with some key block j below some query block i < nbb carry work
+  if (i0 >= nbb || j0 >= min(i0 + C::NI, nbb) - 1) return;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(256, 1)
     ptx::tc_fence_after();
     const int r = ((warp & 3) << 5) + lane;  // TMEM lane = key block row
     const int j = j0 + r;
-    const bool row_ok = dok && j < nb;
+    const bool row_ok = dok && j < nbb;
     const float bonus = row_ok ? alpha[static_cast<size_t>(gb) * nb + j] * radius[static_cast<size_t>(gb) * nb + j] : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
 #pragma unroll 1
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(256, 1)
           dm = fmaxf(dm, x);
           rm = fmaxf(rm, fmaf(snbar[col + h], bonus, x));
         }
-        if (row_ok && j < i && i < nb) {
+        if (row_ok && j < i && i < nbb) {
           const size_t o = (static_cast<size_t>(gb) * nb + i) * nb + j;
           s_c[o] = dm * scale;
           s_r[o] = rm * scale;
@@ -239,17 +247,18 @@ cudaError_t launch_t(const MaskShape &s, const ScoreOperands &op, float scale, f
   using C = ScoreCfg<D, G>;
   ScoreMaps maps;
   const uint64_t groups = static_cast<uint64_t>(s.batch) * s.hkv;
-  if (!make_map_2d(&maps.c_hi, op.c_hi, D, groups * s.nb, C::ROWS) ||
-      !make_map_2d(&maps.c_lo, op.c_lo, D, groups * s.nb, C::ROWS) ||
-      !make_map_2d(&maps.q_hi, op.q_hi, D, groups * s.nb * G, C::COLS) ||
-      !make_map_2d(&maps.q_lo, op.q_lo, D, groups * s.nb * G, C::COLS))
+  if (!make_map_2d(&maps.c_hi, op.c_hi, D, groups * s.nbs, C::ROWS) ||
+      !make_map_2d(&maps.c_lo, op.c_lo, D, groups * s.nbs, C::ROWS) ||
+      !make_map_2d(&maps.q_hi, op.q_hi, D, groups * s.nbs * G, C::COLS) ||
+      !make_map_2d(&maps.q_lo, op.q_lo, D, groups * s.nbs * G, C::COLS))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((s.nb + C::ROWS - 1) / C::ROWS, (s.nb + C::NI - 1) / C::NI, static_cast<unsigned>(groups));
+  dim3 grid((s.nbs + C::ROWS - 1) / C::ROWS, (s.nbs + C::NI - 1) / C::NI, static_cast<unsigned>(groups));
+  const ScoreSeq sq{s.cu, s.seq, s.total, s.block, s.hkv};
   score_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps, op.nbar, op.radius, op.alpha,
-                                                                  s_c, s_r, s.nb, scale, status);
+                                                                  s_c, s_r, s.nbs, sq, scale, status);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,8 @@
  *     A failed launch returns BSA_ERR_CUDA.
  *   - `dev_status` (nullable) is a device int32 the kernels set to a nonzero
  *     bsa_status when a bounded device-side wait gives up (the kernel then
- *     returns without hanging the GPU).  The caller zeroes it and reads it
+ *     returns without hanging the GPU) or, for packed ragged batches, when a
+ *     cu_seqlens entry is inconsistent.  The caller zeroes it and reads it
  *     after its own synchronisation.
  *   - NaN or Inf inputs give undefined (but memory-safe) results.
  */
@@ -45,7 +46,8 @@ typedef struct CUstream_st *bsa_stream_t;
 
 typedef enum {
   BSA_OK = 0,
-  BSA_ERR_INVALID_ARG = 1,    /* null pointer, misaligned pointer, bad ratio */
+  BSA_ERR_INVALID_ARG = 1,    /* null pointer, misaligned pointer, bad ratio; also written to
+                                 *dev_status for an inconsistent cu_seqlens entry */
   BSA_ERR_SHAPE = 2,          /* inconsistent shape (seq % block, hq % hkv, ...) */
   BSA_ERR_UNSUPPORTED = 3,    /* consistent but not implemented (head_dim, block, ...) */
   BSA_ERR_WORKSPACE = 4,      /* workspace missing or too small */
@@ -63,8 +65,8 @@ typedef struct {
 } bsa_shape;
 
 /*
- * Selection parameters (rescue branch section: "the two branches are then
- * thresholded independently").  Each path keeps a fraction of the causal row:
+ * Selection parameters (rescue branch section: each of the two paths has its
+ * own threshold).  Each path keeps a fraction of the causal row:
  * query block i keeps ceil(ratio * (i + 1)) candidates on each path, computed
  * as (ppm * (i + 1) + 999999) / 1000000 with ppm = floor(ratio * 1e6 + 0.5),
  * clipped to the available candidates.  Ratios must lie in [0, 1].
@@ -84,11 +86,10 @@ typedef struct {
 /*
  * bsa_block_meta - key-block summaries and the rescue coefficient.
  *
- * Rescue branch section: "for each key block, compute the centroid, then
- * compute the maximum distance from any key in that block to that centroid";
- * the coefficient is "derived from the distribution of those radii, using the
- * median and the 90th percentile as the reference points", computed "for each
- * layer and each key-value head".
+ * Rescue branch section: every key block is summarised by its centroid and by
+ * the largest distance from one of its keys to that centroid; the rescue
+ * coefficient adapts to the distribution of those radii, anchored at their
+ * median and 90th percentile, taken per layer and per KV head.
  *
  *   centroid[b][g][j][x]  (fp32, [batch, hkv, nb, head_dim])
  *                         = mean over the block's keys of k[x]
@@ -106,9 +107,8 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
  * bsa_select_mask - score every causal key block and emit the kept lists.
  *
  * Rescue branch section: the centroid branch scores every block on average
- * relevance and keeps the high ones; the rescue branch rescues wide-radius
- * blocks "even when their average score says otherwise"; the two masks are
- * combined.  With s = 1/sqrt(head_dim), qbar_{h,i} the mean query of block i
+ * relevance and keeps the high ones; the rescue branch brings back wide-radius
+ * blocks that the mean score alone would drop; the two masks are OR-ed.  With s = 1/sqrt(head_dim), qbar_{h,i} the mean query of block i
  * for head h and nbar_{h,i} the mean of those queries' L2 norms:
  *   S_c[i][j] = max over the G heads of KV head g of s * qbar_{h,i}.c_j
  *   R[i][j]   = max over those heads of s * (qbar_{h,i}.c_j + alpha_j * nbar_{h,i} * r_j)
@@ -167,8 +167,8 @@ bsa_status bsa_select_mask_noalloc(const bsa_shape *shape, const bsa_select_para
 /*
  * bsa_prefill_fwd - causal attention over the kept key blocks.
  *
- * Rescue branch section: "the combined mask still runs as regular
- * block-sparse FlashAttention".  For every query token t of block i and head h:
+ * Rescue branch section: the combined mask is consumed by an ordinary
+ * block-sparse FlashAttention.  For every query token t of block i and head h:
  *   O[t][h] = sum_s softmax_s(scale * q_t . k_s) v_s,  over the tokens s <= t
  *             of the key blocks kv_idx[b][g][i][0..kv_cnt-1], g = h / G;
  *   lse[b][h][t] = natural log of that softmax's normaliser (fp32, nullable).
@@ -207,6 +207,73 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
  * quant, alpha, kv_idx, kv_cnt (in that order, 6 entries written to offsets).
  */
 bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets);
+
+/* ------------------------------------------------------------------------
+ * Packed ragged batches ("varlen").
+ *
+ * Serving batches mix prompt lengths (the article's prefill section measures
+ * single long prompts; nothing in the method depends on a common length).  A
+ * varlen batch packs its sequences along one token axis: sequence b is tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 of q [total_tokens, hq, head_dim] and of
+ * k, v [total_tokens, hkv, head_dim]; o is [total_tokens, hq, head_dim] and
+ * lse is [hq, total_tokens].  A sequence may have any length >= 0, not only a
+ * multiple of the block: its blocks are nb_b = ceil(len_b / block) and the
+ * last one holds the remaining len_b - (nb_b - 1) * block tokens, which is
+ * then summarised, ranked and attended over those tokens only.  Every
+ * sequence is processed exactly as a batch of one.
+ *
+ * cu_seqlens: DEVICE int32 [batch + 1], 4-byte aligned, with cu_seqlens[0] =
+ * 0, non-decreasing, cu_seqlens[batch] <= total_tokens and every length <=
+ * max_seqlen.  The host cannot read it without synchronising, so the kernels
+ * check each entry: an inconsistent sequence writes BSA_ERR_INVALID_ARG to
+ * *dev_status (when given), is treated as empty, and nothing outside the
+ * caller's buffers is touched.
+ *
+ * Per-block arrays use nbs = bsa_varlen_block_stride(shape) =
+ * ceil(ceil(max_seqlen / block) / 4) * 4 blocks per sequence:
+ *   centroid [batch, hkv, nbs, head_dim], radius and alpha [batch, hkv, nbs],
+ *   quant [batch, hkv, 2], kv_idx [batch, hkv, nbs, nbs], kv_cnt [batch, hkv,
+ *   nbs], mask [batch, hkv, nbs, nbs].
+ * Entries past a sequence's own nb_b blocks are written as zeros (kv_cnt 0);
+ * an empty sequence gets quant 0.  Supported head_dim, block and group sizes
+ * are those of bsa_shape; ceil(max_seqlen / block) <= 4096.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t batch;         /* number of sequences */
+  int32_t total_tokens;  /* rows of the packed q, k, v, o (>= 1) */
+  int32_t max_seqlen;    /* upper bound of every sequence length (>= 1, <= total_tokens) */
+  int32_t hq, hkv, head_dim, block;
+} bsa_varlen_shape;
+
+/* nbs of the layouts above, or 0 for an invalid shape. */
+int32_t bsa_varlen_block_stride(const bsa_varlen_shape *shape);
+
+/* bsa_block_meta for a packed batch; partial last blocks average their own keys. */
+bsa_status bsa_varlen_block_meta(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                 const void *k, float *centroid, float *radius, float *quant,
+                                 float *alpha, int32_t *dev_status, bsa_stream_t stream);
+
+/* bsa_select_workspace_bytes / bsa_select_mask for a packed batch: rows i < nb_b of each
+ * sequence, keep counts from i + 1 as for a fixed-length sequence. */
+size_t bsa_varlen_select_workspace_bytes(const bsa_varlen_shape *shape);
+bsa_status bsa_varlen_select_mask(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                                  const int32_t *cu_seqlens, const void *q, const float *centroid,
+                                  const float *radius, const float *alpha, int32_t *kv_idx,
+                                  int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status,
+                                  bsa_stream_t stream);
+
+/* bsa_prefill_fwd / bsa_prefill_dense_fwd for a packed batch: causal within each sequence;
+ * the rows of a partial last block past the sequence end are not written. */
+bsa_status bsa_varlen_prefill_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                  const void *q, const void *k, const void *v,
+                                  const int32_t *kv_idx, const int32_t *kv_cnt,
+                                  float softmax_scale, void *o, float *lse, int32_t *dev_status,
+                                  bsa_stream_t stream);
+bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                                        const void *q, const void *k, const void *v,
+                                        float softmax_scale, void *o, float *lse,
+                                        int32_t *dev_status, bsa_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status status);

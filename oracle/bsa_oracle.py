@@ -40,10 +40,10 @@ FORCED, CENTROID, RESCUE = 1, 2, 4
 def block_meta(k: np.ndarray, block: int):
     """Centroid and radius of every key block.
 
-    Rescue branch section: "for each key block, compute the centroid, then
-    compute the maximum distance from any key in that block to that centroid".
-    The centroid is the mean of the block's keys (mean-dilution section: "the
-    average of the keys inside it"); the distance is read as plain Euclidean.
+    Rescue branch section: every key block is summarised by its centroid and
+    by the largest distance from one of its keys to that centroid.  The
+    centroid is the mean of the block's keys (mean-dilution section); the
+    distance is read as plain Euclidean.
 
     k: [b, N, Hkv, d].  Returns centroid [b, Hkv, nb, d], radius [b, Hkv, nb].
     """
@@ -72,9 +72,9 @@ def nearest_rank(count: int, num: int, den: int) -> int:
 def radius_quantiles(radius: np.ndarray):
     """Median and 90th-percentile radius per (batch, KV head).
 
-    Rescue branch section: the coefficient uses "the median and the 90th
-    percentile as the reference points", computed "separately for each layer
-    and each key-value head" over the prompt's blocks.  Reading: nearest-rank
+    Rescue branch section: the coefficient is anchored at the median and the
+    90th percentile of the radii, taken per layer and per KV head over the
+    prompt's blocks.  Reading: nearest-rank
     quantiles over all nb blocks, q(p) = r_(ceil(p nb)) of the ascending sort
     (so the median is the lower median for even nb).
 
@@ -90,8 +90,8 @@ def radius_quantiles(radius: np.ndarray):
 def rescue_coefficient(radius: np.ndarray, med: np.ndarray, p90: np.ndarray):
     """Radius-adaptive rescue coefficient alpha_j in [0, 1].
 
-    Rescue branch section: a coefficient "derived from the distribution of
-    those radii, using the median and the 90th percentile".  Reading: a block
+    Rescue branch section: the coefficient adapts to where a block's radius
+    falls between the median and the 90th percentile.  Reading: a block
     no wider than the median gets no bonus, a block at or beyond p90 the full
     bonus, linear in between:
         alpha_j = clamp((r_j - med) / (p90 - med), 0, 1),
@@ -109,8 +109,8 @@ def rescue_coefficient(radius: np.ndarray, med: np.ndarray, p90: np.ndarray):
 def query_summary(q: np.ndarray, block: int):
     """Per query block: mean query and mean query norm.
 
-    Rescue branch section: the centroid branch scores each block on "average
-    relevance".  Reading: the query side of a block is summarised by the mean
+    Rescue branch section: the centroid branch ranks blocks by how relevant
+    they are on average.  Reading: the query side of a block is summarised by the mean
     of its queries (qbar) and the mean of their Euclidean norms (nbar).
 
     q: [b, N, Hq, d].  Returns qbar [b, Hq, nb, d], nbar [b, Hq, nb].
@@ -132,11 +132,11 @@ def query_summary(q: np.ndarray, block: int):
 def block_scores(qbar, nbar, centroid, radius, alpha, scale: float, b: int, g: int):
     """Centroid-path and rescue-path scores for one (batch, KV head).
 
-    Centroid path (rescue branch section, "scores every block on average
-    relevance"):  S_c[i, j] = max over the group's query heads h of
+    Centroid path (rescue branch section: blocks ranked by average
+    relevance):  S_c[i, j] = max over the group's query heads h of
     scale * (qbar_{h,i} . c_j).
-    Rescue path ("scores rescue candidates against the base path with that
-    coefficient applied"):  R[i, j] = max_h scale * (qbar_{h,i} . c_j +
+    Rescue path (the base score plus the radius term weighted by the
+    coefficient):  R[i, j] = max_h scale * (qbar_{h,i} . c_j +
     alpha_j * nbar_{h,i} * r_j).  Since |qbar| <= nbar, with alpha_j = 1 the
     rescue score bounds every key of block j (Cauchy-Schwarz), so a single
     outlier key cannot be diluted away.  Reading: the group's heads are
@@ -170,7 +170,7 @@ def ratio_ppm(ratio: float) -> int:
 def keep_count(ppm: int, i: int) -> int:
     """ceil(ratio * (i + 1)) in integer arithmetic (ratio = ppm / 1e6).
 
-    Reading of "thresholded independently": each path keeps a fixed fraction
+    Reading of the independent per-path thresholds: each path keeps a fixed fraction
     of the causal row (i + 1 blocks), rounded up.
     """
     return (ppm * (i + 1) + PPM - 1) // PPM
@@ -194,8 +194,8 @@ def select_row(s_c_row, r_row, alpha_row, i: int, ppm_c: int, ppm_r: int):
       j in 1..i-1 by S_c.
     * Rescue path: among the candidates the centroid path dropped and whose
       radius is above the median (alpha_j > 0), the top
-      k_r = min(ceil(rho_r (i+1)), #eligible) by R ("rescued into the mask
-      even when their average score says otherwise").
+      k_r = min(ceil(rho_r (i+1)), #eligible) by R (wide blocks come back
+      even when their mean score alone would drop them).
     * The two paths are thresholded independently and combined by OR.
 
     Returns (centroid_kept, rescue_kept) as ascending int arrays.
@@ -289,8 +289,8 @@ def _attend(qi, keys, vals, qpos, kpos, scale):
 def sparse_attention_rows(q, k, v, mask, block: int, rows, scale: float | None = None):
     """Attention for selected (batch, query head, query block) rows only.
 
-    Rescue branch section: "the combined mask still runs as regular
-    block-sparse FlashAttention".  For each query token t of block i and head
+    Rescue branch section: the OR-combined mask is consumed by an ordinary
+    block-sparse FlashAttention.  For each query token t of block i and head
     h (KV head g = h // (Hq/Hkv)) the keys are the tokens s <= t of the key
     blocks kept in mask[b, g, i]; the output is the explicit softmax-weighted
     sum of their values and lse the natural log of the softmax normaliser.

@@ -126,3 +126,53 @@ def test_product_path_has_no_oracle_or_fallback():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in src.replace("oracle-free", ""), fn
                 assert "import synth" not in src, fn
+
+
+def vshape(**kw):
+    from block_sparse_long_kv_gb300 import _lib
+    base = dict(batch=3, total_tokens=2000, max_seqlen=1000, hq=4, hkv=2, head_dim=64, block=64)
+    base.update(kw)
+    return _lib.VarlenShape(**base)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(batch=0), 2), (dict(total_tokens=0), 2), (dict(max_seqlen=0), 2),
+    (dict(max_seqlen=2001), 2), (dict(hq=3), 2),
+    (dict(head_dim=96), 3), (dict(block=32), 3), (dict(hq=3, hkv=1), 3),
+    (dict(total_tokens=300000, max_seqlen=64 * 4097), 3),                     # nb > 4096
+])
+def test_varlen_shape_validation(lib, kw, code):
+    s = vshape(**kw)
+    f = ctypes.c_void_p(FAKE)
+    assert lib.bsa_varlen_block_meta(ctypes.byref(s), f, f, f, f, f, f, None, None) == code
+    assert lib.bsa_varlen_prefill_dense_fwd(ctypes.byref(s), f, f, f, f, ctypes.c_float(0.1), f,
+                                            None, None, None) == code
+    assert lib.bsa_varlen_block_stride(ctypes.byref(s)) == 0
+    assert lib.bsa_varlen_select_workspace_bytes(ctypes.byref(s)) == 0
+
+
+def test_varlen_stride_workspace_and_pointer_checks(lib):
+    from block_sparse_long_kv_gb300 import _lib
+    # ceil(max_seqlen / block) rounded up to a multiple of 4
+    for mx, blk, want in [(1000, 64, 16), (1025, 64, 20), (64, 64, 4), (1, 128, 4), (8192, 128, 64)]:
+        s = vshape(max_seqlen=mx, total_tokens=max(mx, 2000), block=blk)
+        assert lib.bsa_varlen_block_stride(ctypes.byref(s)) == want
+    s = vshape()                                            # nbs = 16, rows = 3 * 4 * 16
+    need = lib.bsa_varlen_select_workspace_bytes(ctypes.byref(s))
+    r256 = lambda x: (x + 255) // 256 * 256
+    rows, blocks = 3 * 4 * 16, 3 * 2 * 16
+    assert need == 2 * r256(rows * 64 * 4) + r256(rows * 4) + 2 * r256(blocks * 64 * 4) + \
+        2 * r256(blocks * 16 * 4)
+    f = ctypes.c_void_p(FAKE)
+    prm = _lib.SelectParams(0.25, 0.05, 0)
+    big = ctypes.c_size_t(1 << 40)
+    # cu_seqlens missing or misaligned
+    assert lib.bsa_varlen_block_meta(ctypes.byref(s), None, f, f, f, f, f, None, None) == 1
+    assert lib.bsa_varlen_block_meta(ctypes.byref(s), ctypes.c_void_p(FAKE + 2), f, f, f, f, f,
+                                     None, None) == 1
+    assert lib.bsa_varlen_select_mask(ctypes.byref(s), ctypes.byref(prm), f, f, f, f, f, f, f, None,
+                                      None, big, None, None) == 4
+    assert lib.bsa_varlen_select_mask(ctypes.byref(s), ctypes.byref(prm), f, f, f, f, f, f, f, None,
+                                      f, ctypes.c_size_t(need - 1), None, None) == 4
+    assert lib.bsa_varlen_prefill_fwd(ctypes.byref(s), f, f, f, f, None, f, ctypes.c_float(0.1), f,
+                                      None, None, None) == 1
