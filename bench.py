@@ -224,40 +224,69 @@ def threads_used():
 
 # ------------------------------------------------------------------ reference arm
 
+def expected_counts(nb: int, centroid_keep: float, rescue_keep: float):
+    """Kept blocks per row when every path fills its quota (an upper bound of kv_cnt)."""
+    import oracle as O
+    cnt = np.zeros(nb, dtype=np.int64)
+    for i in range(nb):
+        nc = max(i - 1, 0)
+        kc = min(O.keep_count(O.ratio_ppm(centroid_keep), i), nc)
+        kr = min(O.keep_count(O.ratio_ppm(rescue_keep), i), max(nc - kc, 0))
+        cnt[i] = (1 if i == 0 else 2) + kc + kr
+    return cnt
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import synth
-    w = synth.workload(args.workload)
-    lay = synth.make_layer(w, layer=0)
+    if args.workload in synth.VARLEN_WORKLOADS:
+        vw = synth.VARLEN_WORKLOADS[args.workload]
+        b = int(np.argmax(vw.lengths))
+        w = synth.Workload(f"{vw.name}_seq{b}", 1, vw.lengths[b], vw.hq, vw.hkv, vw.head_dim,
+                           vw.block, vw.centroid_keep, vw.rescue_keep, needles_fixed=vw.needles_fixed)
+        lay = synth.make_layer(w, seed=vw.seed_base + b)
+        factor = sum(-(-n // vw.block) for n in vw.lengths) / w.nb
+        nbs = max(-(-n // vw.block) for n in vw.lengths)
+        cnt = np.zeros((vw.batch, vw.hkv, nbs), dtype=np.int64)
+        for bi, n in enumerate(vw.lengths):
+            nb = -(-n // vw.block)
+            cnt[bi, :, :nb] = expected_counts(nb, vw.centroid_keep, vw.rescue_keep)
+        fl = kept_flops_varlen(cnt, vw.lengths, vw.block, vw.head_dim, vw.group)
+        cfg = {"workload": vw.name, "batch": vw.batch, "total_tokens": vw.total,
+               "max_seqlen": vw.max_seqlen, "lengths": list(vw.lengths), "hq": vw.hq,
+               "hkv": vw.hkv, "head_dim": vw.head_dim, "block": vw.block,
+               "centroid_keep": vw.centroid_keep, "rescue_keep": vw.rescue_keep}
+        extra = (f"; taken on the longest sequence ({w.seq} tokens) and scaled to the packed batch "
+                 f"by its block count (x{factor:.2f}) and its kept FLOPs")
+    else:
+        w = synth.workload(args.workload)
+        lay = synth.make_layer(w, layer=0)
+        factor = 1.0
+        cnt = np.broadcast_to(expected_counts(w.nb, w.centroid_keep, w.rescue_keep),
+                              (w.batch, w.hkv, w.nb))
+        fl = kept_flops(cnt, w.block, w.head_dim, w.group)
+        cfg = {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
+               "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
+               "rescue_keep": w.rescue_keep}
+        extra = ""
     per_step = max(3.0, min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup)))
     est = []
     for s in range(args.warmup + args.steps):
         r = oracle_sample(w, lay, per_step, rng_seed=s)
         if s >= args.warmup:
             est.append(r)
-    # kept FLOPs of the layer from the oracle's expected keep counts (ratios fixed per row)
-    import oracle as O
-    cnt = np.zeros((w.batch, w.hkv, w.nb), dtype=np.int64)
-    for i in range(w.nb):
-        nc = max(i - 1, 0)
-        kc = min(O.keep_count(O.ratio_ppm(w.centroid_keep), i), nc)
-        kr = min(O.keep_count(O.ratio_ppm(w.rescue_keep), i), max(nc - kc, 0))
-        cnt[..., i] = (1 if i == 0 else 2) + kc + kr
-    fl = kept_flops(cnt, w.block, w.head_dim, w.group)
-    ms = [1e3 * (r["t_meta"] + r["t_sel"] + r["t_att_per_flop"] * fl) for r in est]
+    ms = [1e3 * (factor * (r["t_meta"] + r["t_sel"]) + r["t_att_per_flop"] * fl) for r in est]
     val = float(np.median(ms))
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "ms/layer",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": val, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded generator, same workload)",
-        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
-                   "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
-                   "rescue_keep": w.rescue_keep},
+        "config": cfg,
         "cpu_baseline": {"value": val, "unit": "ms/layer", "cores": threads_used(),
-                         "kind": "oracle", "sample": est[0]["sample"]},
+                         "kind": "oracle", "sample": est[0]["sample"] + extra},
         "e2e": {"value": val, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "fp64 numpy oracle timed on a bounded sample per step, extrapolated (upper bound of "
                 "keep counts used for the FLOP scale)",
@@ -267,6 +296,152 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+
+def kept_flops_varlen(kv_cnt: np.ndarray, lengths, block: int, d: int, group: int) -> float:
+    """Kept-block FLOPs of a packed batch, counted over each block's real tokens: per query
+    head 4 n_q B d for a kept block before the diagonal and 2 n_q^2 d for the diagonal, n_q the
+    query block's tokens."""
+    tot = 0.0
+    for b, n in enumerate(lengths):
+        nb = -(-n // block)
+        for i in range(nb):
+            nq = min(block, n - i * block)
+            cnt = kv_cnt[b, :, i].astype(np.int64)                 # [hkv]
+            tot += group * float((4.0 * nq * block * d * (cnt - 1).clip(min=0)).sum()
+                                 + (2.0 * nq * nq * d * (cnt > 0)).sum())
+    return tot
+
+
+class FixedRunner:
+    """One fixed-length layer per step: bsa_block_meta, bsa_select_mask, bsa_prefill_fwd."""
+
+    def __init__(self, bsa, torch, w, dev):
+        self.bsa, self.torch, self.w, self.dev = bsa, torch, w, dev
+        self.s = bsa.make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
+        self.prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0)
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.meta = bsa.alloc_meta(self.s, dev)
+        self.sel = bsa.alloc_select(self.s, dev, with_mask=False)
+        self.ws = torch.empty(bsa.select_workspace_bytes(self.s), dtype=torch.uint8, device=dev)
+        self.lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=dev)
+        self.tokens = w.batch * w.seq
+
+    def make_layer(self, synth, layer):
+        return synth.make_layer(self.w, layer=layer)
+
+    def upload(self, lay):
+        up = lambda x: self.torch.from_numpy(lay[x].view(np.int16)).to(self.dev).view(self.torch.bfloat16)
+        return {x: up(x) for x in ("q", "k", "v")}
+
+    def meta_call(self, L, status):
+        m = self.meta
+        self.bsa.block_meta(self.s, L["k"], m["centroid"], m["radius"], m["quant"], m["alpha"], status)
+
+    def select_call(self, L, status):
+        m, sl = self.meta, self.sel
+        self.bsa.select_mask(self.s, self.prm, L["q"], m["centroid"], m["radius"], m["alpha"],
+                             sl["kv_idx"], sl["kv_cnt"], None, self.ws, status)
+
+    def attn_call(self, L, o, status):
+        sl = self.sel
+        self.bsa.prefill_fwd(self.s, L["q"], L["k"], L["v"], sl["kv_idx"], sl["kv_cnt"], self.scale,
+                             o, self.lse, status)
+
+    def stats(self):
+        w = self.w
+        cnt = self.sel["kv_cnt"].cpu().numpy()
+        return (kept_flops(cnt, w.block, w.head_dim, w.group), float(cnt.sum()) * 4 + cnt.size * 4,
+                float(cnt.sum()) / (w.batch * w.hkv * w.nb * (w.nb + 1) / 2))
+
+    def e2e_setup(self):
+        self.layer_ws = self.bsa.alloc_layer_workspace(self.s, self.dev)
+
+    def e2e_call(self, L, o, status, stream):
+        self.bsa.prefill_layer(self.s, self.prm, L["q"], L["k"], L["v"], self.scale, o, self.lse,
+                               self.layer_ws, status, stream=stream)
+
+    e2e_api = "bsa_prefill_layer (C ABI)"
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
+                "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
+                "rescue_keep": w.rescue_keep}
+
+    def cpu_sample_workload(self):
+        return self.w, None
+
+
+class VarlenRunner(FixedRunner):
+    """One packed ragged batch per step: the bsa_varlen_* entry points."""
+
+    def __init__(self, bsa, torch, vw, dev):
+        self.bsa, self.torch, self.w, self.dev = bsa, torch, vw, dev
+        self.s = bsa.make_varlen_shape(vw.batch, vw.total, vw.max_seqlen, vw.hq, vw.hkv,
+                                       vw.head_dim, vw.block)
+        self.prm = bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0)
+        self.scale = 1.0 / math.sqrt(vw.head_dim)
+        self.meta = bsa.alloc_varlen_meta(self.s, dev)
+        self.sel = bsa.alloc_varlen_select(self.s, dev, with_mask=False)
+        self.ws = torch.empty(bsa.varlen_select_workspace_bytes(self.s), dtype=torch.uint8, device=dev)
+        self.lse = torch.empty(vw.hq, vw.total, dtype=torch.float32, device=dev)
+        self.cu = torch.from_numpy(vw.cu_seqlens()).to(dev)
+        self.tokens = vw.total
+
+    def make_layer(self, synth, layer):
+        return synth.make_varlen_layer(self.w, layer=layer)
+
+    def meta_call(self, L, status):
+        m = self.meta
+        self.bsa.varlen_block_meta(self.s, self.cu, L["k"], m["centroid"], m["radius"], m["quant"],
+                                   m["alpha"], status)
+
+    def select_call(self, L, status):
+        m, sl = self.meta, self.sel
+        self.bsa.varlen_select_mask(self.s, self.prm, self.cu, L["q"], m["centroid"], m["radius"],
+                                    m["alpha"], sl["kv_idx"], sl["kv_cnt"], None, self.ws, status)
+
+    def attn_call(self, L, o, status):
+        sl = self.sel
+        self.bsa.varlen_prefill_fwd(self.s, self.cu, L["q"], L["k"], L["v"], sl["kv_idx"],
+                                    sl["kv_cnt"], self.scale, o, self.lse, status)
+
+    def stats(self):
+        vw = self.w
+        cnt = self.sel["kv_cnt"].cpu().numpy()
+        causal = sum(vw.hkv * nb * (nb + 1) / 2 for nb in (-(-n // vw.block) for n in vw.lengths))
+        return (kept_flops_varlen(cnt, vw.lengths, vw.block, vw.head_dim, vw.group),
+                float(cnt.sum()) * 4 + cnt.size * 4, float(cnt.sum()) / causal)
+
+    def e2e_setup(self):
+        pass
+
+    def e2e_call(self, L, o, status, stream):
+        self.meta_call(L, status)
+        self.select_call(L, status)
+        self.attn_call(L, o, status)
+
+    e2e_api = "bsa_varlen_block_meta + bsa_varlen_select_mask + bsa_varlen_prefill_fwd (C ABI)"
+
+    def config(self):
+        vw = self.w
+        return {"workload": vw.name, "batch": vw.batch, "total_tokens": vw.total,
+                "max_seqlen": vw.max_seqlen, "lengths": list(vw.lengths), "hq": vw.hq,
+                "hkv": vw.hkv, "head_dim": vw.head_dim, "block": vw.block,
+                "centroid_keep": vw.centroid_keep, "rescue_keep": vw.rescue_keep}
+
+    def cpu_sample_workload(self):
+        """The longest sequence as a fixed-length batch of one, and the factors that scale its
+        per-block and per-row times to the whole packed batch."""
+        import synth
+        vw = self.w
+        b = int(np.argmax(vw.lengths))
+        n = vw.lengths[b]
+        w = synth.Workload(f"{vw.name}_seq{b}", 1, n, vw.hq, vw.hkv, vw.head_dim, vw.block,
+                           vw.centroid_keep, vw.rescue_keep, needles_fixed=vw.needles_fixed)
+        blocks = sum(-(-m // vw.block) for m in vw.lengths)
+        return w, blocks / w.nb
+
 
 def run_ours(args):
     import torch
@@ -288,38 +463,33 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
-    w = synth.workload(args.workload)
-    s = bsa.make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
-    prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0)
-    scale = 1.0 / math.sqrt(w.head_dim)
+    if args.workload in synth.VARLEN_WORKLOADS:
+        run = VarlenRunner(bsa, torch, synth.VARLEN_WORKLOADS[args.workload], dev)
+    else:
+        run = FixedRunner(bsa, torch, synth.workload(args.workload), dev)
+    w = run.w
 
     # resident inputs: `layers` distinct seeded layers per rank (replicas process their own layers)
     host_layers = []
     dev_layers = []
     for li in range(args.layers):
-        lay = synth.make_layer(w, layer=rank * args.layers + li)
+        lay = run.make_layer(synth, rank * args.layers + li)
         host_layers.append(lay)
-        up = lambda x: torch.from_numpy(lay[x].view(np.int16)).to(dev).view(torch.bfloat16)
-        dev_layers.append({x: up(x) for x in ("q", "k", "v")})
-    meta = bsa.alloc_meta(s, dev)
-    sel = bsa.alloc_select(s, dev, with_mask=False)
-    sel_ws = torch.empty(bsa.select_workspace_bytes(s), dtype=torch.uint8, device=dev)
+        dev_layers.append(run.upload(lay))
     o = torch.empty_like(dev_layers[0]["q"])
-    lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(L, evs=None):
         if evs:
             evs[0].record(stream)
-        bsa.block_meta(s, L["k"], meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], status)
+        run.meta_call(L, status)
         if evs:
             evs[1].record(stream)
-        bsa.select_mask(s, prm, L["q"], meta["centroid"], meta["radius"], meta["alpha"],
-                        sel["kv_idx"], sel["kv_cnt"], None, sel_ws, status)
+        run.select_call(L, status)
         if evs:
             evs[2].record(stream)
-        bsa.prefill_fwd(s, L["q"], L["k"], L["v"], sel["kv_idx"], sel["kv_cnt"], scale, o, lse, status)
+        run.attn_call(L, o, status)
         if evs:
             evs[3].record(stream)
 
@@ -328,10 +498,10 @@ def run_ours(args):
     for L in dev_layers:
         step(L)
         torch.cuda.synchronize(dev)
-        cnt = sel["kv_cnt"].cpu().numpy()
-        flops.append(kept_flops(cnt, w.block, w.head_dim, w.group))
-        list_bytes.append(float(cnt.sum()) * 4 + cnt.size * 4)
-        density.append(float(cnt.sum()) / (w.batch * w.hkv * w.nb * (w.nb + 1) / 2))
+        f, lb, dn = run.stats()
+        flops.append(f)
+        list_bytes.append(lb)
+        density.append(dn)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
@@ -370,7 +540,7 @@ def run_ours(args):
     att_ms = np.array([evs[i][2].elapsed_time(evs[i][3]) for i in range(K)])
     fl = np.array([flops[i % len(flops)] for i in range(K)])
     lb = np.array([list_bytes[i % len(list_bytes)] for i in range(K)])
-    mask_bytes = w.batch * w.seq * (w.hq + w.hkv) * w.head_dim * 2 + lb
+    mask_bytes = run.tokens * (w.hq + w.hkv) * w.head_dim * 2 + lb
     kept_tflops = float((fl / (att_ms * 1e-3)).mean() / 1e12)
     mask_ms = meta_ms + sel_ms
     mask_gbs = float((mask_bytes / (mask_ms * 1e-3)).mean() / 1e9)
@@ -378,17 +548,20 @@ def run_ours(args):
     pk, src = peaks()
     bf16_peak = peak_value(pk, "bf16_tflops", "bf16_tflops_burst")
     hbm_peak = peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm_gb_s")
-    traffic, _ = profiled_traffic()
+    # the committed DRAM-traffic capture covers the default 128K workload only
+    default = not isinstance(run, VarlenRunner) and w.name == "gqa32x4_n131072_d128_b128"
+    traffic, _ = profiled_traffic() if default else (None, None)
     ms_per_layer = total_ms / (K * world)
+    q_gb = run.tokens * w.hq * w.head_dim * 2 / 1e9
+    cfg = run.config()
+    cfg.update({"layers_rotated": args.layers,
+                "l2": f"inputs larger than L2 (Q alone is {q_gb:.2f} GB per layer), layers rotated"})
     result = {
         "metric": METRIC, "value": ms_per_layer, "unit": "ms/layer", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator: clustered keys with log-uniform block spreads, planted needles)",
-        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "hq": w.hq, "hkv": w.hkv,
-                   "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
-                   "rescue_keep": w.rescue_keep, "layers_rotated": args.layers,
-                   "l2": "inputs larger than L2 (Q alone is 1.07 GB per layer), layers rotated"},
+        "config": cfg,
         "kept_block_tflops": kept_tflops,
         "attention_ms": float(att_ms.mean()),
         "mask_build_ms": float(mask_ms.mean()),
@@ -408,12 +581,12 @@ def run_ours(args):
         "clocks": clk,
     }
 
-    # end to end through the C ABI: every step copies its Q, K, V from pinned host memory, runs one
-    # bsa_prefill_layer call and copies O back to pinned host memory.  Two buffer sets and two copy
-    # streams let the input copy of step s+1 and the output copy of step s-1 overlap step s, as a
-    # serving loop that prefetches the next layer would.
+    # end to end through the C ABI: every step copies its Q, K, V from pinned host memory, runs the
+    # layer through the library's entry points and copies O back to pinned host memory.  Two buffer
+    # sets and two copy streams let the input copy of step s+1 and the output copy of step s-1
+    # overlap step s, as a serving loop that prefetches the next layer would.
     if not args.no_e2e:
-        ws = bsa.alloc_layer_workspace(s, dev)
+        run.e2e_setup()
         n_e2e = max(1, args.e2e_steps)
         pinned = []
         for x in range(2):
@@ -453,8 +626,7 @@ def run_ours(args):
                 stream.wait_event(ev_in[t])
                 if t >= 2:
                     stream.wait_event(ev_out[t - 2])          # O of step t-2 has reached the host
-                bsa.prefill_layer(s, prm, buf["q"], buf["k"], buf["v"], scale, buf["o"], lse, ws,
-                                  status, stream=stream)
+                run.e2e_call(buf, buf["o"], status, stream)
                 ev_done[t].record(stream)
                 d2h_s.wait_event(ev_done[t])
                 with torch.cuda.stream(d2h_s):
@@ -478,16 +650,25 @@ def run_ours(args):
         result["e2e"] = {"value": e2e_ms / n_e2e, "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host[0].numel() * 2,
                          "steps": n_e2e,
-                         "api": "bsa_prefill_layer (C ABI) + pinned host copies on two copy streams, "
+                         "api": run.e2e_api + " + pinned host copies on two copy streams, "
                                 "double-buffered (input copy of step s+1 and output copy of step s-1 "
                                 "overlap step s)"}
         result["gpu_launches_e2e_per_step"] = 6
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())}")
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_sample(w, host_layers[0], args.cpu_budget)
-        cpu_ms = 1e3 * (r["t_meta"] + r["t_sel"] + r["t_att_per_flop"] * float(np.mean(flops)))
+        sw, factor = run.cpu_sample_workload()
+        lay0 = host_layers[0] if factor is None else synth.make_layer(sw, seed=w.seed_base + int(
+            np.argmax(w.lengths)))
+        r = oracle_sample(sw, lay0, args.cpu_budget)
+        f = 1.0 if factor is None else factor
+        cpu_ms = 1e3 * (f * (r["t_meta"] + r["t_sel"]) + r["t_att_per_flop"] * float(np.mean(flops)))
+        sample = r["sample"] if factor is None else (
+            r["sample"] + f"; taken on the longest sequence ({sw.seq} tokens) and scaled to the "
+            f"packed batch by its block count (x{f:.2f}) and its kept FLOPs")
         result["cpu_baseline"] = {"value": cpu_ms, "unit": "ms/layer", "cores": threads_used(),
-                                  "kind": "oracle", "sample": r["sample"]}
+                                  "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

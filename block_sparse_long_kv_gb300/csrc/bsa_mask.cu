@@ -85,11 +85,17 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
   const uint16_t *base = k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * BLK + u) * tok_stride +
                          static_cast<size_t>(g) * D + v * 8;
   uint4 raw[TPT];
+  if (cnt == BLK) {
 #pragma unroll
-  for (int r = 0; r < TPT; ++r)
-    raw[r] = (r * TL + u < cnt)
-                 ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride))
-                 : make_uint4(0u, 0u, 0u, 0u);
+    for (int r = 0; r < TPT; ++r)
+      raw[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride));
+  } else {  // partial last block of a packed sequence
+#pragma unroll
+    for (int r = 0; r < TPT; ++r)
+      raw[r] = (r * TL + u < cnt)
+                   ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride))
+                   : make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // ---- pass 1: centroid
   float s[8];
@@ -260,6 +266,56 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
 // tf32), lo = x - hi is exact in fp32.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
+// Sums a full block's queries (8 dimensions per lane) and their norms, 8 loads
+// in flight per thread.
+template <int D>
+__device__ __forceinline__ void pool_full(const uint16_t *__restrict__ base, size_t tok_stride,
+                                          int cnt, unsigned wmask, float acc[8], float &nsum) {
+  constexpr int VH = D / 8;  // lanes per head
+  for (int t0 = 0; t0 < cnt; t0 += 8) {
+    uint4 u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride));
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float f[8];
+      unpack_bf16x8(u[r], f);
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[e] += f[e];
+        sq = fmaf(f[e], f[e], sq);
+      }
+#pragma unroll
+      for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
+      nsum += sqrtf(sq);
+    }
+  }
+}
+
+// The same over the cnt < block queries of a packed sequence's partial last
+// block, one token at a time (one such block per sequence).
+template <int D>
+__device__ __forceinline__ void pool_partial(const uint16_t *__restrict__ base, size_t tok_stride,
+                                             int cnt, unsigned wmask, float acc[8], float &nsum) {
+  constexpr int VH = D / 8;
+#pragma unroll 1
+  for (int t = 0; t < cnt; ++t) {
+    float f[8];
+    unpack_bf16x8(__ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride)), f);
+    float sq = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc[e] += f[e];
+      sq = fmaf(f[e], f[e], sq);
+    }
+#pragma unroll
+    for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
+    nsum += sqrtf(sq);
+  }
+}
+
 // One thread per (head, 8 dimensions); the token loop keeps 8 16-byte loads in
 // flight per thread.  Writes the mean query as tf32 hi / lo splits,
 // q_hi/q_lo[b][g][i][hh][x] (one K-major row per (query block, head): the B
@@ -315,33 +371,13 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   float nsum = 0.f;
-  for (int t0 = 0; t0 < cnt; t0 += 8) {
-    uint4 u[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      u[r] = (t0 + r < cnt)
-                 ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride))
-                 : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      float f[8];
-      unpack_bf16x8(u[r], f);
-      float sq = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[e] += f[e];
-        sq = fmaf(f[e], f[e], sq);
-      }
-#pragma unroll
-      for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
-      nsum += sqrtf(sq);
-    }
-  }
-  const float fc = static_cast<float>(cnt);
+  if (cnt == block) pool_full<D>(base, tok_stride, cnt, wmask, acc, nsum);
+  else pool_partial<D>(base, tok_stride, cnt, wmask, acc, nsum);
+  const float inv = 1.f / static_cast<float>(cnt);  // exact for a full block (a power of two)
   float m[8], hi[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    m[e] = acc[e] / fc;
+    m[e] = acc[e] * inv;
     hi[e] = tf32_hi(m[e]);
   }
   float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
@@ -350,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
   qh[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
   ql[0] = make_float4(m[0] - hi[0], m[1] - hi[1], m[2] - hi[2], m[3] - hi[3]);
   ql[1] = make_float4(m[4] - hi[4], m[5] - hi[5], m[6] - hi[6], m[7] - hi[7]);
-  if (xv == 0) nbar[row * grp + hh] = nsum / fc;
+  if (xv == 0) nbar[row * grp + hh] = nsum * inv;
 }
 
 // ---------------------------------------------------------------- select

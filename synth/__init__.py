@@ -250,6 +250,11 @@ VARLEN_WORKLOADS = {
                        32, 4, 128, 128, 0.15, 0.03, seed_base=6000),
         VarlenWorkload("varlen_gqa32x4_d128_b64", (4000, 2113, 65, 6000), 32, 4, 128, 64,
                        0.15, 0.03, seed_base=7000),
+        # a serving mix of 19 prompts, 15 to 32768 tokens, 131072 tokens in all
+        VarlenWorkload("varlen_mix19_gqa32x4_d128_b128_t131072",
+                       (32768, 20000, 16384, 12345, 9000, 8192, 6000, 5000, 4096, 3500, 3000,
+                        2500, 2048, 1800, 1500, 1200, 1024, 700, 15),
+                       32, 4, 128, 128, 0.15, 0.03, seed_base=8000),
     ]
 }
 
