@@ -6,7 +6,7 @@ no code with the CUDA path and imports nothing from it.
 """
 from .bsa_oracle import (  # noqa: F401
     block_meta, radius_quantiles, rescue_coefficient, query_summary,
-    block_scores, keep_count, select_row, select_blocks, kv_lists,
+    block_scores, token_block_scores, keep_count, select_row, select_blocks, kv_lists,
     sparse_attention, dense_attention, sparse_attention_rows, nearest_rank,
     ratio_ppm, PPM, FORCED, CENTROID, RESCUE,
     seq_bounds, varlen_select_blocks, varlen_attention_rows, varlen_dense_attention,

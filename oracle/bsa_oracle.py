@@ -157,6 +157,40 @@ def block_scores(qbar, nbar, centroid, radius, alpha, scale: float, b: int, g: i
     return s_c, r
 
 
+def token_block_scores(q, centroid, radius, alpha, block: int, scale: float, b: int, g: int):
+    """Per-token query aggregation of the two scores for one (batch, KV head).
+
+    The article's selection summarises a query block by its mean; the
+    per-token variant ranks key block j for query block i by the best single
+    query instead:
+        S_c[i, j] = scale * max over the group's heads h and the tokens t of
+                    block i of q_{h,t} . c_j
+        R[i, j]   = scale * max_{h,t} (q_{h,t} . c_j + alpha_j |q_{h,t}| r_j).
+    With alpha_j = 1, R bounds scale * q_{h,t} . k for every key k of block j
+    (Cauchy-Schwarz, |k - c_j| <= r_j), i.e. the block's largest logit.
+    Reading: the maximum over tokens is the plain reading of the article's
+    token-to-centroid comparison (section "The numbers, stated honestly").
+
+    q: [b, N, Hq, d].  Returns (S_c, R), each [nb, nb] (row i = query block).
+    """
+    n, hq = q.shape[1], q.shape[2]
+    hkv = centroid.shape[1]
+    grp = hq // hkv
+    nb = -(-n // block)
+    c = centroid[b, g]                                      # [nb, d]
+    bonus = alpha[b, g] * radius[b, g]                      # [nb]
+    s_c = np.empty((nb, nb))
+    r = np.empty((nb, nb))
+    for i in range(nb):
+        qt = np.asarray(q[b, i * block:min((i + 1) * block, n), g * grp:(g + 1) * grp],
+                        dtype=np.float64)                   # [t, G, d]
+        dots = np.einsum("thd,jd->thj", qt, c)
+        norms = np.sqrt(np.sum(qt * qt, axis=-1))           # [t, G]
+        s_c[i] = scale * dots.max(axis=(0, 1))
+        r[i] = scale * (dots + norms[:, :, None] * bonus[None, None, :]).max(axis=(0, 1))
+    return s_c, r
+
+
 # ------------------------------------------------------------ selection
 
 PPM = 1_000_000
@@ -211,12 +245,14 @@ def select_row(s_c_row, r_row, alpha_row, i: int, ppm_c: int, ppm_r: int):
 
 
 def select_blocks(q, k, block: int, centroid_keep: float, rescue_keep: float,
-                  scale: float | None = None, with_scores: bool = False):
+                  scale: float | None = None, with_scores: bool = False, token_max: bool = False):
     """Whole mask build for one layer: meta, quantiles, alpha, scores, select.
 
-    Returns a dict with centroid, radius, med, p90, alpha, qbar, nbar and the
-    uint8 mask [b, Hkv, nb, nb] (bits FORCED | CENTROID | RESCUE); with
-    ``with_scores`` also the per-(b, g) score matrices.
+    ``token_max`` scores with the per-token aggregation (token_block_scores)
+    instead of the block-mean query.  Returns a dict with centroid, radius,
+    med, p90, alpha, qbar, nbar and the uint8 mask [b, Hkv, nb, nb] (bits
+    FORCED | CENTROID | RESCUE); with ``with_scores`` also the per-(b, g)
+    score matrices.
     """
     b, n, hq, d = q.shape
     hkv = k.shape[2]
@@ -238,7 +274,10 @@ def select_blocks(q, k, block: int, centroid_keep: float, rescue_keep: float,
     scores = {}
     for bi in range(b):
         for g in range(hkv):
-            s_c, r = block_scores(qbar, nbar, centroid, radius, alpha, scale, bi, g)
+            if token_max:
+                s_c, r = token_block_scores(q, centroid, radius, alpha, block, scale, bi, g)
+            else:
+                s_c, r = block_scores(qbar, nbar, centroid, radius, alpha, scale, bi, g)
             if with_scores:
                 scores[(bi, g)] = (s_c, r)
             for i in range(nb):
@@ -364,7 +403,8 @@ def seq_bounds(cu_seqlens, b: int):
 
 
 def varlen_select_blocks(q, k, cu_seqlens, block: int, centroid_keep: float, rescue_keep: float,
-                         scale: float | None = None, with_scores: bool = False):
+                         scale: float | None = None, with_scores: bool = False,
+                         token_max: bool = False):
     """Mask build of every sequence of a packed batch, each as a batch of one.
 
     q: [T, Hq, d], k: [T, Hkv, d].  Returns a list with one ``select_blocks``
@@ -374,7 +414,7 @@ def varlen_select_blocks(q, k, cu_seqlens, block: int, centroid_keep: float, res
     for b in range(len(cu_seqlens) - 1):
         s0, s1 = seq_bounds(cu_seqlens, b)
         out.append(select_blocks(q[None, s0:s1], k[None, s0:s1], block, centroid_keep, rescue_keep,
-                                 scale, with_scores))
+                                 scale, with_scores, token_max))
     return out
 
 

@@ -375,3 +375,84 @@ def test_softmax_rows_sum_to_one_via_lse():
             kept = [s for s in range(t + 1) if keep[0, g, t // w.block, s // w.block]]
             z = sum(math.exp(scale * float(q[0, t, h] @ k[0, s, g]) - lse[0, h, t]) for s in kept)
             assert z == pytest.approx(1.0, abs=1e-12)
+
+
+# ----------------------------------------------------------------- per-token aggregation
+
+def _token_case(seed, n=40, hq=4, hkv=2, d=6, blk=8):
+    rng = np.random.default_rng(seed)
+    q = rng.normal(size=(1, n, hq, d))
+    k = rng.normal(size=(1, n, hkv, d)) * rng.uniform(0.2, 2.0, size=(1, n, 1, 1))
+    cen, rad = O.block_meta(k, blk)
+    med, p90 = O.radius_quantiles(rad)
+    alpha = O.rescue_coefficient(rad, med, p90)
+    return q, k, cen, rad, alpha, blk
+
+
+def test_token_scores_bruteforce():
+    q, k, cen, rad, alpha, blk = _token_case(1, n=37)           # a partial last block too
+    s = 0.3
+    nb = cen.shape[2]
+    for g in range(2):
+        s_c, r = O.token_block_scores(q, cen, rad, alpha, blk, s, 0, g)
+        for i in range(nb):
+            toks = range(i * blk, min((i + 1) * blk, 37))
+            for j in range(nb):
+                best_c = best_r = -math.inf
+                for t in toks:
+                    for h in (2 * g, 2 * g + 1):
+                        dot = sum(q[0, t, h, x] * cen[0, g, j, x] for x in range(6))
+                        nq = math.sqrt(sum(q[0, t, h, x] ** 2 for x in range(6)))
+                        best_c = max(best_c, dot)
+                        best_r = max(best_r, dot + alpha[0, g, j] * rad[0, g, j] * nq)
+                assert s_c[i, j] == pytest.approx(s * best_c, rel=1e-12, abs=1e-12)
+                assert r[i, j] == pytest.approx(s * best_r, rel=1e-12, abs=1e-12)
+
+
+def test_token_scores_dominate_block_mean_scores():
+    # max over tokens >= mean over tokens, for both paths
+    q, k, cen, rad, alpha, blk = _token_case(2)
+    qbar, nbar = O.query_summary(q, blk)
+    for g in range(2):
+        t_c, t_r = O.token_block_scores(q, cen, rad, alpha, blk, 1.0, 0, g)
+        m_c, m_r = O.block_scores(qbar, nbar, cen, rad, alpha, 1.0, 0, g)
+        assert np.all(t_c >= m_c - 1e-12) and np.all(t_r >= m_r - 1e-12)
+
+
+def test_token_scores_equal_mean_scores_for_uniform_blocks():
+    # every query of a block identical: the best token is the mean query
+    q, k, cen, rad, alpha, blk = _token_case(3)
+    q = np.repeat(q[:, ::blk], blk, axis=1)[:, :q.shape[1]]
+    qbar, nbar = O.query_summary(q, blk)
+    for g in range(2):
+        t_c, t_r = O.token_block_scores(q, cen, rad, alpha, blk, 0.7, 0, g)
+        m_c, m_r = O.block_scores(qbar, nbar, cen, rad, alpha, 0.7, 0, g)
+        np.testing.assert_allclose(t_c, m_c, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(t_r, m_r, rtol=1e-12, atol=1e-12)
+
+
+def test_token_rescue_score_bounds_every_logit_when_alpha_is_one():
+    q, k, cen, rad, _, blk = _token_case(4)
+    ones = np.ones_like(rad)
+    nb = cen.shape[2]
+    for g in range(2):
+        _, r = O.token_block_scores(q, cen, rad, ones, blk, 1.0, 0, g)
+        for i in range(nb):
+            qt = q[0, i * blk:(i + 1) * blk, 2 * g:2 * g + 2]
+            for j in range(nb):
+                logits = np.einsum("thd,sd->ths", qt, k[0, j * blk:(j + 1) * blk, g])
+                assert logits.max() <= r[i, j] + 1e-12
+
+
+def test_token_select_blocks_flag_and_permutation_invariance():
+    q, k, cen, rad, alpha, blk = _token_case(5, n=64)
+    a = O.select_blocks(q, k, blk, 0.3, 0.2, token_max=True, with_scores=True)
+    perm = np.concatenate([np.random.default_rng(6).permutation(blk) + i * blk
+                           for i in range(64 // blk)])
+    b = O.select_blocks(q[:, perm], k, blk, 0.3, 0.2, token_max=True, with_scores=True)
+    np.testing.assert_array_equal(a["mask"], b["mask"])
+    for key in a["scores"]:
+        np.testing.assert_allclose(a["scores"][key][0], b["scores"][key][0], rtol=1e-13)
+    # the per-token masks differ from the block-mean masks somewhere on this input
+    m = O.select_blocks(q, k, blk, 0.3, 0.2)
+    assert not np.array_equal(a["mask"], m["mask"])
