@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--token-max", action="store_true",
+                    help="score query blocks by their best token (BSA_SELECT_TOKEN_MAX)")
     return ap.parse_args()
 
 
@@ -312,13 +314,25 @@ def kept_flops_varlen(kv_cnt: np.ndarray, lengths, block: int, d: int, group: in
     return tot
 
 
+def token_score_flops(run) -> float:
+    """2 d FLOPs per (query token, head, key block j < its block i)."""
+    w = run.w
+    lengths = w.lengths if isinstance(run, VarlenRunner) else [w.seq] * w.batch
+    tot = 0
+    for n in lengths:
+        nb = -(-n // w.block)
+        for i in range(nb):
+            tot += min(w.block, n - i * w.block) * i
+    return float(2.0 * w.head_dim * w.hq * tot)
+
+
 class FixedRunner:
     """One fixed-length layer per step: bsa_block_meta, bsa_select_mask, bsa_prefill_fwd."""
 
-    def __init__(self, bsa, torch, w, dev):
+    def __init__(self, bsa, torch, w, dev, flags=0):
         self.bsa, self.torch, self.w, self.dev = bsa, torch, w, dev
         self.s = bsa.make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
-        self.prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0)
+        self.prm = bsa.SelectParams(w.centroid_keep, w.rescue_keep, flags)
         self.scale = 1.0 / math.sqrt(w.head_dim)
         self.meta = bsa.alloc_meta(self.s, dev)
         self.sel = bsa.alloc_select(self.s, dev, with_mask=False)
@@ -375,11 +389,11 @@ class FixedRunner:
 class VarlenRunner(FixedRunner):
     """One packed ragged batch per step: the bsa_varlen_* entry points."""
 
-    def __init__(self, bsa, torch, vw, dev):
+    def __init__(self, bsa, torch, vw, dev, flags=0):
         self.bsa, self.torch, self.w, self.dev = bsa, torch, vw, dev
         self.s = bsa.make_varlen_shape(vw.batch, vw.total, vw.max_seqlen, vw.hq, vw.hkv,
                                        vw.head_dim, vw.block)
-        self.prm = bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0)
+        self.prm = bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, flags)
         self.scale = 1.0 / math.sqrt(vw.head_dim)
         self.meta = bsa.alloc_varlen_meta(self.s, dev)
         self.sel = bsa.alloc_varlen_select(self.s, dev, with_mask=False)
@@ -463,10 +477,11 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
+    flags = bsa.SELECT_TOKEN_MAX if args.token_max else 0
     if args.workload in synth.VARLEN_WORKLOADS:
-        run = VarlenRunner(bsa, torch, synth.VARLEN_WORKLOADS[args.workload], dev)
+        run = VarlenRunner(bsa, torch, synth.VARLEN_WORKLOADS[args.workload], dev, flags)
     else:
-        run = FixedRunner(bsa, torch, synth.workload(args.workload), dev)
+        run = FixedRunner(bsa, torch, synth.workload(args.workload), dev, flags)
     w = run.w
 
     # resident inputs: `layers` distinct seeded layers per rank (replicas process their own layers)
@@ -554,7 +569,8 @@ def run_ours(args):
     ms_per_layer = total_ms / (K * world)
     q_gb = run.tokens * w.hq * w.head_dim * 2 / 1e9
     cfg = run.config()
-    cfg.update({"layers_rotated": args.layers,
+    cfg.update({"aggregation": "token_max" if args.token_max else "block_mean",
+                "layers_rotated": args.layers,
                 "l2": f"inputs larger than L2 (Q alone is {q_gb:.2f} GB per layer), layers rotated"})
     result = {
         "metric": METRIC, "value": ms_per_layer, "unit": "ms/layer", "n_gpus": world,
@@ -577,9 +593,20 @@ def run_ours(args):
                                 "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
                                 "peak_source": f"{src} hbm copy",
                                 "bytes_per_launch": float(np.mean(mask_bytes))},
-        "gpu_launches": 6 * K,       # meta, quant, qpool, score, select, attention
+        "gpu_launches": 6 * K,       # meta, quant, qpool or centroid split, scores, select, attention
         "clocks": clk,
     }
+    if args.token_max:
+        # per-token scores are a dense contraction: report the select call against the bf16 peak
+        # (FLOPs of q . c for every query token and every key block j < i of its block, per head)
+        tf = token_score_flops(run)
+        sel_tflops = float((tf / (sel_ms * 1e-3)).mean() / 1e12)
+        result["roofline_token_scores"] = {
+            "kernels": "centroid_split16_kernel + token_score_kernel + select_kernel (select call)",
+            "bound": "tensor", "achieved": sel_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": sel_tflops / bf16_peak if bf16_peak else None, "flops_per_launch": tf,
+            "note": "algorithmic FLOPs (one product per (token, head, key block)); the kernel runs "
+                    "two (bf16 hi and lo centroid splits) and whole 128-block tiles"}
 
     # end to end through the C ABI: every step copies its Q, K, V from pinned host memory, runs the
     # layer through the library's entry points and copies O back to pinned host memory.  Two buffer

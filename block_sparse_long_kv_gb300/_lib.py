@@ -11,6 +11,8 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbsa.so")
 
+SELECT_TOKEN_MAX = 1   # bsa_select_params.flags: per-token query aggregation
+
 STATUS = {
     0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_SHAPE", 3: "BSA_ERR_UNSUPPORTED",
     4: "BSA_ERR_WORKSPACE", 5: "BSA_ERR_CUDA", 6: "BSA_ERR_DEVICE_TIMEOUT",

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 __all__ = [
-    "Shape", "SelectParams", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
+    "Shape", "SelectParams", "SELECT_TOKEN_MAX", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
     "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
     "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
     "VarlenShape", "make_varlen_shape", "varlen_block_stride", "varlen_block_meta",
@@ -25,6 +25,7 @@ __all__ = [
 
 Shape = _lib.Shape
 SelectParams = _lib.SelectParams
+SELECT_TOKEN_MAX = _lib.SELECT_TOKEN_MAX
 VarlenShape = _lib.VarlenShape
 
 

@@ -109,7 +109,8 @@ bsa_status select_impl(const bsa::MaskShape &ms, const bsa_select_params *params
                        size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
   if (!params || !q || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
     return BSA_ERR_INVALID_ARG;
-  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
+  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) ||
+      (params->flags & ~static_cast<int32_t>(BSA_SELECT_TOKEN_MAX)) != 0)
     return BSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius) || !aligned16(alpha) ||
       !aligned16(kv_idx) || !aligned16(kv_cnt) || (mask && !aligned16(mask)))
@@ -118,9 +119,10 @@ bsa_status select_impl(const bsa::MaskShape &ms, const bsa_select_params *params
     return BSA_ERR_WORKSPACE;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool token_max = (params->flags & BSA_SELECT_TOKEN_MAX) != 0;
   if (bsa::launch_select(ms, q, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
-                         ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, workspace,
-                         dev_status, s) != cudaSuccess)
+                         ratio_ppm(params->rescue_keep), scale, token_max, kv_idx, kv_cnt, mask,
+                         workspace, dev_status, s) != cudaSuccess)
     return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -51,11 +51,12 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
 // centroids [b, hkv, nbs, d], mean query norms [b, hkv, nbs, G] and the two score matrices
 // [b, hkv, nbs, nbs], all fp32.
 size_t select_workspace_bytes(const MaskShape &s);
-// Query pooling into the workspace, tensor-core block scores, then top-k + list emission.
+// Query pooling into the workspace, tensor-core block scores, then top-k + list emission;
+// token_max scores every query token instead of the block-mean query.
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                          float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                          void *workspace, int32_t *status, cudaStream_t stream);
+                          float scale, bool token_max, int32_t *kv_idx, int32_t *kv_cnt,
+                          uint8_t *mask, void *workspace, int32_t *status, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point.
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -72,6 +73,13 @@ struct ScoreOperands {
 // Block scores S_c and R ([b, hkv, nb, nb] fp32, rows i, columns j < i) on tensor cores.
 cudaError_t launch_scores(const MaskShape &s, const ScoreOperands &op, float scale, float *s_c,
                           float *s_r, int32_t *status, cudaStream_t stream);
+
+// Per-token aggregation of the same scores (flag BSA_SELECT_TOKEN_MAX): splits the centroids
+// into bf16 hi / lo in c16 (2 * b * hkv * nbs * d bf16) and reduces q . c over every token of
+// each query block on tensor cores.
+cudaError_t launch_token_scores(const MaskShape &s, const void *q, const float *centroid, void *c16,
+                                const float *radius, const float *alpha, float scale, float *s_c,
+                                float *s_r, int32_t *status, cudaStream_t stream);
 
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;

@@ -885,8 +885,8 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
 
 cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
                           const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                          float scale, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask,
-                          void *workspace, int32_t *status, cudaStream_t stream) {
+                          float scale, bool token_max, int32_t *kv_idx, int32_t *kv_cnt,
+                          uint8_t *mask, void *workspace, int32_t *status, cudaStream_t stream) {
   const SelectRegions r = select_regions(s);
   char *ws = static_cast<char *>(workspace);
   float *reg[7];
@@ -894,12 +894,17 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
   float *q_hi = reg[0], *q_lo = reg[1], *nbar = reg[2], *c_hi = reg[3], *c_lo = reg[4];
   float *s_c = reg[5], *s_r = reg[6];
   cudaError_t e;
-  if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
-  else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
-  else return cudaErrorInvalidValue;
-  if (e != cudaSuccess) return e;
-  e = launch_scores(s, ScoreOperands{c_hi, c_lo, q_hi, q_lo, nbar, radius, alpha}, scale, s_c, s_r,
-                    status, stream);
+  if (token_max) {
+    // the bf16 centroid splits (2 bytes each, hi then lo) fit in the fp32 c_hi region
+    e = launch_token_scores(s, q, centroid, c_hi, radius, alpha, scale, s_c, s_r, status, stream);
+  } else {
+    if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
+    else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
+    else return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    e = launch_scores(s, ScoreOperands{c_hi, c_lo, q_hi, q_lo, nbar, radius, alpha}, scale, s_c, s_r,
+                      status, stream);
+  }
   if (e != cudaSuccess) return e;
   const size_t smem = kSelWarps * select_warp_bytes(s.nbs);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -70,13 +70,27 @@ typedef struct {
  * query block i keeps ceil(ratio * (i + 1)) candidates on each path, computed
  * as (ppm * (i + 1) + 999999) / 1000000 with ppm = floor(ratio * 1e6 + 0.5),
  * clipped to the available candidates.  Ratios must lie in [0, 1].
- * flags: reserved, must be 0.
+ * flags: 0 or BSA_SELECT_TOKEN_MAX.
  */
 typedef struct {
   float centroid_keep;
   float rescue_keep;
   int32_t flags;
 } bsa_select_params;
+
+/*
+ * BSA_SELECT_TOKEN_MAX - per-token query aggregation.  The article's selector
+ * summarises a query block by its mean query; with this flag a query block is
+ * represented by its best single token instead ("The numbers, stated honestly"
+ * section: the comparison is between tokens and centroids, done as a tiled
+ * reduction so no tokens x blocks tensor is stored):
+ *   S_c[i][j] = s * max over the G heads and the tokens t of block i of q_t . c_j
+ *   R[i][j]   = s * max over the same (h, t) of (q_t . c_j + alpha_j * |q_t| * r_j)
+ * With alpha_j = 1, R bounds every logit of block j.  Ranking, keep counts and
+ * outputs are unchanged.  The dot products run on tensor cores with the
+ * centroids split into bf16 hi + lo (about 16 significant bits).
+ */
+#define BSA_SELECT_TOKEN_MAX 1
 
 /* Bits of the optional mask written by bsa_select_mask. */
 #define BSA_MASK_FORCED 1u    /* key block 0 or the diagonal block */

@@ -171,17 +171,18 @@ def token_block_scores(q, centroid, radius, alpha, block: int, scale: float, b: 
     Reading: the maximum over tokens is the plain reading of the article's
     token-to-centroid comparison (section "The numbers, stated honestly").
 
-    q: [b, N, Hq, d].  Returns (S_c, R), each [nb, nb] (row i = query block).
+    q: [b, N, Hq, d].  Returns (S_c, R), each [ceil(N / block), nb] (row i =
+    query block of q, column j = key block of centroid).
     """
     n, hq = q.shape[1], q.shape[2]
     hkv = centroid.shape[1]
     grp = hq // hkv
-    nb = -(-n // block)
+    nq = -(-n // block)
     c = centroid[b, g]                                      # [nb, d]
     bonus = alpha[b, g] * radius[b, g]                      # [nb]
-    s_c = np.empty((nb, nb))
-    r = np.empty((nb, nb))
-    for i in range(nb):
+    s_c = np.empty((nq, c.shape[0]))
+    r = np.empty((nq, c.shape[0]))
+    for i in range(nq):
         qt = np.asarray(q[b, i * block:min((i + 1) * block, n), g * grp:(g + 1) * grp],
                         dtype=np.float64)                   # [t, G, d]
         dots = np.einsum("thd,jd->thj", qt, c)

@@ -34,7 +34,7 @@ def shape_of(w):
     return make_shape(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.block)
 
 
-def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda"):
+def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda", flags=0):
     """Run bsa_block_meta + bsa_select_mask; return numpy results."""
     import block_sparse_long_kv_gb300 as bsa
     s = shape_of(w)
@@ -44,7 +44,7 @@ def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda"):
     status = torch.zeros(1, dtype=torch.int32, device=device)
     bsa.block_meta(s, k, meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], status)
     prm = bsa.SelectParams(w.centroid_keep if centroid_keep is None else centroid_keep,
-                           w.rescue_keep if rescue_keep is None else rescue_keep, 0)
+                           w.rescue_keep if rescue_keep is None else rescue_keep, flags)
     bsa.select_mask(s, prm, q, meta["centroid"], meta["radius"], meta["alpha"], sel["kv_idx"],
                     sel["kv_cnt"], sel["mask"], dev_status=status)
     torch.cuda.synchronize()
@@ -63,11 +63,13 @@ def check_lists_match_mask(mask, kv_idx, kv_cnt):
                 np.testing.assert_array_equal(kv_idx[bi, g, i, :js.size], js)
 
 
-def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None):
+def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None, token_max=False):
     """Oracle mask rows for selected query blocks only.
 
     rows_by_bg: {(b, g): [i, ...]}.  Returns dict with per-(b, g, i) mask rows
     and the row scores, plus the oracle meta (centroid, radius, med, p90, alpha).
+    token_max: per-token aggregation of the scores (oracle token_block_scores,
+    restricted to the selected rows).
     """
     rc = w.centroid_keep if centroid_keep is None else centroid_keep
     rr = w.rescue_keep if rescue_keep is None else rescue_keep
@@ -81,6 +83,22 @@ def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None):
     rows = {}
     for (b, g), ilist in rows_by_bg.items():
         ilist = sorted(ilist)
+        if token_max:
+            for i in ilist:
+                # the oracle's per-token scores of block i alone (a one-block query slice)
+                qs = synth.bf16_to_f64(lay["q"][b:b + 1, i * w.block:(i + 1) * w.block])
+                cen1 = centroid[b:b + 1]
+                s_c, r = O.token_block_scores(qs, cen1, radius[b:b + 1], alpha[b:b + 1], w.block,
+                                              scale, 0, g)
+                cent, resc = O.select_row(s_c[0], r[0], alpha[b, g], i, O.ratio_ppm(rc),
+                                          O.ratio_ppm(rr))
+                m = np.zeros(w.nb, dtype=np.uint8)
+                m[0] |= O.FORCED
+                m[i] |= O.FORCED
+                m[cent] |= O.CENTROID
+                m[resc] |= O.RESCUE
+                rows[(b, g, i)] = (m, s_c[0], r[0])
+            continue
         # mean query / norm of just these blocks (oracle query_summary on each block's tokens)
         qbar = np.zeros((grp, len(ilist), w.head_dim))
         nbar = np.zeros((grp, len(ilist)))

@@ -76,7 +76,8 @@ def test_null_and_misaligned_pointers(lib):
     big = ctypes.c_size_t(1 << 40)
     assert lib.bsa_select_mask(ctypes.byref(s), None, *args, None, f, big, None, None) == 1
     for bad in (_lib.SelectParams(1.5, 0.0, 0), _lib.SelectParams(0.1, -0.1, 0),
-                _lib.SelectParams(float("nan"), 0.0, 0), _lib.SelectParams(0.1, 0.1, 1)):
+                _lib.SelectParams(float("nan"), 0.0, 0), _lib.SelectParams(0.1, 0.1, 2),
+                _lib.SelectParams(0.1, 0.1, -1)):
         assert lib.bsa_select_mask(ctypes.byref(s), ctypes.byref(bad), *args, None, f, big,
                                    None, None) == 1
     need = lib.bsa_select_workspace_bytes(ctypes.byref(s))

@@ -225,3 +225,56 @@ def test_long_prefill_128k_sampled():
             if np.array_equal(got["mask"][b, g, i], orc["rows"][(b, g, i)][0]):
                 att_rows += [(b, g * w.group + hh, i) for hh in (0, w.group - 1)]
     check_attention_rows(w, lay, o, lse, oracle_keep(w, orc) != 0, att_rows)
+
+
+# ------------------------------------------------------------------ per-token aggregation
+
+def token_parity(w, lay, rc=None, rr=None):
+    from block_sparse_long_kv_gb300 import SELECT_TOKEN_MAX
+    got = gpu_mask_build(w, lay, rc, rr, flags=SELECT_TOKEN_MAX)
+    check_lists_match_mask(got["mask"], got["kv_idx"], got["kv_cnt"])
+    orc = oracle_rows(w, lay, all_rows(w), rc, rr, token_max=True)
+    compared, excused = compare_mask_rows(got["mask"], orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)
+    return got, orc
+
+
+@pytest.mark.parametrize("name", ["tiny_h2x1_n1024_d64_b64", "gqa32x4_n8192_d128_b128"])
+def test_token_max_masks_full(name):
+    w = synth.workload(name)
+    lay = synth.make_layer(w)
+    got, orc = token_parity(w, lay)
+    # the per-token selection differs from the block-mean one and keeps the planted needles
+    mean = gpu_mask_build(w, lay)
+    assert not np.array_equal(got["mask"], mean["mask"])
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    check_attention_rows(w, lay, o, lse, keep != 0, sample_rows(w, 2))
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(batch=2, seq=2048, hq=8, hkv=8, head_dim=128, block=128),   # G = 1
+    dict(batch=1, seq=4096, hq=16, hkv=1, head_dim=128, block=128),  # G = 16
+    dict(batch=1, seq=2048, hq=8, hkv=2, head_dim=64, block=64),     # d = 64, block 64
+    dict(batch=1, seq=4096, hq=8, hkv=2, head_dim=128, block=256),   # block 256
+    dict(batch=2, seq=256, hq=4, hkv=2, head_dim=128, block=64),     # nb = 4, minimum
+])
+def test_token_max_shape_variants(cfg):
+    w = synth.Workload("tok", cfg["batch"], cfg["seq"], cfg["hq"], cfg["hkv"], cfg["head_dim"],
+                       cfg["block"], 0.25, 0.05, seed_base=123, needles_fixed=1)
+    token_parity(w, synth.make_layer(w))
+
+
+def test_token_max_long_rows_sampled():
+    # 32K tokens: 256 key blocks, two 128-block key tiles per CTA; sampled rows
+    w = synth.workload("gqa32x4_n32768_d128_b128")
+    lay = synth.make_layer(w)
+    from block_sparse_long_kv_gb300 import SELECT_TOKEN_MAX
+    got = gpu_mask_build(w, lay, flags=SELECT_TOKEN_MAX)
+    rng = np.random.default_rng(11)
+    rows = {(0, g): sorted({1, 2, 129, 130, 255} | set(rng.integers(0, w.nb, 12).tolist()))
+            for g in range(w.hkv)}
+    orc = oracle_rows(w, lay, rows, token_max=True)
+    compared, excused = compare_mask_rows(got["mask"], orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)

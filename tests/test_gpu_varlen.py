@@ -34,7 +34,7 @@ def vshape(vw):
                                  vw.block)
 
 
-def gpu_varlen(vw, lay, kv=None, rc=None, rr=None, cu=None, dense=False):
+def gpu_varlen(vw, lay, kv=None, rc=None, rr=None, cu=None, dense=False, flags=0):
     """Mask build + attention of a packed batch; numpy results and the device status."""
     import block_sparse_long_kv_gb300 as bsa
     s = vshape(vw)
@@ -46,7 +46,7 @@ def gpu_varlen(vw, lay, kv=None, rc=None, rr=None, cu=None, dense=False):
     bsa.varlen_block_meta(s, cu_d, k, meta["centroid"], meta["radius"], meta["quant"],
                           meta["alpha"], st)
     prm = bsa.SelectParams(vw.centroid_keep if rc is None else rc,
-                           vw.rescue_keep if rr is None else rr, 0)
+                           vw.rescue_keep if rr is None else rr, flags)
     bsa.varlen_select_mask(s, prm, cu_d, q, meta["centroid"], meta["radius"], meta["alpha"],
                            sel["kv_idx"], sel["kv_cnt"], sel["mask"], dev_status=st)
     o = torch.full_like(q, float("nan"))
@@ -66,12 +66,13 @@ def gpu_varlen(vw, lay, kv=None, rc=None, rr=None, cu=None, dense=False):
     return out
 
 
-def oracle_varlen(vw, lay, rc=None, rr=None):
+def oracle_varlen(vw, lay, rc=None, rr=None, token_max=False):
     q = synth.bf16_to_f64(lay["q"])
     k = synth.bf16_to_f64(lay["k"])
     return O.varlen_select_blocks(q, k, lay["cu_seqlens"], vw.block,
                                   vw.centroid_keep if rc is None else rc,
-                                  vw.rescue_keep if rr is None else rr, with_scores=True)
+                                  vw.rescue_keep if rr is None else rr, with_scores=True,
+                                  token_max=token_max)
 
 
 def padded_oracle(vw, res, nbs):
@@ -229,3 +230,13 @@ def test_inconsistent_cu_seqlens_is_reported_not_faulted():
         np.testing.assert_array_equal(got[x][:last], good[x][:last])
     n = int(lay["cu_seqlens"][last])
     np.testing.assert_array_equal(got["o"][:n], good["o"][:n])
+
+
+def test_varlen_token_max_masks():
+    from block_sparse_long_kv_gb300 import SELECT_TOKEN_MAX
+    vw = synth.VARLEN_WORKLOADS["varlen_h2x1_d64_b64"]
+    lay = synth.make_varlen_layer(vw)
+    res = oracle_varlen(vw, lay, token_max=True)
+    got = gpu_varlen(vw, lay, flags=SELECT_TOKEN_MAX)
+    assert got["status"] == 0
+    check_meta_and_masks(vw, got, padded_oracle(vw, res, got["nbs"]))
