@@ -10,4 +10,5 @@ from .bsa_oracle import (  # noqa: F401
     sparse_attention, dense_attention, sparse_attention_rows, nearest_rank,
     ratio_ppm, PPM, FORCED, CENTROID, RESCUE,
     seq_bounds, varlen_select_blocks, varlen_attention_rows, varlen_dense_attention,
+    decode_select, decode_attention, varlen_decode,
 )

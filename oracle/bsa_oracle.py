@@ -450,3 +450,90 @@ def varlen_dense_attention(q, k, v, cu_seqlens, scale: float | None = None):
         o[s0:s1] = ob[0]
         lse[:, s0:s1] = lb[0]
     return o, lse
+
+
+# ------------------------------------------------------------ decode (one new token)
+
+def decode_select(q_tok, centroid, radius, alpha, n: int, block: int, centroid_keep: float,
+                  rescue_keep: float, g: int, scale: float | None = None):
+    """Kept key blocks of one KV head for a single new query token.
+
+    The new token sits at position n - 1 of a sequence whose cache (including
+    the token's own key) holds n tokens, so its row is the block
+    i = (n - 1) // block.  Reading: the decode query is a query block of one
+    token, so its summary is the token itself (mean = q, mean norm = |q|) and
+    the row is selected exactly like a prefill row: forced 0 and i, the top
+    k_c of 1..i-1 by S_c, the top k_r of the dropped blocks with alpha > 0 by R.
+
+    q_tok: [Hq, d]; centroid [Hkv, nb, d], radius and alpha [Hkv, nb] of the
+    cache.  Returns (kept ascending int array, S_c row, R row).
+    """
+    hq, d = q_tok.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    i = (n - 1) // block
+    qbar = np.asarray(q_tok, dtype=np.float64)[None, :, None, :]        # [1, Hq, 1, d]
+    nbar = np.sqrt(np.sum(qbar * qbar, axis=-1))                         # [1, Hq, 1]
+    s_c, r = block_scores(qbar, nbar, centroid[None], radius[None], alpha[None], scale, 0, g)
+    cent, resc = select_row(s_c[0], r[0], alpha[g], i, ratio_ppm(centroid_keep),
+                            ratio_ppm(rescue_keep))
+    kept = np.union1d(np.union1d(cent, resc), np.array([0, i]))
+    return kept, s_c[0], r[0]
+
+
+def decode_attention(q_tok, k, v, kept_by_g, n: int, block: int, scale: float | None = None):
+    """Attention of one new token (position n - 1) over the kept key blocks.
+
+    q_tok: [Hq, d]; k, v: [n', Hkv, d] with n' >= n (tokens past n - 1 are
+    ignored); kept_by_g[g]: kept key blocks of KV head g.  Returns o [Hq, d]
+    and lse [Hq].
+    """
+    hq, d = q_tok.shape
+    hkv = k.shape[1]
+    grp = hq // hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((hq, d))
+    lse = np.zeros(hq)
+    for h in range(hq):
+        g = h // grp
+        kept = np.asarray(kept_by_g[g])
+        kpos = (kept[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+        kpos = kpos[kpos < n]
+        oi, li = _attend(np.asarray(q_tok[h:h + 1], dtype=np.float64),
+                         np.asarray(k[kpos, g], dtype=np.float64),
+                         np.asarray(v[kpos, g], dtype=np.float64), np.array([n - 1]), kpos, scale)
+        o[h] = oi[0]
+        lse[h] = li[0]
+    return o, lse
+
+
+def varlen_decode(q_new, k, v, cu_seqlens, block: int, centroid_keep: float, rescue_keep: float,
+                  scale: float | None = None):
+    """One decode step of a packed batch: the cache of sequence b is tokens
+    cu_seqlens[b] .. cu_seqlens[b+1]-1 of k, v (its last token is the new one);
+    q_new [batch, Hq, d].  Block summaries and the rescue coefficient are those
+    of the whole cache (block_meta, quantiles over its blocks).  Returns the
+    kept lists [(b, g) -> array], o [batch, Hq, d] and lse [batch, Hq]."""
+    bsz, hq, d = q_new.shape
+    hkv = k.shape[1]
+    kept = {}
+    o = np.zeros((bsz, hq, d))
+    lse = np.zeros((bsz, hq))
+    for b in range(bsz):
+        s0, s1 = seq_bounds(cu_seqlens, b)
+        n = s1 - s0
+        if n == 0:
+            continue
+        kc, vc = k[s0:s1], v[s0:s1]
+        cen, rad = block_meta(np.asarray(kc, dtype=np.float64)[None], block)
+        med, p90 = radius_quantiles(rad)
+        alpha = rescue_coefficient(rad, med, p90)
+        per_g = []
+        for g in range(hkv):
+            kp, _, _ = decode_select(q_new[b], cen[0], rad[0], alpha[0], n, block, centroid_keep,
+                                     rescue_keep, g, scale)
+            kept[(b, g)] = kp
+            per_g.append(kp)
+        o[b], lse[b] = decode_attention(q_new[b], kc, vc, per_g, n, block, scale)
+    return kept, o, lse
