@@ -21,6 +21,7 @@ __all__ = [
     "VarlenShape", "make_varlen_shape", "varlen_block_stride", "varlen_block_meta",
     "varlen_select_workspace_bytes", "varlen_select_mask", "varlen_prefill_fwd",
     "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
+    "decode_workspace_bytes", "decode_select", "decode_fwd",
 ]
 
 Shape = _lib.Shape
@@ -275,6 +276,46 @@ def alloc_varlen_select(shape: VarlenShape, device="cuda", with_mask: bool = Tru
     out["mask"] = (torch.empty(b, hkv, nbs, nbs, dtype=torch.uint8, device=device)
                    if with_mask else None)
     return out
+
+
+# ---------------------------------------------------------------- decode
+
+def decode_workspace_bytes(shape: VarlenShape) -> int:
+    return int(_lib.load().bsa_decode_workspace_bytes(ctypes.byref(shape)))
+
+
+def decode_select(shape: VarlenShape, params: SelectParams, cu_seqlens, q_new, centroid, radius,
+                  alpha, kv_idx, kv_cnt, dev_status=None, stream=None):
+    """bsa_decode_select: kept blocks of each sequence's new token (kv_idx [b, hkv, nbs],
+    kv_cnt [b, hkv])."""
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_decode_select", lib.bsa_decode_select(
+        ctypes.byref(shape), ctypes.byref(params), _cu(cu_seqlens, b),
+        _ptr(q_new, "q_new", torch.bfloat16, b * hq * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * nbs * d),
+        _ptr(radius, "radius", torch.float32, b * hkv * nbs),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nbs),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def decode_fwd(shape: VarlenShape, cu_seqlens, q_new, k, v, kv_idx, kv_cnt, softmax_scale, o,
+               lse=None, workspace=None, dev_status=None, stream=None):
+    """bsa_decode_fwd: o [b, hq, d] of each sequence's new token over its kept blocks."""
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(shape), dtype=torch.uint8, device=q_new.device)
+    _lib.check("bsa_decode_fwd", lib.bsa_decode_fwd(
+        ctypes.byref(shape), _cu(cu_seqlens, b), _ptr(q_new, "q_new", torch.bfloat16, b * hq * d),
+        _ptr(k, "k", torch.bfloat16, t * hkv * d), _ptr(v, "v", torch.bfloat16, t * hkv * d),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv), ctypes.c_float(softmax_scale),
+        _ptr(o, "o", torch.bfloat16, b * hq * d), _ptr(lse, "lse", torch.float32, b * hq),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 
 def status_string(code: int) -> str:

@@ -309,4 +309,55 @@ bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int
                       lse, dev_status, stream);
 }
 
+// ---------------------------------------------------------------- decode
+
+size_t bsa_decode_workspace_bytes(const bsa_varlen_shape *shape) {
+  static const int32_t probe = 0;
+  if (check_varlen(shape, &probe) != BSA_OK) return 0;
+  return bsa::decode_workspace_bytes(mask_shape(shape, &probe));
+}
+
+bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                             const int32_t *cu_seqlens, const void *q_new, const float *centroid,
+                             const float *radius, const float *alpha, int32_t *kv_idx,
+                             int32_t *kv_cnt, int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  if (!params || !q_new || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
+    return BSA_ERR_INVALID_ARG;
+  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
+    return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(centroid) || !aligned16(radius) || !aligned16(alpha) ||
+      !aligned16(kv_idx) || !aligned16(kv_cnt))
+    return BSA_ERR_INVALID_ARG;
+  const bsa::MaskShape ms = mask_shape(shape, cu_seqlens);
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
+  if (bsa::launch_decode_select(ms, q_new, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
+                                ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, dev_status,
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                          const void *q_new, const void *k, const void *v, const int32_t *kv_idx,
+                          const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  if (!q_new || !k || !v || !kv_idx || !kv_cnt || !o) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(k) || !aligned16(v) || !aligned16(kv_idx) ||
+      !aligned16(kv_cnt) || !aligned16(o) || (lse && !aligned16(lse)))
+    return BSA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  const bsa::MaskShape ms = mask_shape(shape, cu_seqlens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::decode_workspace_bytes(ms))
+    return BSA_ERR_WORKSPACE;
+  if (bsa::launch_decode(ms, q_new, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, workspace,
+                         dev_status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
 }  // extern "C"

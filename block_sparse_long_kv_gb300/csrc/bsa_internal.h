@@ -81,6 +81,18 @@ cudaError_t launch_token_scores(const MaskShape &s, const void *q, const float *
                                 const float *radius, const float *alpha, float scale, float *s_c,
                                 float *s_r, int32_t *status, cudaStream_t stream);
 
+// Decode of one new token per packed sequence (its cache's last token): selection of the
+// kept blocks (kv_idx [b, hkv, nbs], kv_cnt [b, hkv]) and split-KV attention (o [b, hq, d],
+// lse [b, hq]) with fp32 partials in the workspace.
+cudaError_t launch_decode_select(const MaskShape &s, const void *q_new, const float *centroid,
+                                 const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
+                                 float scale, int32_t *kv_idx, int32_t *kv_cnt, int32_t *status,
+                                 cudaStream_t stream);
+size_t decode_workspace_bytes(const MaskShape &s);
+cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, const void *v,
+                          const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,
+                          void *workspace, int32_t *status, cudaStream_t stream);
+
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;
   const int32_t *cu;  // packed ragged batch (o [total, hq, d], lse [hq, total]) or null

@@ -28,6 +28,7 @@
 #include <stdint.h>
 
 #include "bsa_internal.h"
+#include "bsa_topk.cuh"
 
 namespace bsa {
 namespace {
@@ -391,252 +392,10 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
 
 // ---------------------------------------------------------------- select
 
-// Order-preserving key of a float score: a higher score gives a larger key.
-// Every non-NaN score maps to a key >= 1, so key 0 marks "not a candidate".
-__device__ __forceinline__ uint32_t score_key(float s) {
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+using namespace topk;
 
 constexpr int kSelWarps = 8;   // rows per select CTA, one warp each
-constexpr int kCompact = 256;  // capacity of the per-warp list of threshold-bin keys
 
-__host__ __device__ constexpr size_t select_warp_bytes(int nb) {
-  return static_cast<size_t>(nb) * 4 + 1024 + kCompact * 4 +
-         ((static_cast<size_t>(nb) + 15) & ~static_cast<size_t>(15));
-}
-
-// Inverse of score_key for a nonzero key.
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-// Exclusive prefix sum of c over the lanes of a warp; *total receives the sum.
-__device__ __forceinline__ unsigned warp_exclusive_scan(unsigned c, unsigned *total) {
-  const int lane = threadIdx.x & 31;
-  unsigned incl = c;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  *total = __shfl_sync(0xffffffffu, incl, 31);
-  return incl - c;
-}
-
-// In a 256-bin histogram (lane l reads bins 8l .. 8l+7), the bin holding the
-// take-th largest entry counting down from the top bin, the number of entries
-// in the bins above it, and its own count.  Requires 1 <= take <= total.
-__device__ __forceinline__ void warp_find_bin(const unsigned *hist, unsigned take, unsigned *bin,
-                                              unsigned *above, unsigned *count) {
-  const int lane = threadIdx.x & 31;
-  const uint4 h0 = reinterpret_cast<const uint4 *>(hist)[2 * lane];
-  const uint4 h1 = reinterpret_cast<const uint4 *>(hist)[2 * lane + 1];
-  const unsigned c[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-  unsigned s = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) s += c[e];
-  unsigned suf = s;  // entries in the bins of lanes >= this lane
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned o = __shfl_down_sync(0xffffffffu, suf, off);
-    if (lane + off < 32) suf += o;
-  }
-  unsigned acc = suf - s, my_bin = 0, my_above = 0, my_count = 0;
-  bool hit = false;
-#pragma unroll
-  for (int e = 7; e >= 0; --e) {
-    if (!hit && acc < take && take <= acc + c[e]) {
-      hit = true;
-      my_bin = 8 * lane + e;
-      my_above = acc;
-      my_count = c[e];
-    }
-    acc += c[e];
-  }
-  const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-  *bin = __shfl_sync(0xffffffffu, my_bin, src);
-  *above = __shfl_sync(0xffffffffu, my_above, src);
-  *count = __shfl_sync(0xffffffffu, my_count, src);
-  __syncwarp();
-}
-
-// Radix threshold of the k largest nonzero keys of keys[0, n) (1 <= k < number
-// of nonzero keys), one warp, 8-bit digits from the top.  The selection is:
-// every key with (key & pmask) > prefix, plus the first `take` in index order
-// of the `n_eq` nonzero keys with (key & pmask) == prefix.
-struct Threshold {
-  uint32_t prefix, pmask;
-  unsigned take, n_eq;
-};
-
-__device__ Threshold warp_radix_threshold(const uint32_t *keys, int n, unsigned k, unsigned *hist) {
-  const int lane = threadIdx.x & 31;
-  Threshold t{0u, 0u, k, 0u};
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    for (int j0 = 0; j0 < n; j0 += 32) {  // warp-uniform trip count: every lane reaches the match
-      const int j = j0 + lane;
-      const uint32_t key = j < n ? keys[j] : 0u;
-      const bool ok = key != 0u && (key & t.pmask) == t.prefix;
-      const unsigned digit = (key >> shift) & 255u;
-      const unsigned peers = __match_any_sync(0xffffffffu, ok ? digit : 256u);
-      if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-    }
-    __syncwarp();
-    unsigned digit, above, count;
-    warp_find_bin(hist, t.take, &digit, &above, &count);
-    t.take -= above;
-    t.n_eq = count;
-    t.prefix |= digit << shift;
-    t.pmask |= 0xFFu << shift;
-    if (t.n_eq == t.take) break;  // the whole bin is in: no finer digit needed
-  }
-  return t;
-}
-
-// The k best candidates of a row.  A linear 256-bin histogram of the
-// candidates' values over [lo, hi] finds the bin holding the threshold; bins
-// above it are in, and inside it the radix threshold t over the bin's keys
-// (gathered into a short list) decides, unless the whole bin is in.  The bin
-// map is monotone in the value, so this is the exact top-k of the keys.  With
-// no usable value range, or a threshold bin too crowded for the list, every
-// candidate falls in bin 0 and t is taken over the whole row.
-struct RowSelect {
-  float lo, inv;  // bin(v) = min(255, trunc((v - lo) * inv)); inv == 0 maps everything to bin 0
-  int bstar;
-  bool whole;
-  Threshold t;
-};
-
-__device__ __forceinline__ int value_bin(uint32_t key, float lo, float inv) {
-  return min(255, static_cast<int>((key_value(key) - lo) * inv));
-}
-
-// keys[0, n) are readable 4 at a time: the entries from n up to the next
-// multiple of 4 are zero.
-__device__ RowSelect warp_select(const uint32_t *keys, int n, unsigned k, float lo, float hi,
-                                 unsigned *hist, uint32_t *ckeys) {
-  const int lane = threadIdx.x & 31;
-  RowSelect r;
-  r.lo = lo;
-  r.inv = 0.f;
-  r.bstar = 0;
-  r.whole = false;
-  if (hi > lo) {
-    const float inv = 256.f / (hi - lo);
-    if (inv <= 1.0e38f) r.inv = inv;
-  }
-  if (r.inv > 0.f) {
-    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    for (int j = 4 * lane; j < n; j += 128) {
-      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (kv[e] != 0u) atomicAdd(&hist[value_bin(kv[e], r.lo, r.inv)], 1u);
-    }
-    __syncwarp();
-    unsigned bstar, above, count;
-    warp_find_bin(hist, k, &bstar, &above, &count);
-    r.bstar = static_cast<int>(bstar);
-    const unsigned take = k - above;
-    if (count == take) {
-      r.whole = true;
-      return r;
-    }
-    if (count <= static_cast<unsigned>(kCompact)) {
-      unsigned base = 0;
-      for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
-        const int j = j0 + 4 * lane;
-        uint32_t kv[4] = {0u, 0u, 0u, 0u};
-        unsigned m = 0;
-        if (j < n) {
-          const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-          kv[0] = kk.x; kv[1] = kk.y; kv[2] = kk.z; kv[3] = kk.w;
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (kv[e] != 0u && value_bin(kv[e], r.lo, r.inv) == r.bstar) m |= 1u << e;
-        }
-        unsigned tot;
-        unsigned pos = base + warp_exclusive_scan(__popc(m), &tot);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((m >> e) & 1u) ckeys[pos++] = kv[e];
-        base += tot;
-      }
-      __syncwarp();
-      r.t = warp_radix_threshold(ckeys, static_cast<int>(count), take, hist);
-      return r;
-    }
-  }
-  r.inv = 0.f;
-  r.bstar = 0;
-  r.t = warp_radix_threshold(keys, n, k, hist);
-  return r;
-}
-
-// flags[j] |= bit for the candidates RowSelect r keeps among keys[0, n).  Each
-// lane owns 4 consecutive entries (one flags word); equal keys at the
-// threshold are ranked in index order.
-__device__ void warp_mark(const uint32_t *keys, int n, const RowSelect &r, uint8_t *flags, uint8_t bit) {
-  const int lane = threadIdx.x & 31;
-  const bool ranked = !r.whole && r.t.n_eq != r.t.take;
-  unsigned taken = 0;
-  for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
-    const int j = j0 + 4 * lane;
-    unsigned in = 0, eq = 0;  // bit e: entry j + e
-    if (j < n) {
-      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (kv[e] == 0u) continue;
-        const int bn = value_bin(kv[e], r.lo, r.inv);
-        if (bn > r.bstar || (bn == r.bstar && r.whole)) {
-          in |= 1u << e;
-        } else if (bn == r.bstar) {
-          const uint32_t top = kv[e] & r.t.pmask;
-          if (top > r.t.prefix) in |= 1u << e;
-          else if (top == r.t.prefix) eq |= 1u << e;
-        }
-      }
-    }
-    if (ranked) {
-      unsigned tot;
-      unsigned rank = taken + warp_exclusive_scan(__popc(eq), &tot);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((eq >> e) & 1u) {
-          if (rank < r.t.take) in |= 1u << e;
-          ++rank;
-        }
-      taken += tot;
-    } else {
-      in |= eq;
-    }
-    if (in != 0u) {
-      uint32_t *fw = reinterpret_cast<uint32_t *>(flags) + (j >> 2);
-      uint32_t w = *fw;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((in >> e) & 1u) w |= static_cast<uint32_t>(bit) << (8 * e);
-      *fw = w;
-    }
-  }
-}
-
-__device__ __forceinline__ void warp_minmax(float &lo, float &hi) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-  }
-}
 
 // One warp per (b, g, i) row, longest rows first; kSelWarps rows per CTA.
 // Loads the row's centroid-path keys (scores from the tensor-core score
@@ -666,123 +425,12 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
       return;
     }
   }
-  // per warp: keys [nb] u32, hist [256] u32, ckeys [kCompact] u32, flags [nb] u8
-  // (nb % 4 == 0 keeps each 16-byte aligned)
-  unsigned char *wbase = smem + static_cast<size_t>(warp) * select_warp_bytes(nb);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(wbase);
-  unsigned *hist = reinterpret_cast<unsigned *>(wbase + static_cast<size_t>(nb) * 4);
-  uint32_t *ckeys = reinterpret_cast<uint32_t *>(wbase + static_cast<size_t>(nb) * 4 + 1024);
-  uint8_t *flags = wbase + static_cast<size_t>(nb) * 4 + 1024 + kCompact * 4;
-
+  const RowScratch w = row_scratch(smem + static_cast<size_t>(warp) * row_scratch_bytes(nb), nb);
   const size_t gb = static_cast<size_t>(b) * hkv + g;
   const size_t row = gb * nb + i;
-  const float *ab = alpha + gb * nb;
-  const int n4 = (i + 4) & ~3;  // keys / flags [0, n4) cover 0..i; entries j >= i are never candidates
-
-  // ---- centroid path: top kc of candidates 1..i-1 by S_c
-  float lo = INFINITY, hi = -INFINITY;
-  {
-    const float4 *rc = reinterpret_cast<const float4 *>(s_c + row * nb);
-    for (int j4 = lane * 4; j4 < n4; j4 += 128) {
-      const float4 v = rc[j4 >> 2];
-      const float x[4] = {v.x, v.y, v.z, v.w};
-      uint32_t kp[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = j4 + e;
-        const bool cand = j >= 1 && j < i;
-        kp[e] = cand ? score_key(x[e]) : 0u;
-        if (cand) {
-          lo = fminf(lo, x[e]);
-          hi = fmaxf(hi, x[e]);
-        }
-      }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
-      reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
-    }
-  }
-  warp_minmax(lo, hi);
-  __syncwarp();
-  const int ncand = i > 1 ? i - 1 : 0;
-  const long long kc_full = (ppm_c * (i + 1) + 999999LL) / 1000000LL;
-  const int kc = static_cast<int>(kc_full < ncand ? kc_full : ncand);
-  if (kc == ncand) {
-    for (int j = 1 + lane; j < i; j += 32) flags[j] = BSA_MASK_CENTROID;
-  } else if (kc > 0) {
-    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kc), lo, hi, hist, ckeys);
-    warp_mark(keys, i, r, flags, BSA_MASK_CENTROID);
-  }
-  __syncwarp();
-
-  // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
-  int nelig = 0;
-  lo = INFINITY;
-  hi = -INFINITY;
-  {
-    const float4 *rr = reinterpret_cast<const float4 *>(s_r + row * nb);
-    for (int j4 = lane * 4; j4 < n4; j4 += 128) {
-      const float4 v = rr[j4 >> 2];
-      const float4 a = *reinterpret_cast<const float4 *>(ab + j4);
-      const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
-      const float x[4] = {v.x, v.y, v.z, v.w}, al[4] = {a.x, a.y, a.z, a.w};
-      uint32_t kp[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = j4 + e;
-        const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
-        kp[e] = elig ? score_key(x[e]) : 0u;
-        nelig += elig ? 1 : 0;
-        if (elig) {
-          lo = fminf(lo, x[e]);
-          hi = fmaxf(hi, x[e]);
-        }
-      }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) nelig += __shfl_xor_sync(0xffffffffu, nelig, off);
-  warp_minmax(lo, hi);
-  __syncwarp();
-  const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
-  const int kr = static_cast<int>(kr_full < nelig ? kr_full : nelig);
-  if (kr > 0 && kr == nelig) {
-    for (int j = lane; j < i; j += 32)
-      if (keys[j] != 0u) flags[j] |= BSA_MASK_RESCUE;
-  } else if (kr > 0) {
-    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kr), lo, hi, hist, ckeys);
-    warp_mark(keys, i, r, flags, BSA_MASK_RESCUE);
-  }
-  __syncwarp();
-  if (lane == 0) {
-    flags[0] |= BSA_MASK_FORCED;
-    flags[i] |= BSA_MASK_FORCED;
-  }
-  __syncwarp();
-
-  // ---- emit the ascending kept list of row i and the optional mask row
-  int32_t *dst = kv_idx + row * static_cast<size_t>(nb);
-  const unsigned lt = (1u << lane) - 1u;
-  int kept = 0;
-  for (int j0 = 0; j0 <= i; j0 += 32) {
-    const int j = j0 + lane;
-    const bool keep = j <= i && flags[j] != 0;
-    const unsigned bl = __ballot_sync(0xffffffffu, keep);
-    if (keep) dst[kept + __popc(bl & lt)] = j;
-    kept += __popc(bl);
-  }
-  if (lane == 0) kv_cnt[row] = kept;
-  if (mask != nullptr) {
-    uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nb));
-    for (int j4 = lane * 4; j4 < nb; j4 += 128) {
-      uint32_t m = 0;
-      if (j4 <= i) {
-        m = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
-        if (j4 + 3 > i) m &= 0xFFFFFFFFu >> (8 * (j4 + 3 - i));  // zero the bytes past i
-      }
-      mrow[j4 >> 2] = m;
-    }
-  }
+  warp_select_row(s_c + row * nb, s_r + row * nb, alpha + gb * nb, i, ppm_c, ppm_r, w);
+  warp_emit_row(w, i, kv_idx + row * static_cast<size_t>(nb), kv_cnt + row,
+                mask != nullptr ? mask + row * static_cast<size_t>(nb) : nullptr, nb);
 }
 
 template <int D, int BLK>
@@ -906,7 +554,7 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
                       status, stream);
   }
   if (e != cudaSuccess) return e;
-  const size_t smem = kSelWarps * select_warp_bytes(s.nbs);
+  const size_t smem = kSelWarps * row_scratch_bytes(s.nbs);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((s.nbs + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);

@@ -289,6 +289,43 @@ bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int
                                         float softmax_scale, void *o, float *lse,
                                         int32_t *dev_status, bsa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Decode: one new token per sequence (q_len = 1) over a packed cache.
+ *
+ * The cache of sequence b is tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of the
+ * packed k, v [total_tokens, hkv, head_dim] (varlen layout above); its last
+ * token is the new one, already appended, so the new query sits at position
+ * len_b - 1 and its row is block i = (len_b - 1) / block.  q_new is bf16
+ * [batch, hq, head_dim]; centroid, radius and alpha are those of the cache
+ * (bsa_varlen_block_meta on it; a block's summary only matters once the block
+ * is complete, since the current block is always kept).
+ *
+ * bsa_decode_select: the selection of a prefill row for a one-token query
+ * block (rescue branch section): scores of the G heads of the new token
+ * against the centroids of blocks 1..i-1, S_c = s max_h q_h . c_j and
+ * R = s max_h (q_h . c_j + alpha_j |q_h| r_j), forced blocks 0 and i, keep
+ * counts from i + 1.  Writes the ascending kept list kv_idx [batch, hkv, nbs]
+ * (int32) and kv_cnt [batch, hkv].  params.flags must be 0.
+ *
+ * bsa_decode_fwd: attention of the new token over the kept blocks' tokens,
+ * split over the kept blocks (a split-KV kernel: decode is bound by memory
+ * traffic, and splitting keeps the whole GPU busy at small batch; section on
+ * decode in "Your Context Length Decides What a Kernel Is Worth").  o: bf16
+ * [batch, hq, head_dim]; lse (nullable) fp32 [batch, hq]; workspace of
+ * bsa_decode_workspace_bytes(shape) bytes, 16-byte aligned, for the fp32
+ * partial results.  An empty sequence gets o = 0 and lse = -inf.
+ * ------------------------------------------------------------------------ */
+size_t bsa_decode_workspace_bytes(const bsa_varlen_shape *shape);
+bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                             const int32_t *cu_seqlens, const void *q_new, const float *centroid,
+                             const float *radius, const float *alpha, int32_t *kv_idx,
+                             int32_t *kv_cnt, int32_t *dev_status, bsa_stream_t stream);
+bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
+                          const void *q_new, const void *k, const void *v, const int32_t *kv_idx,
+                          const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          bsa_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status status);
 
