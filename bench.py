@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--token-max", action="store_true",
                     help="score query blocks by their best token (BSA_SELECT_TOKEN_MAX)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time one decode step (new token per sequence) over the workload as a cache")
     return ap.parse_args()
 
 
@@ -703,10 +705,130 @@ def run_ours(args):
     return 0
 
 
+def run_decode(args):
+    """One decode step per timed step: bsa_decode_select + bsa_decode_fwd for the last token of
+    every sequence of the workload (taken as the KV cache; its block summaries are computed once,
+    as a server keeps them between steps)."""
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import block_sparse_long_kv_gb300 as bsa
+    from block_sparse_long_kv_gb300 import build as bld
+    import synth
+    bld.build()
+    if args.workload in synth.VARLEN_WORKLOADS:
+        vw = synth.VARLEN_WORKLOADS[args.workload]
+        lay = synth.make_varlen_layer(vw)
+    else:
+        w = synth.workload(args.workload)
+        lay0 = synth.make_layer(w)
+        vw = synth.VarlenWorkload(w.name, tuple([w.seq] * w.batch), w.hq, w.hkv, w.head_dim, w.block,
+                                  w.centroid_keep, w.rescue_keep)
+        lay = {x: np.ascontiguousarray(lay0[x].reshape(-1, *lay0[x].shape[2:])) for x in ("q", "k", "v")}
+        lay["cu_seqlens"] = vw.cu_seqlens()
+        del lay0
+    s = bsa.make_varlen_shape(vw.batch, vw.total, vw.max_seqlen, vw.hq, vw.hkv, vw.head_dim, vw.block)
+    nbs = bsa.varlen_block_stride(s)
+    up = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    k, v = up(lay["k"]), up(lay["v"])
+    cu = torch.from_numpy(lay["cu_seqlens"]).to(dev)
+    q_new_h = np.zeros((vw.batch, vw.hq, vw.head_dim), dtype=np.uint16)
+    for b in range(vw.batch):
+        if lay["cu_seqlens"][b + 1] > lay["cu_seqlens"][b]:
+            q_new_h[b] = lay["q"][lay["cu_seqlens"][b + 1] - 1]
+    q_new = up(q_new_h)
+    meta = bsa.alloc_varlen_meta(s, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    bsa.varlen_block_meta(s, cu, k, meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], st)
+    kv_idx = torch.zeros(vw.batch, vw.hkv, nbs, dtype=torch.int32, device=dev)
+    kv_cnt = torch.zeros(vw.batch, vw.hkv, dtype=torch.int32, device=dev)
+    o = torch.empty(vw.batch, vw.hq, vw.head_dim, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(vw.batch, vw.hq, dtype=torch.float32, device=dev)
+    ws = torch.empty(bsa.decode_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    prm = bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0)
+    scale = 1.0 / math.sqrt(vw.head_dim)
+    stream = torch.cuda.current_stream(dev)
+    # an L2-sized buffer rewritten between steps: every step reads its K / V from HBM
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        bsa.decode_select(s, prm, cu, q_new, meta["centroid"], meta["radius"], meta["alpha"], kv_idx,
+                          kv_cnt, ws, st)
+        if evs:
+            evs[1].record(stream)
+        bsa.decode_fwd(s, cu, q_new, k, v, kv_idx, kv_cnt, scale, o, lse, ws, st)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    sel_us = np.array([1e3 * e[0].elapsed_time(e[1]) for e in evs])
+    att_us = np.array([1e3 * e[1].elapsed_time(e[2]) for e in evs])
+    cnt = kv_cnt.cpu().numpy()
+    # algorithmic bytes: the kept blocks' keys and values (the current block only up to the new
+    # token), the candidates' centroids, radii and alphas, q and o
+    kept_tokens = 0
+    for b, n in enumerate(vw.lengths):
+        if n == 0:
+            continue
+        last = (n - 1) // vw.block
+        idx = kv_idx[b].cpu().numpy()
+        for g in range(vw.hkv):
+            js = idx[g, :cnt[b, g]]
+            kept_tokens += sum(min(vw.block, n - j * vw.block) for j in js)
+    kv_bytes = kept_tokens * vw.head_dim * 2 * 2
+    meta_bytes = sum(vw.hkv * (-(-n // vw.block)) * (vw.head_dim + 2) * 4 for n in vw.lengths)
+    io_bytes = vw.batch * vw.hq * vw.head_dim * 2 * 2
+    step_us = sel_us + att_us
+    hbm = float(((kv_bytes + meta_bytes + io_bytes) / (step_us * 1e-6)).mean() / 1e9)
+    att_gbs = float((kv_bytes / (att_us * 1e-6)).mean() / 1e9)
+    pk, src = peaks()
+    hbm_peak = peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm_gb_s")
+    result = {
+        "metric": "decode us/step (new token per sequence, block-sparse split-KV)",
+        "value": float(step_us.mean()), "unit": "us/step", "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": vw.name, "batch": vw.batch, "max_seqlen": vw.max_seqlen,
+                   "total_tokens": vw.total, "hq": vw.hq, "hkv": vw.hkv, "head_dim": vw.head_dim,
+                   "block": vw.block, "centroid_keep": vw.centroid_keep, "rescue_keep": vw.rescue_keep,
+                   "l2": "a 256 MB buffer is rewritten before every step"},
+        "select_us": float(sel_us.mean()), "attention_us": float(att_us.mean()),
+        "kept_fraction": float(cnt.sum()) / sum(vw.hkv * (-(-n // vw.block)) for n in vw.lengths),
+        "roofline": {"kernel": "decode_attn_kernel + decode_combine_kernel (bsa_decode_fwd)",
+                     "bound": "hbm", "achieved": att_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": att_gbs / hbm_peak if hbm_peak else None, "peak_source": f"{src} hbm copy",
+                     "traffic": None, "bytes_per_launch": float(kv_bytes)},
+        "step_hbm_gbs": hbm,
+        "gpu_launches": 4 * K,      # decode score, top-k, attention, combine (the flush is torch's)
+        "clocks": clk,
+    }
+    print(json.dumps(result), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode:
+        return run_decode(args)
     return run_ours(args)
 
 

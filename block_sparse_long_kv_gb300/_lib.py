@@ -65,7 +65,8 @@ SIGNATURES = {
     "bsa_varlen_prefill_dense_fwd": (ctypes.c_int, [_VP, _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                                     _P, _P]),
     "bsa_decode_workspace_bytes": (ctypes.c_size_t, [_VP]),
-    "bsa_decode_select": (ctypes.c_int, [_VP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "bsa_decode_select": (ctypes.c_int, [_VP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                         _P, _P]),
     "bsa_decode_fwd": (ctypes.c_int, [_VP, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                       ctypes.c_size_t, _P, _P]),
     "bsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -285,11 +285,13 @@ def decode_workspace_bytes(shape: VarlenShape) -> int:
 
 
 def decode_select(shape: VarlenShape, params: SelectParams, cu_seqlens, q_new, centroid, radius,
-                  alpha, kv_idx, kv_cnt, dev_status=None, stream=None):
+                  alpha, kv_idx, kv_cnt, workspace=None, dev_status=None, stream=None):
     """bsa_decode_select: kept blocks of each sequence's new token (kv_idx [b, hkv, nbs],
-    kv_cnt [b, hkv])."""
+    kv_cnt [b, hkv]).  ``workspace``: uint8 tensor of decode_workspace_bytes(shape) bytes."""
     b, t, hq, hkv, d, nbs = _vdims(shape)
     lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(shape), dtype=torch.uint8, device=q_new.device)
     _lib.check("bsa_decode_select", lib.bsa_decode_select(
         ctypes.byref(shape), ctypes.byref(params), _cu(cu_seqlens, b),
         _ptr(q_new, "q_new", torch.bfloat16, b * hq * d),
@@ -298,6 +300,7 @@ def decode_select(shape: VarlenShape, params: SelectParams, cu_seqlens, q_new, c
         _ptr(alpha, "alpha", torch.float32, b * hkv * nbs),
         _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs),
         _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 

@@ -320,7 +320,8 @@ size_t bsa_decode_workspace_bytes(const bsa_varlen_shape *shape) {
 bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_params *params,
                              const int32_t *cu_seqlens, const void *q_new, const float *centroid,
                              const float *radius, const float *alpha, int32_t *kv_idx,
-                             int32_t *kv_cnt, int32_t *dev_status, bsa_stream_t stream) {
+                             int32_t *kv_cnt, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, bsa_stream_t stream) {
   const bsa_status st = check_varlen(shape, cu_seqlens);
   if (st != BSA_OK) return st;
   if (!params || !q_new || !centroid || !radius || !alpha || !kv_idx || !kv_cnt)
@@ -331,10 +332,12 @@ bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_par
       !aligned16(kv_idx) || !aligned16(kv_cnt))
     return BSA_ERR_INVALID_ARG;
   const bsa::MaskShape ms = mask_shape(shape, cu_seqlens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::decode_workspace_bytes(ms))
+    return BSA_ERR_WORKSPACE;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
   if (bsa::launch_decode_select(ms, q_new, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
-                                ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, dev_status,
-                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                                ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, workspace,
+                                dev_status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return BSA_ERR_CUDA;
   return BSA_OK;
 }

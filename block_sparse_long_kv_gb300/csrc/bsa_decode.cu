@@ -8,17 +8,19 @@
 // decode paragraphs: decode attention is bound by memory traffic, and a
 // split-KV kernel is what brings a small batch near the card's peak rate.
 //
-// Three launches per step:
-//   decode_select_kernel   one CTA per (b, g): scores of the new token's G
-//                          heads against every earlier key block's centroid
-//                          (one warp per key block, coalesced centroid rows),
-//                          then the same two-path exact top-k as a prefill row
-//                          (shared warp code, bsa_topk.cuh)
-//   decode_attn_kernel     one CTA per (split of kBlocksPerSplit kept blocks,
-//                          b, g): the G heads' logits against each kept key
-//                          (one thread per key), an online softmax over the
-//                          split, and P V with 2 dims x 2 key halves per thread;
-//                          writes the split's unnormalised O, max and sum
+// Selection (bsa_decode_select), two launches:
+//   decode_score_kernel    64 key blocks per CTA, one warp per key block: the
+//                          new token's G heads against the centroid row
+//                          (coalesced), S_c and R into the workspace
+//   decode_topk_kernel     one warp per (b, g): the same two-path exact top-k
+//                          as a prefill row (shared code, bsa_topk.cuh)
+// Attention (bsa_decode_fwd), two launches:
+//   decode_attn_kernel     one CTA per (kept block, b, g): the block's keys and
+//                          values staged in shared memory by cp.async, the G
+//                          heads' logits (one thread per key), an online
+//                          softmax, and P V with 2 dimensions x one key group
+//                          per thread; writes the split's unnormalised O, max
+//                          and sum
 //   decode_combine_kernel  one CTA per (b, h): merges the splits (log-sum-exp)
 //                          and writes O and LSE
 // The cache is a packed batch (sequence b = tokens cu[b] .. cu[b+1]-1, its
@@ -35,46 +37,41 @@ namespace {
 
 using namespace topk;
 
-constexpr int kSelThreads = 256;
 constexpr int kAttnThreads = 128;
-constexpr int kBlocksPerSplit = 2;
+constexpr int kBlocksPerSplit = 1;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-// Dynamic shared memory of the select CTA: q [G][D] fp32, |q| [G], S_c and R
-// rows [nbs] fp32, then one warp's row scratch.
-size_t decode_select_smem(int group, int d, int nbs) {
-  return (static_cast<size_t>(group) * d + 16 + 2 * static_cast<size_t>(nbs)) * 4 + row_scratch_bytes(nbs);
-}
+// ---------------------------------------------------------------- selection
 
+constexpr int kScoreWarps = 8;
+constexpr int kScoreBlocksPerWarp = 8;  // key blocks per warp: 64 per CTA
+
+// S_c[j] and R[j] of the new token of (b, g) for the candidates 1 <= j < i, one
+// warp per key block (a coalesced centroid row per lane group), 64 key blocks
+// per CTA so every SM takes part even at batch 1.
 template <int D>
-__global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
+__global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
     const uint16_t *__restrict__ q_new, const float *__restrict__ centroid, const float *__restrict__ radius,
-    const float *__restrict__ alpha, int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt,
-    const int32_t *__restrict__ cu, int seq, int total, int block, int hq, int hkv, int nbs, long long ppm_c,
-    long long ppm_r, float scale, int32_t *status) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int g = blockIdx.x, b = blockIdx.y;
+    const float *__restrict__ alpha, float *__restrict__ s_c, float *__restrict__ s_r,
+    const int32_t *__restrict__ cu, int seq, int total, int block, int hq, int hkv, int nbs, float scale,
+    int32_t *status) {
+  __shared__ __align__(16) float qs[16 * D];
+  __shared__ float qn[16];
+  const int jt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int grp = hq / hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t gb = static_cast<size_t>(b) * hkv + g;
-  float *qs = reinterpret_cast<float *>(smem);           // [G][D]
-  float *qn = qs + grp * D;                              // [G] (16 slots)
-  float *sc = qn + 16;                                   // [nbs]
-  float *sr = sc + nbs;                                  // [nbs]
-  const RowScratch w = row_scratch(reinterpret_cast<unsigned char *>(sr + nbs), nbs);
-
   const SeqSpan sp = seq_span(cu, b, seq, total, status);
-  if (sp.len == 0) {
-    if (tid == 0) kv_cnt[gb] = 0;
-    return;
-  }
+  if (sp.len == 0) return;
   const int i = (sp.len - 1) / block;  // the new token's block
+  const int j0 = jt * kScoreWarps * kScoreBlocksPerWarp;
+  if (j0 >= i) return;
   const uint16_t *qrow = q_new + (static_cast<size_t>(b) * hq + static_cast<size_t>(g) * grp) * D;
-  for (int e = tid; e < grp * D; e += kSelThreads) qs[e] = bf16f(qrow[e]);
+  for (int e = tid; e < grp * D; e += kScoreWarps * 32) qs[e] = bf16f(qrow[e]);
   __syncthreads();
-  for (int h = warp; h < grp; h += kSelThreads / 32) {
+  for (int h = warp; h < grp; h += kScoreWarps) {
     float s2 = 0.f;
     for (int x = lane; x < D; x += 32) s2 = fmaf(qs[h * D + x], qs[h * D + x], s2);
 #pragma unroll
@@ -82,10 +79,10 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
     if (lane == 0) qn[h] = sqrtf(s2);
   }
   __syncthreads();
-
-  // S_c[j], R[j] for the candidates 1 <= j < i: one warp per key block
   constexpr int DPL = D / 32;  // dimensions per lane
-  for (int j = 1 + warp; j < i; j += kSelThreads / 32) {
+  for (int r = 0; r < kScoreBlocksPerWarp; ++r) {
+    const int j = j0 + warp * kScoreBlocksPerWarp + r;
+    if (j < 1 || j >= i) continue;  // warp-uniform
     const float *crow = centroid + (gb * nbs + j) * D + lane * DPL;
     float c[DPL];
 #pragma unroll
@@ -102,34 +99,78 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
       rm = fmaxf(rm, fmaf(qn[h], bonus, p));
     }
     if (lane == 0) {
-      sc[j] = dm * scale;
-      sr[j] = rm * scale;
+      s_c[gb * nbs + j] = dm * scale;
+      s_r[gb * nbs + j] = rm * scale;
     }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    warp_select_row(sc, sr, alpha + gb * nbs, i, ppm_c, ppm_r, w);
-    warp_emit_row(w, i, kv_idx + gb * nbs, kv_cnt + gb, nullptr, nbs);
   }
 }
 
+// One warp per (b, g): the two-path exact top-k of the new token's row (the
+// prefill row code, bsa_topk.cuh) and the ascending kept list.
+__global__ void __launch_bounds__(32) decode_topk_kernel(
+    const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
+    int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, const int32_t *__restrict__ cu, int seq,
+    int total, int block, int hkv, int nbs, long long ppm_c, long long ppm_r, int32_t *status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int g = blockIdx.x, b = blockIdx.y;
+  const size_t gb = static_cast<size_t>(b) * hkv + g;
+  const SeqSpan sp = seq_span(cu, b, seq, total, status);
+  if (sp.len == 0) {
+    if (threadIdx.x == 0) kv_cnt[gb] = 0;
+    return;
+  }
+  const int i = (sp.len - 1) / block;
+  const RowScratch w = row_scratch(smem, nbs);
+  warp_select_row(s_c + gb * nbs, s_r + gb * nbs, alpha + gb * nbs, i, ppm_c, ppm_r, w);
+  warp_emit_row(w, i, kv_idx + gb * nbs, kv_cnt + gb, nullptr, nbs);
+}
+
+// ---------------------------------------------------------------- attention
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+template <int D, int G>
+struct DecCfg {
+  static constexpr int KCH = 128;                    // keys per chunk = threads
+  static constexpr int KROW = D * 2 + 16;            // padded key row (bytes): conflict-free row reads
+  static constexpr int DP = D / 2;                   // dimension pairs
+  static constexpr int KH = kAttnThreads / DP;       // key groups in P V
+  static constexpr size_t OFF_K = 0;
+  static constexpr size_t OFF_V = OFF_K + static_cast<size_t>(KCH) * KROW;
+  static constexpr size_t OFF_Q = OFF_V + static_cast<size_t>(KCH) * D * 2;
+  static constexpr size_t OFF_P = OFF_Q + static_cast<size_t>(G) * D * 4;
+  static constexpr size_t SMEM = OFF_P + static_cast<size_t>(G) * KCH * 4;
+  // the key-half O partials reuse the key buffer after the last chunk
+  static_assert(static_cast<size_t>(KH > 1 ? KH - 1 : 1) * G * D * 4 <= static_cast<size_t>(KCH) * KROW,
+                "O partials fit in the key buffer");
+};
+
 // Split s of row (b, g): kept blocks [s * kBlocksPerSplit, ...) of the list.
-// Thread t is key t of a 128-key chunk for the logits and, for P V, owns the
-// dimension pair 2 * (t % (D/2)) of key half t / (D/2).
+// Each 128-key chunk is staged in shared memory by cp.async (key rows padded,
+// value rows dense); thread t takes key t for the G logits and, for P V, the
+// dimension pair 2 * (t % (D/2)) of key group t / (D/2).
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
     const uint16_t *__restrict__ q_new, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const int32_t *__restrict__ kv_idx, const int32_t *__restrict__ kv_cnt, float *__restrict__ part_o,
     float *__restrict__ part_ml, const int32_t *__restrict__ cu, int seq, int total, int block, int hkv,
     int nbs, int nsplit, float scale_log2, int32_t *status) {
-  constexpr int KCH = 128;          // keys per chunk = threads
-  constexpr int DP = D / 2;         // dimension pairs
-  constexpr int KH = kAttnThreads / DP;  // key groups in P V (2 for D = 128, 4 for D = 64)
-  __shared__ __align__(16) float qs[G][D];
-  __shared__ float ps[G][KCH];
+  using C = DecCfg<D, G>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char *ks = smem + C::OFF_K;
+  const uint16_t *vs = reinterpret_cast<const uint16_t *>(smem + C::OFF_V);
+  float (*qs)[D] = reinterpret_cast<float (*)[D]>(smem + C::OFF_Q);
+  float (*ps)[C::KCH] = reinterpret_cast<float (*)[C::KCH]>(smem + C::OFF_P);
   __shared__ float red[G][kAttnThreads / 32];
   __shared__ float mrun[G];
-  __shared__ float oacc[KH > 1 ? KH - 1 : 1][G][D];
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,10 +184,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
   const uint16_t *qrow = q_new + (static_cast<size_t>(b) * hq + static_cast<size_t>(g) * G) * D;
   for (int e = tid; e < G * D; e += kAttnThreads) qs[e / D][e % D] = bf16f(qrow[e]) * scale_log2;
   if (tid < G) mrun[tid] = -INFINITY;
-  __syncthreads();
 
   const size_t tok_stride = static_cast<size_t>(hkv) * D;
-  const int dp = tid % DP, kh = tid / DP;
+  const int dp = tid % C::DP, kh = tid / C::DP;
   float o[G][2];
   float lsum[G];
 #pragma unroll
@@ -156,20 +196,35 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
   }
   const int last = (sp.len - 1) / block;
   for (int e = e0; e < e1; ++e) {
-    int j = kv_idx[gb * nbs + e];
-    if (j < 0 || j > last) continue;  // a malformed list entry is skipped
+    const int j = kv_idx[gb * nbs + e];
+    if (j < 0 || j > last) continue;  // a malformed list entry is skipped (CTA-uniform)
     const int nk = min(block, sp.len - j * block);  // keys of block j
-    for (int c0 = 0; c0 < nk; c0 += KCH) {
-      const int kk = c0 + tid;
-      const bool valid = kk < nk;
-      // ---- logits of key kk for the G heads (log2 units)
+    for (int c0 = 0; c0 < nk; c0 += C::KCH) {
+      const int kend = min(C::KCH, nk - c0);
+      __syncthreads();  // the previous chunk's K, V and P are no longer read
+      {
+        // stage the chunk's key and value rows: D*2/16 pieces of 16 bytes per row
+        constexpr int PR = D * 2 / 16;
+        const uint16_t *kg = k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * block + c0) * tok_stride +
+                             static_cast<size_t>(g) * D;
+        const uint16_t *vg = v + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * block + c0) * tok_stride +
+                             static_cast<size_t>(g) * D;
+        for (int x = tid; x < kend * PR; x += kAttnThreads) {
+          const int r = x / PR, pc = x - r * PR;
+          cp_async16(ks + r * C::KROW + pc * 16, kg + static_cast<size_t>(r) * tok_stride + pc * 8);
+          cp_async16(smem + C::OFF_V + (static_cast<size_t>(r) * D + pc * 8) * 2,
+                     vg + static_cast<size_t>(r) * tok_stride + pc * 8);
+        }
+        cp_async_wait_all();
+      }
+      __syncthreads();
+      const bool valid = tid < kend;
+      // ---- logits of key c0 + tid for the G heads (log2 units)
       float lg[G];
-      if (valid) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(
-            k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * block + kk) * tok_stride +
-            static_cast<size_t>(g) * D);
 #pragma unroll
-        for (int h = 0; h < G; ++h) lg[h] = 0.f;
+      for (int h = 0; h < G; ++h) lg[h] = valid ? 0.f : -INFINITY;
+      if (valid) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(ks + tid * C::KROW);
 #pragma unroll 4
         for (int x8 = 0; x8 < D / 8; ++x8) {
           const uint4 u = kr[x8];
@@ -184,19 +239,18 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
           for (int h = 0; h < G; ++h) {
             const float4 qa = *reinterpret_cast<const float4 *>(&qs[h][x8 * 8]);
             const float4 qb = *reinterpret_cast<const float4 *>(&qs[h][x8 * 8 + 4]);
-            lg[h] = fmaf(qa.x, kf[0], lg[h]);
-            lg[h] = fmaf(qa.y, kf[1], lg[h]);
-            lg[h] = fmaf(qa.z, kf[2], lg[h]);
-            lg[h] = fmaf(qa.w, kf[3], lg[h]);
-            lg[h] = fmaf(qb.x, kf[4], lg[h]);
-            lg[h] = fmaf(qb.y, kf[5], lg[h]);
-            lg[h] = fmaf(qb.z, kf[6], lg[h]);
-            lg[h] = fmaf(qb.w, kf[7], lg[h]);
+            float a = lg[h];
+            a = fmaf(qa.x, kf[0], a);
+            a = fmaf(qa.y, kf[1], a);
+            a = fmaf(qa.z, kf[2], a);
+            a = fmaf(qa.w, kf[3], a);
+            a = fmaf(qb.x, kf[4], a);
+            a = fmaf(qb.y, kf[5], a);
+            a = fmaf(qb.z, kf[6], a);
+            a = fmaf(qb.w, kf[7], a);
+            lg[h] = a;
           }
         }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) lg[h] = -INFINITY;
       }
       // ---- chunk max per head, new running max, probabilities
 #pragma unroll
@@ -224,19 +278,17 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
 #pragma unroll
         for (int h = 0; h < G; ++h) mrun[h] = lg[h];
       }
-      // ---- P V for this thread's dimension pair and key half
+      // ---- P V for this thread's dimension pair and key group
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         o[h][0] *= factor[h];
         o[h][1] *= factor[h];
         lsum[h] *= factor[h];
       }
-      const uint32_t *vcol = reinterpret_cast<const uint32_t *>(
-          v + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * block + c0) * tok_stride +
-          static_cast<size_t>(g) * D + 2 * dp);
-      const int kend = min(KCH, nk - c0);
-      for (int s = kh; s < kend; s += KH) {
-        const uint32_t vv = vcol[static_cast<size_t>(s) * (tok_stride / 2)];
+      const uint32_t *vcol = reinterpret_cast<const uint32_t *>(vs) + dp;
+#pragma unroll 4
+      for (int s = kh; s < kend; s += C::KH) {
+        const uint32_t vv = vcol[s * (D / 2)];
         const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -246,10 +298,10 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
           lsum[h] += p;
         }
       }
-      __syncthreads();  // ps and mrun are rewritten by the next chunk
     }
   }
-  // ---- combine the key halves in a fixed order, write the split's partials
+  __syncthreads();  // the key buffer becomes the key groups' O partials
+  float (*oacc)[G][D] = reinterpret_cast<float (*)[G][D]>(ks);
   if (kh > 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -263,7 +315,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
     for (int h = 0; h < G; ++h) {
       float a0 = o[h][0], a1 = o[h][1];
 #pragma unroll
-      for (int x = 0; x < KH - 1; ++x) {
+      for (int x = 0; x < C::KH - 1; ++x) {
         a0 += oacc[x][h][2 * dp];
         a1 += oacc[x][h][2 * dp + 1];
       }
@@ -272,7 +324,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
       part_o[po + 2 * dp + 1] = a1;
     }
   }
-  // the normaliser: each key half summed its own keys' probabilities; add the halves of
+  // the normaliser: each key group summed its own keys' probabilities; add the groups of
   // dimension pair 0 in the same fixed order
   __syncthreads();
   if (dp == 0 && kh > 0) {
@@ -285,7 +337,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
     for (int h = 0; h < G; ++h) {
       float l = lsum[h];
 #pragma unroll
-      for (int x = 0; x < KH - 1; ++x) l += oacc[x][h][0];
+      for (int x = 0; x < C::KH - 1; ++x) l += oacc[x][h][0];
       const size_t pm = ((static_cast<size_t>(b) * hq + static_cast<size_t>(g) * G + h) * nsplit + split) * 2;
       part_ml[pm] = mrun[h];
       part_ml[pm + 1] = l;
@@ -293,26 +345,55 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
   }
 }
 
+// One CTA per (b, h): the splits' maxima and sums reduced across the CTA, then
+// O = sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max m), 8 splits'
+// partial rows in flight per thread.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(
     const float *__restrict__ part_o, const float *__restrict__ part_ml, const int32_t *__restrict__ kv_cnt,
     uint16_t *__restrict__ o, float *__restrict__ lse, const int32_t *__restrict__ cu, int seq, int total,
     int block, int hq, int hkv, int nsplit, int32_t *status) {
-  const int h = blockIdx.x, b = blockIdx.y, x = threadIdx.x;
+  extern __shared__ float wsm[];  // [nsplit] weights
+  __shared__ float redm[D / 32], redl[D / 32];
+  const int h = blockIdx.x, b = blockIdx.y, x = threadIdx.x, lane = x & 31, warp = x >> 5;
   const int g = h / (hq / hkv);
   const SeqSpan sp = seq_span(cu, b, seq, total, status);
   const int cnt = sp.len > 0 ? min(kv_cnt[static_cast<size_t>(b) * hkv + g], (sp.len - 1) / block + 1) : 0;
   const int ns = (cnt + kBlocksPerSplit - 1) / kBlocksPerSplit;
   const size_t base = (static_cast<size_t>(b) * hq + h) * nsplit;
   float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, part_ml[(base + s) * 2]);
-  float l = 0.f, acc = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  for (int s = x; s < ns; s += D) m = fmaxf(m, part_ml[(base + s) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) redm[warp] = m;
+  __syncthreads();
+  m = redm[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) m = fmaxf(m, redm[w]);
+  float l = 0.f;
+  for (int s = x; s < ns; s += D) {
     const float ms = part_ml[(base + s) * 2];
-    const float f = ms == -INFINITY ? 0.f : exp2f(ms - m);
-    l = fmaf(part_ml[(base + s) * 2 + 1], f, l);
-    acc = fmaf(part_o[(base + s) * D + x], f, acc);
+    const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - m);
+    wsm[s] = wgt;
+    l = fmaf(part_ml[(base + s) * 2 + 1], wgt, l);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  if (lane == 0) redl[warp] = l;
+  __syncthreads();
+  l = 0.f;
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) l += redl[w];
+  float acc = 0.f;
+  int s = 0;
+  for (; s + 8 <= ns; s += 8) {
+    float pv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) pv[u] = part_o[(base + s + u) * D + x];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc = fmaf(pv[u], wsm[s + u], acc);
+  }
+  for (; s < ns; ++s) acc = fmaf(part_o[(base + s) * D + x], wsm[s], acc);
   const float r = l > 0.f ? acc / l : 0.f;
   const __nv_bfloat16 rb = __float2bfloat16_rn(r);
   o[(static_cast<size_t>(b) * hq + h) * D + x] = *reinterpret_cast<const uint16_t *>(&rb);
@@ -324,8 +405,12 @@ template <int D, int G>
 cudaError_t launch_attn_g(const MaskShape &s, const void *q_new, const void *k, const void *v,
                           const int32_t *kv_idx, const int32_t *kv_cnt, float *po, float *pml, int nsplit,
                           float scale_log2, int32_t *status, cudaStream_t stream) {
+  using C = DecCfg<D, G>;
+  auto kern = decode_attn_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
   dim3 grid(nsplit, s.hkv, s.batch);
-  decode_attn_kernel<D, G><<<grid, kAttnThreads, 0, stream>>>(
+  kern<<<grid, kAttnThreads, C::SMEM, stream>>>(
       static_cast<const uint16_t *>(q_new), static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
       kv_idx, kv_cnt, po, pml, s.cu, s.seq, s.total, s.block, s.hkv, s.nbs, nsplit, scale_log2, status);
   return cudaGetLastError();
@@ -347,37 +432,55 @@ cudaError_t launch_attn_d(const MaskShape &s, const void *q_new, const void *k, 
 
 int decode_splits(const MaskShape &s) { return (s.nbs + kBlocksPerSplit - 1) / kBlocksPerSplit; }
 
+// Workspace regions (each 256-byte aligned): partial O [b, hq, nsplit, d], partial (max, sum)
+// [b, hq, nsplit, 2], then the selection's S_c and R rows [b, hkv, nbs].
+struct DecRegions {
+  size_t po, pml, sc, sr, total;
+};
+
+DecRegions decode_regions(const MaskShape &s) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(s.batch) * s.hq * decode_splits(s);
+  const size_t srow = static_cast<size_t>(s.batch) * s.hkv * s.nbs * 4;
+  DecRegions r;
+  r.po = 0;
+  r.pml = r.po + r256(rows * s.d * 4);
+  r.sc = r.pml + r256(rows * 2 * 4);
+  r.sr = r.sc + r256(srow);
+  r.total = r.sr + r256(srow);
+  return r;
+}
+
 }  // namespace
 
-size_t decode_workspace_bytes(const MaskShape &s) {
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * decode_splits(s);
-  return (rows * s.d * 4 + 255) / 256 * 256 + rows * 2 * 4;
-}
+size_t decode_workspace_bytes(const MaskShape &s) { return decode_regions(s).total; }
 
 cudaError_t launch_decode_select(const MaskShape &s, const void *q_new, const float *centroid,
                                  const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                                 float scale, int32_t *kv_idx, int32_t *kv_cnt, int32_t *status,
-                                 cudaStream_t stream) {
-  const size_t smem = decode_select_smem(s.group, s.d, s.nbs);
-  dim3 grid(s.hkv, s.batch);
-  cudaError_t e;
-  if (s.d == 64) {
-    e = cudaFuncSetAttribute(decode_select_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_select_kernel<64><<<grid, kSelThreads, smem, stream>>>(
-        static_cast<const uint16_t *>(q_new), centroid, radius, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
-        s.block, s.hq, s.hkv, s.nbs, static_cast<long long>(ppm_c), static_cast<long long>(ppm_r), scale, status);
-  } else if (s.d == 128) {
-    e = cudaFuncSetAttribute(decode_select_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_select_kernel<128><<<grid, kSelThreads, smem, stream>>>(
-        static_cast<const uint16_t *>(q_new), centroid, radius, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
-        s.block, s.hq, s.hkv, s.nbs, static_cast<long long>(ppm_c), static_cast<long long>(ppm_r), scale, status);
-  } else {
+                                 float scale, int32_t *kv_idx, int32_t *kv_cnt, void *workspace,
+                                 int32_t *status, cudaStream_t stream) {
+  const DecRegions r = decode_regions(s);
+  float *sc = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.sc);
+  float *sr = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.sr);
+  dim3 grid((s.nbs + kScoreWarps * kScoreBlocksPerWarp - 1) / (kScoreWarps * kScoreBlocksPerWarp), s.hkv, s.batch);
+  if (s.d == 64)
+    decode_score_kernel<64><<<grid, kScoreWarps * 32, 0, stream>>>(
+        static_cast<const uint16_t *>(q_new), centroid, radius, alpha, sc, sr, s.cu, s.seq, s.total, s.block,
+        s.hq, s.hkv, s.nbs, scale, status);
+  else if (s.d == 128)
+    decode_score_kernel<128><<<grid, kScoreWarps * 32, 0, stream>>>(
+        static_cast<const uint16_t *>(q_new), centroid, radius, alpha, sc, sr, s.cu, s.seq, s.total, s.block,
+        s.hq, s.hkv, s.nbs, scale, status);
+  else
     return cudaErrorInvalidValue;
-  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = row_scratch_bytes(s.nbs);
+  e = cudaFuncSetAttribute(decode_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  decode_topk_kernel<<<dim3(s.hkv, s.batch), 32, smem, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
+                                                                 s.block, s.hkv, s.nbs, static_cast<long long>(ppm_c),
+                                                                 static_cast<long long>(ppm_r), status);
   return cudaGetLastError();
 }
 
@@ -385,9 +488,9 @@ cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, 
                           const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,
                           void *workspace, int32_t *status, cudaStream_t stream) {
   const int nsplit = decode_splits(s);
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * nsplit;
-  float *po = static_cast<float *>(workspace);
-  float *pml = reinterpret_cast<float *>(static_cast<char *>(workspace) + (rows * s.d * 4 + 255) / 256 * 256);
+  const DecRegions r = decode_regions(s);
+  float *po = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.po);
+  float *pml = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.pml);
   const float sl2 = scale * kLog2e;
   cudaError_t e;
   if (s.d == 64) e = launch_attn_d<64>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, sl2, status, stream);
@@ -395,12 +498,14 @@ cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, 
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   dim3 grid(s.hq, s.batch);
+  const size_t csmem = static_cast<size_t>(nsplit) * 4;
   if (s.d == 64)
-    decode_combine_kernel<64><<<grid, 64, 0, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o), lse, s.cu,
-                                                       s.seq, s.total, s.block, s.hq, s.hkv, nsplit, status);
+    decode_combine_kernel<64><<<grid, 64, csmem, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o), lse, s.cu,
+                                                           s.seq, s.total, s.block, s.hq, s.hkv, nsplit, status);
   else
-    decode_combine_kernel<128><<<grid, 128, 0, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o), lse, s.cu,
-                                                         s.seq, s.total, s.block, s.hq, s.hkv, nsplit, status);
+    decode_combine_kernel<128><<<grid, 128, csmem, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o), lse,
+                                                             s.cu, s.seq, s.total, s.block, s.hq, s.hkv, nsplit,
+                                                             status);
   return cudaGetLastError();
 }
 

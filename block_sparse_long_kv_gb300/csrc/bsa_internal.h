@@ -86,8 +86,8 @@ cudaError_t launch_token_scores(const MaskShape &s, const void *q, const float *
 // lse [b, hq]) with fp32 partials in the workspace.
 cudaError_t launch_decode_select(const MaskShape &s, const void *q_new, const float *centroid,
                                  const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                                 float scale, int32_t *kv_idx, int32_t *kv_cnt, int32_t *status,
-                                 cudaStream_t stream);
+                                 float scale, int32_t *kv_idx, int32_t *kv_cnt, void *workspace,
+                                 int32_t *status, cudaStream_t stream);
 size_t decode_workspace_bytes(const MaskShape &s);
 cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, const void *v,
                           const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,

@@ -305,7 +305,8 @@ bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int
  * against the centroids of blocks 1..i-1, S_c = s max_h q_h . c_j and
  * R = s max_h (q_h . c_j + alpha_j |q_h| r_j), forced blocks 0 and i, keep
  * counts from i + 1.  Writes the ascending kept list kv_idx [batch, hkv, nbs]
- * (int32) and kv_cnt [batch, hkv].  params.flags must be 0.
+ * (int32) and kv_cnt [batch, hkv].  params.flags must be 0.  workspace: as
+ * for bsa_decode_fwd (the same buffer may serve both calls on one stream).
  *
  * bsa_decode_fwd: attention of the new token over the kept blocks' tokens,
  * split over the kept blocks (a split-KV kernel: decode is bound by memory
@@ -319,7 +320,8 @@ size_t bsa_decode_workspace_bytes(const bsa_varlen_shape *shape);
 bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_params *params,
                              const int32_t *cu_seqlens, const void *q_new, const float *centroid,
                              const float *radius, const float *alpha, int32_t *kv_idx,
-                             int32_t *kv_cnt, int32_t *dev_status, bsa_stream_t stream);
+                             int32_t *kv_cnt, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, bsa_stream_t stream);
 bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqlens,
                           const void *q_new, const void *k, const void *v, const int32_t *kv_idx,
                           const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,

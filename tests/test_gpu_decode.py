@@ -50,12 +50,14 @@ def gpu_decode(vw, lay, q_new, rc=None, rr=None, lists=None):
     kv_idx = torch.zeros(vw.batch, vw.hkv, nbs, dtype=torch.int32, device="cuda")
     kv_cnt = torch.zeros(vw.batch, vw.hkv, dtype=torch.int32, device="cuda")
     prm = bsa.SelectParams(vw.centroid_keep if rc is None else rc, vw.rescue_keep if rr is None else rr, 0)
-    bsa.decode_select(s, prm, cu, qn, meta["centroid"], meta["radius"], meta["alpha"], kv_idx, kv_cnt, st)
+    ws = torch.empty(bsa.decode_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    bsa.decode_select(s, prm, cu, qn, meta["centroid"], meta["radius"], meta["alpha"], kv_idx, kv_cnt,
+                      ws, st)
     if lists is not None:
         kv_idx, kv_cnt = lists
     o = torch.full((vw.batch, vw.hq, vw.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((vw.batch, vw.hq), float("nan"), dtype=torch.float32, device="cuda")
-    bsa.decode_fwd(s, cu, qn, k, v, kv_idx, kv_cnt, 1.0 / math.sqrt(vw.head_dim), o, lse, dev_status=st)
+    bsa.decode_fwd(s, cu, qn, k, v, kv_idx, kv_cnt, 1.0 / math.sqrt(vw.head_dim), o, lse, ws, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return dict(kv_idx=kv_idx.cpu().numpy(), kv_cnt=kv_cnt.cpu().numpy(), o=o.float().cpu().numpy(),
