@@ -35,6 +35,7 @@ __all__ = [
     "Workload", "WORKLOADS", "workload", "sweep_workloads", "make_layer",
     "VarlenWorkload", "VARLEN_WORKLOADS", "make_varlen_layer",
     "bf16_bits", "bf16_to_f64", "bf16_to_f32",
+    "E4M3_VALUES", "e4m3_bits", "e4m3_to_f64", "fp8_layer",
 ]
 
 _CHUNK_TOKENS = 4096
@@ -119,6 +120,58 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_to_f32(bits).astype(np.float64)
+
+
+# ---------------------------------------------------------------- fp8 (e4m3) helpers
+#
+# OCP FP8 E4M3 as used by the tensor cores' e4m3 type: 1 sign bit, 4 exponent
+# bits (bias 7), 3 mantissa bits, no infinities, S.1111.111 is NaN, largest
+# finite 448, subnormals m * 2^-9.
+
+def _e4m3_table() -> np.ndarray:
+    vals = np.zeros(128)
+    for code in range(128):
+        e, m = code >> 3, code & 7
+        vals[code] = m * 2.0 ** -9 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    vals[127] = np.nan
+    return vals
+
+
+E4M3_VALUES = _e4m3_table()  # value of each non-negative code 0..127 (127 is NaN)
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float -> e4m3 codes (uint8): round to nearest, ties to the even code, saturating at
+    +-448 (finite inputs only)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    finite = E4M3_VALUES[:127]                        # ascending, codes 0..126
+    hi = np.clip(np.searchsorted(finite, a, side="left"), 0, 126)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - finite[lo]
+    d_hi = finite[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(a == finite[hi], hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    return np.where(np.signbit(x) & (code != 0), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint8)
+    v = E4M3_VALUES[b & 0x7F]
+    return np.where(b & 0x80, -v, v)
+
+
+def fp8_layer(lay: dict) -> dict:
+    """The layer's Q, K, V (bf16 bits) as e4m3 codes with one power-of-two scale per tensor:
+    value = e4m3 * scale, scale = 2^ceil(log2(max|x| / 448))."""
+    out = {}
+    for name in ("q", "k", "v"):
+        x = bf16_to_f32(lay[name]).astype(np.float64)
+        mx = float(np.abs(x).max()) if x.size else 1.0
+        scale = 2.0 ** int(np.ceil(np.log2(max(mx, 1e-30) / 448.0)))
+        out[name] = e4m3_bits(x / scale)
+        out[name + "_scale"] = scale
+    return out
 
 
 # ---------------------------------------------------------------- generator
