@@ -22,6 +22,7 @@ __all__ = [
     "varlen_select_workspace_bytes", "varlen_select_mask", "varlen_prefill_fwd",
     "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
     "decode_workspace_bytes", "decode_select", "decode_fwd",
+    "block_meta_fp8", "select_mask_fp8", "prefill_fwd_fp8", "prefill_dense_fwd_fp8",
 ]
 
 Shape = _lib.Shape
@@ -174,6 +175,68 @@ def alloc_select(shape: Shape, device="cuda", with_mask: bool = True) -> dict:
 
 def alloc_layer_workspace(shape: Shape, device="cuda") -> torch.Tensor:
     return torch.empty(prefill_layer_workspace_bytes(shape), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- fp8 (e4m3) inputs
+# q, k, v: uint8 CUDA tensors of e4m3 codes in the bf16 layouts; value = code * scale.
+
+def block_meta_fp8(shape: Shape, k, k_scale, centroid, radius, quant, alpha, dev_status=None,
+                   stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_block_meta_fp8", lib.bsa_block_meta_fp8(
+        ctypes.byref(shape), _ptr(k, "k", torch.uint8, b * n * hkv * d), ctypes.c_float(k_scale),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
+        _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(quant, "quant", torch.float32, b * hkv * 2),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def select_mask_fp8(shape: Shape, params: SelectParams, q, q_scale, centroid, radius, alpha, kv_idx,
+                    kv_cnt, mask=None, workspace=None, dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(select_workspace_bytes(shape), dtype=torch.uint8, device=q.device)
+    _lib.check("bsa_select_mask_fp8", lib.bsa_select_mask_fp8(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.uint8, b * n * hq * d),
+        ctypes.c_float(q_scale),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
+        _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb),
+        _ptr(mask, "mask", torch.uint8, b * hkv * nb * nb),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def prefill_fwd_fp8(shape: Shape, q, k, v, q_scale, k_scale, v_scale, kv_idx, kv_cnt, softmax_scale,
+                    o, lse=None, dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_prefill_fwd_fp8", lib.bsa_prefill_fwd_fp8(
+        ctypes.byref(shape), _ptr(q, "q", torch.uint8, b * n * hq * d),
+        _ptr(k, "k", torch.uint8, b * n * hkv * d), _ptr(v, "v", torch.uint8, b * n * hkv * d),
+        ctypes.c_float(q_scale), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb), ctypes.c_float(softmax_scale),
+        _ptr(o, "o", torch.bfloat16, b * n * hq * d), _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def prefill_dense_fwd_fp8(shape: Shape, q, k, v, q_scale, k_scale, v_scale, softmax_scale, o,
+                          lse=None, dev_status=None, stream=None):
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    _lib.check("bsa_prefill_dense_fwd_fp8", lib.bsa_prefill_dense_fwd_fp8(
+        ctypes.byref(shape), _ptr(q, "q", torch.uint8, b * n * hq * d),
+        _ptr(k, "k", torch.uint8, b * n * hkv * d), _ptr(v, "v", torch.uint8, b * n * hkv * d),
+        ctypes.c_float(q_scale), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+        ctypes.c_float(softmax_scale), _ptr(o, "o", torch.bfloat16, b * n * hq * d),
+        _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 
 # ---------------------------------------------------------------- packed ragged batches

@@ -67,7 +67,19 @@ bsa::MaskShape mask_shape(const bsa_varlen_shape *s, const int32_t *cu) {
 }
 
 bsa::AttnShape attn_shape(const bsa::MaskShape &m) {
-  return bsa::AttnShape{m.batch, m.seq, m.hq, m.hkv, m.d, m.block, m.nb, m.group, m.cu, m.total, m.nbs};
+  return bsa::AttnShape{m.batch, m.seq, m.hq, m.hkv, m.d, m.block, m.nb, m.group, m.cu, m.total, m.nbs,
+                        m.fp8, m.q_scale, m.k_scale, m.v_scale};
+}
+
+bool scale_ok(float x) { return x > 0.f && !isinf(x); }  // false for NaN
+
+bsa::MaskShape fp8_shape(const bsa_shape *s, float q_scale, float k_scale, float v_scale) {
+  bsa::MaskShape m = mask_shape(s);
+  m.fp8 = 1;
+  m.q_scale = q_scale;
+  m.k_scale = k_scale;
+  m.v_scale = v_scale;
+  return m;
 }
 
 bool ratio_ok(float r) { return r >= 0.f && r <= 1.f; }  // false for NaN
@@ -249,6 +261,56 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
   if (st != BSA_OK) return st;
   return layer_impl(mask_shape(shape), params, q, k, v, softmax_scale, o, lse, workspace,
                     workspace_bytes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------- fp8 (e4m3) inputs
+
+bsa_status bsa_block_meta_fp8(const bsa_shape *shape, const void *k, float k_scale, float *centroid,
+                              float *radius, float *quant, float *alpha, int32_t *dev_status,
+                              bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  if (!scale_ok(k_scale)) return BSA_ERR_INVALID_ARG;
+  return meta_impl(fp8_shape(shape, 1.f, k_scale, 1.f), k, centroid, radius, quant, alpha, dev_status,
+                   stream);
+}
+
+bsa_status bsa_select_mask_fp8(const bsa_shape *shape, const bsa_select_params *params,
+                               const void *q, float q_scale, const float *centroid,
+                               const float *radius, const float *alpha, int32_t *kv_idx,
+                               int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  if (!scale_ok(q_scale)) return BSA_ERR_INVALID_ARG;
+  if (params != nullptr && (params->flags & BSA_SELECT_TOKEN_MAX)) return BSA_ERR_UNSUPPORTED;
+  return select_impl(fp8_shape(shape, q_scale, 1.f, 1.f), params, q, centroid, radius, alpha, kv_idx,
+                     kv_cnt, mask, workspace, workspace_bytes, dev_status, stream);
+}
+
+bsa_status bsa_prefill_fwd_fp8(const bsa_shape *shape, const void *q, const void *k, const void *v,
+                               float q_scale, float k_scale, float v_scale, const int32_t *kv_idx,
+                               const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
+                               int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  if (!kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
+  if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale)) return BSA_ERR_INVALID_ARG;
+  if (shape->head_dim != 128) return BSA_ERR_UNSUPPORTED;
+  return prefill_impl(fp8_shape(shape, q_scale, k_scale, v_scale), q, k, v, kv_idx, kv_cnt, softmax_scale,
+                      o, lse, dev_status, stream);
+}
+
+bsa_status bsa_prefill_dense_fwd_fp8(const bsa_shape *shape, const void *q, const void *k,
+                                     const void *v, float q_scale, float k_scale, float v_scale,
+                                     float softmax_scale, void *o, float *lse, int32_t *dev_status,
+                                     bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale)) return BSA_ERR_INVALID_ARG;
+  if (shape->head_dim != 128) return BSA_ERR_UNSUPPORTED;
+  return prefill_impl(fp8_shape(shape, q_scale, k_scale, v_scale), q, k, v, nullptr, nullptr,
+                      softmax_scale, o, lse, dev_status, stream);
 }
 
 // ---------------------------------------------------------------- packed ragged batches

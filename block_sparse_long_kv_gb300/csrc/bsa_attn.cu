@@ -28,6 +28,13 @@
 // setmaxnreg moves registers from the producer / MMA warpgroup to the softmax
 // warps; the host refuses to launch if the compiled register count differs
 // from the budget the split assumes.
+// FP8 inputs (F8): Q, K and V arrive as e4m3 codes with per-tensor scales.
+// S = Q K^T runs as kind::f8f6f4 (both operands K-major, K = 32 per MMA);
+// warps 2-3 convert each e4m3 V tile (loaded unswizzled by TMA) into the
+// bf16 MN-major layout the P V MMA reads (exact: e4m3 values are bf16
+// values), so P stays bf16 in TMEM and O matches the bf16 path's accuracy on
+// the dequantised inputs.  The scales fold into the softmax scale and the
+// final 1 / l.
 // TMEM columns: S_t at t*KT, O_t at NT*KT + t*D (fp32 accumulators, one TMEM
 // lane per query row).  Every mbarrier wait is bounded: on timeout the kernel
 // records BSA_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs, frees
@@ -39,6 +46,7 @@
 
 #include <mutex>
 
+#include "bsa_fp8.cuh"
 #include "bsa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -57,19 +65,29 @@ struct AttnParams {
   const int32_t *cu;      // packed ragged batch: sequence b is tokens cu[b] .. cu[b+1]-1; or null
   int batch, seq, hq, hkv, nb, group;  // seq: fixed length, or max_seqlen when packed
   int total, nbs;         // tokens in q / k / v / o; per-sequence stride of per-block arrays
-  float scale_log2;       // softmax scale * log2(e)
+  float scale_log2;       // softmax scale * log2(e) (times q_scale * k_scale for fp8 inputs)
+  float v_scale;          // 1, or the fp8 value scale
 };
 
-template <int D, int BLK, int NT>
+template <int D, int BLK, int NT, bool F8 = false>
 struct Cfg {
   static constexpr int KT = BLK < 128 ? BLK : 128;  // key-tile rows
   static constexpr int QH = BLK == 64 ? 2 : 1;      // heads stacked in one 128-row Q tile
   static constexpr int QTOK = 128 / QH;             // tokens per Q tile
   static constexpr int NQS = BLK == 256 ? 2 : 1;    // Q tiles along one query block
   static constexpr int SUB = BLK / KT;              // key tiles per key block
-  static constexpr int NCH = D / 64;                // 128-byte swizzle chunks per row
-  static constexpr uint32_t Q_TILE = 128u * D * 2;
-  static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;
+  static constexpr int QKB = F8 ? 1 : 2;            // bytes per Q / K element
+  static constexpr int CE = 128 / QKB;              // Q / K elements per 128-byte swizzle row
+  static constexpr int NCH = D * QKB / 128;         // 128-byte swizzle chunks per Q / K row
+  static constexpr int NCHV = D / 64;               // chunks per bf16 V row
+  static constexpr int NKK = D * QKB / 32;          // 32-byte K steps of one S = Q K^T
+  static_assert(NCH >= 1 && D * QKB % 128 == 0, "Q / K rows are whole 128-byte swizzle rows");
+  static_assert(NCHV >= 1, "V rows are whole 128-byte swizzle rows");
+  static constexpr uint32_t Q_TILE = 128u * D * QKB;
+  static constexpr uint32_t K_TILE = static_cast<uint32_t>(KT) * D * QKB;
+  static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;  // a bf16 V tile
+  static constexpr uint32_t V8_TILE = F8 ? static_cast<uint32_t>(KT) * D : 0u;  // an e4m3 V tile
+  static constexpr int V8S = F8 ? 2 : 0;            // e4m3 V staging stages
   static constexpr uint32_t Q_CHUNK = 128u * 128;
   static constexpr uint32_t KV_CHUNK = static_cast<uint32_t>(KT) * 128;
   // Softmax threads per query row: with 128-column key tiles two warps share each
@@ -81,19 +99,21 @@ struct Cfg {
   static constexpr int KS = 2;  // K stages: K(n+KS) only needs S(n) done
   // V stages: V(n+VS) needs PV_1(n) done, which comes late; use 3 when they fit
   static constexpr int VS =
-      (NT * Q_TILE + KS * KV_TILE + 3 * KV_TILE + RED_BYTES + 1024 + 512 <= 227u * 1024) ? 3 : 2;
+      (NT * Q_TILE + KS * K_TILE + 3 * KV_TILE + V8S * V8_TILE + RED_BYTES + 1024 + 512 <= 227u * 1024) ? 3 : 2;
   static constexpr int TM_O = NT * KT;
   static constexpr int TM_NEED = NT * (KT + D);
   static constexpr uint32_t TM_COLS =
       TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128 : TM_NEED <= 256 ? 256 : 512;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NT * Q_TILE;
-  static constexpr uint32_t OFF_V = OFF_K + KS * KV_TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_TILE;
-  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain
+  static constexpr uint32_t OFF_V = OFF_K + KS * K_TILE;
+  static constexpr uint32_t OFF_V8 = OFF_V + VS * KV_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V8 + V8S * V8_TILE;
+  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain,
+  // e4m3 V staging full/empty[V8S] (F8; V full then means "converted")
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
                        B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
-                       NBARS = B_FIN + 1;
+                       B_8F = B_FIN + 1, B_8E = B_8F + V8S, NBARS = B_8E + V8S;
   static constexpr uint32_t OFF_RED = (OFF_BAR + NBARS * 8 + 16 + 15) / 16 * 16;
   static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr int THREADS = 128 + 128 * NT * CH;
@@ -105,7 +125,7 @@ struct Cfg {
   static constexpr int REG_HIGH = THREADS == 640 ? 104 : 216;
   static_assert(REG_LAUNCH == 0 || 128 * REG_LOW + (THREADS - 128) * REG_HIGH <= THREADS * REG_LAUNCH,
                 "register split exceeds the launch allocation");
-  static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, KT, false);
+  static constexpr uint32_t IDESC_S = F8 ? ptx::idesc_e4m3_f32(128, KT) : ptx::idesc_bf16_f32(128, KT, false);
   static constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(128, D, true);
   static_assert(TM_NEED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared-memory budget");
@@ -150,11 +170,11 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D, int BLK, int NT, bool DENSE>
-__global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
+template <int D, int BLK, int NT, bool DENSE, bool F8>
+__global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = Cfg<D, BLK, NT>;
+  using C = Cfg<D, BLK, NT, F8>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -199,6 +219,8 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
     for (int x = 0; x < C::NBARS; ++x) {
       uint32_t count = 1;
       if (x >= C::B_PR && x < C::B_PR + NT) count = 4 * C::CH;  // one arrive per softmax warp
+      if (F8 && x >= C::B_VF && x < C::B_VF + C::VS) count = 2;  // the two converter warps
+      if (F8 && x >= C::B_8E && x < C::B_8E + C::V8S) count = 2;
       ptx::mbar_init(bar(x), count);
     }
     *abort_flag = 0;
@@ -227,7 +249,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       for (int t = 0; t < NT; ++t) {
         const int h0 = g * p.group + (hp * NT + t) * C::QH;
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * 64, h0,
+          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * C::CE, h0,
                            sp.start + qtok0, 0);
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
@@ -235,15 +257,25 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         const int ktok0 = sp.start + key_block(n) * BLK + (n % C::SUB) * C::KT;
         const int ks = n % C::KS, ku = n / C::KS;
         if (ku > 0 && !wait_bar(bar(C::B_KE + ks), (ku - 1) & 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::KV_TILE);
+        ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::K_TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sK + ks * C::KV_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * 64, g, ktok0, 0);
+          ptx::tma_load_4d(sK + ks * C::K_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * C::CE, g,
+                           ktok0, 0);
         k_issued = n + 1;
-        const int vs = n % C::VS, vu = n / C::VS;
-        if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g, ktok0, 0);
+        if constexpr (F8) {
+          // e4m3 V into a staging buffer; the converter warps fill the bf16 V stage
+          const int s8 = n % C::V8S, u8 = n / C::V8S;
+          if (u8 > 0 && !wait_bar(bar(C::B_8E + s8), (u8 - 1) & 1, ctl)) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_8F + s8), C::V8_TILE);
+          ptx::tma_load_4d(base + C::OFF_V8 + s8 * C::V8_TILE, &tm_v, bar(C::B_8F + s8), 0, g, ktok0, 0);
+        } else {
+          const int vs = n % C::VS, vu = n / C::VS;
+          if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
+          for (int c = 0; c < C::NCHV; ++c)
+            ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g,
+                             ktok0, 0);
+        }
         v_issued = n + 1;
       }
       if (*abort_flag) {
@@ -251,8 +283,13 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         drain_bar(bar(C::B_Q), 0);
         for (int n = k_issued - C::KS > 0 ? k_issued - C::KS : 0; n < k_issued; ++n)
           drain_bar(bar(C::B_KF + n % C::KS), (n / C::KS) & 1);
-        for (int n = v_issued - C::VS > 0 ? v_issued - C::VS : 0; n < v_issued; ++n)
-          drain_bar(bar(C::B_VF + n % C::VS), (n / C::VS) & 1);
+        if constexpr (F8) {
+          for (int n = v_issued - C::V8S > 0 ? v_issued - C::V8S : 0; n < v_issued; ++n)
+            drain_bar(bar(C::B_8F + n % C::V8S), (n / C::V8S) & 1);
+        } else {
+          for (int n = v_issued - C::VS > 0 ? v_issued - C::VS : 0; n < v_issued; ++n)
+            drain_bar(bar(C::B_VF + n % C::VS), (n / C::VS) & 1);
+        }
       }
     }
     __syncwarp();
@@ -266,13 +303,14 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       const uint64_t dv0 = ptx::sdesc_sw128(sV, C::KV_CHUNK, 1024);
       auto issue_s = [&](int t, int ks) {
         const uint64_t dq = dq0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
-        const uint64_t dk = dk0 + static_cast<uint64_t>(ks) * (C::KV_TILE >> 4);
+        const uint64_t dk = dk0 + static_cast<uint64_t>(ks) * (C::K_TILE >> 4);
         const uint32_t dst = tmem + t * C::KT;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::NKK; ++kk) {  // 32 bytes of K per MMA (16 bf16 or 32 e4m3)
           const uint64_t qo = ((kk / 4) * C::Q_CHUNK + (kk % 4) * 32) >> 4;
           const uint64_t ko = ((kk / 4) * C::KV_CHUNK + (kk % 4) * 32) >> 4;
-          ptx::mma_ss(dst, dq + qo, dk + ko, C::IDESC_S, kk > 0 ? 1u : 0u);
+          if constexpr (F8) ptx::mma_ss_f8(dst, dq + qo, dk + ko, C::IDESC_S, kk > 0 ? 1u : 0u);
+          else ptx::mma_ss(dst, dq + qo, dk + ko, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(C::B_SF + t));
       };
@@ -327,6 +365,37 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
         // every MMA issued so far must finish before TMEM is released
         ptx::mma_commit(bar(C::B_FIN));
         drain_bar(bar(C::B_FIN), 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    if constexpr (F8) {
+      // ================================================================ V converters (warps 2-3)
+      // e4m3 V tile (row r = key, D bytes, unswizzled) -> bf16 MN-major tile in the layout a
+      // 128-byte-swizzled TMA load would give: chunk of 64 dims, row r of 128 bytes, 16-byte
+      // unit u at position u ^ (r % 8)
+      const int ct = threadIdx.x - 64;
+      for (int n = 0; n < T; ++n) {
+        const int s8 = n % C::V8S, vs = n % C::VS, vu = n / C::VS;
+        if (!wait_bar(bar(C::B_8F + s8), (n / C::V8S) & 1, ctl)) break;
+        if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
+        const unsigned char *src = sb + C::OFF_V8 + s8 * C::V8_TILE;
+        unsigned char *dst = sb + C::OFF_V + vs * C::KV_TILE;
+        for (int it = ct; it < C::KT * (D / 8); it += 64) {
+          const int r = it / (D / 8), unit = it - r * (D / 8);
+          const int c = unit >> 3, uu = unit & 7;
+          float f[8];
+          e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(src + r * D + unit * 8), f);
+          const uint4 o = make_uint4(ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]),
+                                     ptx::pack_bf16x2(f[4], f[5]), ptx::pack_bf16x2(f[6], f[7]));
+          *reinterpret_cast<uint4 *>(dst + c * C::KV_CHUNK + r * 128 + ((uu ^ (r & 7)) << 4)) = o;
+        }
+        ptx::fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(bar(C::B_8E + s8));
+          ptx::mbar_arrive(bar(C::B_VF + vs));
+        }
       }
     }
     __syncwarp();
@@ -444,7 +513,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
       ptx::named_barrier(pair_bar, 64);
       l = lsh[r] + lsh[128 + r];
     }
-    const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
+    const float inv = (ok && l > 0.f) ? p.v_scale / l : 0.f;
     const bool row_valid = qtok < sp.len;  // a partial last block's tile rows past the sequence end
     uint16_t *orow = p.o + ((static_cast<size_t>(sp.start) + qtok) * p.hq + head) * D + hf * OD_COLS;
 #pragma unroll
@@ -486,27 +555,30 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT>::THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-// [batch, seq, heads, d] bf16 viewed as a 4-D tensor (d innermost), tile box
-// {64, box_heads, box_tokens, 1} with 128-byte swizzling.
+// [batch, seq, heads, d] viewed as a 4-D tensor (d innermost), tile box
+// {box_inner, box_heads, box_tokens, 1}: bf16 or e4m3 (fp8) elements, 128-byte
+// swizzling or none.
 bool make_map(EncodeTiledFn fn, CUtensorMap *map, const void *ptr, int batch, int seq, int heads,
-              int d, int box_heads, int box_tokens) {
+              int d, int box_heads, int box_tokens, bool fp8, int box_inner, bool swizzle) {
+  const cuuint64_t eb = fp8 ? 1 : 2;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(seq), static_cast<cuuint64_t>(batch)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(heads) * d * 2,
-                                 static_cast<cuuint64_t>(seq) * heads * d * 2};
-  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_heads),
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * eb,
+                                 static_cast<cuuint64_t>(heads) * d * eb,
+                                 static_cast<cuuint64_t>(seq) * heads * d * eb};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_heads),
                              static_cast<cuuint32_t>(box_tokens), 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BLK, int NT, bool DENSE>
+template <int D, int BLK, int NT, bool DENSE, bool F8>
 bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void *v,
                     const AttnParams &prm, cudaStream_t stream, cudaError_t *cerr) {
-  using C = Cfg<D, BLK, NT>;
+  using C = Cfg<D, BLK, NT, F8>;
   cudaError_t e = cudaSuccess;
   EncodeTiledFn fn = tensor_map_encoder(&e);
   if (fn == nullptr || e != cudaSuccess) {
@@ -515,13 +587,16 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
   }
   // one token axis over the whole batch: sequence b starts at token b * seq, or at cu[b] when packed
   CUtensorMap mq, mk, mv;
-  if (!make_map(fn, &mq, q, 1, s.total, s.hq, D, C::QH, C::QTOK) ||
-      !make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KT) ||
-      !make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT)) {
+  const bool maps_ok =
+      make_map(fn, &mq, q, 1, s.total, s.hq, D, C::QH, C::QTOK, F8, C::CE, true) &&
+      make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KT, F8, C::CE, true) &&
+      (F8 ? make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, true, D, false)   // staged, converted
+          : make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, false, 64, true));
+  if (!maps_ok) {
     *cerr = cudaErrorInvalidValue;
     return BSA_ERR_CUDA;
   }
-  auto kern = attn_kernel<D, BLK, NT, DENSE>;
+  auto kern = attn_kernel<D, BLK, NT, DENSE, F8>;
   if constexpr (C::REG_LAUNCH != 0) {
     // setmaxnreg.inc waits until the registers it asks for are free: the split is only
     // safe if the kernel really launches with REG_LAUNCH registers per thread
@@ -548,21 +623,21 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
   return BSA_OK;
 }
 
-template <int D, int BLK, bool DENSE>
+template <int D, int BLK, bool DENSE, bool F8>
 bsa_status launch_nt(const AttnShape &s, const void *q, const void *k, const void *v,
                      const AttnParams &prm, cudaStream_t st, cudaError_t *cerr) {
   constexpr int QH = BLK == 64 ? 2 : 1;
-  if ((s.group / QH) % 2 == 0) return launch_t<D, BLK, 2, DENSE>(s, q, k, v, prm, st, cerr);
-  return launch_t<D, BLK, 1, DENSE>(s, q, k, v, prm, st, cerr);
+  if ((s.group / QH) % 2 == 0) return launch_t<D, BLK, 2, DENSE, F8>(s, q, k, v, prm, st, cerr);
+  return launch_t<D, BLK, 1, DENSE, F8>(s, q, k, v, prm, st, cerr);
 }
 
-template <int D, bool DENSE>
+template <int D, bool DENSE, bool F8>
 bsa_status launch_blk(const AttnShape &s, const void *q, const void *k, const void *v,
                       const AttnParams &prm, cudaStream_t st, cudaError_t *cerr) {
   switch (s.block) {
-    case 64: return launch_nt<D, 64, DENSE>(s, q, k, v, prm, st, cerr);
-    case 128: return launch_nt<D, 128, DENSE>(s, q, k, v, prm, st, cerr);
-    case 256: return launch_nt<D, 256, DENSE>(s, q, k, v, prm, st, cerr);
+    case 64: return launch_nt<D, 64, DENSE, F8>(s, q, k, v, prm, st, cerr);
+    case 128: return launch_nt<D, 128, DENSE, F8>(s, q, k, v, prm, st, cerr);
+    case 256: return launch_nt<D, 256, DENSE, F8>(s, q, k, v, prm, st, cerr);
     default: return BSA_ERR_UNSUPPORTED;
   }
 }
@@ -605,14 +680,22 @@ bsa_status launch_attention(const AttnShape &s, const void *q, const void *k, co
   prm.group = s.group;
   prm.total = s.total;
   prm.nbs = s.nbs;
-  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const double qk = s.fp8 ? static_cast<double>(s.q_scale) * s.k_scale : 1.0;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * qk * 1.4426950408889634);
+  prm.v_scale = s.fp8 ? s.v_scale : 1.f;
   const bool dense = kv_idx == nullptr;
+  if (s.fp8) {
+    // e4m3 Q / K rows must fill whole 128-byte swizzle rows: head_dim 128
+    if (s.d != 128) return BSA_ERR_UNSUPPORTED;
+    return dense ? launch_blk<128, true, true>(s, q, k, v, prm, stream, cuda_err)
+                 : launch_blk<128, false, true>(s, q, k, v, prm, stream, cuda_err);
+  }
   if (s.d == 64)
-    return dense ? launch_blk<64, true>(s, q, k, v, prm, stream, cuda_err)
-                 : launch_blk<64, false>(s, q, k, v, prm, stream, cuda_err);
+    return dense ? launch_blk<64, true, false>(s, q, k, v, prm, stream, cuda_err)
+                 : launch_blk<64, false, false>(s, q, k, v, prm, stream, cuda_err);
   if (s.d == 128)
-    return dense ? launch_blk<128, true>(s, q, k, v, prm, stream, cuda_err)
-                 : launch_blk<128, false>(s, q, k, v, prm, stream, cuda_err);
+    return dense ? launch_blk<128, true, false>(s, q, k, v, prm, stream, cuda_err)
+                 : launch_blk<128, false, false>(s, q, k, v, prm, stream, cuda_err);
   return BSA_ERR_UNSUPPORTED;
 }
 

@@ -20,6 +20,8 @@ struct MaskShape {
   int batch, seq, hq, hkv, d, block, nb, group;
   const int32_t *cu;
   int total, nbs;
+  int fp8;                          // inputs are e4m3 codes: value = code * scale
+  float q_scale, k_scale, v_scale;  // used when fp8
 };
 
 // Token span of sequence b.  Packed entries are checked against total and
@@ -97,6 +99,8 @@ struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;
   const int32_t *cu;  // packed ragged batch (o [total, hq, d], lse [hq, total]) or null
   int total, nbs;
+  int fp8;                          // q, k, v are e4m3 codes (value = code * scale)
+  float q_scale, k_scale, v_scale;  // used when fp8
 };
 
 // Sparse (kv_idx != nullptr) or dense (kv_idx == nullptr) causal attention.

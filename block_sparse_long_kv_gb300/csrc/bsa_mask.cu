@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "bsa_fp8.cuh"
 #include "bsa_internal.h"
 #include "bsa_topk.cuh"
 
@@ -44,6 +45,23 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float f[8]) {
   }
 }
 
+// Eight consecutive input elements: bf16 (16 bytes) or e4m3 (8 bytes, F8).
+template <bool F8>
+__device__ __forceinline__ uint4 load8(const unsigned char *p) {
+  if constexpr (F8) {
+    const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(p));
+    return make_uint4(x.x, x.y, 0u, 0u);
+  } else {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+  }
+}
+
+template <bool F8>
+__device__ __forceinline__ void unpack8(const uint4 &u, float f[8]) {
+  if constexpr (F8) e4m3x8_to_f32(make_uint2(u.x, u.y), f);
+  else unpack_bf16x8(u, f);
+}
+
 // ---------------------------------------------------------------- block meta
 
 // One CTA per (b, g, j), the key block held in registers: thread t owns the
@@ -55,13 +73,14 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float f[8]) {
 // A partial last block (a packed sequence whose length is not a multiple of
 // BLK) averages over its own tokens; CTAs past a sequence's last block write
 // zeros.
-template <int D, int BLK>
-__global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_kernel(const uint16_t *__restrict__ k,
+template <int D, int BLK, bool F8>
+__global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_kernel(const unsigned char *__restrict__ k,
                                                         float *__restrict__ centroid,
                                                         float *__restrict__ radius,
                                                         const int32_t *__restrict__ cu, int seq,
-                                                        int total, int hkv, int nbs,
+                                                        int total, int hkv, int nbs, float scale,
                                                         int32_t *status) {
+  constexpr int EB = F8 ? 1 : 2;      // bytes per input element
   constexpr int VPR = D / 8;          // 16-byte vectors per key row
   constexpr int TL = kThreads / VPR;  // token lanes
   constexpr int TPT = BLK / TL;       // tokens per thread
@@ -82,20 +101,18 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     if (tid == 0) radius[ob] = 0.f;
     return;
   }
-  const size_t tok_stride = static_cast<size_t>(hkv) * D;
-  const uint16_t *base = k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * BLK + u) * tok_stride +
-                         static_cast<size_t>(g) * D + v * 8;
+  const size_t tok_stride = static_cast<size_t>(hkv) * D * EB;  // bytes
+  const unsigned char *base = k + (static_cast<size_t>(sp.start) + static_cast<size_t>(j) * BLK + u) * tok_stride +
+                              (static_cast<size_t>(g) * D + v * 8) * EB;
   uint4 raw[TPT];
   if (cnt == BLK) {
 #pragma unroll
-    for (int r = 0; r < TPT; ++r)
-      raw[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride));
+    for (int r = 0; r < TPT; ++r) raw[r] = load8<F8>(base + static_cast<size_t>(r) * TL * tok_stride);
   } else {  // partial last block of a packed sequence
 #pragma unroll
     for (int r = 0; r < TPT; ++r)
-      raw[r] = (r * TL + u < cnt)
-                   ? __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(r) * TL * tok_stride))
-                   : make_uint4(0u, 0u, 0u, 0u);
+      raw[r] = (r * TL + u < cnt) ? load8<F8>(base + static_cast<size_t>(r) * TL * tok_stride)
+                                  : make_uint4(0u, 0u, 0u, 0u);
   }
 
   // ---- pass 1: centroid
@@ -105,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
 #pragma unroll
   for (int r = 0; r < TPT; ++r) {
     float f[8];
-    unpack_bf16x8(raw[r], f);
+    unpack8<F8>(raw[r], f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) s[e] += f[e];
   }
@@ -125,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     for (int w = 0; w < NW; ++w) c += part[w][tid];
     c /= static_cast<float>(cnt);
     sc[tid] = c;
-    centroid[ob * D + tid] = c;
+    centroid[ob * D + tid] = c * scale;  // in the inputs' units (scale 1 for bf16)
   }
   __syncthreads();
 
@@ -141,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
 #pragma unroll
   for (int r = 0; r < TPT; ++r) {
     float f[8];
-    unpack_bf16x8(raw[r], f);
+    unpack8<F8>(raw[r], f);
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -160,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     float m = wmax[0];
 #pragma unroll
     for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
-    radius[ob] = sqrtf(m);
+    radius[ob] = sqrtf(m) * scale;
   }
 }
 
@@ -269,19 +286,18 @@ __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__flo
 
 // Sums a full block's queries (8 dimensions per lane) and their norms, 8 loads
 // in flight per thread.
-template <int D>
-__device__ __forceinline__ void pool_full(const uint16_t *__restrict__ base, size_t tok_stride,
+template <int D, bool F8>
+__device__ __forceinline__ void pool_full(const unsigned char *__restrict__ base, size_t tok_stride,
                                           int cnt, unsigned wmask, float acc[8], float &nsum) {
   constexpr int VH = D / 8;  // lanes per head
   for (int t0 = 0; t0 < cnt; t0 += 8) {
     uint4 u[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      u[r] = __ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t0 + r) * tok_stride));
+    for (int r = 0; r < 8; ++r) u[r] = load8<F8>(base + static_cast<size_t>(t0 + r) * tok_stride);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       float f[8];
-      unpack_bf16x8(u[r], f);
+      unpack8<F8>(u[r], f);
       float sq = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -297,14 +313,14 @@ __device__ __forceinline__ void pool_full(const uint16_t *__restrict__ base, siz
 
 // The same over the cnt < block queries of a packed sequence's partial last
 // block, one token at a time (one such block per sequence).
-template <int D>
-__device__ __forceinline__ void pool_partial(const uint16_t *__restrict__ base, size_t tok_stride,
+template <int D, bool F8>
+__device__ __forceinline__ void pool_partial(const unsigned char *__restrict__ base, size_t tok_stride,
                                              int cnt, unsigned wmask, float acc[8], float &nsum) {
   constexpr int VH = D / 8;
 #pragma unroll 1
   for (int t = 0; t < cnt; ++t) {
     float f[8];
-    unpack_bf16x8(__ldcs(reinterpret_cast<const uint4 *>(base + static_cast<size_t>(t) * tok_stride)), f);
+    unpack8<F8>(load8<F8>(base + static_cast<size_t>(t) * tok_stride), f);
     float sq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -323,8 +339,8 @@ __device__ __forceinline__ void pool_partial(const uint16_t *__restrict__ base, 
 // operand of the score GEMM), and nbar[b][g][i][hh].  The extra row of CTAs
 // (blockIdx.y == nhc) splits the centroids of key block blockIdx.x of every KV
 // head into c_hi / c_lo, the GEMM's A operand.
-template <int D>
-__global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restrict__ q,
+template <int D, bool F8>
+__global__ void __launch_bounds__(kThreads) qpool_kernel(const unsigned char *__restrict__ q,
                                                          float *__restrict__ q_hi,
                                                          float *__restrict__ q_lo,
                                                          float *__restrict__ nbar,
@@ -333,9 +349,10 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
                                                          float *__restrict__ c_lo,
                                                          const int32_t *__restrict__ cu, int seq,
                                                          int total, int hq, int hkv, int block,
-                                                         int nbs, int hpc, int nhc,
+                                                         int nbs, int hpc, int nhc, float scale,
                                                          int32_t *status) {
   constexpr int VH = D / 8;  // lanes per head
+  constexpr int EB = F8 ? 1 : 2;  // bytes per input element
   const int i = blockIdx.x, hc = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   if (hc == nhc) {
@@ -362,9 +379,9 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
     if (xv == 0) nbar[row * grp + hh] = 0.f;
     return;
   }
-  const size_t tok_stride = static_cast<size_t>(hq) * D;
-  const uint16_t *base = q + (static_cast<size_t>(sp.start) + static_cast<size_t>(i) * block) * tok_stride +
-                         static_cast<size_t>(h) * D + xv * 8;
+  const size_t tok_stride = static_cast<size_t>(hq) * D * EB;  // bytes
+  const unsigned char *base = q + (static_cast<size_t>(sp.start) + static_cast<size_t>(i) * block) * tok_stride +
+                              (static_cast<size_t>(h) * D + xv * 8) * EB;
   // lanes present in this warp (the last warp may be partial); a head's lanes never straddle warps
   const int present = min(32, static_cast<int>(blockDim.x) - (tid & ~31));
   const unsigned wmask = present >= 32 ? 0xffffffffu : ((1u << present) - 1u);
@@ -372,9 +389,9 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const uint16_t *__restr
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   float nsum = 0.f;
-  if (cnt == block) pool_full<D>(base, tok_stride, cnt, wmask, acc, nsum);
-  else pool_partial<D>(base, tok_stride, cnt, wmask, acc, nsum);
-  const float inv = 1.f / static_cast<float>(cnt);  // exact for a full block (a power of two)
+  if (cnt == block) pool_full<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
+  else pool_partial<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
+  const float inv = scale / static_cast<float>(cnt);  // exact for a full bf16 block (scale 1, cnt 2^k)
   float m[8], hi[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -437,8 +454,13 @@ template <int D, int BLK>
 cudaError_t launch_meta_t(const MaskShape &s, const void *k, float *centroid, float *radius,
                           int32_t *status, cudaStream_t stream) {
   dim3 grid(s.nbs, s.hkv, s.batch);
-  meta_kernel<D, BLK><<<grid, kThreads, 0, stream>>>(static_cast<const uint16_t *>(k), centroid, radius,
-                                                     s.cu, s.seq, s.total, s.hkv, s.nbs, status);
+  const unsigned char *kb = static_cast<const unsigned char *>(k);
+  if (s.fp8)
+    meta_kernel<D, BLK, true><<<grid, kThreads, 0, stream>>>(kb, centroid, radius, s.cu, s.seq, s.total, s.hkv,
+                                                             s.nbs, s.k_scale, status);
+  else
+    meta_kernel<D, BLK, false><<<grid, kThreads, 0, stream>>>(kb, centroid, radius, s.cu, s.seq, s.total, s.hkv,
+                                                              s.nbs, 1.f, status);
   return cudaGetLastError();
 }
 
@@ -468,9 +490,15 @@ cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *q_hi, float
   const int hpc = qpool_heads(s.hq, D);
   const int nhc = s.hq / hpc;
   dim3 grid(s.nbs, nhc + 1, s.batch);
-  qpool_kernel<D><<<grid, hpc * (D / 8), 0, stream>>>(static_cast<const uint16_t *>(q), q_hi, q_lo,
-                                                      nbar, centroid, c_hi, c_lo, s.cu, s.seq, s.total,
-                                                      s.hq, s.hkv, s.block, s.nbs, hpc, nhc, status);
+  const unsigned char *qb = static_cast<const unsigned char *>(q);
+  if (s.fp8)
+    qpool_kernel<D, true><<<grid, hpc * (D / 8), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
+                                                              s.seq, s.total, s.hq, s.hkv, s.block, s.nbs, hpc,
+                                                              nhc, s.q_scale, status);
+  else
+    qpool_kernel<D, false><<<grid, hpc * (D / 8), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
+                                                               s.seq, s.total, s.hq, s.hkv, s.block, s.nbs, hpc,
+                                                               nhc, 1.f, status);
   return cudaGetLastError();
 }
 

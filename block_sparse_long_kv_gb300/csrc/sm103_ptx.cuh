@@ -176,6 +176,27 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uin
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (type code 0), D f32,
+// both operands K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+  return (1u << 4)                                  // D format f32
+         | (0u << 7)                                // A format e4m3
+         | (0u << 10)                               // B format e4m3
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+
+// D (+)= A B, kind::f8f6f4: A and B 8-bit in shared memory, K = 32 per instruction.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(

@@ -223,6 +223,42 @@ bsa_status bsa_prefill_layer(const bsa_shape *shape, const bsa_select_params *pa
 bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets);
 
 /* ------------------------------------------------------------------------
+ * FP8 (e4m3) inputs.
+ *
+ * The article measures an FP8 model (prefill section: the benchmark model is
+ * an FP8 checkpoint, and the rescue signal is reported to survive 8-bit keys).
+ * These entry points take Q, K and V as OCP e4m3 codes (1 byte per element,
+ * same [batch, seq, heads, head_dim] layouts) with one positive scale per
+ * tensor: value = e4m3(code) * scale.  They compute exactly what the bf16
+ * entry points compute on the dequantised values:
+ *   - bsa_block_meta_fp8: centroids, radii, quantiles, alpha of k * k_scale;
+ *   - bsa_select_mask_fp8: the selection with q * q_scale (flags must be 0:
+ *     BSA_SELECT_TOKEN_MAX returns BSA_ERR_UNSUPPORTED here);
+ *   - bsa_prefill_fwd_fp8 / bsa_prefill_dense_fwd_fp8: attention with
+ *     S = Q K^T on the tensor cores' e4m3 path (kind::f8f6f4), V converted to
+ *     bf16 on chip, O written as bf16; head_dim 128 only (other head_dims
+ *     return BSA_ERR_UNSUPPORTED).
+ * Scales must be finite and positive (BSA_ERR_INVALID_ARG otherwise).  Other
+ * arguments, layouts and errors as the bf16 entry points.
+ * ------------------------------------------------------------------------ */
+bsa_status bsa_block_meta_fp8(const bsa_shape *shape, const void *k, float k_scale, float *centroid,
+                              float *radius, float *quant, float *alpha, int32_t *dev_status,
+                              bsa_stream_t stream);
+bsa_status bsa_select_mask_fp8(const bsa_shape *shape, const bsa_select_params *params,
+                               const void *q, float q_scale, const float *centroid,
+                               const float *radius, const float *alpha, int32_t *kv_idx,
+                               int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream);
+bsa_status bsa_prefill_fwd_fp8(const bsa_shape *shape, const void *q, const void *k, const void *v,
+                               float q_scale, float k_scale, float v_scale, const int32_t *kv_idx,
+                               const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
+                               int32_t *dev_status, bsa_stream_t stream);
+bsa_status bsa_prefill_dense_fwd_fp8(const bsa_shape *shape, const void *q, const void *k,
+                                     const void *v, float q_scale, float k_scale, float v_scale,
+                                     float softmax_scale, void *o, float *lse, int32_t *dev_status,
+                                     bsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Packed ragged batches ("varlen").
  *
  * Serving batches mix prompt lengths (the article's prefill section measures

@@ -177,3 +177,21 @@ def test_varlen_stride_workspace_and_pointer_checks(lib):
                                       f, ctypes.c_size_t(need - 1), None, None) == 4
     assert lib.bsa_varlen_prefill_fwd(ctypes.byref(s), f, f, f, f, None, f, ctypes.c_float(0.1), f,
                                       None, None, None) == 1
+
+
+def test_fp8_entry_point_validation(lib):
+    from block_sparse_long_kv_gb300 import _lib
+    s = shp(batch=1, seq=1024, hq=4, hkv=2, head_dim=128, block=64)
+    f = ctypes.c_void_p(FAKE)
+    one = ctypes.c_float(1.0)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        b = ctypes.c_float(bad)
+        assert lib.bsa_block_meta_fp8(ctypes.byref(s), f, b, f, f, f, f, None, None) == 1
+        assert lib.bsa_prefill_dense_fwd_fp8(ctypes.byref(s), f, f, f, one, b, one, ctypes.c_float(0.1),
+                                             f, None, None, None) == 1
+    s64 = shp(head_dim=64)                                   # e4m3 attention needs head_dim 128
+    assert lib.bsa_prefill_dense_fwd_fp8(ctypes.byref(s64), f, f, f, one, one, one, ctypes.c_float(0.1),
+                                         f, None, None, None) == 3
+    tok = _lib.SelectParams(0.1, 0.1, 1)                     # per-token aggregation reads bf16 Q
+    assert lib.bsa_select_mask_fp8(ctypes.byref(s), ctypes.byref(tok), f, one, f, f, f, f, f, None, f,
+                                   ctypes.c_size_t(1 << 40), None, None) == 3
