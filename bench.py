@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--token-max", action="store_true",
                     help="score query blocks by their best token (BSA_SELECT_TOKEN_MAX)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="e4m3 Q / K / V inputs with per-tensor scales (the *_fp8 entry points)")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (new token per sequence) over the workload as a cache")
     return ap.parse_args()
@@ -388,6 +390,50 @@ class FixedRunner:
         return self.w, None
 
 
+class Fp8Runner(FixedRunner):
+    """FixedRunner on e4m3 inputs: bsa_block_meta_fp8, bsa_select_mask_fp8, bsa_prefill_fwd_fp8."""
+
+    def make_layer(self, synth, layer):
+        lay = synth.make_layer(self.w, layer=layer)
+        f8 = synth.fp8_layer(lay)
+        out = dict(lay)
+        out.update({x: f8[x] for x in ("q", "k", "v")})
+        out.update({x + "16": lay[x] for x in ("q", "k", "v")})   # bf16 originals for the CPU oracle
+        self.scales = {x: f8[x + "_scale"] for x in ("q", "k", "v")}
+        return out
+
+    def upload(self, lay):
+        return {x: self.torch.from_numpy(lay[x]).to(self.dev) for x in ("q", "k", "v")}
+
+    def meta_call(self, L, status):
+        m = self.meta
+        self.bsa.block_meta_fp8(self.s, L["k"], self.scales["k"], m["centroid"], m["radius"], m["quant"],
+                                m["alpha"], status)
+
+    def select_call(self, L, status):
+        m, sl = self.meta, self.sel
+        self.bsa.select_mask_fp8(self.s, self.prm, L["q"], self.scales["q"], m["centroid"], m["radius"],
+                                 m["alpha"], sl["kv_idx"], sl["kv_cnt"], None, self.ws, status)
+
+    def attn_call(self, L, o, status):
+        sl, sc = self.sel, self.scales
+        if not hasattr(self, "wide_v"):
+            self.wide_v = self.torch.empty(self.bsa.prefill_fp8_workspace_bytes(self.s), dtype=self.torch.uint8,
+                                           device=self.dev)
+        self.bsa.prefill_fwd_fp8(self.s, L["q"], L["k"], L["v"], sc["q"], sc["k"], sc["v"], sl["kv_idx"],
+                                 sl["kv_cnt"], self.scale, o, self.lse, self.wide_v, status)
+
+    def e2e_setup(self):
+        pass
+
+    def e2e_call(self, L, o, status, stream):
+        self.meta_call(L, status)
+        self.select_call(L, status)
+        self.attn_call(L, o, status)
+
+    e2e_api = "bsa_block_meta_fp8 + bsa_select_mask_fp8 + bsa_prefill_fwd_fp8 (C ABI)"
+
+
 class VarlenRunner(FixedRunner):
     """One packed ragged batch per step: the bsa_varlen_* entry points."""
 
@@ -482,6 +528,8 @@ def run_ours(args):
     flags = bsa.SELECT_TOKEN_MAX if args.token_max else 0
     if args.workload in synth.VARLEN_WORKLOADS:
         run = VarlenRunner(bsa, torch, synth.VARLEN_WORKLOADS[args.workload], dev, flags)
+    elif args.fp8:
+        run = Fp8Runner(bsa, torch, synth.workload(args.workload), dev, flags)
     else:
         run = FixedRunner(bsa, torch, synth.workload(args.workload), dev, flags)
     w = run.w
@@ -493,7 +541,7 @@ def run_ours(args):
         lay = run.make_layer(synth, rank * args.layers + li)
         host_layers.append(lay)
         dev_layers.append(run.upload(lay))
-    o = torch.empty_like(dev_layers[0]["q"])
+    o = torch.empty(dev_layers[0]["q"].shape, dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -557,7 +605,8 @@ def run_ours(args):
     att_ms = np.array([evs[i][2].elapsed_time(evs[i][3]) for i in range(K)])
     fl = np.array([flops[i % len(flops)] for i in range(K)])
     lb = np.array([list_bytes[i % len(list_bytes)] for i in range(K)])
-    mask_bytes = run.tokens * (w.hq + w.hkv) * w.head_dim * 2 + lb
+    in_bytes = 1 if args.fp8 else 2
+    mask_bytes = run.tokens * (w.hq + w.hkv) * w.head_dim * in_bytes + lb
     kept_tflops = float((fl / (att_ms * 1e-3)).mean() / 1e12)
     mask_ms = meta_ms + sel_ms
     mask_gbs = float((mask_bytes / (mask_ms * 1e-3)).mean() / 1e9)
@@ -565,19 +614,26 @@ def run_ours(args):
     pk, src = peaks()
     bf16_peak = peak_value(pk, "bf16_tflops", "bf16_tflops_burst")
     hbm_peak = peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm_gb_s")
+    peak_note = f"{src} bf16 burst"
+    if args.fp8 and bf16_peak:
+        # half the kept FLOPs (S = Q K^T) run on the e4m3 path at the nominal 2x bf16 rate, half
+        # (P V) on bf16: the time-weighted peak is 4/3 of the bf16 peak
+        bf16_peak = bf16_peak * 4.0 / 3.0
+        peak_note = f"{src} bf16 burst x 4/3 (S on e4m3 at 2x, P V on bf16)"
     # the committed DRAM-traffic capture covers the default 128K workload only
-    default = not isinstance(run, VarlenRunner) and w.name == "gqa32x4_n131072_d128_b128"
+    default = (not isinstance(run, (VarlenRunner, Fp8Runner)) and w.name == "gqa32x4_n131072_d128_b128")
     traffic, _ = profiled_traffic() if default else (None, None)
     ms_per_layer = total_ms / (K * world)
-    q_gb = run.tokens * w.hq * w.head_dim * 2 / 1e9
+    q_gb = run.tokens * w.hq * w.head_dim * in_bytes / 1e9
     cfg = run.config()
     cfg.update({"aggregation": "token_max" if args.token_max else "block_mean",
+                "inputs": "e4m3 + per-tensor scales" if args.fp8 else "bf16",
                 "layers_rotated": args.layers,
                 "l2": f"inputs larger than L2 (Q alone is {q_gb:.2f} GB per layer), layers rotated"})
     result = {
         "metric": METRIC, "value": ms_per_layer, "unit": "ms/layer", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 inputs, bf16 P / O" if args.fp8 else "bf16",
         "data": "synthetic (seeded generator: clustered keys with log-uniform block spreads, planted needles)",
         "config": cfg,
         "kept_block_tflops": kept_tflops,
@@ -588,14 +644,15 @@ def run_ours(args):
         "roofline": {"kernel": "attn_kernel (bsa_prefill_fwd)", "bound": "tensor",
                      "achieved": kept_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": kept_tflops / bf16_peak if bf16_peak else None,
-                     "peak_source": f"{src} bf16 burst", "traffic": traffic,
+                     "peak_source": peak_note, "traffic": traffic,
                      "flops_per_launch": float(np.mean(flops))},
         "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + qpool_kernel + score_kernel + select_kernel",
                                 "bound": "hbm", "achieved": mask_gbs, "peak": hbm_peak,
                                 "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
                                 "peak_source": f"{src} hbm copy",
                                 "bytes_per_launch": float(np.mean(mask_bytes))},
-        "gpu_launches": 6 * K,       # meta, quant, qpool or centroid split, scores, select, attention
+        "gpu_launches": (7 if args.fp8 else 6) * K,  # meta, quant, qpool or centroid split, scores, select,
+                                                     # (V widening,) attention
         "clocks": clk,
     }
     if args.token_max:
@@ -620,11 +677,14 @@ def run_ours(args):
         pinned = []
         for x in range(2):
             hl = host_layers[x % len(host_layers)]
-            pinned.append({n: torch.from_numpy(hl[n].view(np.int16)).view(torch.bfloat16).pin_memory()
-                           for n in ("q", "k", "v")})
+            if hl["q"].dtype == np.uint8:          # e4m3 codes
+                pinned.append({n: torch.from_numpy(hl[n]).pin_memory() for n in ("q", "k", "v")})
+            else:
+                pinned.append({n: torch.from_numpy(hl[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+                               for n in ("q", "k", "v")})
         o_host = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-        dbuf = [{n: torch.empty_like(dev_layers[0]["q" if n == "o" else n]) for n in ("q", "k", "v", "o")}
-                for _ in range(2)]
+        dbuf = [{n: (torch.empty_like(o) if n == "o" else torch.empty_like(dev_layers[0][n]))
+                 for n in ("q", "k", "v", "o")} for _ in range(2)]
         h2d_s = torch.cuda.Stream(dev)
         d2h_s = torch.cuda.Stream(dev)
 
@@ -675,7 +735,7 @@ def run_ours(args):
             t = torch.tensor([e2e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        h2d = sum(pinned[0][n].numel() * 2 for n in ("q", "k", "v"))
+        h2d = sum(pinned[0][n].numel() * pinned[0][n].element_size() for n in ("q", "k", "v"))
         result["e2e"] = {"value": e2e_ms / n_e2e, "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host[0].numel() * 2,
                          "steps": n_e2e,
@@ -690,6 +750,8 @@ def run_ours(args):
         sw, factor = run.cpu_sample_workload()
         lay0 = host_layers[0] if factor is None else synth.make_layer(sw, seed=w.seed_base + int(
             np.argmax(w.lengths)))
+        if "q16" in lay0:  # time the oracle on the same layer's bf16 values
+            lay0 = {x: lay0[x + "16"] for x in ("q", "k", "v")}
         r = oracle_sample(sw, lay0, args.cpu_budget)
         f = 1.0 if factor is None else factor
         cpu_ms = 1e3 * (f * (r["t_meta"] + r["t_sel"]) + r["t_att_per_flop"] * float(np.mean(flops)))

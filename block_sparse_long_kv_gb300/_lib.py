@@ -58,10 +58,13 @@ SIGNATURES = {
     "bsa_block_meta_fp8": (ctypes.c_int, [_SP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P]),
     "bsa_select_mask_fp8": (ctypes.c_int, [_SP, _PP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_size_t, _P, _P]),
+    "bsa_prefill_fp8_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "bsa_prefill_fwd_fp8": (ctypes.c_int, [_SP, _P, _P, _P, ctypes.c_float, ctypes.c_float,
-                                           ctypes.c_float, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
+                                           ctypes.c_float, _P, _P, ctypes.c_float, _P, _P, _P,
+                                           ctypes.c_size_t, _P, _P]),
     "bsa_prefill_dense_fwd_fp8": (ctypes.c_int, [_SP, _P, _P, _P, ctypes.c_float, ctypes.c_float,
-                                                 ctypes.c_float, ctypes.c_float, _P, _P, _P, _P]),
+                                                 ctypes.c_float, ctypes.c_float, _P, _P, _P,
+                                                 ctypes.c_size_t, _P, _P]),
     "bsa_varlen_block_stride": (ctypes.c_int32, [_VP]),
     "bsa_varlen_block_meta": (ctypes.c_int, [_VP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "bsa_varlen_select_workspace_bytes": (ctypes.c_size_t, [_VP]),

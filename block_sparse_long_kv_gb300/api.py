@@ -23,6 +23,7 @@ __all__ = [
     "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
     "decode_workspace_bytes", "decode_select", "decode_fwd",
     "block_meta_fp8", "select_mask_fp8", "prefill_fwd_fp8", "prefill_dense_fwd_fp8",
+    "prefill_fp8_workspace_bytes",
 ]
 
 Shape = _lib.Shape
@@ -212,10 +213,21 @@ def select_mask_fp8(shape: Shape, params: SelectParams, q, q_scale, centroid, ra
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 
+def prefill_fp8_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.load().bsa_prefill_fp8_workspace_bytes(ctypes.byref(shape)))
+
+
+def _fp8_ws(shape, workspace, like):
+    if workspace is None:
+        workspace = torch.empty(prefill_fp8_workspace_bytes(shape), dtype=torch.uint8, device=like.device)
+    return workspace
+
+
 def prefill_fwd_fp8(shape: Shape, q, k, v, q_scale, k_scale, v_scale, kv_idx, kv_cnt, softmax_scale,
-                    o, lse=None, dev_status=None, stream=None):
+                    o, lse=None, workspace=None, dev_status=None, stream=None):
     b, n, hq, hkv, d, nb = _dims(shape)
     lib = _lib.load()
+    workspace = _fp8_ws(shape, workspace, q)
     _lib.check("bsa_prefill_fwd_fp8", lib.bsa_prefill_fwd_fp8(
         ctypes.byref(shape), _ptr(q, "q", torch.uint8, b * n * hq * d),
         _ptr(k, "k", torch.uint8, b * n * hkv * d), _ptr(v, "v", torch.uint8, b * n * hkv * d),
@@ -223,19 +235,22 @@ def prefill_fwd_fp8(shape: Shape, q, k, v, q_scale, k_scale, v_scale, kv_idx, kv
         _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
         _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb), ctypes.c_float(softmax_scale),
         _ptr(o, "o", torch.bfloat16, b * n * hq * d), _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 
 def prefill_dense_fwd_fp8(shape: Shape, q, k, v, q_scale, k_scale, v_scale, softmax_scale, o,
-                          lse=None, dev_status=None, stream=None):
+                          lse=None, workspace=None, dev_status=None, stream=None):
     b, n, hq, hkv, d, nb = _dims(shape)
     lib = _lib.load()
+    workspace = _fp8_ws(shape, workspace, q)
     _lib.check("bsa_prefill_dense_fwd_fp8", lib.bsa_prefill_dense_fwd_fp8(
         ctypes.byref(shape), _ptr(q, "q", torch.uint8, b * n * hq * d),
         _ptr(k, "k", torch.uint8, b * n * hkv * d), _ptr(v, "v", torch.uint8, b * n * hkv * d),
         ctypes.c_float(q_scale), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
         ctypes.c_float(softmax_scale), _ptr(o, "o", torch.bfloat16, b * n * hq * d),
         _ptr(lse, "lse", torch.float32, b * hq * n),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
 
 

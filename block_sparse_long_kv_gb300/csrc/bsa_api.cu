@@ -288,29 +288,46 @@ bsa_status bsa_select_mask_fp8(const bsa_shape *shape, const bsa_select_params *
                      kv_cnt, mask, workspace, workspace_bytes, dev_status, stream);
 }
 
+size_t bsa_prefill_fp8_workspace_bytes(const bsa_shape *shape) {
+  if (check_shape(shape) != BSA_OK || shape->head_dim != 128) return 0;
+  return round_up(static_cast<size_t>(shape->batch) * shape->seq * shape->hkv * shape->head_dim * 2, 256);
+}
+
+static bsa_status prefill_fp8_common(const bsa_shape *shape, const void *q, const void *k,
+                                     const void *v, float q_scale, float k_scale, float v_scale,
+                                     const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale,
+                                     void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                     int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale)) return BSA_ERR_INVALID_ARG;
+  if (shape->head_dim != 128) return BSA_ERR_UNSUPPORTED;
+  if (!v || !aligned16(v)) return BSA_ERR_INVALID_ARG;
+  const size_t need = bsa_prefill_fp8_workspace_bytes(shape);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return BSA_ERR_WORKSPACE;
+  const size_t nv = static_cast<size_t>(shape->batch) * shape->seq * shape->hkv * shape->head_dim;
+  if (bsa::launch_widen_e4m3(v, workspace, nv, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return prefill_impl(fp8_shape(shape, q_scale, k_scale, v_scale), q, k, workspace, kv_idx, kv_cnt,
+                      softmax_scale, o, lse, dev_status, stream);
+}
+
 bsa_status bsa_prefill_fwd_fp8(const bsa_shape *shape, const void *q, const void *k, const void *v,
                                float q_scale, float k_scale, float v_scale, const int32_t *kv_idx,
                                const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
-                               int32_t *dev_status, bsa_stream_t stream) {
-  const bsa_status st = check_shape(shape);
-  if (st != BSA_OK) return st;
-  if (!kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
-  if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale)) return BSA_ERR_INVALID_ARG;
-  if (shape->head_dim != 128) return BSA_ERR_UNSUPPORTED;
-  return prefill_impl(fp8_shape(shape, q_scale, k_scale, v_scale), q, k, v, kv_idx, kv_cnt, softmax_scale,
-                      o, lse, dev_status, stream);
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               bsa_stream_t stream) {
+  if (!kv_idx || !kv_cnt) return check_shape(shape) != BSA_OK ? check_shape(shape) : BSA_ERR_INVALID_ARG;
+  return prefill_fp8_common(shape, q, k, v, q_scale, k_scale, v_scale, kv_idx, kv_cnt, softmax_scale, o,
+                            lse, workspace, workspace_bytes, dev_status, stream);
 }
 
 bsa_status bsa_prefill_dense_fwd_fp8(const bsa_shape *shape, const void *q, const void *k,
                                      const void *v, float q_scale, float k_scale, float v_scale,
-                                     float softmax_scale, void *o, float *lse, int32_t *dev_status,
-                                     bsa_stream_t stream) {
-  const bsa_status st = check_shape(shape);
-  if (st != BSA_OK) return st;
-  if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale)) return BSA_ERR_INVALID_ARG;
-  if (shape->head_dim != 128) return BSA_ERR_UNSUPPORTED;
-  return prefill_impl(fp8_shape(shape, q_scale, k_scale, v_scale), q, k, v, nullptr, nullptr,
-                      softmax_scale, o, lse, dev_status, stream);
+                                     float softmax_scale, void *o, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  return prefill_fp8_common(shape, q, k, v, q_scale, k_scale, v_scale, nullptr, nullptr, softmax_scale, o,
+                            lse, workspace, workspace_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------- packed ragged batches

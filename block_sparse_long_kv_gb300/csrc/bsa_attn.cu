@@ -28,13 +28,12 @@
 // setmaxnreg moves registers from the producer / MMA warpgroup to the softmax
 // warps; the host refuses to launch if the compiled register count differs
 // from the budget the split assumes.
-// FP8 inputs (F8): Q, K and V arrive as e4m3 codes with per-tensor scales.
-// S = Q K^T runs as kind::f8f6f4 (both operands K-major, K = 32 per MMA);
-// warps 2-3 convert each e4m3 V tile (loaded unswizzled by TMA) into the
-// bf16 MN-major layout the P V MMA reads (exact: e4m3 values are bf16
-// values), so P stays bf16 in TMEM and O matches the bf16 path's accuracy on
-// the dequantised inputs.  The scales fold into the softmax scale and the
-// final 1 / l.
+// FP8 inputs (F8): Q and K arrive as e4m3 codes with per-tensor scales and
+// S = Q K^T runs as kind::f8f6f4 (both operands K-major, K = 32 per MMA).  V
+// is widened to bf16 codes once per layer by a streaming pass (exact: every
+// e4m3 value is a bf16 value) and read by the unchanged P V path, so P stays
+// bf16 in TMEM and O matches the bf16 path's accuracy on the dequantised
+// inputs.  The scales fold into the softmax scale and the final 1 / l.
 // TMEM columns: S_t at t*KT, O_t at NT*KT + t*D (fp32 accumulators, one TMEM
 // lane per query row).  Every mbarrier wait is bounded: on timeout the kernel
 // records BSA_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs, frees
@@ -86,8 +85,6 @@ struct Cfg {
   static constexpr uint32_t Q_TILE = 128u * D * QKB;
   static constexpr uint32_t K_TILE = static_cast<uint32_t>(KT) * D * QKB;
   static constexpr uint32_t KV_TILE = static_cast<uint32_t>(KT) * D * 2;  // a bf16 V tile
-  static constexpr uint32_t V8_TILE = F8 ? static_cast<uint32_t>(KT) * D : 0u;  // an e4m3 V tile
-  static constexpr int V8S = F8 ? 2 : 0;            // e4m3 V staging stages
   static constexpr uint32_t Q_CHUNK = 128u * 128;
   static constexpr uint32_t KV_CHUNK = static_cast<uint32_t>(KT) * 128;
   // Softmax threads per query row: with 128-column key tiles two warps share each
@@ -99,7 +96,7 @@ struct Cfg {
   static constexpr int KS = 2;  // K stages: K(n+KS) only needs S(n) done
   // V stages: V(n+VS) needs PV_1(n) done, which comes late; use 3 when they fit
   static constexpr int VS =
-      (NT * Q_TILE + KS * K_TILE + 3 * KV_TILE + V8S * V8_TILE + RED_BYTES + 1024 + 512 <= 227u * 1024) ? 3 : 2;
+      (NT * Q_TILE + KS * K_TILE + 3 * KV_TILE + RED_BYTES + 1024 + 512 <= 227u * 1024) ? 3 : 2;
   static constexpr int TM_O = NT * KT;
   static constexpr int TM_NEED = NT * (KT + D);
   static constexpr uint32_t TM_COLS =
@@ -107,13 +104,11 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NT * Q_TILE;
   static constexpr uint32_t OFF_V = OFF_K + KS * K_TILE;
-  static constexpr uint32_t OFF_V8 = OFF_V + VS * KV_TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V8 + V8S * V8_TILE;
-  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain,
-  // e4m3 V staging full/empty[V8S] (F8; V full then means "converted")
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_TILE;
+  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
                        B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
-                       B_8F = B_FIN + 1, B_8E = B_8F + V8S, NBARS = B_8E + V8S;
+                       NBARS = B_FIN + 1;
   static constexpr uint32_t OFF_RED = (OFF_BAR + NBARS * 8 + 16 + 15) / 16 * 16;
   static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr int THREADS = 128 + 128 * NT * CH;
@@ -219,8 +214,6 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     for (int x = 0; x < C::NBARS; ++x) {
       uint32_t count = 1;
       if (x >= C::B_PR && x < C::B_PR + NT) count = 4 * C::CH;  // one arrive per softmax warp
-      if (F8 && x >= C::B_VF && x < C::B_VF + C::VS) count = 2;  // the two converter warps
-      if (F8 && x >= C::B_8E && x < C::B_8E + C::V8S) count = 2;
       ptx::mbar_init(bar(x), count);
     }
     *abort_flag = 0;
@@ -262,20 +255,12 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
           ptx::tma_load_4d(sK + ks * C::K_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * C::CE, g,
                            ktok0, 0);
         k_issued = n + 1;
-        if constexpr (F8) {
-          // e4m3 V into a staging buffer; the converter warps fill the bf16 V stage
-          const int s8 = n % C::V8S, u8 = n / C::V8S;
-          if (u8 > 0 && !wait_bar(bar(C::B_8E + s8), (u8 - 1) & 1, ctl)) break;
-          ptx::mbar_arrive_expect_tx(bar(C::B_8F + s8), C::V8_TILE);
-          ptx::tma_load_4d(base + C::OFF_V8 + s8 * C::V8_TILE, &tm_v, bar(C::B_8F + s8), 0, g, ktok0, 0);
-        } else {
-          const int vs = n % C::VS, vu = n / C::VS;
-          if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
-          ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
-          for (int c = 0; c < C::NCHV; ++c)
-            ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g,
-                             ktok0, 0);
-        }
+        const int vs = n % C::VS, vu = n / C::VS;
+        if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
+        for (int c = 0; c < C::NCHV; ++c)
+          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g,
+                           ktok0, 0);
         v_issued = n + 1;
       }
       if (*abort_flag) {
@@ -283,13 +268,8 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         drain_bar(bar(C::B_Q), 0);
         for (int n = k_issued - C::KS > 0 ? k_issued - C::KS : 0; n < k_issued; ++n)
           drain_bar(bar(C::B_KF + n % C::KS), (n / C::KS) & 1);
-        if constexpr (F8) {
-          for (int n = v_issued - C::V8S > 0 ? v_issued - C::V8S : 0; n < v_issued; ++n)
-            drain_bar(bar(C::B_8F + n % C::V8S), (n / C::V8S) & 1);
-        } else {
-          for (int n = v_issued - C::VS > 0 ? v_issued - C::VS : 0; n < v_issued; ++n)
-            drain_bar(bar(C::B_VF + n % C::VS), (n / C::VS) & 1);
-        }
+        for (int n = v_issued - C::VS > 0 ? v_issued - C::VS : 0; n < v_issued; ++n)
+          drain_bar(bar(C::B_VF + n % C::VS), (n / C::VS) & 1);
       }
     }
     __syncwarp();
@@ -365,37 +345,6 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         // every MMA issued so far must finish before TMEM is released
         ptx::mma_commit(bar(C::B_FIN));
         drain_bar(bar(C::B_FIN), 0);
-      }
-    }
-    __syncwarp();
-  } else {
-    if constexpr (F8) {
-      // ================================================================ V converters (warps 2-3)
-      // e4m3 V tile (row r = key, D bytes, unswizzled) -> bf16 MN-major tile in the layout a
-      // 128-byte-swizzled TMA load would give: chunk of 64 dims, row r of 128 bytes, 16-byte
-      // unit u at position u ^ (r % 8)
-      const int ct = threadIdx.x - 64;
-      for (int n = 0; n < T; ++n) {
-        const int s8 = n % C::V8S, vs = n % C::VS, vu = n / C::VS;
-        if (!wait_bar(bar(C::B_8F + s8), (n / C::V8S) & 1, ctl)) break;
-        if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
-        const unsigned char *src = sb + C::OFF_V8 + s8 * C::V8_TILE;
-        unsigned char *dst = sb + C::OFF_V + vs * C::KV_TILE;
-        for (int it = ct; it < C::KT * (D / 8); it += 64) {
-          const int r = it / (D / 8), unit = it - r * (D / 8);
-          const int c = unit >> 3, uu = unit & 7;
-          float f[8];
-          e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(src + r * D + unit * 8), f);
-          const uint4 o = make_uint4(ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]),
-                                     ptx::pack_bf16x2(f[4], f[5]), ptx::pack_bf16x2(f[6], f[7]));
-          *reinterpret_cast<uint4 *>(dst + c * C::KV_CHUNK + r * 128 + ((uu ^ (r & 7)) << 4)) = o;
-        }
-        ptx::fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(bar(C::B_8E + s8));
-          ptx::mbar_arrive(bar(C::B_VF + vs));
-        }
       }
     }
     __syncwarp();
@@ -590,8 +539,7 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
   const bool maps_ok =
       make_map(fn, &mq, q, 1, s.total, s.hq, D, C::QH, C::QTOK, F8, C::CE, true) &&
       make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KT, F8, C::CE, true) &&
-      (F8 ? make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, true, D, false)   // staged, converted
-          : make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, false, 64, true));
+      make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, false, 64, true);  // bf16 V (widened if fp8)
   if (!maps_ok) {
     *cerr = cudaErrorInvalidValue;
     return BSA_ERR_CUDA;
@@ -642,7 +590,34 @@ bsa_status launch_blk(const AttnShape &s, const void *q, const void *k, const vo
   }
 }
 
+// e4m3 codes -> bf16 codes of the same values (exact), 16 per thread per step.
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                         size_t n16) {
+  for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < n16;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 u = __ldcs(src + e);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      float f[8];
+      e4m3x8_to_f32(make_uint2(w[x], 0u), f);  // the low four bytes of each word
+      o[2 * x] = ptx::pack_bf16x2(f[0], f[1]);
+      o[2 * x + 1] = ptx::pack_bf16x2(f[2], f[3]);
+    }
+    __stcs(dst + 2 * e, make_uint4(o[0], o[1], o[2], o[3]));
+    __stcs(dst + 2 * e + 1, make_uint4(o[4], o[5], o[6], o[7]));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_e4m3(const void *src, void *dst, size_t n, cudaStream_t stream) {
+  const size_t n16 = n / 16;  // n is a multiple of 16 (head_dim 128 rows)
+  const unsigned grid = static_cast<unsigned>(n16 / 256 + 1 < 152 * 16 ? n16 / 256 + 1 : 152 * 16);
+  widen_e4m3_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16);
+  return cudaGetLastError();
+}
 
 EncodeTiledFn tensor_map_encoder(cudaError_t *err) {
   static EncodeTiledFn fn = nullptr;

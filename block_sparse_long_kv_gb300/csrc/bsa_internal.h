@@ -95,6 +95,9 @@ cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, 
                           const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,
                           void *workspace, int32_t *status, cudaStream_t stream);
 
+// e4m3 codes -> bf16 codes of the same values; n elements, a multiple of 16.
+cudaError_t launch_widen_e4m3(const void *src, void *dst, size_t n, cudaStream_t stream);
+
 struct AttnShape {
   int batch, seq, hq, hkv, d, block, nb, group;
   const int32_t *cu;  // packed ragged batch (o [total, hq, d], lse [hq, total]) or null

@@ -284,18 +284,19 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
 // tf32), lo = x - hi is exact in fp32.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
-// Sums a full block's queries (8 dimensions per lane) and their norms, 8 loads
-// in flight per thread.
+// Sums a full block's queries (8 dimensions per lane) and their norms, 8 (bf16)
+// or 16 (e4m3) loads in flight per thread.
 template <int D, bool F8>
 __device__ __forceinline__ void pool_full(const unsigned char *__restrict__ base, size_t tok_stride,
                                           int cnt, unsigned wmask, float acc[8], float &nsum) {
-  constexpr int VH = D / 8;  // lanes per head
-  for (int t0 = 0; t0 < cnt; t0 += 8) {
-    uint4 u[8];
+  constexpr int VH = D / 8;        // lanes per head
+  constexpr int TB = F8 ? 16 : 8;  // tokens in flight per lane (8-byte e4m3 loads: twice as many)
+  for (int t0 = 0; t0 < cnt; t0 += TB) {
+    uint4 u[TB];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) u[r] = load8<F8>(base + static_cast<size_t>(t0 + r) * tok_stride);
+    for (int r = 0; r < TB; ++r) u[r] = load8<F8>(base + static_cast<size_t>(t0 + r) * tok_stride);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < TB; ++r) {
       float f[8];
       unpack8<F8>(u[r], f);
       float sq = 0.f;

@@ -235,12 +235,16 @@ bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets);
  *   - bsa_select_mask_fp8: the selection with q * q_scale (flags must be 0:
  *     BSA_SELECT_TOKEN_MAX returns BSA_ERR_UNSUPPORTED here);
  *   - bsa_prefill_fwd_fp8 / bsa_prefill_dense_fwd_fp8: attention with
- *     S = Q K^T on the tensor cores' e4m3 path (kind::f8f6f4), V converted to
- *     bf16 on chip, O written as bf16; head_dim 128 only (other head_dims
- *     return BSA_ERR_UNSUPPORTED).
+ *     S = Q K^T on the tensor cores' e4m3 path (kind::f8f6f4); V is first
+ *     widened to bf16 codes of the same values (exact) in the workspace
+ *     (bsa_prefill_fp8_workspace_bytes(shape) bytes, 16-byte aligned, owned
+ *     by the caller, dead after the call's kernels); O written as bf16;
+ *     head_dim 128 only (other head_dims return BSA_ERR_UNSUPPORTED, and the
+ *     workspace size function returns 0 for them).
  * Scales must be finite and positive (BSA_ERR_INVALID_ARG otherwise).  Other
  * arguments, layouts and errors as the bf16 entry points.
  * ------------------------------------------------------------------------ */
+size_t bsa_prefill_fp8_workspace_bytes(const bsa_shape *shape);
 bsa_status bsa_block_meta_fp8(const bsa_shape *shape, const void *k, float k_scale, float *centroid,
                               float *radius, float *quant, float *alpha, int32_t *dev_status,
                               bsa_stream_t stream);
@@ -252,11 +256,12 @@ bsa_status bsa_select_mask_fp8(const bsa_shape *shape, const bsa_select_params *
 bsa_status bsa_prefill_fwd_fp8(const bsa_shape *shape, const void *q, const void *k, const void *v,
                                float q_scale, float k_scale, float v_scale, const int32_t *kv_idx,
                                const int32_t *kv_cnt, float softmax_scale, void *o, float *lse,
-                               int32_t *dev_status, bsa_stream_t stream);
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               bsa_stream_t stream);
 bsa_status bsa_prefill_dense_fwd_fp8(const bsa_shape *shape, const void *q, const void *k,
                                      const void *v, float q_scale, float k_scale, float v_scale,
-                                     float softmax_scale, void *o, float *lse, int32_t *dev_status,
-                                     bsa_stream_t stream);
+                                     float softmax_scale, void *o, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Packed ragged batches ("varlen").

@@ -161,15 +161,27 @@ def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x80, -v, v)
 
 
-def fp8_layer(lay: dict) -> dict:
+def fp8_layer(lay: dict, threads: int | None = None) -> dict:
     """The layer's Q, K, V (bf16 bits) as e4m3 codes with one power-of-two scale per tensor:
     value = e4m3 * scale, scale = 2^ceil(log2(max|x| / 448))."""
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
     out = {}
     for name in ("q", "k", "v"):
-        x = bf16_to_f32(lay[name]).astype(np.float64)
-        mx = float(np.abs(x).max()) if x.size else 1.0
+        bits = lay[name]
+        flat = bits.reshape(-1)
+        mx = float(np.abs(bf16_to_f32(flat)).max()) if flat.size else 1.0
         scale = 2.0 ** int(np.ceil(np.log2(max(mx, 1e-30) / 448.0)))
-        out[name] = e4m3_bits(x / scale)
+        codes = np.empty(flat.shape, dtype=np.uint8)
+        step = 1 << 22
+
+        def conv(lo):
+            hi = min(lo + step, flat.size)
+            codes[lo:hi] = e4m3_bits(bf16_to_f64(flat[lo:hi]) / scale)   # exact division by 2^k
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(conv, range(0, flat.size, step)))
+        out[name] = codes.reshape(bits.shape)
         out[name + "_scale"] = scale
     return out
 

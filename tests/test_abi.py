@@ -188,10 +188,15 @@ def test_fp8_entry_point_validation(lib):
         b = ctypes.c_float(bad)
         assert lib.bsa_block_meta_fp8(ctypes.byref(s), f, b, f, f, f, f, None, None) == 1
         assert lib.bsa_prefill_dense_fwd_fp8(ctypes.byref(s), f, f, f, one, b, one, ctypes.c_float(0.1),
-                                             f, None, None, None) == 1
+                                             f, None, f, ctypes.c_size_t(1 << 40), None, None) == 1
     s64 = shp(head_dim=64)                                   # e4m3 attention needs head_dim 128
     assert lib.bsa_prefill_dense_fwd_fp8(ctypes.byref(s64), f, f, f, one, one, one, ctypes.c_float(0.1),
-                                         f, None, None, None) == 3
+                                         f, None, f, ctypes.c_size_t(1 << 40), None, None) == 3
+    assert lib.bsa_prefill_fp8_workspace_bytes(ctypes.byref(s64)) == 0
+    need = lib.bsa_prefill_fp8_workspace_bytes(ctypes.byref(s))
+    assert need == 1 * 1024 * 2 * 128 * 2                    # V widened to bf16
+    assert lib.bsa_prefill_dense_fwd_fp8(ctypes.byref(s), f, f, f, one, one, one, ctypes.c_float(0.1),
+                                         f, None, f, ctypes.c_size_t(need - 1), None, None) == 4
     tok = _lib.SelectParams(0.1, 0.1, 1)                     # per-token aggregation reads bf16 Q
     assert lib.bsa_select_mask_fp8(ctypes.byref(s), ctypes.byref(tok), f, one, f, f, f, f, f, None, f,
                                    ctypes.c_size_t(1 << 40), None, None) == 3

@@ -60,10 +60,11 @@ def gpu_fp8_attention(w, f8, kv=None):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     sc = 1.0 / math.sqrt(w.head_dim)
     if kv is None:
-        bsa.prefill_dense_fwd_fp8(s, q, k, v, f8["q_scale"], f8["k_scale"], f8["v_scale"], sc, o, lse, st)
+        bsa.prefill_dense_fwd_fp8(s, q, k, v, f8["q_scale"], f8["k_scale"], f8["v_scale"], sc, o, lse,
+                                  dev_status=st)
     else:
         bsa.prefill_fwd_fp8(s, q, k, v, f8["q_scale"], f8["k_scale"], f8["v_scale"], kv[0], kv[1], sc,
-                            o, lse, st)
+                            o, lse, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return o.float().cpu().numpy(), lse.cpu().numpy()
