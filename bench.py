@@ -48,6 +48,10 @@ def parse():
                     help="score query blocks by their best token (BSA_SELECT_TOKEN_MAX)")
     ap.add_argument("--fp8", action="store_true",
                     help="e4m3 Q / K / V inputs with per-tensor scales (the *_fp8 entry points)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="block size x keep-ratio sweep at 64K tokens: density, ms/layer, needle recall")
+    ap.add_argument("--crossover", action="store_true",
+                    help="sparse vs dense path at 32K over a centroid keep-ratio sweep; break-even density")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (new token per sequence) over the workload as a cache")
     return ap.parse_args()
@@ -885,12 +889,169 @@ def run_decode(args):
     return 0
 
 
+def needle_recall(w, needles, mask):
+    """Fraction of (needle query block, needle key block) pairs the mask keeps."""
+    hit = tot = 0
+    for (b, g, jb, slot, pos) in needles:
+        for i in sorted(set((pos // w.block).tolist())):
+            tot += 1
+            hit += bool(mask[b, g, i, jb])
+    return hit / tot if tot else float("nan")
+
+
+def run_sweep(args):
+    """The 27 block-size x keep-ratio combinations at 64K tokens (GQA 32/4, d 128): per
+    combination the kept density, ms per layer (mask build + attention, CUDA events) and the
+    needle recall of the GPU mask; one JSON line each, then a summary line."""
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import block_sparse_long_kv_gb300 as bsa
+    from block_sparse_long_kv_gb300 import build as bld
+    import synth
+    bld.build()
+    # the oracle's figures, stored by tests/golden/make_sweep_oracle.py (oracle only)
+    gold_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tests", "golden",
+                             "sweep_oracle.json")
+    gold = json.load(open(gold_path))["workloads"]
+    rows = []
+    layers = {}
+    for w in synth.sweep_workloads():
+        if w.block not in layers:
+            lay = synth.make_layer(w)
+            up = lambda x: torch.from_numpy(lay[x].view(np.int16)).to(dev).view(torch.bfloat16)
+            layers.clear()
+            layers[w.block] = (lay, {x: up(x) for x in ("q", "k", "v")})
+        lay, L = layers[w.block]
+        run = FixedRunner(bsa, torch, w, dev)
+        o = torch.empty_like(L["q"])
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        masked = bsa.alloc_select(run.s, dev, with_mask=True)
+        m = run.meta
+        bsa.block_meta(run.s, L["k"], m["centroid"], m["radius"], m["quant"], m["alpha"], st)
+        bsa.select_mask(run.s, run.prm, L["q"], m["centroid"], m["radius"], m["alpha"], masked["kv_idx"],
+                        masked["kv_cnt"], masked["mask"], run.ws, st)
+        torch.cuda.synchronize(dev)
+        recall = needle_recall(w, lay["needles"], masked["mask"].cpu().numpy())
+        for _ in range(max(3, args.warmup)):
+            run.meta_call(L, st)
+            run.select_call(L, st)
+            run.attn_call(L, o, st)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        steps = max(3, min(args.steps, 10))
+        times = []
+        for _ in range(steps):
+            ev[0].record()
+            run.meta_call(L, st)
+            run.select_call(L, st)
+            ev[1].record()
+            run.attn_call(L, o, st)
+            ev[2].record()
+            torch.cuda.synchronize(dev)
+            times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        f, _, dens = run.stats()
+        mk = float(np.median([t[0] for t in times]))
+        at = float(np.median([t[1] for t in times]))
+        row = {"workload": w.name, "block": w.block, "centroid_keep": w.centroid_keep,
+               "rescue_keep": w.rescue_keep, "density": dens, "ms_per_layer": mk + at,
+               "mask_build_ms": mk, "attention_ms": at, "kept_block_tflops": f / (at * 1e-3) / 1e12,
+               "needle_recall": recall, "oracle_density": gold[w.name]["density"],
+               "oracle_needle_recall": gold[w.name]["needle_recall"]}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+    # the rescue path's contribution: recall with rho_r > 0 against the centroid-only run (rho_r = 0)
+    summary = {"metric": "sweep: block size x keep ratios at 64K GQA 32/4 (density, ms/layer, needle recall)",
+               "configs": len(rows), "data": "synthetic",
+               "recall_centroid_only_mean": float(np.mean([r["needle_recall"] for r in rows if r["rescue_keep"] == 0])),
+               "recall_with_rescue_mean": float(np.mean([r["needle_recall"] for r in rows if r["rescue_keep"] > 0]))}
+    print(json.dumps(summary), flush=True)
+    return 0
+
+
+def _time_calls(torch, calls, steps, warmup):
+    """Median CUDA-event time (ms) of each callable in ``calls`` run back to back."""
+    for _ in range(warmup):
+        for c in calls:
+            c()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+    times = [[] for _ in calls]
+    for _ in range(steps):
+        ev[0].record()
+        for n, c in enumerate(calls):
+            c()
+            ev[n + 1].record()
+        torch.cuda.synchronize()
+        for n in range(len(calls)):
+            times[n].append(ev[n].elapsed_time(ev[n + 1]))
+    return [float(np.median(t)) for t in times]
+
+
+def run_crossover(args):
+    """The sparse path (mask build + attention over the kept blocks) against the dense causal
+    path at 32K tokens (GQA 32/4, d 128, block 128, rescue keep-ratio 0.03) while the centroid
+    keep-ratio grows to 1; reports density, times, and the density where the two cross."""
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import block_sparse_long_kv_gb300 as bsa
+    from block_sparse_long_kv_gb300 import build as bld
+    import synth
+    bld.build()
+    w0 = synth.workload("gqa32x4_n32768_d128_b128")
+    lay = synth.make_layer(w0)
+    L = {x: torch.from_numpy(lay[x].view(np.int16)).to(dev).view(torch.bfloat16) for x in ("q", "k", "v")}
+    o = torch.empty_like(L["q"])
+    lse = torch.empty(w0.batch, w0.hq, w0.seq, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = bsa.make_shape(w0.batch, w0.seq, w0.hq, w0.hkv, w0.head_dim, w0.block)
+    scale = 1.0 / math.sqrt(w0.head_dim)
+    steps, warm = max(3, min(args.steps, 20)), max(3, args.warmup)
+    dense_ms, = _time_calls(torch, [lambda: bsa.prefill_dense_fwd(s, L["q"], L["k"], L["v"], scale, o,
+                                                                    lse, st)], steps, warm)
+    dense_flops = 4.0 * w0.batch * w0.hq * w0.head_dim * w0.seq * (w0.seq + 1) / 2
+    rows = []
+    for rc in (0.02, 0.05, 0.1, 0.15, 0.2, 0.3, 0.4, 0.5, 0.6, 0.7, 0.8, 0.9, 1.0):
+        w = w0.with_(centroid_keep=rc)
+        run = FixedRunner(bsa, torch, w, dev)
+        mk, sl, at = _time_calls(torch, [lambda: run.meta_call(L, st), lambda: run.select_call(L, st),
+                                         lambda: run.attn_call(L, o, st)], steps, warm)
+        f, _, dens = run.stats()
+        row = {"centroid_keep": rc, "rescue_keep": w.rescue_keep, "density": dens,
+               "mask_build_ms": mk + sl, "attention_ms": at, "sparse_ms": mk + sl + at,
+               "dense_ms": dense_ms, "speedup_vs_dense": dense_ms / (mk + sl + at),
+               "kept_block_tflops": f / (at * 1e-3) / 1e12}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    # break-even: the first density where the sparse path is no faster, by linear interpolation
+    cross = None
+    for a, b in zip(rows, rows[1:]):
+        if a["sparse_ms"] < dense_ms <= b["sparse_ms"]:
+            t = (dense_ms - a["sparse_ms"]) / (b["sparse_ms"] - a["sparse_ms"])
+            cross = a["density"] + t * (b["density"] - a["density"])
+            break
+    print(json.dumps({"metric": "sparse vs dense crossover at 32K GQA 32/4 d128 b128",
+                      "dense_ms": dense_ms, "dense_tflops": dense_flops / (dense_ms * 1e-3) / 1e12,
+                      "break_even_density": cross, "points": len(rows), "data": "synthetic"}),
+          flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.decode:
         return run_decode(args)
+    if args.sweep:
+        return run_sweep(args)
+    if args.crossover:
+        return run_crossover(args)
     return run_ours(args)
 
 
