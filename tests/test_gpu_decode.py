@@ -211,3 +211,53 @@ def test_decode_shape_variants(cfg):
     lists = upload(vw, orc, got["nbs"])
     got2 = gpu_decode(vw, lay, q_new, lists=lists)
     check_outputs(vw, lay, q_new, got2, {bg: d["kept"] for bg, d in orc.items()})
+
+
+@pytest.mark.parametrize("nb", [1000, 2000, 3000, 4096])
+def test_decode_select_long_rows_synthetic_meta(nb):
+    """Rows of 1000 to 4096 blocks (every register width of the CTA-wide select, up to the
+    library's block limit) on synthetic block summaries: sequence 0 random, sequence 1 with
+    every centroid, radius and alpha equal so both paths rank pure ties (lowest index
+    first)."""
+    import block_sparse_long_kv_gb300 as bsa
+    block, hq, hkv, d = 64, 8, 2, 64
+    lengths = (nb * block, nb * block - 37)
+    vw = synth.VarlenWorkload("dec_meta", lengths, hq, hkv, d, block, 0.1, 0.05)
+    s = bsa.make_varlen_shape(vw.batch, vw.total, vw.max_seqlen, hq, hkv, d, block)
+    nbs = bsa.varlen_block_stride(s)
+    rng = np.random.default_rng(nb)
+    cen = rng.standard_normal((2, hkv, nbs, d)).astype(np.float32)
+    rad = np.exp(rng.uniform(-1, 1, (2, hkv, nbs))).astype(np.float32)
+    alpha = np.where(rng.random((2, hkv, nbs)) < 0.5, 0.0, rng.random((2, hkv, nbs))).astype(np.float32)
+    cen[1] = cen[1, :, :1]
+    rad[1] = 1.5
+    alpha[1] = 0.5
+    q_new = synth.bf16_bits(rng.standard_normal((2, hq, d)).astype(np.float32))
+    cu = torch.tensor(vw.cu_seqlens(), dtype=torch.int32, device="cuda")
+    kv_idx = torch.zeros(2, hkv, nbs, dtype=torch.int32, device="cuda")
+    kv_cnt = torch.zeros(2, hkv, dtype=torch.int32, device="cuda")
+    ws = torch.empty(bsa.decode_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsa.decode_select(s, bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0), cu, to_dev(q_new),
+                      torch.from_numpy(cen).cuda(), torch.from_numpy(rad).cuda(),
+                      torch.from_numpy(alpha).cuda(), kv_idx, kv_cnt, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = dict(kv_idx=kv_idx.cpu().numpy(), kv_cnt=kv_cnt.cpu().numpy(), nbs=nbs)
+    qn = synth.bf16_to_f64(q_new)
+    orc = {}
+    for b, n in enumerate(lengths):
+        nbb = -(-n // block)
+        i = (n - 1) // block
+        for g in range(hkv):
+            c64, r64, a64 = (x[b, :, :nbb].astype(np.float64) for x in (cen, rad, alpha))
+            kept, s_c, r = O.decode_select(qn[b], c64, r64, a64, n, block, vw.centroid_keep,
+                                           vw.rescue_keep, g)
+            cent, resc = O.select_row(s_c, r, a64[g], i, O.ratio_ppm(vw.centroid_keep),
+                                      O.ratio_ppm(vw.rescue_keep))
+            orc[(b, g)] = dict(kept=kept, s_c=s_c, r=r, med=-1.0, radius=r64[g], n=n, cent=cent,
+                               resc=resc)
+    compared, excused = compare_lists(vw, got, orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)
+    for g in range(hkv):  # pure ties: bit-exact, lowest indices first
+        np.testing.assert_array_equal(got["kv_idx"][1, g, :got["kv_cnt"][1, g]], orc[(1, g)]["kept"])
