@@ -82,6 +82,26 @@ def kept_flops(kv_cnt: np.ndarray, block: int, d: int, group: int) -> float:
     return float(group * (per * (cnt - 1).clip(min=0).sum() + 0.5 * per * (cnt > 0).sum()))
 
 
+def replica_layers(rank: int, layers: int) -> list:
+    """Seeded layer indices of one replica: each rank draws its own layers, disjoint across ranks."""
+    return [rank * layers + li for li in range(layers)]
+
+
+def reduce_max(value: float, dist=None, device="cpu") -> float:
+    """The maximum of ``value`` over the ranks (the slowest rank sets the job's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_ms_per_layer(max_total_ms: float, steps: int, world: int) -> float:
+    """Whole-job ms per layer: every rank ran ``steps`` layers in at most ``max_total_ms``."""
+    return max_total_ms / (steps * world)
+
+
 def source_sha(*files):
     h = hashlib.sha256()
     for f in files:
@@ -541,8 +561,8 @@ def run_ours(args):
     # resident inputs: `layers` distinct seeded layers per rank (replicas process their own layers)
     host_layers = []
     dev_layers = []
-    for li in range(args.layers):
-        lay = run.make_layer(synth, rank * args.layers + li)
+    for li in replica_layers(rank, args.layers):
+        lay = run.make_layer(synth, li)
         host_layers.append(lay)
         dev_layers.append(run.upload(lay))
     o = torch.empty(dev_layers[0]["q"].shape, dtype=torch.bfloat16, device=dev)
@@ -596,11 +616,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(t_start.elapsed_time(t_end), dist if world > 1 else None, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
@@ -627,7 +643,7 @@ def run_ours(args):
     # the committed DRAM-traffic capture covers the default 128K workload only
     default = (not isinstance(run, (VarlenRunner, Fp8Runner)) and w.name == "gqa32x4_n131072_d128_b128")
     traffic, _ = profiled_traffic() if default else (None, None)
-    ms_per_layer = total_ms / (K * world)
+    ms_per_layer = job_ms_per_layer(total_ms, K, world)
     q_gb = run.tokens * w.hq * w.head_dim * in_bytes / 1e9
     cfg = run.config()
     cfg.update({"aggregation": "token_max" if args.token_max else "block_mean",
@@ -734,13 +750,9 @@ def run_ours(args):
         e2e_run(2)
         if world > 1:
             dist.barrier()
-        e2e_ms = e2e_run(n_e2e)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = reduce_max(e2e_run(n_e2e), dist if world > 1 else None, dev)
         h2d = sum(pinned[0][n].numel() * pinned[0][n].element_size() for n in ("q", "k", "v"))
-        result["e2e"] = {"value": e2e_ms / n_e2e, "unit": "ms/layer",
+        result["e2e"] = {"value": job_ms_per_layer(e2e_ms, n_e2e, world), "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host[0].numel() * 2,
                          "steps": n_e2e,
                          "api": run.e2e_api + " + pinned host copies on two copy streams, "

@@ -10,7 +10,10 @@
 // One CTA owns NT query tiles of 128 rows that share one kept-block list: the
 // rows are 128 tokens of one head (block 128 / 256) or 64 tokens x 2 heads of
 // the same KV group (block 64), so K and V tiles are loaded once per CTA for
-// NT tiles (GQA sharing).  Warp roles:
+// NT tiles (GQA sharing).  Key tiles are always 128 keys wide: with block 64
+// a tile holds two kept blocks (two TMA boxes into one tile; an odd count
+// leaves the last tile's second half masked), so every S MMA is N = 128.
+// Warp roles:
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of every kept
 //               block through mbarrier rings (KS K stages, VS V stages)
 //   warp 1      TMEM owner and single-thread MMA issuer:
@@ -70,11 +73,13 @@ struct AttnParams {
 
 template <int D, int BLK, int NT, bool F8 = false>
 struct Cfg {
-  static constexpr int KT = BLK < 128 ? BLK : 128;  // key-tile rows
+  static constexpr int KT = 128;                    // key-tile rows
+  static constexpr bool PAIR = BLK == 64;           // a key tile holds two kept 64-key blocks
+  static constexpr int KBOX = PAIR ? 64 : KT;       // key rows per TMA box
   static constexpr int QH = BLK == 64 ? 2 : 1;      // heads stacked in one 128-row Q tile
   static constexpr int QTOK = 128 / QH;             // tokens per Q tile
   static constexpr int NQS = BLK == 256 ? 2 : 1;    // Q tiles along one query block
-  static constexpr int SUB = BLK / KT;              // key tiles per key block
+  static constexpr int SUB = PAIR ? 1 : BLK / KT;   // key tiles per key block (pairs: half a tile each)
   static constexpr int QKB = F8 ? 1 : 2;            // bytes per Q / K element
   static constexpr int CE = 128 / QKB;              // Q / K elements per 128-byte swizzle row
   static constexpr int NCH = D * QKB / 128;         // 128-byte swizzle chunks per Q / K row
@@ -206,9 +211,11 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     cnt = cnt < 0 ? 0 : (cnt > i + 1 ? i + 1 : cnt);
   }
   const int32_t *kvrow = DENSE ? nullptr : p.kv_idx + row * p.nbs;
-  // the diagonal block of the first half of a 256-row block has an all-masked second key tile
-  const int T = cnt * C::SUB - ((C::NQS == 2 && qs == 0 && cnt > 0) ? 1 : 0);
-  auto key_block = [&](int n) -> int { return DENSE ? n / C::SUB : __ldg(kvrow + n / C::SUB); };
+  // the diagonal block of the first half of a 256-row block has an all-masked second key tile;
+  // 64-key blocks go two to a tile (an odd count leaves the last tile's second half empty)
+  const int T = C::PAIR ? (cnt + 1) / 2 : cnt * C::SUB - ((C::NQS == 2 && qs == 0 && cnt > 0) ? 1 : 0);
+  auto entry_block = [&](int e) -> int { return DENSE ? e : __ldg(kvrow + e); };
+  auto key_block = [&](int n) -> int { return entry_block(n / C::SUB); };
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < C::NBARS; ++x) {
@@ -246,21 +253,36 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
                            sp.start + qtok0, 0);
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
+      // first key token of each TMA box of tile n: one box of 128 keys, or (pairs) two
+      // boxes of 64, the second a copy of the first when the tile holds one block
+      int kt0[2];
+      auto tile_tokens = [&](int n) {
+        if constexpr (C::PAIR) {
+          kt0[0] = sp.start + entry_block(2 * n) * BLK;
+          kt0[1] = 2 * n + 1 < cnt ? sp.start + entry_block(2 * n + 1) * BLK : kt0[0];
+        } else {
+          kt0[0] = sp.start + key_block(n) * BLK + (n % C::SUB) * C::KT;
+        }
+      };
+      constexpr int NBOX = C::PAIR ? 2 : 1;
+      constexpr uint32_t BOX_ROWS_BYTES = static_cast<uint32_t>(C::KBOX) * 128;  // one box within a chunk
       for (int n = 0; n < T; ++n) {
-        const int ktok0 = sp.start + key_block(n) * BLK + (n % C::SUB) * C::KT;
+        tile_tokens(n);
         const int ks = n % C::KS, ku = n / C::KS;
         if (ku > 0 && !wait_bar(bar(C::B_KE + ks), (ku - 1) & 1, ctl)) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::K_TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sK + ks * C::K_TILE + c * C::KV_CHUNK, &tm_k, bar(C::B_KF + ks), c * C::CE, g,
-                           ktok0, 0);
+        for (int x = 0; x < NBOX; ++x)
+          for (int c = 0; c < C::NCH; ++c)
+            ptx::tma_load_4d(sK + ks * C::K_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_k,
+                             bar(C::B_KF + ks), c * C::CE, g, kt0[x], 0);
         k_issued = n + 1;
         const int vs = n % C::VS, vu = n / C::VS;
         if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
-        for (int c = 0; c < C::NCHV; ++c)
-          ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK, &tm_v, bar(C::B_VF + vs), c * 64, g,
-                           ktok0, 0);
+        for (int x = 0; x < NBOX; ++x)
+          for (int c = 0; c < C::NCHV; ++c)
+            ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_v,
+                             bar(C::B_VF + vs), c * 64, g, kt0[x], 0);
         v_issued = n + 1;
       }
       if (*abort_flag) {
@@ -374,16 +396,23 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     for (int n = 0; n < T; ++n) {
       if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
       ptx::tc_fence_after();
-      const int j = key_block(n);
-      const int ktok0 = j * BLK + (n % C::SUB) * C::KT + hf * C::CW;  // key of this thread's column 0
+      int ktok0;        // key of this thread's column 0
+      bool half = true;  // pairs: this thread's half of the tile holds a kept block
+      if constexpr (C::PAIR) {
+        half = 2 * n + hf < cnt;
+        ktok0 = entry_block(half ? 2 * n + hf : 2 * n) * BLK;
+      } else {
+        ktok0 = key_block(n) * BLK + (n % C::SUB) * C::KT + hf * C::CW;
+      }
       uint32_t sr[C::CW];
 #pragma unroll
       for (int c = 0; c < C::CW / 32; ++c)
         ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       ptx::tmem_wait_ld();
-      if (ktok0 + C::CW - 1 > qtok0) {
-        // columns that overlap the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok
-        const int lim = qtok - ktok0;
+      if (!half || ktok0 + C::CW - 1 > qtok0) {
+        // columns that overlap the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok;
+        // an empty half masks every column
+        const int lim = half ? qtok - ktok0 : -1;
 #pragma unroll
         for (int c = 0; c < C::CW; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
@@ -538,8 +567,8 @@ bsa_status launch_t(const AttnShape &s, const void *q, const void *k, const void
   CUtensorMap mq, mk, mv;
   const bool maps_ok =
       make_map(fn, &mq, q, 1, s.total, s.hq, D, C::QH, C::QTOK, F8, C::CE, true) &&
-      make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KT, F8, C::CE, true) &&
-      make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KT, false, 64, true);  // bf16 V (widened if fp8)
+      make_map(fn, &mk, k, 1, s.total, s.hkv, D, 1, C::KBOX, F8, C::CE, true) &&
+      make_map(fn, &mv, v, 1, s.total, s.hkv, D, 1, C::KBOX, false, 64, true);  // bf16 V (widened if fp8)
   if (!maps_ok) {
     *cerr = cudaErrorInvalidValue;
     return BSA_ERR_CUDA;
