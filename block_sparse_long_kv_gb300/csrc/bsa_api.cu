@@ -434,6 +434,7 @@ bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqle
     return BSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BSA_ERR_INVALID_ARG;
   const bsa::MaskShape ms = mask_shape(shape, cu_seqlens);
+  if (static_cast<long long>(ms.batch) * ms.hkv > bsa::kMaxDecodeRows) return BSA_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::decode_workspace_bytes(ms))
     return BSA_ERR_WORKSPACE;
   if (bsa::launch_decode(ms, q_new, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, workspace,

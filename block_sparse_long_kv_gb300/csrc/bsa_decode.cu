@@ -18,24 +18,28 @@
 //                          threshold bin, as the prefill row code in
 //                          bsa_topk.cuh does per warp; ties by index)
 // Attention (bsa_decode_fwd), two launches:
-//   decode_attn_kernel     P CTAs per (b, g), about 456 in all: CTA s takes the
-//                          kept entries s, s + P, ... in chunks of 128 keys
-//                          staged by cp.async (keys and values as separate
-//                          groups, the next keys in flight during P V), the G
-//                          heads' logits (one thread per key), an online
-//                          softmax, and P V with 2 dimensions x one key group
-//                          per thread; writes the split's unnormalised O, max
-//                          and sum
-//   decode_combine_kernel  one CTA per (b, h): merges the splits (log-sum-exp)
-//                          and writes O and LSE
+//   decode_attn_kernel     as many CTAs as fit on the GPU (up to 1024): the kept
+//                          entries of all rows (b, g) laid end to end and cut
+//                          into equal runs, one per CTA, so a short batch and a
+//                          mix of long and short sequences load every SM alike.
+//                          A CTA streams its entries in 64-key chunks through a
+//                          three-stage cp.async ring, computes the G heads'
+//                          logits, an online softmax and P V on CUDA cores, and
+//                          writes one unnormalised partial (O, max, sum) per row
+//                          it touches
+//   decode_combine_kernel  one CTA per (b, h): merges the row's partials
+//                          (log-sum-exp) and writes O and LSE
 // The cache is a packed batch (sequence b = tokens cu[b] .. cu[b+1]-1, its
 // last token the new one), checked like every packed batch (seq_span).
 
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "bsa_internal.h"
 #include "bsa_topk.cuh"
+#include "sm103_ptx.cuh"
 
 namespace bsa {
 namespace {
@@ -390,315 +394,498 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+constexpr int kChunk = 64;       // keys per chunk
+constexpr int kStages = 4;       // chunks in shared memory: the current one and three in flight
+constexpr int kMaxDecodeCtas = 1024;
+
 template <int D, int G>
 struct DecCfg {
-  static constexpr int KCH = 128;                    // keys per chunk = threads
-  static constexpr int KROW = D * 2 + 16;            // padded key row (bytes): conflict-free row reads
-  static constexpr int DP = D / 2;                   // dimension pairs
-  static constexpr int KH = kAttnThreads / DP;       // key groups in P V
+  static constexpr int ROW = D * 2 + 16;   // padded key / value row (bytes): conflict-free fragment loads
+  static constexpr int NKS = D / 16;       // k-steps of S = Q K^T
+  static constexpr int NNT = D / 8;        // n-tiles of O = P V
+  static constexpr size_t STAGE = static_cast<size_t>(kChunk) * ROW;  // keys or values of one chunk
   static constexpr size_t OFF_K = 0;
-  static constexpr size_t OFF_V = OFF_K + static_cast<size_t>(KCH) * KROW;
-  static constexpr size_t OFF_Q = OFF_V + static_cast<size_t>(KCH) * D * 2;
-  static constexpr size_t OFF_P = OFF_Q + static_cast<size_t>(G) * D * 4;
-  static constexpr size_t SMEM = OFF_P + static_cast<size_t>(G) * KCH * 4;
-  // the key-group O partials reuse the key buffer after the last chunk
-  static_assert(static_cast<size_t>(KH > 1 ? KH - 1 : 1) * G * D * 4 <= static_cast<size_t>(KCH) * KROW,
-                "O partials fit in the key buffer");
+  static constexpr size_t OFF_V = OFF_K + kStages * STAGE;
+  static constexpr size_t OFF_O = OFF_V + kStages * STAGE;                 // [warps][G][D] fp32
+  static constexpr size_t OFF_ML = OFF_O + static_cast<size_t>(kAttnThreads / 32) * G * D * 4;  // [2][warps][16]
+  static constexpr size_t OFF_ROWS = OFF_ML + 2 * (kAttnThreads / 32) * 16 * 4;
+  // + (rows + 1) prefix counts and (rows + 1) partial offsets (int32)
+  static size_t smem(int rows) { return OFF_ROWS + static_cast<size_t>(rows + 1) * 2 * 4; }
+  static_assert(kChunk == 16 * (kAttnThreads / 32), "one 16-key slice of a chunk per warp");
+  static_assert(G <= 16, "the heads of a group fill at most the 16 rows of one MMA");
 };
 
-// The work of one split: kept entries e = split, split + P, ... of the list,
-// each cut into chunks of up to KCH keys.  A chunk is (entry, first key, keys).
-struct Chunk {
-  int e, j, c0, n;
-};
+// D = A B + C on the tensor cores, one warp, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
-// The first chunk at entry e or later (stepping by P) whose block index is a
-// valid block of the sequence; e == cnt when there is none.
-__device__ __forceinline__ Chunk first_chunk(const int32_t *list, int e, int cnt, int step, int last, int len,
-                                             int block) {
-  for (; e < cnt; e += step) {
-    const int j = list[e];
-    if (j >= 0 && j <= last) return Chunk{e, j, 0, min(min(block, len - j * block), 128)};
+// Four 8x8 bf16 matrices from shared memory, transposed (lane l names row l % 8 of matrix l / 8).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(row))));
+}
+
+// cp.async of 16 bytes that fills the destination with zeros (reads nothing).
+__device__ __forceinline__ void cp_async16_zero(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+
+// CTA-wide exclusive prefix sum over the threads (kAttnThreads) in thread order.
+__device__ __forceinline__ int block_exclusive_scan(int c, int *total, int *wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned wt;
+  const unsigned ex = warp_exclusive_scan(static_cast<unsigned>(c), &wt);
+  if (lane == 0) wsum[warp] = static_cast<int>(wt);
+  __syncthreads();
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kAttnThreads / 32; ++w) {
+    off += w < warp ? wsum[w] : 0;
+    tot += wsum[w];
   }
-  return Chunk{cnt, 0, 0, 0};
+  __syncthreads();
+  *total = tot;
+  return off + static_cast<int>(ex);
 }
 
-__device__ __forceinline__ Chunk next_chunk(const Chunk &c, const int32_t *list, int cnt, int step, int last,
-                                            int len, int block) {
-  const int nk = min(block, len - c.j * block);
-  if (c.c0 + 128 < nk) return Chunk{c.e, c.j, c.c0 + 128, min(128, nk - c.c0 - 128)};
-  return first_chunk(list, c.e + step, cnt, step, last, len, block);
+// The kept entries of the rows (b, g) laid end to end: row r holds entries
+// pre[r] .. pre[r+1]-1.  CTA c of C takes the W = ceil(N / C) entries c W ..,
+// so each row is covered by a run of consecutive CTAs; the partial of (row r,
+// CTA c) goes to slot off[r] + c - pre[r] / W.  Every CTA builds pre and off in
+// shared memory (rows <= kMaxDecodeRows); CTA 0 also stores W and off for the
+// combine.  Returns W (0 when no row keeps anything).
+__device__ int decode_plan(const int32_t *kv_cnt, const int32_t *cu, int seq, int total, int block, int hkv,
+                           int rows, int *pre, int *off, int *plan, int32_t *status, int *wsum) {
+  const int tid = threadIdx.x;
+  const int per = (rows + kAttnThreads - 1) / kAttnThreads;
+  const int r0 = min(rows, tid * per), r1 = min(rows, r0 + per);
+  int local = 0;
+  for (int r = r0; r < r1; ++r) {
+    const SeqSpan sp = seq_span(cu, r / hkv, seq, total, status);
+    const int c = sp.len > 0 ? min(kv_cnt[r], (sp.len - 1) / block + 1) : 0;
+    pre[r] = max(c, 0);  // the count for now; the prefix below
+    local += max(c, 0);
+  }
+  int n;
+  int run = block_exclusive_scan(local, &n, wsum);
+  for (int r = r0; r < r1; ++r) {
+    const int c = pre[r];
+    pre[r] = run;
+    run += c;
+  }
+  if (tid == 0) pre[rows] = n;
+  __syncthreads();
+  const int W = n > 0 ? (n + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
+  int parts = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int a = pre[r], b = pre[r + 1];
+    off[r] = b > a ? (b - 1) / W - a / W + 1 : 0;
+    parts += off[r];
+  }
+  int np;
+  run = block_exclusive_scan(parts, &np, wsum);
+  for (int r = r0; r < r1; ++r) {
+    const int c = off[r];
+    off[r] = run;
+    run += c;
+  }
+  if (tid == 0) off[rows] = np;
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int r = tid; r <= rows; r += kAttnThreads) plan[1 + r] = off[r];
+    if (tid == 0) plan[0] = W;
+  }
+  return W;
 }
 
-// Split `split` of row (b, g) (P splits per row): the G heads of the new token
-// over its kept entries, one chunk of up to 128 keys at a time.  A chunk's
-// keys and values are two cp.async groups into one key and one value buffer:
-// the logits wait only for the keys, and the next chunk's keys are requested
-// as soon as the logits are done, so they arrive while this chunk's P V runs
-// (its values requested after P V).  Thread t takes key t for the logits and,
-// for P V, the dimension pair t % (D/2) of key group t / (D/2).  Writes the
-// split's unnormalised O, running max and sum (log2 units); a split with no
-// valid entry writes an empty partial (max -inf, sum 0, O 0).
+// One chunk of keys: row r, first token (in the packed k / v) and key count.
+struct DChunk {
+  int r, tok, n;
+};
+
+// Walks the chunks of entries [x, x1) in order, skipping list entries that
+// name no block of the row's sequence.  Every thread walks the same sequence.
+struct DecWalk {
+  int x, x1, r, c0, nk, jtok;
+  int e0, rend, start, len, last;  // the row's first entry number, end, sequence and last block
+  const int32_t *list;             // the row's kept list
+  int pfx, pf;                     // entry pfx's block index, loaded ahead (pfx = -1: none)
+};
+
+__device__ __forceinline__ void walk_row(DecWalk &w, const int *pre, const int32_t *kv_idx, const int32_t *cu,
+                                         int seq, int total, int block, int hkv, int nbs, int32_t *status) {
+  while (w.x >= pre[w.r + 1]) ++w.r;  // rows with no entries are passed over
+  w.e0 = pre[w.r];
+  w.rend = pre[w.r + 1];
+  const SeqSpan sp = seq_span(cu, w.r / hkv, seq, total, status);
+  w.start = sp.start;
+  w.len = sp.len;
+  w.last = (sp.len - 1) / block;
+  w.list = kv_idx + static_cast<size_t>(w.r) * nbs;
+}
+
+// Moves w to the next valid entry at or after w.x (c0 = 0); w.x == w.x1 when none is left.
+// The block index of the entry after it is requested at once, so that its load is in flight
+// while this entry's chunks stream.
+__device__ __forceinline__ void walk_entry(DecWalk &w, const int *pre, const int32_t *kv_idx, const int32_t *cu,
+                                           int seq, int total, int block, int hkv, int nbs, int32_t *status) {
+  for (; w.x < w.x1; ++w.x) {
+    if (w.x >= w.rend) walk_row(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+    const int j = w.x == w.pfx ? w.pf : w.list[w.x - w.e0];
+    w.pfx = -1;
+    if (w.x + 1 < w.x1 && w.x + 1 < w.rend) {
+      w.pfx = w.x + 1;
+      w.pf = w.list[w.x + 1 - w.e0];
+    }
+    if (j >= 0 && j <= w.last) {
+      w.c0 = 0;
+      w.nk = min(block, w.len - j * block);
+      w.jtok = w.start + j * block;
+      return;
+    }
+  }
+}
+
+// The chunk at w, then w advanced past it; r = -1 when the walk is over.
+__device__ __forceinline__ DChunk walk_next(DecWalk &w, const int *pre, const int32_t *kv_idx, const int32_t *cu,
+                                            int seq, int total, int block, int hkv, int nbs, int32_t *status) {
+  if (w.x >= w.x1) return DChunk{-1, 0, 0};
+  const DChunk c{w.r, w.jtok + w.c0, min(kChunk, w.nk - w.c0)};
+  w.c0 += kChunk;
+  if (w.c0 >= w.nk) {
+    ++w.x;
+    walk_entry(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+  }
+  return c;
+}
+
+// Split-KV decode attention over the plan above.  CTA c walks its entries in
+// chunks of 64 keys through a three-stage cp.async ring (a chunk's keys and
+// values are one group; two chunks are in flight while one is computed).
+// Each warp owns 16 keys of a chunk and keeps its own online softmax: the G
+// heads of the row are the rows of a 16 x 8 x 16 bf16 tensor-core MMA, so
+// S = Q K^T is two n-tiles of 8 keys over D / 16 k-steps (Q held as A
+// fragments in registers), and O += P V is one k-step of the warp's 16 keys
+// over D / 8 n-tiles (P repacked from the S accumulators, V fragments by
+// transposing matrix loads).  When the walk enters a new row (b, g) the
+// warps' partials of the previous row are merged in shared memory and written
+// to its slot (unnormalised O, max and sum in log2 units).  A slot whose
+// entries name no valid block keeps max -inf, which the combine skips.
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
     const uint16_t *__restrict__ q_new, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const int32_t *__restrict__ kv_idx, const int32_t *__restrict__ kv_cnt, float *__restrict__ part_o,
-    float *__restrict__ part_ml, const int32_t *__restrict__ cu, int seq, int total, int block, int hkv,
-    int nbs, int nsplit, float scale_log2, int32_t *status) {
+    float *__restrict__ part_ml, int *__restrict__ plan, const int32_t *__restrict__ cu, int seq, int total,
+    int block, int hkv, int nbs, int rows, float scale_log2, int32_t *status) {
   using C = DecCfg<D, G>;
+  constexpr int NW = kAttnThreads / 32;
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char *ks = smem + C::OFF_K;
-  const uint16_t *vs = reinterpret_cast<const uint16_t *>(smem + C::OFF_V);
-  float (*qs)[D] = reinterpret_cast<float (*)[D]>(smem + C::OFF_Q);
-  float (*ps)[C::KCH] = reinterpret_cast<float (*)[C::KCH]>(smem + C::OFF_P);
-  __shared__ float red[G][kAttnThreads / 32];
-  __shared__ float mrun[G];
+  float (*oacc)[G][D] = reinterpret_cast<float (*)[G][D]>(smem + C::OFF_O);
+  float (*wm)[16] = reinterpret_cast<float (*)[16]>(smem + C::OFF_ML);  // [warp][head]: max
+  float (*wl)[16] = wm + NW;                                             // [warp][head]: sum
+  int *pre = reinterpret_cast<int *>(smem + C::OFF_ROWS);
+  int *off = pre + rows + 1;
+  __shared__ int wsum[NW];
 
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const size_t gb = static_cast<size_t>(b) * hkv + g;
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
   const int hq = hkv * G;
-  const SeqSpan sp = seq_span(cu, b, seq, total, status);
-  const int cnt = sp.len > 0 ? min(kv_cnt[gb], (sp.len - 1) / block + 1) : 0;
-  if (split >= cnt) return;  // the combine reads the partials of splits < min(P, cnt) only
-  const int last = (sp.len - 1) / block;
-  const int32_t *list = kv_idx + gb * nbs;
+  const int c = blockIdx.x;
+  const int W = decode_plan(kv_cnt, cu, seq, total, block, hkv, rows, pre, off, plan, status, wsum);
+  const int n_all = pre[rows];
+  const int x0 = c * W, x1 = min(n_all, x0 + W);
+  if (x0 >= x1) return;  // CTA-uniform
 
-  const size_t tok_stride = static_cast<size_t>(hkv) * D;
-  const uint16_t *kbase = k + static_cast<size_t>(sp.start) * tok_stride + static_cast<size_t>(g) * D;
-  const uint16_t *vbase = v + static_cast<size_t>(sp.start) * tok_stride + static_cast<size_t>(g) * D;
-  constexpr int PR = D * 2 / 16;  // 16-byte pieces per row
-  auto stage_k = [&](const Chunk &c) {
-    const uint16_t *kg = kbase + (static_cast<size_t>(c.j) * block + c.c0) * tok_stride;
-    for (int x = tid; x < c.n * PR; x += kAttnThreads) {
-      const int r = x / PR, pc = x - r * PR;
-      cp_async16(ks + r * C::KROW + pc * 16, kg + static_cast<size_t>(r) * tok_stride + pc * 8);
-    }
-    cp_async_commit();
-  };
-  auto stage_v = [&](const Chunk &c) {
-    const uint16_t *vg = vbase + (static_cast<size_t>(c.j) * block + c.c0) * tok_stride;
-    for (int x = tid; x < c.n * PR; x += kAttnThreads) {
-      const int r = x / PR, pc = x - r * PR;
-      cp_async16(smem + C::OFF_V + (static_cast<size_t>(r) * D + pc * 8) * 2,
-                 vg + static_cast<size_t>(r) * tok_stride + pc * 8);
-    }
-    cp_async_commit();
-  };
-
-  Chunk cur = first_chunk(list, split, cnt, nsplit, last, sp.len, block);
-  if (cur.e < cnt) {
-    stage_k(cur);
-    stage_v(cur);
+  // the row holding entry x0: the last r with pre[r] <= x0
+  int lo = 0, hi = rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x0) lo = mid;
+    else hi = mid - 1;
   }
-  const uint16_t *qrow = q_new + (static_cast<size_t>(b) * hq + static_cast<size_t>(g) * G) * D;
-  for (int e = tid; e < G * D; e += kAttnThreads) qs[e / D][e % D] = bf16f(qrow[e]) * scale_log2;
-  if (tid < G) mrun[tid] = -INFINITY;
+  auto slot_of = [&](int r) { return off[r] + c - pre[r] / W; };
+  // every slot of this CTA starts empty (a flush below overwrites it)
+  for (int r = lo + tid; r < rows && pre[r] < x1; r += kAttnThreads)
+    if (pre[r + 1] > pre[r])
+      for (int h = 0; h < G; ++h)
+        *reinterpret_cast<float2 *>(part_ml + (static_cast<size_t>(slot_of(r)) * G + h) * 2) =
+            make_float2(-INFINITY, 0.f);
 
-  const int dp = tid % C::DP, kh = tid / C::DP;
-  float o[G][2];
-  float lsum[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    o[h][0] = o[h][1] = 0.f;
-    lsum[h] = 0.f;
-  }
-  while (cur.e < cnt) {  // CTA-uniform: every thread walks the same list
-    const Chunk nxt = next_chunk(cur, list, cnt, nsplit, last, sp.len, block);
-    const bool more = nxt.e < cnt;
-    cp_async_wait<1>();  // this chunk's keys (its values may still be in flight)
-    __syncthreads();
-    const bool valid = tid < cur.n;
-    // ---- logits of key cur.c0 + tid for the G heads (log2 units)
-    float lg[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) lg[h] = valid ? 0.f : -INFINITY;
-    if (valid) {
-      const uint4 *kr = reinterpret_cast<const uint4 *>(ks + tid * C::KROW);
-#pragma unroll 4
-      for (int x8 = 0; x8 < D / 8; ++x8) {
-        const uint4 u = kr[x8];
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-        float kf[8];
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          kf[2 * q2] = __uint_as_float(wv[q2] << 16);
-          kf[2 * q2 + 1] = __uint_as_float(wv[q2] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 qa = *reinterpret_cast<const float4 *>(&qs[h][x8 * 8]);
-          const float4 qb = *reinterpret_cast<const float4 *>(&qs[h][x8 * 8 + 4]);
-          float a = lg[h];
-          a = fmaf(qa.x, kf[0], a);
-          a = fmaf(qa.y, kf[1], a);
-          a = fmaf(qa.z, kf[2], a);
-          a = fmaf(qa.w, kf[3], a);
-          a = fmaf(qb.x, kf[4], a);
-          a = fmaf(qb.y, kf[5], a);
-          a = fmaf(qb.z, kf[6], a);
-          a = fmaf(qb.w, kf[7], a);
-          lg[h] = a;
+  DecWalk w;
+  w.x = x0;
+  w.x1 = x1;
+  w.r = lo;
+  w.pfx = -1;
+  walk_row(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+  walk_entry(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+
+  constexpr int PR = D * 2 / 16;  // 16-byte pieces per key or value row
+  auto issue = [&](const DChunk &ch, int stage) {
+    if (ch.r >= 0) {
+      const size_t gofs = static_cast<size_t>(ch.r % hkv) * D;
+      unsigned char *kst = smem + C::OFF_K + stage * C::STAGE;
+      unsigned char *vst = smem + C::OFF_V + stage * C::STAGE;
+      for (int x = tid; x < kChunk * PR; x += kAttnThreads) {
+        const int r = x / PR, pc = x - r * PR;
+        if (r < ch.n) {
+          const size_t src = (static_cast<size_t>(ch.tok) + r) * hkv * D + gofs + pc * 8;
+          cp_async16(kst + r * C::ROW + pc * 16, k + src);
+          cp_async16(vst + r * C::ROW + pc * 16, v + src);
+        } else {
+          // past the chunk's keys: zero values, so that P = 0 meets finite numbers in P V
+          cp_async16_zero(vst + r * C::ROW + pc * 16, v);
         }
       }
     }
-    // ---- chunk max per head, new running max, probabilities
+    cp_async_commit();  // one group per chunk, empty past the end of the walk
+  };
+
+  uint32_t qa[C::NKS][4];  // Q as A fragments: rows gq and gq + 8 are heads of the group
+  float o[C::NNT][4];      // O accumulators: heads gq (0, 1) and gq + 8 (2, 3), dims 8 nt + 2 tq
+  float m_lo = -INFINITY, m_hi = -INFINITY;  // running max (log2 units) over this warp's keys
+  float l_lo = 0.f, l_hi = 0.f;              // this thread's share of the sums
+  int arow = -1;
+
+  auto start_row = [&](int r) {
+    const uint16_t *qb = q_new + (static_cast<size_t>(r / hkv) * hq + static_cast<size_t>(r % hkv) * G) * D;
+    auto ld = [&](int h, int col) -> uint32_t {
+      return h < G ? *reinterpret_cast<const uint32_t *>(qb + static_cast<size_t>(h) * D + col) : 0u;
+    };
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float mx = lg[h];
+    for (int ks = 0; ks < C::NKS; ++ks) {
+      const int col = 16 * ks + 2 * tq;
+      qa[ks][0] = ld(gq, col);
+      qa[ks][1] = ld(gq + 8, col);
+      qa[ks][2] = ld(gq, col + 8);
+      qa[ks][3] = ld(gq + 8, col + 8);
+    }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if (lane == 0) red[h][warp] = mx;
+    for (int nt = 0; nt < C::NNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    m_lo = m_hi = -INFINITY;
+    l_lo = l_hi = 0.f;
+  };
+
+  auto flush = [&](int r) {
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    if (tq == 0) {
+      wm[warp][gq] = m_lo;
+      wm[warp][gq + 8] = m_hi;
+      wl[warp][gq] = l_lo;
+      wl[warp][gq + 8] = l_hi;
     }
     __syncthreads();
-    float factor[G];
+    float mlo = -INFINITY, mhi = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float mx = red[h][0];
-#pragma unroll
-      for (int x = 1; x < kAttnThreads / 32; ++x) mx = fmaxf(mx, red[h][x]);
-      const float mold = mrun[h];
-      const float mnew = fmaxf(mold, mx);
-      factor[h] = mold == -INFINITY ? 0.f : exp2f(mold - mnew);
-      ps[h][tid] = valid ? exp2f(lg[h] - mnew) : 0.f;
-      lg[h] = mnew;  // keep the new max
+    for (int x = 0; x < NW; ++x) {
+      mlo = fmaxf(mlo, wm[x][gq]);
+      mhi = fmaxf(mhi, wm[x][gq + 8]);
     }
-    __syncthreads();  // ps written; every thread is done with the key buffer
-    if (tid == 0) {
+    const float slo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - mlo);
+    const float shi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - mhi);
 #pragma unroll
-      for (int h = 0; h < G; ++h) mrun[h] = lg[h];
-    }
-    if (more) {
-      stage_k(nxt);
-      cp_async_wait<1>();  // this chunk's values (the next keys may still be in flight)
-    } else {
-      cp_async_wait<0>();
+    for (int nt = 0; nt < C::NNT; ++nt) {
+      if (gq < G)
+        *reinterpret_cast<float2 *>(&oacc[warp][gq][8 * nt + 2 * tq]) = make_float2(o[nt][0] * slo, o[nt][1] * slo);
+      if (gq + 8 < G)
+        *reinterpret_cast<float2 *>(&oacc[warp][gq + 8][8 * nt + 2 * tq]) =
+            make_float2(o[nt][2] * shi, o[nt][3] * shi);
     }
     __syncthreads();
-    // ---- P V for this thread's dimension pair and key group
+    const size_t sl = static_cast<size_t>(slot_of(r));
+    for (int e = tid; e < G * D / 2; e += kAttnThreads) {
+      const int h = e / (D / 2), d2 = 2 * (e % (D / 2));
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      o[h][0] *= factor[h];
-      o[h][1] *= factor[h];
-      lsum[h] *= factor[h];
+      for (int x = 0; x < NW; ++x) {
+        a0 += oacc[x][h][d2];
+        a1 += oacc[x][h][d2 + 1];
+      }
+      *reinterpret_cast<float2 *>(part_o + (sl * G + h) * D + d2) = make_float2(a0, a1);
     }
-    const uint32_t *vcol = reinterpret_cast<const uint32_t *>(vs) + dp;
-#pragma unroll 4
-    for (int s = kh; s < cur.n; s += C::KH) {
-      const uint32_t vv = vcol[s * (D / 2)];
-      const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
+    if (tid < G) {
+      float m = -INFINITY, l = 0.f;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = ps[h][s];
-        o[h][0] = fmaf(p, v0, o[h][0]);
-        o[h][1] = fmaf(p, v1, o[h][1]);
-        lsum[h] += p;
+      for (int x = 0; x < NW; ++x) m = fmaxf(m, wm[x][tid]);
+#pragma unroll
+      for (int x = 0; x < NW; ++x)
+        if (wm[x][tid] != -INFINITY) l = fmaf(exp2f(wm[x][tid] - m), wl[x][tid], l);
+      *reinterpret_cast<float2 *>(part_ml + (sl * G + tid) * 2) = make_float2(m, l);
+    }
+    __syncthreads();
+  };
+
+  // this lane's row addresses for the transposing value loads: matrix lane / 8 of a pair of
+  // n-tiles is keys (lane / 8) % 2 * 8 .. + 7 of the warp's 16, dims (lane / 16) * 8 .. + 7
+  const int vkey = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int vcol = (lane >> 4) * 8;
+
+  // chunks u .. u + kStages - 2 are in flight at the top of step u; ring[] holds their rows
+  DChunk ring[kStages - 1];
+#pragma unroll
+  for (int x = 0; x < kStages - 1; ++x) {
+    ring[x] = walk_next(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+    issue(ring[x], x);
+  }
+  for (int u = 0; ring[0].r >= 0; ++u) {  // CTA-uniform: every thread walks the same chunks
+    const DChunk cur = ring[0];
+#pragma unroll
+    for (int x = 0; x < kStages - 2; ++x) ring[x] = ring[x + 1];
+    ring[kStages - 2] = walk_next(w, pre, kv_idx, cu, seq, total, block, hkv, nbs, status);
+    issue(ring[kStages - 2], (u + kStages - 1) % kStages);  // the stage of chunk u-1, free since its step
+    cp_async_wait<kStages - 1>();  // chunk u has landed (the later ones may be in flight)
+    __syncthreads();
+    if (cur.r != arow) {
+      if (arow >= 0) flush(arow);
+      start_row(cur.r);
+      arow = cur.r;
+    }
+    const int stage = u % kStages;
+    const unsigned char *kst = smem + C::OFF_K + stage * C::STAGE;
+    const unsigned char *vst = smem + C::OFF_V + stage * C::STAGE;
+
+    // ---- S = Q K^T for this warp's 16 keys (two n-tiles of 8)
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    const unsigned char *krow = kst + (warp * 16 + gq) * C::ROW + 4 * tq;
+#pragma unroll
+    for (int ks = 0; ks < C::NKS; ++ks) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const unsigned char *kp = krow + nt * 8 * C::ROW + 32 * ks;
+        mma_bf16_16816(s[nt], qa[ks], *reinterpret_cast<const uint32_t *>(kp),
+                       *reinterpret_cast<const uint32_t *>(kp + 16));
       }
     }
-    __syncthreads();  // the value buffer and ps are free
-    if (more) stage_v(nxt);
-    cur = nxt;
-  }
-  __syncthreads();  // no copy is in flight; the key buffer becomes the key groups' O partials
-  float (*oacc)[G][D] = reinterpret_cast<float (*)[G][D]>(ks);
-  if (kh > 0) {
+
+    // ---- online softmax per head over the warp's keys (log2 units)
+    float x[2][4];
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      oacc[kh - 1][h][2 * dp] = o[h][0];
-      oacc[kh - 1][h][2 * dp + 1] = o[h][1];
-    }
-  }
-  __syncthreads();
-  if (kh == 0) {
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float a0 = o[h][0], a1 = o[h][1];
-#pragma unroll
-      for (int x = 0; x < C::KH - 1; ++x) {
-        a0 += oacc[x][h][2 * dp];
-        a1 += oacc[x][h][2 * dp + 1];
+      for (int e = 0; e < 4; ++e) {
+        const int key = warp * 16 + nt * 8 + 2 * tq + (e & 1);
+        x[nt][e] = key < cur.n ? s[nt][e] * scale_log2 : -INFINITY;
+        if (e < 2) mx_lo = fmaxf(mx_lo, x[nt][e]);
+        else mx_hi = fmaxf(mx_hi, x[nt][e]);
       }
-      const size_t po = ((static_cast<size_t>(b) * hq + static_cast<size_t>(g) * G + h) * nsplit + split) * D;
-      *reinterpret_cast<float2 *>(part_o + po + 2 * dp) = make_float2(a0, a1);
+#pragma unroll
+    for (int offs = 1; offs <= 2; offs <<= 1) {
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, offs));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, offs));
     }
-  }
-  // the normaliser: each key group summed its own keys' probabilities; add the groups of
-  // dimension pair 0 in the same fixed order
-  __syncthreads();
-  if (dp == 0 && kh > 0) {
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float f_lo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - mn_lo);
+    const float f_hi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - mn_hi);
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    float p[2][4];
+    float ps_lo = 0.f, ps_hi = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) oacc[kh - 1][h][0] = lsum[h];
-  }
-  __syncthreads();
-  if (tid == 0) {
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float l = lsum[h];
+      for (int e = 0; e < 4; ++e) {
+        const float mref = e < 2 ? mn_lo : mn_hi;
+        p[nt][e] = x[nt][e] == -INFINITY ? 0.f : exp2f(x[nt][e] - mref);
+        if (e < 2) ps_lo += p[nt][e];
+        else ps_hi += p[nt][e];
+      }
+    l_lo = fmaf(l_lo, f_lo, ps_lo);
+    l_hi = fmaf(l_hi, f_hi, ps_hi);
+    if (f_lo != 1.f || f_hi != 1.f) {
 #pragma unroll
-      for (int x = 0; x < C::KH - 1; ++x) l += oacc[x][h][0];
-      const size_t pm = ((static_cast<size_t>(b) * hq + static_cast<size_t>(g) * G + h) * nsplit + split) * 2;
-      *reinterpret_cast<float2 *>(part_ml + pm) = make_float2(mrun[h], l);
+      for (int nt = 0; nt < C::NNT; ++nt) {
+        o[nt][0] *= f_lo;
+        o[nt][1] *= f_lo;
+        o[nt][2] *= f_hi;
+        o[nt][3] *= f_hi;
+      }
     }
+
+    // ---- O += P V over the warp's 16 keys
+    const uint32_t pa[4] = {ptx::pack_bf16x2(p[0][0], p[0][1]), ptx::pack_bf16x2(p[0][2], p[0][3]),
+                            ptx::pack_bf16x2(p[1][0], p[1][1]), ptx::pack_bf16x2(p[1][2], p[1][3])};
+    const unsigned char *vrow = vst + vkey * C::ROW + vcol * 2;
+#pragma unroll
+    for (int np = 0; np < C::NNT / 2; ++np) {
+      uint32_t vb[4];
+      ldmatrix_x4_trans(vb, vrow + np * 32);
+      mma_bf16_16816(o[2 * np], pa, vb[0], vb[1]);
+      mma_bf16_16816(o[2 * np + 1], pa, vb[2], vb[3]);
+    }
+    __syncthreads();  // every warp is done with the stage before it is refilled
   }
+  cp_async_wait<0>();  // only empty groups can remain
+  if (arow >= 0) flush(arow);
 }
 
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
 
-// One CTA per (b, h): O = sum_s w_s O_s / sum_s w_s l_s over the ns = min(P, cnt)
-// splits, w_s = 2^(m_s - max m).  Warp w takes the splits s = w, w + 8, ...
-// (every warp first finds max m itself), each lane D/32 dimensions; the warps'
-// sums meet in shared memory in a fixed order.
+// One CTA per (b, h): O = sum_s w_s O_s / sum_s w_s l_s over the slots of the
+// head's row, w_s = 2^(m_s - max m) (slots with max -inf are empty).  Warp w
+// takes the slots w, w + 8, ... (every warp first finds max m itself), each
+// lane D/32 dimensions; the warps' sums meet in shared memory in a fixed order.
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
-    const float *__restrict__ part_o, const float *__restrict__ part_ml, const int32_t *__restrict__ kv_cnt,
-    uint16_t *__restrict__ o, float *__restrict__ lse, const int32_t *__restrict__ cu, int seq, int total,
-    int block, int hq, int hkv, int nsplit, int32_t *status) {
+    const float *__restrict__ part_o, const float *__restrict__ part_ml, const int *__restrict__ plan,
+    uint16_t *__restrict__ o, float *__restrict__ lse, int hq, int hkv) {
   constexpr int VL = D / 32;  // dimensions per lane
   __shared__ __align__(16) float red_o[kCombineWarps][D];
   __shared__ float red_l[kCombineWarps];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = h / (hq / hkv);
-  const SeqSpan sp = seq_span(cu, b, seq, total, status);
-  const int cnt = sp.len > 0 ? min(kv_cnt[static_cast<size_t>(b) * hkv + g], (sp.len - 1) / block + 1) : 0;
-  const int ns = max(0, min(nsplit, cnt));
-  const size_t base = (static_cast<size_t>(b) * hq + h) * nsplit;
+  const int grp = hq / hkv;
+  const int r = b * hkv + h / grp, hl = h % grp;
+  const int s0 = plan[1 + r], ns = plan[2 + r] - s0;
   float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, part_ml[(base + s) * 2]);
+  for (int s = lane; s < ns; s += 32) m = fmaxf(m, part_ml[(static_cast<size_t>(s0 + s) * grp + hl) * 2]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  for (int offs = 16; offs > 0; offs >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, offs));
   float acc[VL];
 #pragma unroll
   for (int x = 0; x < VL; ++x) acc[x] = 0.f;
   float l = 0.f;
-  for (int s0 = warp; s0 < ns; s0 += 4 * kCombineWarps) {
+  for (int sb = warp; sb < ns; sb += 4 * kCombineWarps) {
     float2 ml[4];
     float pv[4][VL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int s = s0 + u * kCombineWarps;
-      ml[u] = make_float2(-INFINITY, 0.f);
+    for (int uu = 0; uu < 4; ++uu) {
+      const int s = sb + uu * kCombineWarps;
+      ml[uu] = make_float2(-INFINITY, 0.f);
 #pragma unroll
-      for (int x = 0; x < VL; ++x) pv[u][x] = 0.f;
+      for (int x = 0; x < VL; ++x) pv[uu][x] = 0.f;
       if (s < ns) {
-        ml[u] = *reinterpret_cast<const float2 *>(part_ml + (base + s) * 2);
-        const float *src = part_o + (base + s) * D + lane * VL;
+        const size_t at = static_cast<size_t>(s0 + s) * grp + hl;
+        ml[uu] = *reinterpret_cast<const float2 *>(part_ml + at * 2);
+        const float *src = part_o + at * D + lane * VL;
         if constexpr (VL == 4) {
           const float4 t = *reinterpret_cast<const float4 *>(src);
-          pv[u][0] = t.x; pv[u][1] = t.y; pv[u][2] = t.z; pv[u][3] = t.w;
+          pv[uu][0] = t.x; pv[uu][1] = t.y; pv[uu][2] = t.z; pv[uu][3] = t.w;
         } else {
           const float2 t = *reinterpret_cast<const float2 *>(src);
-          pv[u][0] = t.x; pv[u][1] = t.y;
+          pv[uu][0] = t.x; pv[uu][1] = t.y;
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (ml[u].x == -INFINITY) continue;  // an empty split (or past ns)
-      const float w = exp2f(ml[u].x - m);
-      l = fmaf(ml[u].y, w, l);
+    for (int uu = 0; uu < 4; ++uu) {
+      if (ml[uu].x == -INFINITY) continue;  // an empty slot (or past ns)
+      const float wgt = exp2f(ml[uu].x - m);
+      l = fmaf(ml[uu].y, wgt, l);
 #pragma unroll
-      for (int x = 0; x < VL; ++x) acc[x] = fmaf(pv[u][x], w, acc[x]);
+      for (int x = 0; x < VL; ++x) acc[x] = fmaf(pv[uu][x], wgt, acc[x]);
     }
   }
 #pragma unroll
@@ -708,12 +895,12 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   if (tid < D) {
     float a = 0.f, ls = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-      a += red_o[w][tid];
-      ls += red_l[w];
+    for (int wi = 0; wi < kCombineWarps; ++wi) {
+      a += red_o[wi][tid];
+      ls += red_l[wi];
     }
-    const float r = ls > 0.f ? a / ls : 0.f;
-    const __nv_bfloat16 rb = __float2bfloat16_rn(r);
+    const float rr = ls > 0.f ? a / ls : 0.f;
+    const __nv_bfloat16 rb = __float2bfloat16_rn(rr);
     o[(static_cast<size_t>(b) * hq + h) * D + tid] = *reinterpret_cast<const uint16_t *>(&rb);
     if (lse != nullptr && tid == 0)
       lse[static_cast<size_t>(b) * hq + h] = ls > 0.f ? (m + log2f(ls)) * 0.69314718055994531f : -INFINITY;
@@ -722,57 +909,58 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
 
 template <int D, int G>
 cudaError_t launch_attn_g(const MaskShape &s, const void *q_new, const void *k, const void *v,
-                          const int32_t *kv_idx, const int32_t *kv_cnt, float *po, float *pml, int nsplit,
+                          const int32_t *kv_idx, const int32_t *kv_cnt, float *po, float *pml, int *plan,
                           float scale_log2, int32_t *status, cudaStream_t stream) {
   using C = DecCfg<D, G>;
   auto kern = decode_attn_kernel<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  const int rows = s.batch * s.hkv;
+  const size_t smem = C::smem(rows);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(nsplit, s.hkv, s.batch);
-  kern<<<grid, kAttnThreads, C::SMEM, stream>>>(
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAttnThreads, smem)) != cudaSuccess)
+    return e;
+  const int ctas = std::max(1, std::min(kMaxDecodeCtas, sms * std::max(per_sm, 1)));
+  kern<<<ctas, kAttnThreads, smem, stream>>>(
       static_cast<const uint16_t *>(q_new), static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
-      kv_idx, kv_cnt, po, pml, s.cu, s.seq, s.total, s.block, s.hkv, s.nbs, nsplit, scale_log2, status);
+      kv_idx, kv_cnt, po, pml, plan, s.cu, s.seq, s.total, s.block, s.hkv, s.nbs, rows, scale_log2, status);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_attn_d(const MaskShape &s, const void *q_new, const void *k, const void *v,
-                          const int32_t *kv_idx, const int32_t *kv_cnt, float *po, float *pml, int nsplit,
+                          const int32_t *kv_idx, const int32_t *kv_cnt, float *po, float *pml, int *plan,
                           float scale_log2, int32_t *status, cudaStream_t st) {
   switch (s.group) {
-    case 1: return launch_attn_g<D, 1>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, scale_log2, status, st);
-    case 2: return launch_attn_g<D, 2>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, scale_log2, status, st);
-    case 4: return launch_attn_g<D, 4>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, scale_log2, status, st);
-    case 8: return launch_attn_g<D, 8>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, scale_log2, status, st);
-    case 16: return launch_attn_g<D, 16>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, scale_log2, status, st);
+    case 1: return launch_attn_g<D, 1>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, scale_log2, status, st);
+    case 2: return launch_attn_g<D, 2>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, scale_log2, status, st);
+    case 4: return launch_attn_g<D, 4>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, scale_log2, status, st);
+    case 8: return launch_attn_g<D, 8>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, scale_log2, status, st);
+    case 16: return launch_attn_g<D, 16>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, scale_log2, status, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// Splits per (b, g) row: enough CTAs for about kDecodeCtas in all (152 SMs x 3
-// resident CTAs), at most one per block of the row.
-constexpr int kDecodeCtas = 456;
-
-int decode_splits(const MaskShape &s) {
-  const long long rows = static_cast<long long>(s.hkv) * s.batch;
-  const long long p = (kDecodeCtas + rows - 1) / rows;
-  return static_cast<int>(p < s.nbs ? p : s.nbs);
-}
-
-// Workspace regions (each 256-byte aligned): partial O [b, hq, nsplit, d], partial (max, sum)
-// [b, hq, nsplit, 2], then the selection's S_c and R rows [b, hkv, nbs].
+// Workspace regions (each 256-byte aligned): partial O [slots, G, d] and partial (max, sum)
+// [slots, G, 2] with slots = kMaxDecodeCtas + b * hkv (each row's run of CTAs adds at most one
+// slot to the CTA count), the plan [b * hkv + 2] int32, then the selection's S_c and R rows
+// [b, hkv, nbs].
 struct DecRegions {
-  size_t po, pml, sc, sr, total;
+  size_t po, pml, plan, sc, sr, total;
 };
 
 DecRegions decode_regions(const MaskShape &s) {
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t rows = static_cast<size_t>(s.batch) * s.hq * decode_splits(s);
-  const size_t srow = static_cast<size_t>(s.batch) * s.hkv * s.nbs * 4;
+  const size_t rows = static_cast<size_t>(s.batch) * s.hkv;
+  const size_t slots = (kMaxDecodeCtas + rows) * static_cast<size_t>(s.group);
+  const size_t srow = rows * s.nbs * 4;
   DecRegions r;
   r.po = 0;
-  r.pml = r.po + r256(rows * s.d * 4);
-  r.sc = r.pml + r256(rows * 2 * 4);
+  r.pml = r.po + r256(slots * s.d * 4);
+  r.plan = r.pml + r256(slots * 2 * 4);
+  r.sc = r.plan + r256((rows + 2) * 4);
   r.sr = r.sc + r256(srow);
   r.total = r.sr + r256(srow);
   return r;
@@ -821,25 +1009,24 @@ cudaError_t launch_decode_select(const MaskShape &s, const void *q_new, const fl
 cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, const void *v,
                           const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,
                           void *workspace, int32_t *status, cudaStream_t stream) {
-  const int nsplit = decode_splits(s);
+  if (static_cast<long long>(s.batch) * s.hkv > kMaxDecodeRows) return cudaErrorInvalidValue;
   const DecRegions r = decode_regions(s);
   float *po = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.po);
   float *pml = reinterpret_cast<float *>(static_cast<char *>(workspace) + r.pml);
+  int *plan = reinterpret_cast<int *>(static_cast<char *>(workspace) + r.plan);
   const float sl2 = scale * kLog2e;
   cudaError_t e;
-  if (s.d == 64) e = launch_attn_d<64>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, sl2, status, stream);
-  else if (s.d == 128) e = launch_attn_d<128>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, nsplit, sl2, status, stream);
+  if (s.d == 64) e = launch_attn_d<64>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, sl2, status, stream);
+  else if (s.d == 128) e = launch_attn_d<128>(s, q_new, k, v, kv_idx, kv_cnt, po, pml, plan, sl2, status, stream);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   dim3 grid(s.hq, s.batch);
   if (s.d == 64)
-    decode_combine_kernel<64><<<grid, kCombineThreads, 0, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o),
-                                                                   lse, s.cu, s.seq, s.total, s.block, s.hq, s.hkv,
-                                                                   nsplit, status);
+    decode_combine_kernel<64><<<grid, kCombineThreads, 0, stream>>>(po, pml, plan, static_cast<uint16_t *>(o), lse,
+                                                                   s.hq, s.hkv);
   else
-    decode_combine_kernel<128><<<grid, kCombineThreads, 0, stream>>>(po, pml, kv_cnt, static_cast<uint16_t *>(o),
-                                                                    lse, s.cu, s.seq, s.total, s.block, s.hq, s.hkv,
-                                                                    nsplit, status);
+    decode_combine_kernel<128><<<grid, kCombineThreads, 0, stream>>>(po, pml, plan, static_cast<uint16_t *>(o),
+                                                                    lse, s.hq, s.hkv);
   return cudaGetLastError();
 }
 

@@ -10,6 +10,7 @@
 namespace bsa {
 
 constexpr int kMaxBlocks = 4096;  // nb limit (select kernel keeps one score row in smem)
+constexpr int kMaxDecodeRows = 4096;  // batch * hkv limit of decode (its plan sits in smem)
 
 // A batch is either fixed-length (cu == nullptr: sequence b is tokens
 // b*seq .. b*seq+seq-1) or packed ragged (sequence b is tokens cu[b] ..

@@ -355,7 +355,9 @@ bsa_status bsa_varlen_prefill_dense_fwd(const bsa_varlen_shape *shape, const int
  * decode in "Your Context Length Decides What a Kernel Is Worth").  o: bf16
  * [batch, hq, head_dim]; lse (nullable) fp32 [batch, hq]; workspace of
  * bsa_decode_workspace_bytes(shape) bytes, 16-byte aligned, for the fp32
- * partial results.  An empty sequence gets o = 0 and lse = -inf.
+ * partial results.  An empty sequence gets o = 0 and lse = -inf.  The kept
+ * entries of all rows (b, g) are spread evenly over the GPU's CTAs; batch *
+ * hkv above 4096 returns BSA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------ */
 size_t bsa_decode_workspace_bytes(const bsa_varlen_shape *shape);
 bsa_status bsa_decode_select(const bsa_varlen_shape *shape, const bsa_select_params *params,

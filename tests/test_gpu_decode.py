@@ -261,3 +261,38 @@ def test_decode_select_long_rows_synthetic_meta(nb):
     assert excused <= max(4, compared // 1000), (compared, excused)
     for g in range(hkv):  # pure ties: bit-exact, lowest indices first
         np.testing.assert_array_equal(got["kv_idx"][1, g, :got["kv_cnt"][1, g]], orc[(1, g)]["kept"])
+
+
+def test_decode_many_rows_and_malformed_entries():
+    """64 sequences (some empty, some one block, some long) so the even cut of all
+    rows' entries over the CTAs falls both inside rows and between them; then the same
+    lists with malformed entries appended (a block past the sequence, a negative index):
+    the attention skips them and still equals the oracle over the valid entries."""
+    rng = np.random.default_rng(77)
+    lengths = tuple(int(x) for x in rng.choice([0, 1, 63, 64, 65, 700, 3000, 9000, 20000], size=64))
+    vw = synth.VarlenWorkload("dec_many", lengths, 16, 2, 128, 64, 0.15, 0.05, seed_base=909,
+                              needles_fixed=1)
+    lay = synth.make_varlen_layer(vw)
+    q_new = last_queries(vw, lay)
+    got = gpu_decode(vw, lay, q_new)
+    orc = oracle_decode(vw, lay, q_new)
+    compared, excused = compare_lists(vw, got, orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)
+    lists = upload(vw, orc, got["nbs"])
+    got2 = gpu_decode(vw, lay, q_new, lists=lists)
+    kept = {bg: d["kept"] for bg, d in orc.items()}
+    check_outputs(vw, lay, q_new, got2, kept)
+    for b, n in enumerate(vw.lengths):
+        if n == 0:
+            assert np.all(got2["o"][b] == 0) and np.all(np.isneginf(got2["lse"][b]))
+    # malformed entries after the valid ones: skipped by the attention
+    idx, cnt = (x.cpu().numpy().copy() for x in lists)
+    for (b, g), d in orc.items():
+        c = d["kept"].size
+        nb = -(-vw.lengths[b] // vw.block)
+        extra = [nb + 3, -1]
+        room = min(len(extra), got["nbs"] - c)
+        idx[b, g, c:c + room] = extra[:room]
+        cnt[b, g] = c + room
+    got3 = gpu_decode(vw, lay, q_new, lists=(torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda()))
+    check_outputs(vw, lay, q_new, got3, kept)
