@@ -188,17 +188,19 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: heavy rows first (i descending), head tiles of one row adjacent
+  // ---- work item: one (KV head, sequence) after another, so the CTAs running at any time
+  // share one head's K and V (64 MB at 128K tokens, inside L2) and re-read it from L2, not
+  // HBM; within it heavy rows first (i descending), the head tiles of one row adjacent
   const int nhp = p.group / C::QH / NT;
   int item = blockIdx.x;
   const int hp = item % nhp;
   item /= nhp;
-  const int g = item % p.hkv;
-  item /= p.hkv;
-  const int b = item % p.batch;
-  item /= p.batch;
   const int qs = item % C::NQS;
-  const int i = p.nb - 1 - item / C::NQS;
+  item /= C::NQS;
+  const int i = p.nb - 1 - item % p.nb;
+  item /= p.nb;
+  const int b = item % p.batch;
+  const int g = item / p.batch;
   const int qtok0 = i * BLK + qs * 128;  // first query token of the CTA's tiles (in its sequence)
   const SeqSpan sp = seq_span(p.cu, b, p.seq, p.total, p.dev_status);
   if (qtok0 >= sp.len) return;           // past the end of a shorter sequence: no rows
@@ -394,8 +396,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     bool ok = true;
 
     for (int n = 0; n < T; ++n) {
-      if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
-      ptx::tc_fence_after();
+      // the tile's key block is read before the wait for S, so the read overlaps the wait
       int ktok0;        // key of this thread's column 0
       bool half = true;  // pairs: this thread's half of the tile holds a kept block
       if constexpr (C::PAIR) {
@@ -404,6 +405,8 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
       } else {
         ktok0 = key_block(n) * BLK + (n % C::SUB) * C::KT + hf * C::CW;
       }
+      if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
+      ptx::tc_fence_after();
       uint32_t sr[C::CW];
 #pragma unroll
       for (int c = 0; c < C::CW / 32; ++c)

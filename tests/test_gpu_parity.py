@@ -227,6 +227,23 @@ def test_long_prefill_128k_sampled():
     check_attention_rows(w, lay, o, lse, oracle_keep(w, orc) != 0, att_rows)
 
 
+@pytest.mark.parametrize("layer", [1, 47])
+def test_long_prefill_128k_full_masks(layer):
+    """Two more of the 48 seeded 128K layers (the second and the last): every mask row of
+    every KV head against the oracle, the block summaries and quantiles, and sampled
+    attention rows through the GPU's own lists where its mask row equals the oracle's."""
+    w = synth.workload("gqa32x4_n131072_d128_b128")
+    lay = synth.make_layer(w, layer=layer)
+    got, orc, _ = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    o, lse = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                           torch.from_numpy(got["kv_cnt"]).cuda())
+    rows = [(b, h, i) for (b, h, i) in sample_rows(w, 1, seed=layer)
+            if np.array_equal(got["mask"][b, h // w.group, i], keep[b, h // w.group, i])]
+    assert len(rows) >= w.hq
+    check_attention_rows(w, lay, o, lse, keep != 0, rows[::4])
+
+
 # ------------------------------------------------------------------ per-token aggregation
 
 def token_parity(w, lay, rc=None, rr=None):
