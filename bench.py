@@ -423,24 +423,26 @@ class Fp8Runner(FixedRunner):
         out = dict(lay)
         out.update({x: f8[x] for x in ("q", "k", "v")})
         out.update({x + "16": lay[x] for x in ("q", "k", "v")})   # bf16 originals for the CPU oracle
-        self.scales = {x: f8[x + "_scale"] for x in ("q", "k", "v")}
+        out["scales"] = {x: f8[x + "_scale"] for x in ("q", "k", "v")}  # each layer its own
         return out
 
     def upload(self, lay):
-        return {x: self.torch.from_numpy(lay[x]).to(self.dev) for x in ("q", "k", "v")}
+        L = {x: self.torch.from_numpy(lay[x]).to(self.dev) for x in ("q", "k", "v")}
+        L["scales"] = lay["scales"]
+        return L
 
     def meta_call(self, L, status):
         m = self.meta
-        self.bsa.block_meta_fp8(self.s, L["k"], self.scales["k"], m["centroid"], m["radius"], m["quant"],
+        self.bsa.block_meta_fp8(self.s, L["k"], L["scales"]["k"], m["centroid"], m["radius"], m["quant"],
                                 m["alpha"], status)
 
     def select_call(self, L, status):
         m, sl = self.meta, self.sel
-        self.bsa.select_mask_fp8(self.s, self.prm, L["q"], self.scales["q"], m["centroid"], m["radius"],
+        self.bsa.select_mask_fp8(self.s, self.prm, L["q"], L["scales"]["q"], m["centroid"], m["radius"],
                                  m["alpha"], sl["kv_idx"], sl["kv_cnt"], None, self.ws, status)
 
     def attn_call(self, L, o, status):
-        sl, sc = self.sel, self.scales
+        sl, sc = self.sel, L["scales"]
         if not hasattr(self, "wide_v"):
             self.wide_v = self.torch.empty(self.bsa.prefill_fp8_workspace_bytes(self.s), dtype=self.torch.uint8,
                                            device=self.dev)
@@ -705,6 +707,9 @@ def run_ours(args):
         o_host = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         dbuf = [{n: (torch.empty_like(o) if n == "o" else torch.empty_like(dev_layers[0][n]))
                  for n in ("q", "k", "v", "o")} for _ in range(2)]
+        for x in range(2):  # per-layer input scales travel with the buffers they describe (e4m3)
+            if "scales" in host_layers[x % len(host_layers)]:
+                dbuf[x]["scales"] = host_layers[x % len(host_layers)]["scales"]
         h2d_s = torch.cuda.Stream(dev)
         d2h_s = torch.cuda.Stream(dev)
 
