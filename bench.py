@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa32x4_n131072_d128_b128")
     ap.add_argument("--layers", type=int, default=2, help="distinct seeded layers rotated per step")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=48,
+                    help="layers streamed end to end (48: one pass over the 128K configuration's layers)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
