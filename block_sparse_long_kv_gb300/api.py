@@ -18,6 +18,7 @@ __all__ = [
     "Shape", "SelectParams", "SELECT_TOKEN_MAX", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
     "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
     "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
+    "selftest_wait_timeout",
     "VarlenShape", "make_varlen_shape", "varlen_block_stride", "varlen_block_meta",
     "varlen_select_workspace_bytes", "varlen_select_mask", "varlen_prefill_fwd",
     "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
@@ -397,6 +398,16 @@ def decode_fwd(shape: VarlenShape, cu_seqlens, q_new, k, v, kv_idx, kv_cnt, soft
         _ptr(o, "o", torch.bfloat16, b * hq * d), _ptr(lse, "lse", torch.float32, b * hq),
         _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def selftest_wait_timeout(dev_status, limit_ns: int, ctas: int = 1, stream=None):
+    """bsa_selftest_wait_timeout: CTAs that wait on a barrier nothing completes; CTA 0 gives
+    up after limit_ns and writes BSA_ERR_DEVICE_TIMEOUT into dev_status, the others stop on
+    seeing it."""
+    lib = _lib.load()
+    _lib.check("bsa_selftest_wait_timeout", lib.bsa_selftest_wait_timeout(
+        _ptr(dev_status, "dev_status", torch.int32, 1), ctypes.c_uint64(limit_ns), ctypes.c_int32(ctas),
+        _stream(stream)))
 
 
 def status_string(code: int) -> str:

@@ -1,6 +1,6 @@
 """Build libbsa.so in-tree with nvcc for sm_103a.
 
-The three translation units compile in parallel, then link into
+The translation units compile in parallel, then link into
 ``block_sparse_long_kv_gb300/libbsa.so``.  Objects go to ``_build/`` next to the
 sources (git-ignored).  Run ``python -m block_sparse_long_kv_gb300.build``.
 """
@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsa.so")
-SOURCES = ["bsa_api.cu", "bsa_mask.cu", "bsa_score.cu", "bsa_token_score.cu", "bsa_attn.cu", "bsa_decode.cu", "bsa_select_noalloc.cu"]
+SOURCES = ["bsa_api.cu", "bsa_mask.cu", "bsa_score.cu", "bsa_token_score.cu", "bsa_attn.cu", "bsa_decode.cu",
+           "bsa_select_noalloc.cu", "bsa_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I" + INCLUDE]

@@ -371,6 +371,19 @@ bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqle
                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
                           bsa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Self-test of the device wait limits (no compute).  Launches `ctas` CTAs
+ * (1..8) whose first thread waits, through the bounded wait the attention
+ * kernel uses, on an mbarrier that nothing completes.  CTA 0 gives up after
+ * limit_ns nanoseconds (1e6 .. 1e9) and writes BSA_ERR_DEVICE_TIMEOUT into
+ * *dev_status (int32, caller-owned, 4-byte aligned, 0 before the call); the
+ * other CTAs wait with the library's own 4 s limit and stop as soon as they
+ * see the status.  Returns BSA_ERR_INVALID_ARG for a null or misaligned
+ * status word or out-of-range arguments, BSA_ERR_CUDA if the launch fails.
+ * ------------------------------------------------------------------------ */
+bsa_status bsa_selftest_wait_timeout(int32_t *dev_status, uint64_t limit_ns, int32_t ctas,
+                                     bsa_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status status);
 

@@ -200,3 +200,14 @@ def test_fp8_entry_point_validation(lib):
     tok = _lib.SelectParams(0.1, 0.1, 1)                     # per-token aggregation reads bf16 Q
     assert lib.bsa_select_mask_fp8(ctypes.byref(s), ctypes.byref(tok), f, one, f, f, f, f, f, None, f,
                                    ctypes.c_size_t(1 << 40), None, None) == 3
+
+
+def test_selftest_argument_validation(lib):
+    import ctypes
+    INVALID = 1
+    assert lib.bsa_selftest_wait_timeout(None, ctypes.c_uint64(10_000_000), 1, None) == INVALID
+    buf = (ctypes.c_int32 * 4)()
+    base = ctypes.addressof(buf)
+    for limit, ctas in ((999_999, 1), (1_000_000_001, 1), (10_000_000, 0), (10_000_000, 9)):
+        assert lib.bsa_selftest_wait_timeout(ctypes.c_void_p(base), ctypes.c_uint64(limit), ctas, None) == INVALID
+    assert lib.bsa_selftest_wait_timeout(ctypes.c_void_p(base + 2), ctypes.c_uint64(10_000_000), 1, None) == INVALID
