@@ -23,7 +23,7 @@
 //                          into equal runs, one per CTA, so a short batch and a
 //                          mix of long and short sequences load every SM alike.
 //                          A CTA streams its entries in 64-key chunks through a
-//                          three-stage cp.async ring, computes the G heads'
+//                          two-stage cp.async ring, computes the G heads'
 //                          logits, an online softmax and P V on CUDA cores, and
 //                          writes one unnormalised partial (O, max, sum) per row
 //                          it touches
@@ -395,7 +395,8 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 constexpr int kChunk = 64;       // keys per chunk
-constexpr int kStages = 4;       // chunks in shared memory: the current one and three in flight
+constexpr int kStages = 2;       // chunks in shared memory: the current one and the next in flight;
+                                 // small enough for two CTAs per SM
 constexpr int kMaxDecodeCtas = 1024;
 
 template <int D, int G>
@@ -568,8 +569,9 @@ __device__ __forceinline__ DChunk walk_next(DecWalk &w, const int *pre, const in
 }
 
 // Split-KV decode attention over the plan above.  CTA c walks its entries in
-// chunks of 64 keys through a three-stage cp.async ring (a chunk's keys and
-// values are one group; two chunks are in flight while one is computed).
+// chunks of 64 keys through a two-stage cp.async ring (a chunk's keys and
+// values are one group; the next chunk is in flight while one is computed,
+// and the ring is small enough for two CTAs per SM).
 // Each warp owns 16 keys of a chunk and keeps its own online softmax: the G
 // heads of the row are the rows of a 16 x 8 x 16 bf16 tensor-core MMA, so
 // S = Q K^T is two n-tiles of 8 keys over D / 16 k-steps (Q held as A
