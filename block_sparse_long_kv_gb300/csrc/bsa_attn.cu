@@ -394,41 +394,68 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      if constexpr (C::CH == 2) {
-        // exchange partial maxima with the other half of the row, rounded up to bf16: any
-        // upper bound of the row max is a valid reference, and both halves then hold the
-        // same value.  The slot is rewritten only after the partner has arrived on P ready,
-        // which the next S tile waits for.
-        uint32_t u = __float_as_uint(mx);
-        if ((u & 0xFFFFu) != 0u && !(u >> 31)) u += 0x10000u;
-        const uint16_t mine = static_cast<uint16_t>(u >> 16);
-        red[hf * 128 + r] = mine;
-        ptx::named_barrier(pair_bar, 64);
-        const uint16_t other = red[(1 - hf) * 128 + r];
-        mx = fmaxf(__uint_as_float(static_cast<uint32_t>(mine) << 16),
-                   __uint_as_float(static_cast<uint32_t>(other) << 16));
-      }
-      const float mt = mx * sl2;
+      // the row max of both halves: each half's partial max rounded up to bf16 (any upper
+      // bound of the row max is a valid reference, and both halves then hold the same
+      // value).  The slot is rewritten only after the partner has arrived on P ready, which
+      // the next S tile waits for.
+      auto row_max = [&](float part) -> float {
+        if constexpr (C::CH == 2) {
+          uint32_t u = __float_as_uint(part);
+          if ((u & 0xFFFFu) != 0u && !(u >> 31)) u += 0x10000u;
+          const uint16_t mine = static_cast<uint16_t>(u >> 16);
+          red[hf * 128 + r] = mine;
+          ptx::named_barrier(pair_bar, 64);
+          const uint16_t other = red[(1 - hf) * 128 + r];
+          return fmaxf(__uint_as_float(static_cast<uint32_t>(mine) << 16),
+                       __uint_as_float(static_cast<uint32_t>(other) << 16));
+        } else {
+          return part;
+        }
+      };
+      float rs4[4];
+      // P = 2^(s * scale - mb) as bf16 pairs into TMEM over S, with the row sums
+      auto exps = [&](float mb) {
+        rs4[0] = rs4[1] = rs4[2] = rs4[3] = 0.f;
+#pragma unroll
+        for (int c16 = 0; c16 < C::CW / 32; ++c16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e]), sl2, -mb));
+            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e + 1]), sl2, -mb));
+            rs4[e & 3] += p0 + p1;
+            pk[e] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st16(tP + c16 * 16, pk);
+        }
+      };
       float factor = 1.f;
       bool resc = false;
-      if (mt > m + 8.f) {  // rescale only when the running max grows by more than 2^8
-        factor = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - mt);
-        resc = n > 0;
-        m = mt;
-      }
-      const float mb = (m == -INFINITY) ? 0.f : m;
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c16 = 0; c16 < C::CW / 32; ++c16) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e]), sl2, -mb));
-          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e + 1]), sl2, -mb));
-          rs4[e & 3] += p0 + p1;
-          pk[e] = ptx::pack_bf16x2(p0, p1);
+      if (n == 0) {  // the same branch for every row of the CTA (the named barriers pair warps)
+        // no running max yet: take this tile's first
+        const float mt = row_max(mx) * sl2;
+        if (mt > m + 8.f) {
+          factor = 0.f;
+          m = mt;
         }
-        ptx::tmem_st16(tP + c16 * 16, pk);
+        exps(m == -INFINITY ? 0.f : m);
+      } else {
+        // the exponentials with the running max go first; the row max is settled while
+        // they run, and only a max that grew by more than 2^8 redoes them (rare).  The
+        // decision is per row (the same in both halves: same m, same exchanged max); the
+        // redo is warp-wide, since the TMEM stores are warp-collective, and a row that
+        // keeps its max recomputes the same P
+        exps(m == -INFINITY ? 0.f : m);  // (no max yet only after fully masked tiles)
+        const float mt = row_max(mx) * sl2;
+        if (mt > m + 8.f) {
+          factor = m == -INFINITY ? 0.f : ptx::ex2_approx(m - mt);
+          resc = true;
+          m = mt;
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          ptx::tmem_wait_st();  // the first P stores land before they are overwritten
+          exps(m == -INFINITY ? 0.f : m);
+        }
       }
       l = l * factor + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
       if (__any_sync(0xffffffffu, resc)) {
