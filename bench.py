@@ -155,7 +155,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -166,13 +166,20 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "sm_min_mhz": float(min(sm)),
+               "samples": len(sm), "reasons": sorted(reasons)}
+        if pw:
+            out["power_w_median"] = float(np.median(pw))
+        return out
 
 
 # ------------------------------------------------------------------ CPU oracle sample
@@ -768,11 +775,15 @@ def run_ours(args):
         e2e_run(2)
         if world > 1:
             dist.barrier()
+        e2e_clocks = ClockSampler(local)
+        e2e_clocks.start()
+        time.sleep(0.3)
         e2e_ms = reduce_max(e2e_run(n_e2e), dist if world > 1 else None, dev)
+        e2e_clk = e2e_clocks.stop()
         h2d = sum(pinned[0][n].numel() * pinned[0][n].element_size() for n in ("q", "k", "v"))
         result["e2e"] = {"value": job_ms_per_layer(e2e_ms, n_e2e, world), "unit": "ms/layer",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_host[0].numel() * 2,
-                         "steps": n_e2e,
+                         "steps": n_e2e, "clocks": e2e_clk,
                          "api": run.e2e_api + " + pinned host copies on two copy streams, "
                                 "double-buffered (input copy of step s+1 and output copy of step s-1 "
                                 "overlap step s)"}
