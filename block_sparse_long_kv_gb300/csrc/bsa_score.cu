@@ -20,8 +20,9 @@
 //
 // Warp roles: warp 0 issues TMA loads of 32-dimension chunks (one 128-byte
 // swizzle row) of the four operands; warp 1 owns 256 TMEM columns and issues
-// the MMAs; warps 4..7 read the accumulator (one TMEM lane per key block) and
-// write S_c and R.  Every wait is bounded.
+// the MMAs; then all eight warps read the accumulator (one TMEM lane per key
+// block, each warp half of the columns) and write S_c and R.  Every wait is
+// bounded.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -183,7 +184,10 @@ __global__ void __launch_bounds__(256, 1)
       ptx::mma_commit(bar(C::B_DONE));  // also on abort: every issued MMA completes first
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  // ---- epilogue, all eight warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its key blocks)
+  // and the column half w / 4; the producer and MMA warps join once their work is issued
+  {
     bool dok = true;
     wait_b(bar(C::B_DONE), 0, status, dok);
     ptx::tc_fence_after();
@@ -192,16 +196,20 @@ __global__ void __launch_bounds__(256, 1)
     const bool row_ok = dok && j < nbb;
     const float bonus = row_ok ? alpha[static_cast<size_t>(gb) * nb + j] * radius[static_cast<size_t>(gb) * nb + j] : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    constexpr int HALF = C::COLS / 2;
+    const int cbase = (warp >> 2) * HALF;
 #pragma unroll 1
-    for (int cc = 0; cc < C::COLS / 32; ++cc) {
-      uint32_t v[32];
-      ptx::tmem_ld32(tmem + lane_off + cc * 32, v);
+    for (int cc = 0; cc < HALF / 64; ++cc) {
+      uint32_t v[64];
+      // two 32-column loads in flight before the wait
+      ptx::tmem_ld32(tmem + lane_off + cbase + cc * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      ptx::tmem_ld32(tmem + lane_off + cbase + cc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       ptx::tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 32 / G; ++q) {
-        // columns cc*32 + q*G .. + G-1 hold the G heads of one query block
+      for (int q = 0; q < 64 / G; ++q) {
+        // columns cbase + cc*64 + q*G .. + G-1 hold the G heads of one query block
         const int c0 = q * G;
-        const int col = cc * 32 + c0;
+        const int col = cbase + cc * 64 + c0;
         const int i = i0 + col / G;
         float dm = __uint_as_float(v[c0]);
         float rm = fmaf(snbar[col], bonus, dm);

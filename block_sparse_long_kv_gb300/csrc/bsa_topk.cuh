@@ -294,23 +294,35 @@ __device__ inline void warp_select_row(const float *rc, const float *rr, const f
   const int n4 = (i + 4) & ~3;  // keys / flags [0, n4) cover 0..i; entries j >= i are never candidates
 
   // ---- centroid path: top kc of candidates 1..i-1 by S_c
+  // (the row is read in batches of eight 16-byte loads per lane, all issued before any is used)
+  constexpr int LB = 4;
   float lo = INFINITY, hi = -INFINITY;
-  for (int j4 = lane * 4; j4 < n4; j4 += 128) {
-    const float4 v = reinterpret_cast<const float4 *>(rc)[j4 >> 2];
-    const float x[4] = {v.x, v.y, v.z, v.w};
-    uint32_t kp[4];
+  for (int jb = lane * 4; jb < n4; jb += 128 * LB) {
+    float4 v[LB];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j4 + e;
-      const bool cand = j >= 1 && j < i;
-      kp[e] = cand ? score_key(x[e]) : 0u;
-      if (cand) {
-        lo = fminf(lo, x[e]);
-        hi = fmaxf(hi, x[e]);
-      }
+    for (int u = 0; u < LB; ++u) {
+      const int j4 = jb + u * 128;
+      v[u] = j4 < n4 ? reinterpret_cast<const float4 *>(rc)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
-    reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
+#pragma unroll
+    for (int u = 0; u < LB; ++u) {
+      const int j4 = jb + u * 128;
+      if (j4 >= n4) continue;
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t kp[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j4 + e;
+        const bool cand = j >= 1 && j < i;
+        kp[e] = cand ? score_key(x[e]) : 0u;
+        if (cand) {
+          lo = fminf(lo, x[e]);
+          hi = fmaxf(hi, x[e]);
+        }
+      }
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+      reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
+    }
   }
   warp_minmax(lo, hi);
   __syncwarp();
@@ -329,24 +341,35 @@ __device__ inline void warp_select_row(const float *rc, const float *rr, const f
   int nelig = 0;
   lo = INFINITY;
   hi = -INFINITY;
-  for (int j4 = lane * 4; j4 < n4; j4 += 128) {
-    const float4 v = reinterpret_cast<const float4 *>(rr)[j4 >> 2];
-    const float4 a = reinterpret_cast<const float4 *>(ab)[j4 >> 2];
-    const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
-    const float x[4] = {v.x, v.y, v.z, v.w}, al[4] = {a.x, a.y, a.z, a.w};
-    uint32_t kp[4];
+  for (int jb = lane * 4; jb < n4; jb += 128 * (LB / 2)) {
+    float4 v[LB / 2], a[LB / 2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j4 + e;
-      const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
-      kp[e] = elig ? score_key(x[e]) : 0u;
-      nelig += elig ? 1 : 0;
-      if (elig) {
-        lo = fminf(lo, x[e]);
-        hi = fmaxf(hi, x[e]);
-      }
+    for (int u = 0; u < LB / 2; ++u) {
+      const int j4 = jb + u * 128;
+      const bool in = j4 < n4;
+      v[u] = in ? reinterpret_cast<const float4 *>(rr)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+      a[u] = in ? reinterpret_cast<const float4 *>(ab)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+#pragma unroll
+    for (int u = 0; u < LB / 2; ++u) {
+      const int j4 = jb + u * 128;
+      if (j4 >= n4) continue;
+      const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w}, al[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+      uint32_t kp[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j4 + e;
+        const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
+        kp[e] = elig ? score_key(x[e]) : 0u;
+        nelig += elig ? 1 : 0;
+        if (elig) {
+          lo = fminf(lo, x[e]);
+          hi = fmaxf(hi, x[e]);
+        }
+      }
+      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) nelig += __shfl_xor_sync(0xffffffffu, nelig, off);
