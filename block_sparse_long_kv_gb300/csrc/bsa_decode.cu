@@ -12,7 +12,7 @@
 //   decode_score_kernel    32 key blocks per CTA, one warp per key block: the
 //                          new token's G heads against the centroid row
 //                          (coalesced), S_c and R into the workspace
-//   decode_select_kernel   one 1024-thread CTA per (b, g): the two-path exact
+//   decode_select_kernel   one 256-thread CTA per (b, g): the two-path exact
 //                          top-k of a prefill row, CTA-wide (a histogram of
 //                          the values, then radix digits of the keys in the
 //                          threshold bin, as the prefill row code in
@@ -142,9 +142,9 @@ __global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
 // the threshold bin, then 8-bit radix digits of the order-preserving keys
 // inside that bin; equal keys at the threshold are ranked by index.
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-static_assert(kMaxBlocks <= 4 * kSelThreads, "a row fits in four entries per thread");
+static_assert(kMaxBlocks <= 16 * kSelThreads, "a row fits in sixteen entries per thread");
 
 struct SelShared {
   unsigned hist[256];
@@ -160,7 +160,7 @@ __device__ __forceinline__ unsigned cta_sum(unsigned v, SelShared &sh) {
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   if (lane == 0) sh.wsum[warp] = v;
   __syncthreads();
-  unsigned t = sh.wsum[lane];
+  unsigned t = lane < kSelWarps ? sh.wsum[lane] : 0u;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
   __syncthreads();
@@ -176,8 +176,8 @@ __device__ __forceinline__ void cta_minmax(float &lo, float &hi, SelShared &sh) 
     sh.whi[warp] = hi;
   }
   __syncthreads();
-  lo = sh.wlo[lane];
-  hi = sh.whi[lane];
+  lo = lane < kSelWarps ? sh.wlo[lane] : INFINITY;
+  hi = lane < kSelWarps ? sh.whi[lane] : -INFINITY;
   warp_minmax(lo, hi);
   __syncthreads();
 }
@@ -190,7 +190,7 @@ __device__ __forceinline__ unsigned cta_exclusive_scan(unsigned c, unsigned *tot
   if (lane == 0) sh.wsum[warp] = wt;
   __syncthreads();
   unsigned tot;
-  const unsigned wex = warp_exclusive_scan(sh.wsum[lane], &tot);
+  const unsigned wex = warp_exclusive_scan(lane < kSelWarps ? sh.wsum[lane] : 0u, &tot);
   const unsigned off = __shfl_sync(0xffffffffu, wex, warp);
   __syncthreads();
   *total = tot;
@@ -994,15 +994,15 @@ cudaError_t launch_decode_select(const MaskShape &s, const void *q_new, const fl
   if (e != cudaSuccess) return e;
   const dim3 rows(s.hkv, s.batch);
   const long long pc = static_cast<long long>(ppm_c), pr = static_cast<long long>(ppm_r);
-  if (s.nbs <= kSelThreads)
-    decode_select_kernel<1><<<rows, kSelThreads, 0, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
-                                                              s.block, s.hkv, s.nbs, pc, pr, status);
-  else if (s.nbs <= 2 * kSelThreads)
-    decode_select_kernel<2><<<rows, kSelThreads, 0, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
-                                                              s.block, s.hkv, s.nbs, pc, pr, status);
-  else if (s.nbs <= 4 * kSelThreads)
+  if (s.nbs <= 4 * kSelThreads)
     decode_select_kernel<4><<<rows, kSelThreads, 0, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
                                                               s.block, s.hkv, s.nbs, pc, pr, status);
+  else if (s.nbs <= 8 * kSelThreads)
+    decode_select_kernel<8><<<rows, kSelThreads, 0, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq, s.total,
+                                                              s.block, s.hkv, s.nbs, pc, pr, status);
+  else if (s.nbs <= 16 * kSelThreads)
+    decode_select_kernel<16><<<rows, kSelThreads, 0, stream>>>(sc, sr, alpha, kv_idx, kv_cnt, s.cu, s.seq,
+                                                               s.total, s.block, s.hkv, s.nbs, pc, pr, status);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
