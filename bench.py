@@ -733,9 +733,11 @@ def run_ours(args):
         h2d_s = torch.cuda.Stream(dev)
         d2h_s = torch.cuda.Stream(dev)
 
+        e2e_steps_ms = []  # interval between consecutive steps' compute ends
+
         def e2e_run(nsteps):
             ev_in = [torch.cuda.Event() for _ in range(nsteps)]
-            ev_done = [torch.cuda.Event() for _ in range(nsteps)]
+            ev_done = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
             ev_out = [torch.cuda.Event() for _ in range(nsteps)]
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
@@ -770,6 +772,7 @@ def run_ours(args):
             stream.wait_event(ev_in[nsteps - 1])
             end.record(stream)
             torch.cuda.synchronize(dev)
+            e2e_steps_ms[:] = [ev_done[t].elapsed_time(ev_done[t + 1]) for t in range(nsteps - 1)]
             return start.elapsed_time(end)
 
         e2e_run(2)
@@ -787,6 +790,27 @@ def run_ours(args):
                          "api": run.e2e_api + " + pinned host copies on two copy streams, "
                                 "double-buffered (input copy of step s+1 and output copy of step s-1 "
                                 "overlap step s)"}
+        # the host link on its own, after the timed region: each direction alone, 5 copies
+        def copy_rate(fn, nbytes, reps=5):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(reps):
+                fn()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            return nbytes * reps / (ev0.elapsed_time(ev1) * 1e-3) / 1e9
+
+        def h2d_only():
+            for n in ("q", "k", "v"):
+                dbuf[0][n].copy_(pinned[0][n], non_blocking=True)
+
+        if len(e2e_steps_ms) >= 8:
+            q4 = len(e2e_steps_ms) // 4
+            result["e2e"]["step_ms_median_first_quarter"] = float(np.median(e2e_steps_ms[:q4]))
+            result["e2e"]["step_ms_median_last_quarter"] = float(np.median(e2e_steps_ms[-q4:]))
+        result["e2e"]["copies_alone_gbs"] = {
+            "h2d": copy_rate(h2d_only, h2d),
+            "d2h": copy_rate(lambda: o_host[0].copy_(dbuf[0]["o"], non_blocking=True), o_host[0].numel() * 2)}
         result["gpu_launches_e2e_per_step"] = 6
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")

@@ -227,6 +227,28 @@ def test_long_prefill_128k_sampled():
     check_attention_rows(w, lay, o, lse, oracle_keep(w, orc) != 0, att_rows)
 
 
+def test_maximum_block_count():
+    """The largest row the library takes: 4096 key blocks (262144 tokens at block 64), sampled
+    mask rows (the first, the last and the longest included) and attention rows against the
+    oracle."""
+    w = synth.Workload("max_nb", 1, 4096 * 64, 2, 1, 64, 64, 0.02, 0.01, seed_base=4242, needles_fixed=4)
+    lay = synth.make_layer(w)
+    got = gpu_mask_build(w, lay)
+    rng = np.random.default_rng(11)
+    rows = {(0, 0): sorted({0, 1, 2, w.nb // 2, w.nb - 2, w.nb - 1} | set(rng.integers(0, w.nb, 10).tolist()))}
+    orc = oracle_rows(w, lay, rows)
+    compared, excused = compare_mask_rows(got["mask"], orc)
+    assert excused <= max(4, compared // 1000), (compared, excused)
+    check_lists_match_mask(got["mask"][:, :, -2:], got["kv_idx"][:, :, -2:], got["kv_cnt"][:, :, -2:])
+    o, lse = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                           torch.from_numpy(got["kv_cnt"]).cuda())
+    keep = oracle_keep(w, orc)
+    att = [(0, h, i) for i in rows[(0, 0)] for h in range(w.hq)
+           if np.array_equal(got["mask"][0, 0, i], keep[0, 0, i])]
+    assert att
+    check_attention_rows(w, lay, o, lse, keep != 0, att)
+
+
 @pytest.mark.parametrize("layer", [1, 47])
 def test_long_prefill_128k_full_masks(layer):
     """Two more of the 48 seeded 128K layers (the second and the last): every mask row of
