@@ -808,6 +808,8 @@ def run_ours(args):
             q4 = len(e2e_steps_ms) // 4
             result["e2e"]["step_ms_median_first_quarter"] = float(np.median(e2e_steps_ms[:q4]))
             result["e2e"]["step_ms_median_last_quarter"] = float(np.median(e2e_steps_ms[-q4:]))
+            result["e2e"]["step_ms_mean"] = float(np.mean(e2e_steps_ms))
+            result["e2e"]["step_ms_max"] = float(np.max(e2e_steps_ms))
         result["e2e"]["copies_alone_gbs"] = {
             "h2d": copy_rate(h2d_only, h2d),
             "d2h": copy_rate(lambda: o_host[0].copy_(dbuf[0]["o"], non_blocking=True), o_host[0].numel() * 2)}
