@@ -249,10 +249,10 @@ def test_maximum_block_count():
     check_attention_rows(w, lay, o, lse, keep != 0, att)
 
 
-@pytest.mark.parametrize("layer", [1, 47])
+@pytest.mark.parametrize("layer", [1, 11, 23, 35, 47])
 def test_long_prefill_128k_full_masks(layer):
-    """Two more of the 48 seeded 128K layers (the second and the last): every mask row of
-    every KV head against the oracle, the block summaries and quantiles, and sampled
+    """Five more of the 48 seeded 128K layers (spread from the second to the last): every mask
+    row of every KV head against the oracle, the block summaries and quantiles, and sampled
     attention rows through the GPU's own lists where its mask row equals the oracle's."""
     w = synth.workload("gqa32x4_n131072_d128_b128")
     lay = synth.make_layer(w, layer=layer)
