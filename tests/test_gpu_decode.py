@@ -198,6 +198,8 @@ def test_decode_keep_all_equals_dense():
 @pytest.mark.parametrize("cfg", [
     dict(hq=16, hkv=1, head_dim=128, block=128),   # G = 16
     dict(hq=8, hkv=8, head_dim=64, block=256),     # G = 1, d = 64, block 256
+    dict(hq=8, hkv=2, head_dim=128, block=64),     # G = 4, block 64
+    dict(hq=4, hkv=2, head_dim=64, block=128),     # G = 2, d = 64
 ])
 def test_decode_shape_variants(cfg):
     vw = synth.VarlenWorkload("dec", (3000, 777, 4096), cfg["hq"], cfg["hkv"], cfg["head_dim"],
