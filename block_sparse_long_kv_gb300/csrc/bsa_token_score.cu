@@ -1,10 +1,10 @@
 // Per-token query aggregation of the block scores on tcgen05 tensor cores (sm_103a).
 //
 // Source: "Your 128K Context Is 6x Slower Than It Needs to Be"
-// (articles.phantom-byte.com), section "The numbers, stated honestly": the
-// selector compares tokens against key-block centroids, a tensor that grows
-// with prompt length times block count unless the reduction is tiled.  This
-// kernel is that tiled reduction.  For one (batch, KV head g), query block i
+// (articles.phantom-byte.com), section "The numbers, stated honestly": a
+// selector that compares every token with every block centroid needs a table
+// of tokens x blocks in memory, unless the comparison is reduced tile by tile
+// as it is computed.  This kernel is that tiled reduction.  For one (batch, KV head g), query block i
 // and key block j:
 //   S_c[i][j] = s * max over the G heads h and the tokens t of block i of q_{h,t} . c_j
 //   R[i][j]   = s * max_{h,t} (q_{h,t} . c_j + alpha_j * |q_{h,t}| * r_j)

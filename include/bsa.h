@@ -120,9 +120,9 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
 /*
  * bsa_select_mask - score every causal key block and emit the kept lists.
  *
- * Rescue branch section: the centroid branch scores every block on average
- * relevance and keeps the high ones; the rescue branch brings back wide-radius
- * blocks that the mean score alone would drop; the two masks are OR-ed.  With s = 1/sqrt(head_dim), qbar_{h,i} the mean query of block i
+ * Rescue branch section: one path ranks the key blocks by their mean-based
+ * score and keeps the best; a second path restores blocks with a large radius
+ * that this ranking leaves out; the union of the two is kept.  With s = 1/sqrt(head_dim), qbar_{h,i} the mean query of block i
  * for head h and nbar_{h,i} the mean of those queries' L2 norms:
  *   S_c[i][j] = max over the G heads of KV head g of s * qbar_{h,i}.c_j
  *   R[i][j]   = max over those heads of s * (qbar_{h,i}.c_j + alpha_j * nbar_{h,i} * r_j)
@@ -225,8 +225,8 @@ bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets);
 /* ------------------------------------------------------------------------
  * FP8 (e4m3) inputs.
  *
- * The article measures an FP8 model (prefill section: the benchmark model is
- * an FP8 checkpoint, and the rescue signal is reported to survive 8-bit keys).
+ * The article's measurements use 8-bit weights and keys (prefill section),
+ * and it reports that the radius signal still works with 8-bit keys.
  * These entry points take Q, K and V as OCP e4m3 codes (1 byte per element,
  * same [batch, seq, heads, head_dim] layouts) with one positive scale per
  * tensor: value = e4m3(code) * scale.  They compute exactly what the bf16
