@@ -2,10 +2,13 @@
 
 The translation units compile in parallel, then link into
 ``block_sparse_long_kv_gb300/libbsa.so``.  Objects go to ``_build/`` next to the
-sources (git-ignored).  Run ``python -m block_sparse_long_kv_gb300.build``.
+sources (git-ignored), with the key the library was built under: a hash of the
+sources and headers, the flags and the nvcc version, so a change to any of them
+rebuilds.  Run ``python -m block_sparse_long_kv_gb300.build``.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -32,19 +35,37 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libbsa")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+KEY = os.path.join(OBJ, "libbsa.key")
+
+
+def _build_key(nvcc: str) -> str:
+    """Hash of everything the library is built from: every source and header,
+    the file list, the architecture and compiler flags, and the nvcc version."""
+    h = hashlib.sha256()
+    ver = subprocess.run([nvcc, "--version"], capture_output=True, text=True).stdout
+    h.update(ver.encode())
+    h.update(repr((SOURCES, ARCH, FLAGS)).encode())
+    deps = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(INCLUDE, "bsa.h")]
+    for d in deps:
+        h.update(os.path.basename(d).encode())
+        with open(d, "rb") as f:
+            h.update(hashlib.sha256(f.read()).digest())
+    return h.hexdigest()
+
+
+def _stale(key: str) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(KEY):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "bsa.h")]
-    return any(os.path.getmtime(d) > t for d in deps)
+    with open(KEY) as f:
+        return f.read().strip() != key
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libbsa.so if it is missing or older than its sources."""
-    if not force and not _stale():
-        return LIB
+    """Compile libbsa.so unless it was built from exactly these sources, flags and nvcc."""
     nvcc = _nvcc()
+    key = _build_key(nvcc)
+    if not force and not _stale(key):
+        return LIB
     os.makedirs(OBJ, exist_ok=True)
 
     def compile_one(src):
@@ -65,6 +86,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(KEY, "w") as f:
+        f.write(key + "\n")
     return LIB
 
 

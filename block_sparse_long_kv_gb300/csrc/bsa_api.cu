@@ -35,7 +35,6 @@ bsa_status check_shape(const bsa_shape *s) {
   if (s->seq % s->block != 0) return BSA_ERR_SHAPE;
   if (static_cast<long long>(s->batch) * s->seq > INT32_MAX) return BSA_ERR_UNSUPPORTED;
   const int nb = s->seq / s->block;
-  if (nb % 4 != 0) return BSA_ERR_UNSUPPORTED;
   return check_common(s->batch, s->hq, s->hkv, s->head_dim, s->block, nb);
 }
 
@@ -54,7 +53,8 @@ bsa_status check_varlen(const bsa_varlen_shape *s, const int32_t *cu_seqlens) {
 bsa::MaskShape mask_shape(const bsa_shape *s) {
   const int nb = s->seq / s->block;
   return bsa::MaskShape{s->batch, s->seq, s->hq, s->hkv, s->head_dim, s->block,
-                        nb, s->hq / s->hkv, nullptr, s->batch * s->seq, nb};
+                        nb, s->hq / s->hkv, nullptr, s->batch * s->seq, nb,
+                        0, 1.f, 1.f, 1.f, bsa::round4(nb)};
 }
 
 int varlen_blocks(const bsa_varlen_shape *s) { return (s->max_seqlen + s->block - 1) / s->block; }
@@ -63,7 +63,8 @@ int varlen_stride(const bsa_varlen_shape *s) { return (varlen_blocks(s) + 3) / 4
 
 bsa::MaskShape mask_shape(const bsa_varlen_shape *s, const int32_t *cu) {
   return bsa::MaskShape{s->batch, s->max_seqlen, s->hq, s->hkv, s->head_dim, s->block,
-                        varlen_blocks(s), s->hq / s->hkv, cu, s->total_tokens, varlen_stride(s)};
+                        varlen_blocks(s), s->hq / s->hkv, cu, s->total_tokens, varlen_stride(s),
+                        0, 1.f, 1.f, 1.f, varlen_stride(s)};
 }
 
 bsa::AttnShape attn_shape(const bsa::MaskShape &m) {

@@ -16,14 +16,20 @@ constexpr int kMaxDecodeRows = 4096;  // batch * hkv limit of decode (its plan s
 // b*seq .. b*seq+seq-1) or packed ragged (sequence b is tokens cu[b] ..
 // cu[b+1]-1 of `total`, each at most `seq` = max_seqlen long).  nb is the
 // largest block count of a sequence, nbs the per-sequence stride of every
-// per-block array (nb rounded up to a multiple of 4; equal to nb when fixed).
+// caller-visible per-block array (equal to nb when fixed-length, nb rounded up
+// to a multiple of 4 when packed), nbw the row stride of the block-score
+// matrices in the select workspace (nbs rounded up to a multiple of 4, so
+// every score row starts on a 16-byte boundary).
 struct MaskShape {
   int batch, seq, hq, hkv, d, block, nb, group;
   const int32_t *cu;
   int total, nbs;
   int fp8;                          // inputs are e4m3 codes: value = code * scale
   float q_scale, k_scale, v_scale;  // used when fp8
+  int nbw;
 };
+
+__host__ __device__ constexpr int round4(int x) { return (x + 3) / 4 * 4; }
 
 // Token span of sequence b.  Packed entries are checked against total and
 // max_seqlen: an inconsistent one records BSA_ERR_INVALID_ARG (if status is

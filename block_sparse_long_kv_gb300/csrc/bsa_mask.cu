@@ -420,35 +420,45 @@ constexpr int kSelWarps = 8;   // rows per select CTA, one warp each
 // kernel), selects the top kc, then the rescue-path keys of the candidates the
 // centroid path dropped and whose alpha is positive, selects the top kr, ORs in
 // the forced sink and diagonal blocks and writes the ascending kept list.
+// nbs is the row stride of alpha, kv_idx, kv_cnt and mask (the caller's arrays),
+// nbw the row stride of the score matrices and of the per-warp shared scratch.
+// When nbs is not a multiple of 4 (a fixed-length batch whose block count is
+// not), alpha and mask rows are not 16- / 4-byte aligned and are accessed
+// element by element.
+template <bool ALIGNED>
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
     const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
     int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask,
-    const int32_t *__restrict__ cu, int seq, int total, int block, int hkv, int nb,
+    const int32_t *__restrict__ cu, int seq, int total, int block, int hkv, int nbs, int nbw,
     long long ppm_c, long long ppm_r, int32_t *status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = nb - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
+  const int i = nbs - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
   if (i < 0) return;
   const int g = blockIdx.y, b = blockIdx.z;
   {
     // rows past the sequence's last block: empty list, zero mask row
     const SeqSpan sp = seq_span(cu, b, seq, total, status);
     if (i >= (sp.len + block - 1) / block) {
-      const size_t row = (static_cast<size_t>(b) * hkv + g) * nb + i;
+      const size_t row = (static_cast<size_t>(b) * hkv + g) * nbs + i;
       if (lane == 0) kv_cnt[row] = 0;
       if (mask != nullptr) {
-        uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nb));
-        for (int j4 = lane * 4; j4 < nb; j4 += 128) mrow[j4 >> 2] = 0u;
+        if constexpr (ALIGNED) {
+          uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nbs));
+          for (int j4 = lane * 4; j4 < nbs; j4 += 128) mrow[j4 >> 2] = 0u;
+        } else {
+          for (int j = lane; j < nbs; j += 32) mask[row * static_cast<size_t>(nbs) + j] = 0u;
+        }
       }
       return;
     }
   }
-  const RowScratch w = row_scratch(smem + static_cast<size_t>(warp) * row_scratch_bytes(nb), nb);
+  const RowScratch w = row_scratch(smem + static_cast<size_t>(warp) * row_scratch_bytes(nbw), nbw);
   const size_t gb = static_cast<size_t>(b) * hkv + g;
-  const size_t row = gb * nb + i;
-  warp_select_row(s_c + row * nb, s_r + row * nb, alpha + gb * nb, i, ppm_c, ppm_r, w);
-  warp_emit_row(w, i, kv_idx + row * static_cast<size_t>(nb), kv_cnt + row,
-                mask != nullptr ? mask + row * static_cast<size_t>(nb) : nullptr, nb);
+  const size_t row = gb * nbs + i;
+  warp_select_row<ALIGNED>(s_c + row * nbw, s_r + row * nbw, alpha + gb * nbs, i, ppm_c, ppm_r, w);
+  warp_emit_row<ALIGNED>(w, i, kv_idx + row * static_cast<size_t>(nbs), kv_cnt + row,
+                         mask != nullptr ? mask + row * static_cast<size_t>(nbs) : nullptr, nbs);
 }
 
 template <int D, int BLK>
@@ -506,8 +516,8 @@ cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *q_hi, float
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 
-// Select workspace regions, each 256-byte aligned: q_hi, q_lo [b, hkv, nb, G, d],
-// nbar [b, hkv, nb, G], c_hi, c_lo [b, hkv, nb, d], S_c, R [b, hkv, nb, nb], all fp32.
+// Select workspace regions, each 256-byte aligned: q_hi, q_lo [b, hkv, nbs, G, d],
+// nbar [b, hkv, nbs, G], c_hi, c_lo [b, hkv, nbs, d], S_c, R [b, hkv, nbs, nbw], all fp32.
 struct SelectRegions {
   size_t off[7];
   size_t total;
@@ -517,7 +527,7 @@ SelectRegions select_regions(const MaskShape &s) {
   const size_t rows = static_cast<size_t>(s.batch) * s.hq * s.nbs;  // (b, g, i, h) rows
   const size_t blocks = static_cast<size_t>(s.batch) * s.hkv * s.nbs;
   const size_t sizes[7] = {rows * s.d * 4, rows * s.d * 4, rows * 4, blocks * s.d * 4, blocks * s.d * 4,
-                           blocks * s.nbs * 4, blocks * s.nbs * 4};
+                           blocks * s.nbw * 4, blocks * s.nbw * 4};
   SelectRegions r{};
   size_t at = 0;
   for (int x = 0; x < 7; ++x) {
@@ -583,14 +593,15 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
                       status, stream);
   }
   if (e != cudaSuccess) return e;
-  const size_t smem = kSelWarps * row_scratch_bytes(s.nbs);
-  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const size_t smem = kSelWarps * row_scratch_bytes(s.nbw);
+  const bool aligned = s.nbs % 4 == 0;
+  auto kern = aligned ? select_kernel<true> : select_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((s.nbs + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);
-  select_kernel<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq,
-                                                        s.total, s.block, s.hkv, s.nbs,
-                                                        static_cast<long long>(ppm_c),
-                                                        static_cast<long long>(ppm_r), status);
+  kern<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq, s.total,
+                                               s.block, s.hkv, s.nbs, s.nbw, static_cast<long long>(ppm_c),
+                                               static_cast<long long>(ppm_r), status);
   return cudaGetLastError();
 }
 

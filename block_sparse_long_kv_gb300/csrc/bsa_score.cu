@@ -97,10 +97,11 @@ template <int D, int G>
 __global__ void __launch_bounds__(256, 1)
     score_kernel(const __grid_constant__ ScoreMaps maps, const float *__restrict__ nbar,
                  const float *__restrict__ radius, const float *__restrict__ alpha,
-                 float *__restrict__ s_c, float *__restrict__ s_r, int nb, const ScoreSeq sq,
+                 float *__restrict__ s_c, float *__restrict__ s_r, int nb, int nbw, const ScoreSeq sq,
                  float scale, int32_t *status) {
   using C = ScoreCfg<D, G>;
   const int jt = blockIdx.x, it = blockIdx.y, gb = blockIdx.z;  // gb = b * hkv + g
+  // nb: per-sequence stride of the per-block arrays; nbw: row stride of S_c and R
   const int j0 = jt * C::ROWS, i0 = it * C::NI;
   // this sequence's blocks (nb is the per-sequence stride of every per-block array)
   const SeqSpan sp = seq_span(sq.cu, gb / sq.hkv, sq.seq, sq.total, status);
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(256, 1)
           rm = fmaxf(rm, fmaf(snbar[col + h], bonus, x));
         }
         if (row_ok && j < i && i < nbb) {
-          const size_t o = (static_cast<size_t>(gb) * nb + i) * nb + j;
+          const size_t o = (static_cast<size_t>(gb) * nb + i) * nbw + j;
           s_c[o] = dm * scale;
           s_r[o] = rm * scale;
         }
@@ -266,7 +267,7 @@ cudaError_t launch_t(const MaskShape &s, const ScoreOperands &op, float scale, f
   dim3 grid((s.nbs + C::ROWS - 1) / C::ROWS, (s.nbs + C::NI - 1) / C::NI, static_cast<unsigned>(groups));
   const ScoreSeq sq{s.cu, s.seq, s.total, s.block, s.hkv};
   score_kernel<D, G><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps, op.nbar, op.radius, op.alpha,
-                                                                  s_c, s_r, s.nbs, sq, scale, status);
+                                                                  s_c, s_r, s.nbs, s.nbw, sq, scale, status);
   return cudaGetLastError();
 }
 

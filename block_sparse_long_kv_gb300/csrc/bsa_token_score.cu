@@ -90,6 +90,7 @@ struct TokArgs {
   float *s_c, *s_r;
   const int32_t *cu;
   int seq, total, hkv, nbs, ntt;
+  int nbw;  // row stride of s_c and s_r
   float scale;
   int32_t *status;
 };
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int q = 0; q < C::QB; ++q) {
         const int i = i0 + q;
         if (jv && j < i && i < nbb) {
-          const size_t o = (static_cast<size_t>(gb) * a.nbs + i) * a.nbs + j;
+          const size_t o = (static_cast<size_t>(gb) * a.nbs + i) * a.nbw + j;
           a.s_c[o] = dm[q] * a.scale;
           a.s_r[o] = rm[q] * a.scale;
         }
@@ -402,7 +403,8 @@ cudaError_t launch_token_scores(const MaskShape &s, const void *q, const float *
   if (!map_q(fn, &maps.q, q, s.total, s.hq, s.d) || !map_c16(fn, &maps.c_hi, hi, s.d, rows) ||
       !map_c16(fn, &maps.c_lo, lo, s.d, rows))
     return cudaErrorInvalidValue;
-  TokArgs a{radius, alpha, s_c, s_r, s.cu, s.seq, s.total, s.hkv, s.nbs, (s.seq + 255) / 256, scale, status};
+  TokArgs a{radius, alpha, s_c, s_r, s.cu, s.seq, s.total, s.hkv, s.nbs, (s.seq + 255) / 256, s.nbw, scale,
+            status};
   if (s.d == 64) return launch_blk<64>(s, maps, a, stream);
   if (s.d == 128) return launch_blk<128>(s, maps, a, stream);
   return cudaErrorInvalidValue;

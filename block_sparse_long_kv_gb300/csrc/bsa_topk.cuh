@@ -282,10 +282,12 @@ __device__ __forceinline__ RowScratch row_scratch(unsigned char *base, int nbs) 
 // Selection of one row i by one warp: key blocks 0 and i forced, the top kc
 // of the candidates 1..i-1 by rc, then among the candidates the centroid path
 // dropped whose alpha is positive the top kr by rr; keep counts
-// ceil(ratio * (i + 1)) from ppm, clipped to the candidates.  rc, rr and ab
-// (alpha) point at 16-byte aligned rows readable for round_up(i + 1, 4)
-// entries (shared or global memory).  Leaves the BSA_MASK_* bits in
+// ceil(ratio * (i + 1)) from ppm, clipped to the candidates.  rc and rr point
+// at 16-byte aligned rows readable for round_up(i + 1, 4) entries (shared or
+// global memory); so does ab (alpha) when AB_ALIGNED, otherwise ab is read one
+// entry at a time and only for j < i.  Leaves the BSA_MASK_* bits in
 // w.flags[0..i] and zeros up to round_up(i + 1, 4).
+template <bool AB_ALIGNED = true>
 __device__ inline void warp_select_row(const float *rc, const float *rr, const float *ab, int i,
                                        long long ppm_c, long long ppm_r, const RowScratch &w) {
   const int lane = threadIdx.x & 31;
@@ -348,7 +350,12 @@ __device__ inline void warp_select_row(const float *rc, const float *rr, const f
       const int j4 = jb + u * 128;
       const bool in = j4 < n4;
       v[u] = in ? reinterpret_cast<const float4 *>(rr)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
-      a[u] = in ? reinterpret_cast<const float4 *>(ab)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (AB_ALIGNED) {
+        a[u] = in ? reinterpret_cast<const float4 *>(ab)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        a[u] = make_float4(j4 < i ? ab[j4] : 0.f, j4 + 1 < i ? ab[j4 + 1] : 0.f,
+                           j4 + 2 < i ? ab[j4 + 2] : 0.f, j4 + 3 < i ? ab[j4 + 3] : 0.f);
+      }
     }
 #pragma unroll
     for (int u = 0; u < LB / 2; ++u) {
@@ -393,7 +400,10 @@ __device__ inline void warp_select_row(const float *rc, const float *rr, const f
 }
 
 // Writes the ascending kept list of row i (w.flags[0..i]) to dst and its
-// length to *cnt; with mrow, also the row's mask bits (nbs bytes, zero past i).
+// length to *cnt; with mrow, also the row's mask bits (nbs bytes, zero past i),
+// four bytes per store when MROW_ALIGNED (mrow 4-byte aligned, nbs % 4 == 0),
+// else byte by byte.
+template <bool MROW_ALIGNED = true>
 __device__ inline void warp_emit_row(const RowScratch &w, int i, int32_t *dst, int32_t *cnt,
                                      uint8_t *mrow, int nbs) {
   const int lane = threadIdx.x & 31;
@@ -407,6 +417,10 @@ __device__ inline void warp_emit_row(const RowScratch &w, int i, int32_t *dst, i
     kept += __popc(bl);
   }
   if (lane == 0) *cnt = kept;
+  if (!MROW_ALIGNED && mrow != nullptr) {
+    for (int j = lane; j < nbs; j += 32) mrow[j] = j <= i ? w.flags[j] : 0u;
+    return;
+  }
   if (mrow != nullptr) {
     uint32_t *m4 = reinterpret_cast<uint32_t *>(mrow);
     for (int j4 = lane * 4; j4 < nbs; j4 += 128) {

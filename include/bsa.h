@@ -57,8 +57,9 @@ typedef enum {
 
 /*
  * Problem shape.  Supported: head_dim in {64, 128}; block in {64, 128, 256};
- * seq % block == 0; nb % 4 == 0; 1 <= nb <= 4096; hq % hkv == 0; for block 64
- * the group size G must be even (two heads share one 128-row query tile).
+ * seq % block == 0 with any block count 1 <= nb <= 4096; hq % hkv == 0 with
+ * G in {1, 2, 4, 8, 16}; for block 64 the group size G must be even (two heads
+ * share one 128-row query tile).
  */
 typedef struct {
   int32_t batch, seq, hq, hkv, head_dim, block;
@@ -158,20 +159,25 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
  * owns the whole device pool and forbids allocations outside it, or a
  * latency-critical caller that must not call cudaMalloc because it can
  * synchronise the device.  The call computes exactly what bsa_select_mask
- * computes (same kernels, same outputs), with its scratch in a fixed 12 MiB
- * array inside the library's device image, so it allocates nothing.
+ * computes (same kernels, same outputs, both query aggregations: flags 0 or
+ * BSA_SELECT_TOKEN_MAX), with its scratch in a fixed 12 MiB array inside the
+ * library's device image, so it allocates nothing.
  *   - Every GPU that loads libbsa keeps those 12 MiB until the process exits.
  *   - Shapes needing more than 12 MiB of select scratch
  *     (bsa_select_workspace_bytes(shape) > 12 MiB: at 32 query heads,
- *     4 KV heads, head_dim 128 and block 128 that is beyond 34816 tokens;
+ *     4 KV heads, head_dim 128 and block 128 that is beyond 35072 tokens;
  *     the 65536- and 131072-token layers need 27.3 MB and 71.4 MB) return
- *     BSA_ERR_WORKSPACE.
+ *     BSA_ERR_WORKSPACE before anything is launched.
  *   - All calls on one device share that array: calls whose kernels overlap on
  *     the GPU (unordered streams) race and give wrong results.  Calls ordered
- *     on one stream are safe.
- *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
- * Arguments and errors otherwise as bsa_select_mask.
+ *     on one stream are safe.  Nothing in it needs to start at zero.
+ *   - The first call on a device, and the first call after that device's
+ *     context was reset, looks up the array's device address with that device
+ *     current; make that first call before any stream capture.
+ * Errors: shape errors as bsa_select_mask, then BSA_ERR_WORKSPACE for shapes
+ * beyond the array, then the parameter, pointer and launch errors of
+ * bsa_select_mask.  dev_status receives BSA_ERR_DEVICE_TIMEOUT if the score
+ * kernels' bounded waits give up.
  */
 bsa_status bsa_select_mask_noalloc(const bsa_shape *shape, const bsa_select_params *params,
                                    const void *q, const float *centroid, const float *radius,

@@ -24,6 +24,16 @@ import synth
 
 REL = 1e-4
 
+# (test id, label, compared blocks, excused blocks) of every mask comparison in this
+# process; tests/conftest.py prints them at the end of the run.
+EXCUSE_LOG = []
+
+
+def _current_test() -> str:
+    import os
+    cur = os.environ.get("PYTEST_CURRENT_TEST", "?")
+    return cur.rsplit(" ", 1)[0].split("::", 1)[-1]
+
 
 def to_dev(bits: np.ndarray, device="cuda"):
     return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
@@ -125,8 +135,15 @@ def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None, token_
     return dict(rows=rows, centroid=centroid, radius=radius, med=med, p90=p90, alpha=alpha)
 
 
-def compare_mask_rows(gpu_mask, orc):
-    """Apply the protocol; returns (n_compared_blocks, n_excused).  Raises on an unexcused mismatch."""
+def compare_mask_rows(gpu_mask, orc, label=""):
+    """Apply the protocol; returns (n_compared_blocks, n_excused).  Raises on an unexcused mismatch.
+    Every call is recorded in EXCUSE_LOG (with ``label`` naming the layer or case)."""
+    compared, excused = _compare_mask_rows(gpu_mask, orc)
+    EXCUSE_LOG.append((_current_test(), label, compared, excused))
+    return compared, excused
+
+
+def _compare_mask_rows(gpu_mask, orc):
     excused = 0
     compared = 0
     for (b, g, i), (om, s_c, r) in orc["rows"].items():

@@ -51,7 +51,7 @@ def shp(**kw):
 
 @pytest.mark.parametrize("kw, code", [
     (dict(seq=1000), 2), (dict(hq=3, hkv=2), 2), (dict(batch=0), 2), (dict(seq=0), 2),
-    (dict(head_dim=96), 3), (dict(block=32), 3), (dict(seq=64 * 6), 3),       # nb % 4
+    (dict(head_dim=96), 3), (dict(block=32), 3),
     (dict(seq=64 * 4100), 3), (dict(hq=3, hkv=1, block=64), 3),               # nb > 4096; odd group
     (dict(hq=24, hkv=1, block=128), 3),                                         # group 24
 ])
@@ -211,3 +211,49 @@ def test_selftest_argument_validation(lib):
     for limit, ctas in ((999_999, 1), (1_000_000_001, 1), (10_000_000, 0), (10_000_000, 9)):
         assert lib.bsa_selftest_wait_timeout(ctypes.c_void_p(base), ctypes.c_uint64(limit), ctas, None) == INVALID
     assert lib.bsa_selftest_wait_timeout(ctypes.c_void_p(base + 2), ctypes.c_uint64(10_000_000), 1, None) == INVALID
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 9, 65])
+def test_any_block_count_accepted(lib, nb):
+    """Only seq % block == 0 is required: block counts that are not a multiple of 4 are taken.
+    The caller's per-block arrays keep the plain [b, hkv, nb, ...] layout; only the select
+    scratch pads its score rows to a multiple of 4 entries."""
+    for block, hq, hkv, d in ((128, 32, 4, 128), (64, 4, 2, 64)):
+        s = shp(batch=2, seq=nb * block, hq=hq, hkv=hkv, head_dim=d, block=block)
+        need = lib.bsa_select_workspace_bytes(ctypes.byref(s))
+        rows, blocks, nbw = 2 * hq * nb, 2 * hkv * nb, (nb + 3) // 4 * 4
+        r256 = lambda x: (x + 255) // 256 * 256
+        assert need == (2 * r256(rows * d * 4) + r256(rows * 4) + 2 * r256(blocks * d * 4)
+                        + 2 * r256(blocks * nbw * 4))
+        total = lib.bsa_prefill_layer_workspace_bytes(ctypes.byref(s))
+        offs = (ctypes.c_size_t * 6)()
+        assert lib.bsa_prefill_layer_views(ctypes.byref(s), offs) == 0
+        sizes = [blocks * d * 4, blocks * 4, 2 * hkv * 2 * 4, blocks * 4, blocks * nb * 4, blocks * 4]
+        for x in range(1, 6):
+            assert offs[x] >= offs[x - 1] + sizes[x - 1] and offs[x] % 256 == 0
+        assert total >= offs[5] + sizes[5] + need
+        # argument checks still run (and fail) before anything is launched
+        f = ctypes.c_void_p(FAKE)
+        assert lib.bsa_block_meta(ctypes.byref(s), None, f, f, f, f, None, None) == 1
+
+
+def test_noalloc_scratch_boundary(lib):
+    """bsa_select_mask_noalloc holds 12 MiB of scratch.  At 32 query heads over 4 KV heads,
+    head_dim 128 and block 128 the largest layer it takes has 35072 tokens (274 blocks); the
+    next block count needs more and is refused with BSA_ERR_WORKSPACE before any launch."""
+    from block_sparse_long_kv_gb300 import _lib
+    limit = 12 << 20
+    fits = shp(seq=35072, hq=32, hkv=4, head_dim=128, block=128)
+    over = shp(seq=35072 + 128, hq=32, hkv=4, head_dim=128, block=128)
+    assert lib.bsa_select_workspace_bytes(ctypes.byref(fits)) <= limit
+    assert lib.bsa_select_workspace_bytes(ctypes.byref(over)) > limit
+    f = ctypes.c_void_p(FAKE)
+    for flags in (0, _lib.SELECT_TOKEN_MAX):
+        prm = _lib.SelectParams(0.1, 0.02, flags)
+        assert lib.bsa_select_mask_noalloc(ctypes.byref(over), ctypes.byref(prm), f, f, f, f, f, f,
+                                           None, None, None) == 4
+    # shape errors are reported as by bsa_select_mask
+    bad = shp(seq=1000)
+    prm = _lib.SelectParams(0.1, 0.02, 0)
+    assert lib.bsa_select_mask_noalloc(ctypes.byref(bad), ctypes.byref(prm), f, f, f, f, f, f,
+                                       None, None, None) == 2

@@ -202,6 +202,52 @@ def test_deterministic_and_layer_entry_point():
     np.testing.assert_array_equal(outs[0][2].cpu().numpy(), got["kv_cnt"])
 
 
+# ------------------------------------------------------------------ any block count
+
+@pytest.mark.parametrize("cfg", [
+    dict(batch=2, seq=9 * 128, hq=32, hkv=4, head_dim=128, block=128),   # nb = 9 (1152-token prompt)
+    dict(batch=1, seq=65 * 64, hq=32, hkv=4, head_dim=128, block=64),    # nb = 65 (4160 tokens)
+    dict(batch=1, seq=3 * 256, hq=8, hkv=2, head_dim=64, block=256),     # nb = 3
+    dict(batch=3, seq=2 * 128, hq=4, hkv=1, head_dim=128, block=128),    # nb = 2
+    dict(batch=2, seq=128, hq=4, hkv=2, head_dim=64, block=128),         # nb = 1
+])
+def test_block_counts_not_multiple_of_four(cfg):
+    """seq % block == 0 is the only shape rule: block counts that are not a multiple of 4 give
+    every mask row and every attention row of the oracle (oracle lists), the GPU's own lists on
+    the rows whose masks agree, per-token aggregation masks, and the whole-layer entry point."""
+    import block_sparse_long_kv_gb300 as bsa
+    w = synth.Workload("nb_any", cfg["batch"], cfg["seq"], cfg["hq"], cfg["hkv"], cfg["head_dim"],
+                       cfg["block"], 0.25, 0.1, seed_base=909, needles_fixed=1)
+    lay = synth.make_layer(w)
+    got, orc, _ = full_mask_parity(w, lay)
+    keep = oracle_keep(w, orc)
+    kv_idx, kv_cnt = upload_lists(keep)
+    o, lse = gpu_attention(w, lay, kv_idx, kv_cnt)
+    rows = [(b, h, i) for b in range(w.batch) for h in range(w.hq) for i in range(w.nb)]
+    check_attention_rows(w, lay, o, lse, keep != 0, rows)
+    o2, lse2 = gpu_attention(w, lay, torch.from_numpy(got["kv_idx"]).cuda(),
+                             torch.from_numpy(got["kv_cnt"]).cuda())
+    same = [(b, h, i) for (b, h, i) in rows
+            if np.array_equal(got["mask"][b, h // w.group, i], keep[b, h // w.group, i])]
+    assert len(same) >= len(rows) // 2
+    check_attention_rows(w, lay, o2, lse2, keep != 0, same)
+    token_parity(w, lay)
+    # the whole-layer call equals the three separate calls bit for bit
+    s = shape_of(w)
+    q, k, v = (to_dev(lay[x]) for x in ("q", "k", "v"))
+    ws = bsa.alloc_layer_workspace(s)
+    o3 = torch.empty_like(q)
+    lse3 = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsa.prefill_layer(s, bsa.SelectParams(w.centroid_keep, w.rescue_keep, 0), q, k, v,
+                      1 / math.sqrt(w.head_dim), o3, lse3, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(bsa.layer_views(s, ws)["kv_cnt"].cpu().numpy(), got["kv_cnt"])
+    np.testing.assert_array_equal(o3.float().cpu().numpy(), o2)
+    np.testing.assert_array_equal(lse3.cpu().numpy(), lse2)
+
+
 # ------------------------------------------------------------------ 128K, sampled rows
 
 def test_long_prefill_128k_sampled():

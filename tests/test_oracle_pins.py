@@ -456,3 +456,68 @@ def test_token_select_blocks_flag_and_permutation_invariance():
     # the per-token masks differ from the block-mean masks somewhere on this input
     m = O.select_blocks(q, k, blk, 0.3, 0.2)
     assert not np.array_equal(a["mask"], m["mask"])
+
+
+# ----------------------------------------------------------------- kept lists
+
+def _lists_bruteforce(mask):
+    """Kept lists by explicit enumeration: walk each row left to right and append every
+    block whose mask byte is nonzero."""
+    b, h, nq, nk = mask.shape
+    out = {}
+    for bi in range(b):
+        for g in range(h):
+            for i in range(nq):
+                row = []
+                for j in range(nk):
+                    if int(mask[bi, g, i, j]) != 0:
+                        row.append(j)
+                out[(bi, g, i)] = row
+    return out
+
+
+@pytest.mark.parametrize("nk, density", [(1, 0.5), (5, 0.3), (16, 0.0), (16, 1.0), (37, 0.2), (64, 0.7)])
+def test_kv_lists_match_enumeration(nk, density):
+    """oracle.kv_lists (the lists the GPU attention is fed in the parity tests) against a
+    brute-force enumeration: ascending kept blocks, count = number of nonzero mask bytes,
+    -1 after the count; empty and full rows; any combination of the mask bits counts."""
+    rng = np.random.default_rng(nk * 1000 + int(density * 100))
+    mask = np.zeros((2, 3, nk, nk), dtype=np.uint8)
+    keep = rng.random(mask.shape) < density
+    bits = rng.integers(1, 8, mask.shape).astype(np.uint8)   # any nonzero combination of bits
+    mask[keep] = bits[keep]
+    mask[0, 0, 0] = 0                                        # an empty row
+    mask[1, 2, nk - 1] = O.FORCED | O.CENTROID               # a full row
+    kv_idx, kv_cnt = O.kv_lists(mask)
+    assert kv_idx.shape == mask.shape and kv_idx.dtype == np.int32
+    assert kv_cnt.shape == mask.shape[:3] and kv_cnt.dtype == np.int32
+    ref = _lists_bruteforce(mask)
+    for (bi, g, i), row in ref.items():
+        c = int(kv_cnt[bi, g, i])
+        assert c == len(row)
+        assert list(kv_idx[bi, g, i, :c]) == row
+        assert all(kv_idx[bi, g, i, x] < kv_idx[bi, g, i, x + 1] for x in range(c - 1))
+        assert np.all(kv_idx[bi, g, i, c:] == -1)
+    assert kv_cnt[0, 0, 0] == 0 and np.all(kv_idx[0, 0, 0] == -1)
+    assert kv_cnt[1, 2, nk - 1] == nk and list(kv_idx[1, 2, nk - 1]) == list(range(nk))
+
+
+def test_kv_lists_of_a_selection_cover_sink_and_diagonal():
+    """On a real selection every row's list starts with block 0 and ends with the diagonal
+    block i, and its length equals forced + centroid + rescue blocks (disjoint paths)."""
+    w = synth.Workload("lists", 1, 1024, 4, 2, 32, 64, 0.25, 0.1, seed_base=5, needles_fixed=2)
+    lay = synth.make_layer(w)
+    q, k = synth.bf16_to_f64(lay["q"]), synth.bf16_to_f64(lay["k"])
+    res = O.select_blocks(q, k, w.block, w.centroid_keep, w.rescue_keep)
+    kv_idx, kv_cnt = O.kv_lists(res["mask"])
+    for g in range(w.hkv):
+        for i in range(w.nb):
+            c = kv_cnt[0, g, i]
+            row = kv_idx[0, g, i, :c]
+            assert row[0] == 0 and row[-1] == i
+            m = res["mask"][0, g, i]
+            nforced = 1 if i == 0 else 2
+            ncent = int(np.count_nonzero(m & O.CENTROID))
+            nresc = int(np.count_nonzero(m & O.RESCUE))
+            assert not np.any((m & O.CENTROID) & ((m & O.RESCUE) >> 1))
+            assert c == nforced + ncent + nresc

@@ -1,7 +1,8 @@
 """bsa_select_mask_noalloc: the selection entry point for callers that cannot
 allocate device memory (its scratch is a fixed array in the library's device
 image).  Its kept lists and masks must equal those of bsa_select_mask, which
-uses a caller-provided workspace, on two calls in a row.
+uses a caller-provided workspace, on two calls in a row, for both query
+aggregations (block mean and per-token maximum).
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test.
@@ -27,7 +28,7 @@ def lib():
     return _lib.load()
 
 
-def _noalloc_select(lib, w, lay):
+def _noalloc_select(lib, w, lay, flags=0):
     import block_sparse_long_kv_gb300 as bsa
     from block_sparse_long_kv_gb300 import _lib
     s = shape_of(w)
@@ -36,7 +37,7 @@ def _noalloc_select(lib, w, lay):
     sel = bsa.alloc_select(s, with_mask=True)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     bsa.block_meta(s, k, meta["centroid"], meta["radius"], meta["quant"], meta["alpha"], dev_status=st)
-    prm = _lib.SelectParams(w.centroid_keep, w.rescue_keep, 0)
+    prm = _lib.SelectParams(w.centroid_keep, w.rescue_keep, flags)
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     code = lib.bsa_select_mask_noalloc(
         ctypes.byref(s), ctypes.byref(prm), p(q), p(meta["centroid"]), p(meta["radius"]),
@@ -48,12 +49,13 @@ def _noalloc_select(lib, w, lay):
     return {x: v.cpu().numpy() for x, v in sel.items()}
 
 
-def test_noalloc_matches_workspace_entry_point_twice(lib):
+@pytest.mark.parametrize("flags", [0, 1])   # block-mean and per-token (BSA_SELECT_TOKEN_MAX) scores
+def test_noalloc_matches_workspace_entry_point_twice(lib, flags):
     w = synth.workload("gqa32x4_n32768_d128_b128")
     for layer in (0, 1):                     # two calls in a row, different inputs
         lay = synth.make_layer(w, layer=layer)
-        ref = gpu_mask_build(w, lay)         # bsa_select_mask with its own workspace
-        got = _noalloc_select(lib, w, lay)
+        ref = gpu_mask_build(w, lay, flags=flags)  # bsa_select_mask with its own workspace
+        got = _noalloc_select(lib, w, lay, flags)
         np.testing.assert_array_equal(got["kv_cnt"], ref["kv_cnt"])
         np.testing.assert_array_equal(got["mask"], ref["mask"])
         for b in range(w.batch):
