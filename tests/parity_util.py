@@ -135,6 +135,27 @@ def oracle_rows(w, lay, rows_by_bg, centroid_keep=None, rescue_keep=None, token_
     return dict(rows=rows, centroid=centroid, radius=radius, med=med, p90=p90, alpha=alpha)
 
 
+def check_meta(w, lay, got, orc):
+    """Block summaries within 1e-5 relative of the oracle; quantiles at the oracle's rank (up to
+    near-ties within 1e-4); alpha within 1e-3."""
+    cen = got["centroid"]                                 # [b, hkv, nb, d]
+    scale = np.abs(orc["centroid"]).max()
+    assert np.abs(cen - orc["centroid"]).max() <= 1e-5 * max(scale, 1.0)
+    np.testing.assert_allclose(got["radius"], orc["radius"], rtol=1e-5)
+    # quantiles: the GPU picks the block the oracle's rank names (up to near-ties)
+    nb = w.nb
+    for b in range(w.batch):
+        for g in range(w.hkv):
+            order = np.lexsort((np.arange(nb), orc["radius"][b, g]))
+            for qi, rank in ((0, O.nearest_rank(nb, 1, 2)), (1, O.nearest_rank(nb, 9, 10))):
+                want = got["radius"][b, g, order[rank - 1]]
+                if got["quant"][b, g, qi] != want:
+                    ref = orc["radius"][b, g, order[rank - 1]]
+                    near = np.abs(orc["radius"][b, g] - ref) <= 1e-4 * ref
+                    assert near.sum() > 1, ("quantile rank differs", b, g, qi)
+    assert np.abs(got["alpha"] - orc["alpha"]).max() <= 1e-3
+
+
 def compare_mask_rows(gpu_mask, orc, label=""):
     """Apply the protocol; returns (n_compared_blocks, n_excused).  Raises on an unexcused mismatch.
     Every call is recorded in EXCUSE_LOG (with ``label`` naming the layer or case)."""
