@@ -372,28 +372,34 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
       if (!(ok = wait_bar(bar(C::B_SF + t), n & 1, ctl))) break;
       ptx::tc_fence_after();
       uint32_t sr[C::CW];
+      float pm[C::CW / 32];  // the max of each 32 loaded columns, from the load itself
 #pragma unroll
       for (int c = 0; c < C::CW / 32; ++c)
-        ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        ptx::tmem_ld32_max(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]), pm[c]);
       ptx::tmem_wait_ld();
+      float mx;
       if (!half || ktok0 + C::CW - 1 > qtok0) {
         // columns that overlap the diagonal: key ktok0 + c is visible iff ktok0 + c <= qtok;
-        // an empty half masks every column
+        // an empty half masks every column.  The loaded maxima include the masked columns,
+        // so the max is taken again over the visible ones (one tile per row at most)
         const int lim = half ? qtok - ktok0 : -1;
 #pragma unroll
         for (int c = 0; c < C::CW; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
+#pragma unroll
+        for (int c = 8; c < C::CW; c += 8)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
+        mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      } else {
+        mx = pm[0];
+#pragma unroll
+        for (int c = 1; c < C::CW / 32; ++c) mx = fmaxf(mx, pm[c]);
       }
-      // row max as a tree of eight independent chains
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
-#pragma unroll
-      for (int c = 8; c < C::CW; c += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // the row max of both halves: each half's partial max rounded up to bf16 (any upper
       // bound of the row max is a valid reference, and both halves then hold the same
       // value).  The slot is rewritten only after the partner has arrived on P ready, which
@@ -413,21 +419,30 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         }
       };
       float rs4[4];
-      // P = 2^(s * scale - mb) as bf16 pairs into TMEM over S, with the row sums
+      // P = 2^(s * scale - mb) as bf16 pairs into TMEM over S, with the row sums.  Column
+      // pairs go through packed fp32 FMAs and adds (one instruction per pair, each element
+      // rounded as the scalar operation would be), the sums in four partial chains.
       auto exps = [&](float mb) {
-        rs4[0] = rs4[1] = rs4[2] = rs4[3] = 0.f;
+        uint64_t acc[2] = {0ull, 0ull};  // (+0.0f, +0.0f) pairs
+        const uint64_t scl = ptx::f32x2(sl2, sl2), neg = ptx::f32x2(-mb, -mb);
 #pragma unroll
         for (int c16 = 0; c16 < C::CW / 32; ++c16) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e]), sl2, -mb));
-            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c16 * 32 + 2 * e + 1]), sl2, -mb));
-            rs4[e & 3] += p0 + p1;
+            const uint64_t x = ptx::fma_f32x2(
+                ptx::f32x2(__uint_as_float(sr[c16 * 32 + 2 * e]), __uint_as_float(sr[c16 * 32 + 2 * e + 1])),
+                scl, neg);
+            float x0, x1;
+            ptx::f32x2_split(x, x0, x1);
+            const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+            acc[e & 1] = ptx::add_f32x2(acc[e & 1], ptx::f32x2(p0, p1));
             pk[e] = ptx::pack_bf16x2(p0, p1);
           }
           ptx::tmem_st16(tP + c16 * 16, pk);
         }
+        ptx::f32x2_split(acc[0], rs4[0], rs4[1]);
+        ptx::f32x2_split(acc[1], rs4[2], rs4[3]);
       };
       float factor = 1.f;
       bool resc = false;
