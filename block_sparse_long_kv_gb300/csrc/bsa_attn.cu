@@ -101,6 +101,10 @@ struct Cfg {
   static constexpr int CH = KT == 128 ? 2 : 1;
   static constexpr int CW = KT / CH;                 // S columns per softmax thread
   static constexpr uint32_t RED_BYTES = NT * CH * 128 * 2;  // bf16 partial maxima
+  // A softmax thread releases its P columns to the P V MMAs in NCHK chunks of 32 S columns
+  // (16 key rows of V per MMA, two MMAs per chunk and column half), so the tensor core
+  // starts on the first chunk while the second is still being exponentiated.
+  static constexpr int NCHK = CW / 32;
   static constexpr int KS = 2;  // K stages: K(n+KS) only needs S(n) done
   // V stages: V(n+VS) needs PV_1(n) done, which comes late; use 3 when they fit
   static constexpr int VS =
@@ -113,9 +117,10 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + NT * Q_TILE;
   static constexpr uint32_t OFF_V = OFF_K + KS * K_TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_TILE;
-  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT], O done[NT], final drain
+  // barriers: Q, K full/empty, V full/empty, S full[NT], P ready[NT][NCHK], O done[NT],
+  // final drain
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
-                       B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT, B_FIN = B_OD + NT,
+                       B_SF = B_VE + VS, B_PR = B_SF + NT, B_OD = B_PR + NT * NCHK, B_FIN = B_OD + NT,
                        NBARS = B_FIN + 1;
   static constexpr uint32_t OFF_RED = (OFF_BAR + NBARS * 8 + 16 + 15) / 16 * 16;
   static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;  // + 1 KB alignment slack
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int x = 0; x < C::NBARS; ++x) {
       uint32_t count = 1;
-      if (x >= C::B_PR && x < C::B_PR + NT) count = 4 * C::CH;  // one arrive per softmax warp
+      if (x >= C::B_PR && x < C::B_PR + NT * C::NCHK) count = 4 * C::CH;  // one arrive per softmax warp
       ptx::mbar_init(bar(x), count);
     }
     *abort_flag = 0;
@@ -211,12 +216,15 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
       ptx::tma_prefetch_desc(&tm_q);
       ptx::tma_prefetch_desc(&tm_k);
       ptx::tma_prefetch_desc(&tm_v);
+      // L2 priorities: every Q tile is read by one CTA only, while the CTAs running at the
+      // same time re-read one KV head's K and V tiles, so Q goes first and K / V stay
+      const uint64_t once = ptx::l2_policy_evict_first(), keep = ptx::l2_policy_evict_last();
       ptx::mbar_arrive_expect_tx(bar(C::B_Q), NT * C::Q_TILE);
       for (int t = 0; t < NT; ++t) {
         const int h0 = g * p.group + (hp * NT + t) * C::QH;
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_4d(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * C::CE, h0,
-                           sp.start + qtok0, 0);
+          ptx::tma_load_4d_hint(sQ + t * C::Q_TILE + c * C::Q_CHUNK, &tm_q, bar(C::B_Q), c * C::CE, h0,
+                                sp.start + qtok0, 0, once);
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were issued
       // first key token of each TMA box of tile n: one box of 128 keys, or (pairs) two
@@ -239,16 +247,16 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         ptx::mbar_arrive_expect_tx(bar(C::B_KF + ks), C::K_TILE);
         for (int x = 0; x < NBOX; ++x)
           for (int c = 0; c < C::NCH; ++c)
-            ptx::tma_load_4d(sK + ks * C::K_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_k,
-                             bar(C::B_KF + ks), c * C::CE, g, kt0[x], 0);
+            ptx::tma_load_4d_hint(sK + ks * C::K_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_k,
+                                  bar(C::B_KF + ks), c * C::CE, g, kt0[x], 0, keep);
         k_issued = n + 1;
         const int vs = n % C::VS, vu = n / C::VS;
         if (vu > 0 && !wait_bar(bar(C::B_VE + vs), (vu - 1) & 1, ctl)) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_VF + vs), C::KV_TILE);
         for (int x = 0; x < NBOX; ++x)
           for (int c = 0; c < C::NCHV; ++c)
-            ptx::tma_load_4d(sV + vs * C::KV_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_v,
-                             bar(C::B_VF + vs), c * 64, g, kt0[x], 0);
+            ptx::tma_load_4d_hint(sV + vs * C::KV_TILE + c * C::KV_CHUNK + x * BOX_ROWS_BYTES, &tm_v,
+                                  bar(C::B_VF + vs), c * 64, g, kt0[x], 0, keep);
         v_issued = n + 1;
       }
       if (*abort_flag) {
@@ -282,13 +290,27 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         }
         ptx::mma_commit(bar(C::B_SF + t));
       };
-      auto issue_pv = [&](int t, int vs, int n) {
+      // O_t += P_t V over the key rows of P chunk c: in every column half hf the 32 keys
+      // hf * CW + 32 c .. + 31, two MMAs of 16 keys each; the first MMA of a tile's first
+      // chunk overwrites O (n == 0) or accumulates into it.  Returns false if a wait gave up.
+      auto issue_pv = [&](int t, int vs, int n) -> bool {
         const uint64_t dv = dv0 + static_cast<uint64_t>(vs) * (C::KV_TILE >> 4);
         const uint32_t dst = tmem + C::TM_O + t * D, src = tmem + t * C::KT;
 #pragma unroll
-        for (int kk = 0; kk < C::KT / 16; ++kk)
-          ptx::mma_ts(dst, src + kk * 8, dv + ((kk * 2048) >> 4), C::IDESC_O, (n > 0 || kk > 0) ? 1u : 0u);
+        for (int c = 0; c < C::NCHK; ++c) {
+          if (!wait_bar(bar(C::B_PR + t * C::NCHK + c), n & 1, ctl)) return false;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int hf = 0; hf < C::CH; ++hf)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kk = (hf * C::CW + c * 32) / 16 + e;  // 16 keys of V per MMA
+              ptx::mma_ts(dst, src + kk * 8, dv + ((kk * 2048) >> 4), C::IDESC_O,
+                          (n > 0 || c > 0 || hf > 0 || e > 0) ? 1u : 0u);
+            }
+        }
         ptx::mma_commit(bar(C::B_OD + t));
+        return true;
       };
       bool ok = wait_bar(bar(C::B_Q), 0, ctl);
       ptx::tc_fence_after();
@@ -304,9 +326,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
           if (n > 0) {
             // PV_1(n-1) overlaps softmax_0(n); S_1(n) follows it in issue order
             const int pv = n - 1, vs = pv % C::VS;
-            if (!(ok = wait_bar(bar(C::B_PR + 1), pv & 1, ctl))) break;
-            ptx::tc_fence_after();
-            issue_pv(1, vs, pv);
+            if (!(ok = issue_pv(1, vs, pv))) break;
             ptx::mma_commit(bar(C::B_VE + vs));
           }
           issue_s(1, ks);
@@ -314,19 +334,13 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         ptx::mma_commit(bar(C::B_KE + ks));
         const int vs = n % C::VS;
         if (!(ok = wait_bar(bar(C::B_VF + vs), (n / C::VS) & 1, ctl))) break;
-        if (!(ok = wait_bar(bar(C::B_PR + 0), n & 1, ctl))) break;
-        ptx::tc_fence_after();
-        issue_pv(0, vs, n);
+        if (!(ok = issue_pv(0, vs, n))) break;
         if constexpr (NT == 1) ptx::mma_commit(bar(C::B_VE + vs));
       }
       if constexpr (NT == 2) {
         if (ok) {
           const int pv = T - 1, vs = pv % C::VS;
-          if ((ok = wait_bar(bar(C::B_PR + 1), pv & 1, ctl))) {
-            ptx::tc_fence_after();
-            issue_pv(1, vs, pv);
-            ptx::mma_commit(bar(C::B_VE + vs));
-          }
+          if ((ok = issue_pv(1, vs, pv))) ptx::mma_commit(bar(C::B_VE + vs));
         }
       }
       if (!ok) {
@@ -418,76 +432,64 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
           return part;
         }
       };
-      float rs4[4];
-      // P = 2^(s * scale - mb) as bf16 pairs into TMEM over S, with the row sums.  Column
-      // pairs go through packed fp32 FMAs and adds (one instruction per pair, each element
-      // rounded as the scalar operation would be), the sums in four partial chains.
-      auto exps = [&](float mb) {
-        uint64_t acc[2] = {0ull, 0ull};  // (+0.0f, +0.0f) pairs
-        const uint64_t scl = ptx::f32x2(sl2, sl2), neg = ptx::f32x2(-mb, -mb);
-#pragma unroll
-        for (int c16 = 0; c16 < C::CW / 32; ++c16) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const uint64_t x = ptx::fma_f32x2(
-                ptx::f32x2(__uint_as_float(sr[c16 * 32 + 2 * e]), __uint_as_float(sr[c16 * 32 + 2 * e + 1])),
-                scl, neg);
-            float x0, x1;
-            ptx::f32x2_split(x, x0, x1);
-            const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
-            acc[e & 1] = ptx::add_f32x2(acc[e & 1], ptx::f32x2(p0, p1));
-            pk[e] = ptx::pack_bf16x2(p0, p1);
-          }
-          ptx::tmem_st16(tP + c16 * 16, pk);
-        }
-        ptx::f32x2_split(acc[0], rs4[0], rs4[1]);
-        ptx::f32x2_split(acc[1], rs4[2], rs4[3]);
-      };
+      // the running max moves only when the tile's row max exceeds it by more than 2^8
+      // (exact: O and the normaliser share whatever reference is used); the first tile
+      // always takes its own.  The decision is the same in both halves of a row (same m,
+      // same exchanged max); the O rescale is warp-wide since TMEM accesses are
+      // warp-collective, and lanes that keep their max scale by 1.
+      const float mt = row_max(mx) * sl2;
       float factor = 1.f;
       bool resc = false;
-      if (n == 0) {  // the same branch for every row of the CTA (the named barriers pair warps)
-        // no running max yet: take this tile's first
-        const float mt = row_max(mx) * sl2;
-        if (mt > m + 8.f) {
-          factor = 0.f;
-          m = mt;
-        }
-        exps(m == -INFINITY ? 0.f : m);
-      } else {
-        // the exponentials with the running max go first; the row max is settled while
-        // they run, and only a max that grew by more than 2^8 redoes them (rare).  The
-        // decision is per row (the same in both halves: same m, same exchanged max); the
-        // redo is warp-wide, since the TMEM stores are warp-collective, and a row that
-        // keeps its max recomputes the same P
-        exps(m == -INFINITY ? 0.f : m);  // (no max yet only after fully masked tiles)
-        const float mt = row_max(mx) * sl2;
-        if (mt > m + 8.f) {
-          factor = m == -INFINITY ? 0.f : ptx::ex2_approx(m - mt);
-          resc = true;
-          m = mt;
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-          ptx::tmem_wait_st();  // the first P stores land before they are overwritten
-          exps(m == -INFINITY ? 0.f : m);
-        }
+      if (mt > m + 8.f) {
+        factor = m == -INFINITY ? 0.f : ptx::ex2_approx(m - mt);
+        resc = m != -INFINITY;  // O holds partial sums only once a finite max was taken
+        m = mt;
       }
+      // P = 2^(s * scale - m) as bf16 pairs into TMEM over S, with the row sums.  Column
+      // pairs go through packed fp32 FMAs and adds (one instruction per pair, each element
+      // rounded as the scalar operation would be), the sums in four partial chains.  Each
+      // chunk of 32 columns is released to the P V MMAs as soon as its stores (and, in the
+      // first chunk, any O rescale) have landed.  The rescale follows the first chunk's
+      // stores, when that chunk's S registers are free again.
+      const float mb = m == -INFINITY ? 0.f : m;  // (no max yet only after fully masked tiles)
+      uint64_t acc[2] = {0ull, 0ull};             // (+0.0f, +0.0f) pairs
+      const uint64_t scl = ptx::f32x2(sl2, sl2), neg = ptx::f32x2(-mb, -mb);
+#pragma unroll
+      for (int c16 = 0; c16 < C::NCHK; ++c16) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t x = ptx::fma_f32x2(
+              ptx::f32x2(__uint_as_float(sr[c16 * 32 + 2 * e]), __uint_as_float(sr[c16 * 32 + 2 * e + 1])),
+              scl, neg);
+          float x0, x1;
+          ptx::f32x2_split(x, x0, x1);
+          const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+          acc[e & 1] = ptx::add_f32x2(acc[e & 1], ptx::f32x2(p0, p1));
+          pk[e] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16(tP + c16 * 16, pk);
+        if (c16 == 0 && __any_sync(0xffffffffu, resc)) {
+          // eight columns at a time: the second chunk's S values are still live
+#pragma unroll 1
+          for (int c = 0; c < OD_COLS / 8; ++c) {
+            uint32_t ov[8];
+            ptx::tmem_ld8(tO + c * 8, ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+            ptx::tmem_st8(tO + c * 8, ov);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(C::B_PR + t * C::NCHK + c16));
+      }
+      float rs4[4];
+      ptx::f32x2_split(acc[0], rs4[0], rs4[1]);
+      ptx::f32x2_split(acc[1], rs4[2], rs4[3]);
       l = l * factor + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-      if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-        for (int c = 0; c < OD_COLS / 32; ++c) {
-          uint32_t ov[32];
-          ptx::tmem_ld32(tO + c * 32, ov);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-          ptx::tmem_st32(tO + c * 32, ov);
-        }
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::B_PR + t));
     }
 
     if (ok && T > 0) ok = wait_bar(bar(C::B_OD + t), (T - 1) & 1, ctl);
@@ -502,6 +504,7 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
     }
     const float inv = (ok && l > 0.f) ? p.v_scale / l : 0.f;
     const bool row_valid = qtok < sp.len;  // a partial last block's tile rows past the sequence end
+    const uint64_t o_policy = ptx::l2_policy_evict_first();
     uint16_t *orow = p.o + ((static_cast<size_t>(sp.start) + qtok) * p.hq + head) * D + hf * OD_COLS;
 #pragma unroll
     for (int c = 0; c < OD_COLS / 32; ++c) {
@@ -520,7 +523,9 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
       uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
       if (row_valid) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v)  // O is written once: it leaves L2 first
+          ptx::st_global_v4_hint(dst + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]),
+                                 o_policy);
       }
     }
     if (p.lse != nullptr && hf == 0 && row_valid) {
