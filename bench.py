@@ -39,7 +39,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa32x4_n131072_d128_b128")
-    ap.add_argument("--layers", type=int, default=2, help="distinct seeded layers rotated per step")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="distinct seeded layers resident and rotated per step (default: every seeded "
+                         "layer of the workload, 48 for the 128K one; 2 for the e4m3 and packed modes)")
     ap.add_argument("--e2e-steps", type=int, default=48,
                     help="layers streamed end to end (48: one pass over the 128K configuration's layers)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
@@ -251,6 +253,32 @@ def oracle_sample(w, lay, budget_s: float, rng_seed: int = 0):
                       f"extrapolated to the whole layer by block count, row count and kept FLOPs"}
 
 
+def host_placement(index: int) -> dict:
+    """Where the pinned host buffers sit relative to the GPU: the host's NUMA nodes, the GPU's
+    NUMA node (from its PCI device), transparent huge pages, and how the buffers were made."""
+    out = {"pinned_alloc": "torch pin_memory (cudaHostAlloc), allocated before the layers are drawn"}
+    try:
+        out["numa_nodes"] = len([d for d in os.listdir("/sys/devices/system/node") if d.startswith("node")])
+    except OSError:
+        pass
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{dom[-4:].lower()}:{rest.lower()}/numa_node"
+        with open(path) as f:
+            out["gpu_numa_node"] = int(f.read().strip())
+        out["gpu_pci"] = bus
+    except Exception:
+        pass
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/enabled") as f:
+            out["thp"] = f.read().strip()
+    except OSError:
+        pass
+    return out
+
+
 def threads_used():
     try:
         from threadpoolctl import threadpool_info
@@ -309,25 +337,33 @@ def run_reference(args):
                "head_dim": w.head_dim, "block": w.block, "centroid_keep": w.centroid_keep,
                "rescue_keep": w.rescue_keep}
         extra = ""
+    # each step times the oracle on a bounded sample of the layer (a few seconds of CPU work),
+    # so the whole run stays within minutes; the per-layer value is extrapolated from the sample
     per_step = max(3.0, min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup)))
-    est = []
+    est, wall = [], []
     for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         r = oracle_sample(w, lay, per_step, rng_seed=s)
         if s >= args.warmup:
             est.append(r)
+            wall.append(time.perf_counter() - t0)
     ms = [1e3 * (factor * (r["t_meta"] + r["t_sel"]) + r["t_att_per_flop"] * fl) for r in est]
     val = float(np.median(ms))
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "ms/layer",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": val, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "extrapolated": True,
+        "n_gpus": args.gpus, "steps": len(est), "warmup": args.warmup,
+        "ms_per_step": float(1e3 * np.mean(wall)), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded generator, same workload)",
         "config": cfg,
         "cpu_baseline": {"value": val, "unit": "ms/layer", "cores": threads_used(),
                          "kind": "oracle", "sample": est[0]["sample"] + extra},
         "e2e": {"value": val, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "fp64 numpy oracle timed on a bounded sample per step, extrapolated (upper bound of "
-                "keep counts used for the FLOP scale)",
+        "note": "fp64 numpy oracle: each timed step is one bounded sample of the layer "
+                "(ms_per_step is that sample's wall time); value extrapolates the samples to a whole "
+                "layer by block count, row count and kept FLOPs (upper bound of keep counts for the "
+                "FLOP scale)",
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -382,6 +418,17 @@ class FixedRunner:
     def upload(self, lay):
         up = lambda x: self.torch.from_numpy(lay[x].view(np.int16)).to(self.dev).view(self.torch.bfloat16)
         return {x: up(x) for x in ("q", "k", "v")}
+
+    def host_shapes(self):
+        """Shape and dtype of the host-side q, k, v and o of one step."""
+        w = self.w
+        return {"q": ((w.batch, w.seq, w.hq, w.head_dim), self.torch.bfloat16),
+                "k": ((w.batch, w.seq, w.hkv, w.head_dim), self.torch.bfloat16),
+                "v": ((w.batch, w.seq, w.hkv, w.head_dim), self.torch.bfloat16),
+                "o": ((w.batch, w.seq, w.hq, w.head_dim), self.torch.bfloat16)}
+
+    def to_host(self, lay, x):
+        return self.torch.from_numpy(lay[x].view(np.int16)).view(self.torch.bfloat16)
 
     def meta_call(self, L, status):
         m = self.meta
@@ -439,6 +486,13 @@ class Fp8Runner(FixedRunner):
         L["scales"] = lay["scales"]
         return L
 
+    def host_shapes(self):
+        shp = super().host_shapes()
+        return {x: (v[0], self.torch.uint8 if x != "o" else v[1]) for x, v in shp.items()}
+
+    def to_host(self, lay, x):
+        return self.torch.from_numpy(lay[x])
+
     def meta_call(self, L, status):
         m = self.meta
         self.bsa.block_meta_fp8(self.s, L["k"], L["scales"]["k"], m["centroid"], m["radius"], m["quant"],
@@ -486,6 +540,13 @@ class VarlenRunner(FixedRunner):
 
     def make_layer(self, synth, layer):
         return synth.make_varlen_layer(self.w, layer=layer)
+
+    def host_shapes(self):
+        vw = self.w
+        return {"q": ((vw.total, vw.hq, vw.head_dim), self.torch.bfloat16),
+                "k": ((vw.total, vw.hkv, vw.head_dim), self.torch.bfloat16),
+                "v": ((vw.total, vw.hkv, vw.head_dim), self.torch.bfloat16),
+                "o": ((vw.total, vw.hq, vw.head_dim), self.torch.bfloat16)}
 
     def meta_call(self, L, status):
         m = self.meta
@@ -567,14 +628,36 @@ def run_ours(args):
     else:
         run = FixedRunner(bsa, torch, synth.workload(args.workload), dev, flags)
     w = run.w
+    n_layers = args.layers or (w.layers if type(run) is FixedRunner else 2)
 
-    # resident inputs: `layers` distinct seeded layers per rank (replicas process their own layers)
+    # pinned host buffers of the end-to-end leg come first, while the host's free memory is
+    # still in long contiguous runs: the layers drawn below leave it fragmented, and a pinned
+    # buffer made of scattered small pages copies markedly slower over the host link
+    NBUF = 3
+    e2e_host = None
+    if not args.no_e2e:
+        shp = run.host_shapes()
+        e2e_host = {"in": [{x: torch.empty(shp[x][0], dtype=shp[x][1], pin_memory=True) for x in ("q", "k", "v")}
+                           for _ in range(2)],
+                    "o": [torch.empty(shp["o"][0], dtype=shp["o"][1], pin_memory=True) for _ in range(NBUF)]}
+
+    # resident inputs: `n_layers` distinct seeded layers per rank (replicas process their own
+    # layers), drawn in worker processes when there are many; host copies are kept for two
     host_layers = []
     dev_layers = []
-    for li in replica_layers(rank, args.layers):
-        lay = run.make_layer(synth, li)
-        host_layers.append(lay)
-        dev_layers.append(run.upload(lay))
+    ids = replica_layers(rank, n_layers)
+    if type(run) is FixedRunner and n_layers > 2:
+        from synth import parallel
+        for _, arrays, needles in parallel.layers(w, ids):
+            dev_layers.append(run.upload(arrays))
+            if len(host_layers) < 2:
+                host_layers.append({**{x: np.array(arrays[x]) for x in ("q", "k", "v")}, "needles": needles})
+            del arrays
+    else:
+        for li in ids:
+            lay = run.make_layer(synth, li)
+            host_layers.append(lay)
+            dev_layers.append(run.upload(lay))
     o = torch.empty(dev_layers[0]["q"].shape, dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -658,7 +741,8 @@ def run_ours(args):
     cfg = run.config()
     cfg.update({"aggregation": "token_max" if args.token_max else "block_mean",
                 "inputs": "e4m3 + per-tensor scales" if args.fp8 else "bf16",
-                "layers_rotated": args.layers,
+                "layers_rotated": n_layers,
+                "layers_timed": min(K, n_layers),
                 "l2": f"inputs larger than L2 (Q alone is {q_gb:.2f} GB per layer), layers rotated"})
     result = {
         "metric": METRIC, "value": ms_per_layer, "unit": "ms/layer", "n_gpus": world,
@@ -671,6 +755,7 @@ def run_ours(args):
         "mask_build_ms": float(mask_ms.mean()),
         "mask_build_gbs": mask_gbs,
         "density": float(np.mean(density)),
+        "density_range": [float(np.min(density)), float(np.max(density))],
         "roofline": {"kernel": "attn_kernel (bsa_prefill_fwd)", "bound": "tensor",
                      "achieved": kept_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": kept_tflops / bf16_peak if bf16_peak else None,
@@ -716,18 +801,14 @@ def run_ours(args):
     if not args.no_e2e:
         run.e2e_setup()
         n_e2e = max(1, args.e2e_steps)
-        pinned = []
+        pinned = e2e_host["in"]
         for x in range(2):
             hl = host_layers[x % len(host_layers)]
-            if hl["q"].dtype == np.uint8:          # e4m3 codes
-                pinned.append({n: torch.from_numpy(hl[n]).pin_memory() for n in ("q", "k", "v")})
-            else:
-                pinned.append({n: torch.from_numpy(hl[n].view(np.int16)).view(torch.bfloat16).pin_memory()
-                               for n in ("q", "k", "v")})
+            for n in ("q", "k", "v"):
+                pinned[x][n].copy_(run.to_host(hl, n))
         # three device buffer sets: a step's inputs are requested two steps ahead, so one slow
         # host copy does not hold up the compute
-        NBUF = 3
-        o_host = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
+        o_host = e2e_host["o"]
         dbuf = [{n: (torch.empty_like(o) if n == "o" else torch.empty_like(dev_layers[0][n]))
                  for n in ("q", "k", "v", "o")} for _ in range(NBUF)]
         h2d_s = torch.cuda.Stream(dev)
@@ -814,6 +895,7 @@ def run_ours(args):
             result["e2e"]["step_ms_median_last_quarter"] = float(np.median(e2e_steps_ms[-q4:]))
             result["e2e"]["step_ms_mean"] = float(np.mean(e2e_steps_ms))
             result["e2e"]["step_ms_max"] = float(np.max(e2e_steps_ms))
+        result["e2e"]["host"] = host_placement(local)
         result["e2e"]["copies_alone_gbs"] = {
             "h2d": copy_rate(h2d_only, h2d),
             "d2h": copy_rate(lambda: o_host[0].copy_(dbuf[0]["o"], non_blocking=True), o_host[0].numel() * 2)}

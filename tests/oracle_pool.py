@@ -5,71 +5,18 @@ block 128) names 48 independently seeded layers.  Generating one layer and build
 oracle masks takes seconds of single-core numpy, so the layers are spread over worker
 processes.  Each worker generates its layer, leaves q, k and v in shared memory (files on
 the /dev/shm tmpfs) for the GPU side (which then never generates the layer itself), and returns the oracle's whole-layer
-mask rows plus the oracle attention of sampled rows.  The pool starts with ``spawn``: the
-pytest process has already initialised CUDA, and a forked child of it would hang.  Workers
-run numpy with one BLAS thread each.
+mask rows plus the oracle attention of sampled rows.  The pool and the shared-memory helpers
+are those of synth.parallel (spawn start: the pytest process has already initialised CUDA, and
+a forked child of it would hang; one BLAS thread per worker).
 """
 from __future__ import annotations
 
 import os
-import uuid
-from collections import deque
-from contextlib import contextmanager
-from multiprocessing import get_context
 
 import numpy as np
 
-
-def worker_count() -> int:
-    return max(1, min(8, (os.cpu_count() or 2) - 1))
-
-
-@contextmanager
-def pool(n: int | None = None):
-    """A spawn pool whose workers use one BLAS thread each."""
-    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
-    saved = {k: os.environ.get(k) for k in keys}
-    for k in keys:
-        os.environ[k] = "1"
-    try:
-        p = get_context("spawn").Pool(n or worker_count())
-    finally:
-        for k, v in saved.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-    try:
-        yield p
-    finally:
-        p.terminate()
-        p.join()
-        sweep()
-
-
-# ---------------------------------------------------------------- shared arrays
-#
-# Plain memory-mapped files under /dev/shm (tmpfs): any process opens one by name, and
-# nothing tracks them but the name prefix of the process that consumes them.
-
-SHM_DIR = "/dev/shm"
-
-
-def _prefix(owner_pid: int) -> str:
-    return f"bsaorc{owner_pid}_"
-
-
-def to_shared(arr: np.ndarray, owner_pid: int | None = None):
-    """Copy arr into a new shared file named after the process that will consume it (the
-    pool's parent by default, so ``sweep`` can remove whatever a failure left behind);
-    returns a picklable handle."""
-    owner = os.getppid() if owner_pid is None else owner_pid
-    path = os.path.join(SHM_DIR, _prefix(owner) + uuid.uuid4().hex[:16])
-    mm = np.lib.format.open_memmap(path, mode="w+", dtype=arr.dtype, shape=arr.shape)
-    mm[...] = arr
-    mm.flush()
-    del mm
-    return path
+from synth.parallel import (JOB_TIMEOUT_S, attach, bounded_imap, discard, pool, sweep,  # noqa: F401
+                            threads_per_worker, to_shared, worker_count)
 
 
 class Shared:
@@ -77,28 +24,12 @@ class Shared:
 
     def __init__(self, handle):
         self.path = handle
-        self.a = np.load(handle, mmap_mode="r+")  # writable view: torch.from_numpy takes it without a warning
+        self.a = attach(handle)
 
     def release(self, unlink: bool = False):
         self.a = None
         if unlink:
             discard(self.path)
-
-
-def sweep() -> None:
-    """Remove every shared file made for this process that is still there (after a failure
-    the results still queued in the pool hold files nobody will consume)."""
-    import glob
-    for f in glob.glob(os.path.join(SHM_DIR, _prefix(os.getpid()) + "*")):
-        discard(f)
-
-
-def discard(handle) -> None:
-    """Remove a shared file if it still exists."""
-    try:
-        os.unlink(handle)
-    except FileNotFoundError:
-        pass
 
 
 # ---------------------------------------------------------------- jobs (run in workers)
@@ -132,7 +63,7 @@ def layer_job(wname: str, layer: int, att_blocks: int, seed: int):
     from parity_util import oracle_rows
 
     w = synth.workload(wname)
-    lay = synth.make_layer(w, layer=layer, threads=max(1, (os.cpu_count() or 1) // worker_count()))
+    lay = synth.make_layer(w, layer=layer, threads=threads_per_worker(worker_count()))
     handles = {x: to_shared(lay[x]) for x in ("q", "k", "v")}
     orc = oracle_rows(w, lay, {(b, g): list(range(w.nb)) for b in range(w.batch) for g in range(w.hkv)})
     keep = np.zeros((w.batch, w.hkv, w.nb, w.nb), dtype=np.uint8)
@@ -173,20 +104,3 @@ def attention_rows_job(wname: str, handles: dict, keep: np.ndarray, rows):
     finally:
         for s in sh.values():
             s.release()
-
-
-def bounded_imap(p, fn, arg_list, ahead: int):
-    """Results of fn(*args) in order, with at most ``ahead`` jobs submitted but unconsumed
-    (each layer job holds about 1.3 GB of shared memory until its result is consumed)."""
-    pending = deque()
-    it = iter(arg_list)
-    for args in it:
-        pending.append(p.apply_async(fn, args))
-        if len(pending) >= ahead:
-            break
-    while pending:
-        r = pending.popleft().get()
-        for args in it:
-            pending.append(p.apply_async(fn, args))
-            break
-        yield r

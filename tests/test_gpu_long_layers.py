@@ -118,7 +118,7 @@ def test_layer0_every_attention_row():
     w = synth.workload(W)
     nw = P.worker_count()
     with P.pool(nw) as pool:
-        r = pool.apply(P.layer_job, (W, 0, 0, SEED))
+        r = pool.apply_async(P.layer_job, (W, 0, 0, SEED)).get(P.JOB_TIMEOUT_S)
         handles = dict(r["handles"])
         sh = {x: P.Shared(h) for x, h in handles.items()}
         try:
@@ -147,7 +147,7 @@ def test_layer0_every_attention_row():
                 for part in range(4):
                     rows = [(0, h, i) for i in range(part, w.nb, 4)]
                     jobs.append((W, handles, keep, rows))
-            res = pool.starmap(P.attention_rows_job, jobs)
+            res = pool.starmap_async(P.attention_rows_job, jobs).get(P.JOB_TIMEOUT_S)
         finally:
             for s in sh.values():
                 s.release(unlink=True)
