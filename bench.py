@@ -399,7 +399,8 @@ def token_score_flops(run) -> float:
 
 
 class FixedRunner:
-    """One fixed-length layer per step: bsa_block_meta, bsa_select_mask, bsa_prefill_fwd."""
+    """One fixed-length layer per step: bsa_mask_build (block-mean queries; bsa_block_meta and
+    bsa_select_mask with per-token aggregation), then bsa_prefill_fwd."""
 
     def __init__(self, bsa, torch, w, dev, flags=0):
         self.bsa, self.torch, self.w, self.dev = bsa, torch, w, dev
@@ -408,7 +409,9 @@ class FixedRunner:
         self.scale = 1.0 / math.sqrt(w.head_dim)
         self.meta = bsa.alloc_meta(self.s, dev)
         self.sel = bsa.alloc_select(self.s, dev, with_mask=False)
-        self.ws = torch.empty(bsa.select_workspace_bytes(self.s), dtype=torch.uint8, device=dev)
+        self.fused = flags == 0
+        ws_bytes = bsa.mask_build_workspace_bytes(self.s) if self.fused else bsa.select_workspace_bytes(self.s)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.lse = torch.empty(w.batch, w.hq, w.seq, dtype=torch.float32, device=dev)
         self.tokens = w.batch * w.seq
 
@@ -429,6 +432,19 @@ class FixedRunner:
 
     def to_host(self, lay, x):
         return self.torch.from_numpy(lay[x].view(np.int16)).view(self.torch.bfloat16)
+
+    def build(self, L, status):
+        """The whole mask build: one call when fused, else the meta and select calls."""
+        if self.fused:
+            self.mask_call(L, status)
+        else:
+            self.meta_call(L, status)
+            self.select_call(L, status)
+
+    def mask_call(self, L, status):
+        m, sl = self.meta, self.sel
+        self.bsa.mask_build(self.s, self.prm, L["q"], L["k"], m["centroid"], m["radius"], m["quant"],
+                            m["alpha"], sl["kv_idx"], sl["kv_cnt"], None, self.ws, status)
 
     def meta_call(self, L, status):
         m = self.meta
@@ -471,6 +487,10 @@ class FixedRunner:
 
 class Fp8Runner(FixedRunner):
     """FixedRunner on e4m3 inputs: bsa_block_meta_fp8, bsa_select_mask_fp8, bsa_prefill_fwd_fp8."""
+
+    def __init__(self, *args, **kwargs):
+        super().__init__(*args, **kwargs)
+        self.fused = False  # the e4m3 entry points build the mask in two calls
 
     def make_layer(self, synth, layer):
         lay = synth.make_layer(self.w, layer=layer)
@@ -662,13 +682,19 @@ def run_ours(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    fused = getattr(run, "fused", False)
+
     def step(L, evs=None):
         if evs:
             evs[0].record(stream)
-        run.meta_call(L, status)
+        if fused:  # the whole mask build in one call (events 1 and 2 coincide)
+            run.mask_call(L, status)
+        else:
+            run.meta_call(L, status)
         if evs:
             evs[1].record(stream)
-        run.select_call(L, status)
+        if not fused:
+            run.select_call(L, status)
         if evs:
             evs[2].record(stream)
         run.attn_call(L, o, status)
@@ -761,13 +787,15 @@ def run_ours(args):
                      "frac": kept_tflops / bf16_peak if bf16_peak else None,
                      "peak_source": peak_note, "traffic": traffic,
                      "flops_per_launch": float(np.mean(flops))},
-        "roofline_mask_build": {"kernels": "meta_kernel + quant_kernel + qpool_kernel + score_kernel + select_kernel",
+        "roofline_mask_build": {"kernels": ("meta_pool_kernel + score_kernel + select_kernel" if fused else
+                                             "meta_kernel + quant_kernel + qpool_kernel + score_kernel + select_kernel"),
                                 "bound": "hbm", "achieved": mask_gbs, "peak": hbm_peak,
                                 "unit": "GB/s", "frac": mask_gbs / hbm_peak if hbm_peak else None,
                                 "peak_source": f"{src} hbm copy",
                                 "bytes_per_launch": float(np.mean(mask_bytes))},
-        "gpu_launches": (7 if args.fp8 else 6) * K,  # meta, quant, qpool or centroid split, scores, select,
-                                                     # (V widening,) attention
+        # fused: meta + pooling, scores, select, attention (plus a counter memset node); otherwise
+        # meta, quant, qpool or centroid split, scores, select, (V widening,) attention
+        "gpu_launches": (4 if fused else (7 if args.fp8 else 6)) * K,
         "clocks": clk,
     }
     # the softmax's exponentials: one ex2 on the MUFU units per needed S element (the diagonal
@@ -1088,16 +1116,14 @@ def run_sweep(args):
         torch.cuda.synchronize(dev)
         recall = needle_recall(w, lay["needles"], masked["mask"].cpu().numpy())
         for _ in range(max(3, args.warmup)):
-            run.meta_call(L, st)
-            run.select_call(L, st)
+            run.build(L, st)
             run.attn_call(L, o, st)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         steps = max(3, min(args.steps, 10))
         times = []
         for _ in range(steps):
             ev[0].record()
-            run.meta_call(L, st)
-            run.select_call(L, st)
+            run.build(L, st)
             ev[1].record()
             run.attn_call(L, o, st)
             ev[2].record()
@@ -1170,8 +1196,8 @@ def run_crossover(args):
     for rc in (0.02, 0.05, 0.1, 0.15, 0.2, 0.3, 0.4, 0.5, 0.6, 0.7, 0.8, 0.9, 1.0):
         w = w0.with_(centroid_keep=rc)
         run = FixedRunner(bsa, torch, w, dev)
-        mk, sl, at = _time_calls(torch, [lambda: run.meta_call(L, st), lambda: run.select_call(L, st),
-                                         lambda: run.attn_call(L, o, st)], steps, warm)
+        mk, at = _time_calls(torch, [lambda: run.build(L, st), lambda: run.attn_call(L, o, st)], steps, warm)
+        sl = 0.0
         f, _, dens = run.stats()
         row = {"centroid_keep": rc, "rescue_keep": w.rescue_keep, "density": dens,
                "mask_build_ms": mk + sl, "attention_ms": at, "sparse_ms": mk + sl + at,

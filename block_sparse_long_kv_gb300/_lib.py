@@ -49,6 +49,9 @@ SIGNATURES = {
     "bsa_select_mask": (ctypes.c_int, [_SP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                        _P, _P]),
     "bsa_select_mask_noalloc": (ctypes.c_int, [_SP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "bsa_mask_build_workspace_bytes": (ctypes.c_size_t, [_SP]),
+    "bsa_mask_build": (ctypes.c_int, [_SP, _PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                      _P, _P]),
     "bsa_prefill_fwd": (ctypes.c_int, [_SP, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
     "bsa_prefill_dense_fwd": (ctypes.c_int, [_SP, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
     "bsa_prefill_layer_workspace_bytes": (ctypes.c_size_t, [_SP]),

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 __all__ = [
-    "Shape", "SelectParams", "SELECT_TOKEN_MAX", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "prefill_fwd",
+    "Shape", "SelectParams", "SELECT_TOKEN_MAX", "make_shape", "block_meta", "select_workspace_bytes", "select_mask", "mask_build_workspace_bytes", "mask_build", "prefill_fwd",
     "prefill_dense_fwd", "prefill_layer", "prefill_layer_workspace_bytes", "layer_views",
     "alloc_meta", "alloc_select", "alloc_layer_workspace", "status_string", "version",
     "selftest_wait_timeout",
@@ -90,6 +90,32 @@ def select_mask(shape: Shape, params: SelectParams, q, centroid, radius, alpha, 
         ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
         _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
         _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb),
+        _ptr(mask, "mask", torch.uint8, b * hkv * nb * nb),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def mask_build_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.load().bsa_mask_build_workspace_bytes(ctypes.byref(shape)))
+
+
+def mask_build(shape: Shape, params: SelectParams, q, k, centroid, radius, quant, alpha, kv_idx, kv_cnt,
+               mask=None, workspace=None, dev_status=None, stream=None):
+    """bsa_mask_build (bsa_block_meta then bsa_select_mask in three launches).  ``workspace``:
+    uint8 CUDA tensor of mask_build_workspace_bytes(shape) bytes (allocated here if None)."""
+    b, n, hq, hkv, d, nb = _dims(shape)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(mask_build_workspace_bytes(shape), dtype=torch.uint8, device=q.device)
+    _lib.check("bsa_mask_build", lib.bsa_mask_build(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16, b * n * hq * d),
+        _ptr(k, "k", torch.bfloat16, b * n * hkv * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * d * nb),
+        _ptr(radius, "radius", torch.float32, b * hkv * nb),
+        _ptr(quant, "quant", torch.float32, b * hkv * 2),
         _ptr(alpha, "alpha", torch.float32, b * hkv * nb),
         _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nb * nb),
         _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv * nb),

@@ -89,15 +89,23 @@ int64_t ratio_ppm(float r) { return static_cast<int64_t>(floor(static_cast<doubl
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace of bsa_mask_build: the select scratch, then the per-(b, g)
+// counters of the fused launch.
+size_t mask_build_bytes(const bsa::MaskShape &m, size_t *counters_at) {
+  const size_t at = round_up(bsa::select_workspace_bytes(m), 256);
+  if (counters_at) *counters_at = at;
+  return at + bsa::layer_mask_counter_bytes(m);
+}
+
 // Workspace layout of bsa_prefill_layer: centroid, radius, quant, alpha,
-// kv_idx, kv_cnt, select scratch, each 256-byte aligned.
-void layer_views(const bsa::MaskShape &m, size_t off[7], size_t *total) {
+// kv_idx, kv_cnt, the mask build's workspace, each 256-byte aligned.
+constexpr int kLayerRegions = 7;
+void layer_views(const bsa::MaskShape &m, size_t off[kLayerRegions], size_t *total) {
   const size_t b = m.batch, h = m.hkv, d = m.d, nb = m.nbs;
-  const size_t sizes[7] = {b * h * d * nb * 4, b * h * nb * 4,      b * h * 2 * 4, b * h * nb * 4,
-                           b * h * nb * nb * 4, b * h * nb * 4,
-                           bsa::select_workspace_bytes(m)};
+  const size_t sizes[kLayerRegions] = {b * h * d * nb * 4, b * h * nb * 4,      b * h * 2 * 4, b * h * nb * 4,
+                                       b * h * nb * nb * 4, b * h * nb * 4, mask_build_bytes(m, nullptr)};
   size_t cur = 0;
-  for (int x = 0; x < 7; ++x) {
+  for (int x = 0; x < kLayerRegions; ++x) {
     off[x] = cur;
     cur = round_up(cur + sizes[x], 256);
   }
@@ -140,6 +148,30 @@ bsa_status select_impl(const bsa::MaskShape &ms, const bsa_select_params *params
   return BSA_OK;
 }
 
+bsa_status mask_build_impl(const bsa::MaskShape &ms, const bsa_select_params *params, const void *q,
+                           const void *k, float *centroid, float *radius, float *quant, float *alpha,
+                           int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  if (!params || !q || !k || !centroid || !radius || !quant || !alpha || !kv_idx || !kv_cnt)
+    return BSA_ERR_INVALID_ARG;
+  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
+    return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(centroid) || !aligned16(radius) || !aligned16(quant) ||
+      !aligned16(alpha) || !aligned16(kv_idx) || !aligned16(kv_cnt) || (mask && !aligned16(mask)))
+    return BSA_ERR_INVALID_ARG;
+  size_t counters_at = 0;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < mask_build_bytes(ms, &counters_at))
+    return BSA_ERR_WORKSPACE;
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
+  char *ws = static_cast<char *>(workspace);
+  if (bsa::launch_layer_mask(ms, q, k, centroid, radius, quant, alpha, ratio_ppm(params->centroid_keep),
+                             ratio_ppm(params->rescue_keep), scale, kv_idx, kv_cnt, mask, ws,
+                             reinterpret_cast<unsigned *>(ws + counters_at), dev_status,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
 bsa_status prefill_impl(const bsa::MaskShape &ms, const void *q, const void *k, const void *v,
                         const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale, void *o,
                         float *lse, int32_t *dev_status, bsa_stream_t stream) {
@@ -158,7 +190,7 @@ bsa_status layer_impl(const bsa::MaskShape &ms, const bsa_select_params *params,
                       const void *k, const void *v, float softmax_scale, void *o, float *lse,
                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
                       bsa_stream_t stream) {
-  size_t off[7], total = 0;
+  size_t off[kLayerRegions], total = 0;
   layer_views(ms, off, &total);
   if (!workspace || workspace_bytes < total) return BSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_WORKSPACE;
@@ -169,10 +201,16 @@ bsa_status layer_impl(const bsa::MaskShape &ms, const bsa_select_params *params,
   float *alpha = reinterpret_cast<float *>(ws + off[3]);
   int32_t *kv_idx = reinterpret_cast<int32_t *>(ws + off[4]);
   int32_t *kv_cnt = reinterpret_cast<int32_t *>(ws + off[5]);
-  bsa_status r = meta_impl(ms, k, centroid, radius, quant, alpha, dev_status, stream);
-  if (r != BSA_OK) return r;
-  r = select_impl(ms, params, q, centroid, radius, alpha, kv_idx, kv_cnt, nullptr, ws + off[6],
-                  total - off[6], dev_status, stream);
+  bsa_status r;
+  if (params != nullptr && (params->flags & BSA_SELECT_TOKEN_MAX) != 0) {
+    r = meta_impl(ms, k, centroid, radius, quant, alpha, dev_status, stream);
+    if (r != BSA_OK) return r;
+    r = select_impl(ms, params, q, centroid, radius, alpha, kv_idx, kv_cnt, nullptr, ws + off[6],
+                    total - off[6], dev_status, stream);
+  } else {
+    r = mask_build_impl(ms, params, q, k, centroid, radius, quant, alpha, kv_idx, kv_cnt, nullptr, ws + off[6],
+                        total - off[6], dev_status, stream);
+  }
   if (r != BSA_OK) return r;
   return prefill_impl(ms, q, k, v, kv_idx, kv_cnt, softmax_scale, o, lse, dev_status, stream);
 }
@@ -218,6 +256,21 @@ bsa_status bsa_select_mask(const bsa_shape *shape, const bsa_select_params *para
                      workspace, workspace_bytes, dev_status, stream);
 }
 
+size_t bsa_mask_build_workspace_bytes(const bsa_shape *shape) {
+  if (check_shape(shape) != BSA_OK) return 0;
+  return mask_build_bytes(mask_shape(shape), nullptr);
+}
+
+bsa_status bsa_mask_build(const bsa_shape *shape, const bsa_select_params *params, const void *q,
+                          const void *k, float *centroid, float *radius, float *quant, float *alpha,
+                          int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                          size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream) {
+  const bsa_status st = check_shape(shape);
+  if (st != BSA_OK) return st;
+  return mask_build_impl(mask_shape(shape), params, q, k, centroid, radius, quant, alpha, kv_idx, kv_cnt, mask,
+                         workspace, workspace_bytes, dev_status, stream);
+}
+
 bsa_status bsa_prefill_fwd(const bsa_shape *shape, const void *q, const void *k, const void *v,
                            const int32_t *kv_idx, const int32_t *kv_cnt, float softmax_scale,
                            void *o, float *lse, int32_t *dev_status, bsa_stream_t stream) {
@@ -239,7 +292,7 @@ bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const vo
 
 size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape) {
   if (check_shape(shape) != BSA_OK) return 0;
-  size_t off[7], total = 0;
+  size_t off[kLayerRegions], total = 0;
   layer_views(mask_shape(shape), off, &total);
   return total;
 }
@@ -248,7 +301,7 @@ bsa_status bsa_prefill_layer_views(const bsa_shape *shape, size_t *offsets) {
   const bsa_status st = check_shape(shape);
   if (st != BSA_OK) return st;
   if (!offsets) return BSA_ERR_INVALID_ARG;
-  size_t off[7], total = 0;
+  size_t off[kLayerRegions], total = 0;
   layer_views(mask_shape(shape), off, &total);
   for (int x = 0; x < 6; ++x) offsets[x] = off[x];
   return BSA_OK;

@@ -67,6 +67,15 @@ cudaError_t launch_select(const MaskShape &s, const void *q, const float *centro
                           float scale, bool token_max, int32_t *kv_idx, int32_t *kv_cnt,
                           uint8_t *mask, void *workspace, int32_t *status, cudaStream_t stream);
 
+// The layer path's mask build: key-block meta and query pooling in one launch
+// (the quantiles taken by each KV group's last meta CTA), then the scores and the
+// selection; `done` holds layer_mask_counter_bytes(s) of counters, zeroed here.
+size_t layer_mask_counter_bytes(const MaskShape &s);
+cudaError_t launch_layer_mask(const MaskShape &s, const void *q, const void *k, float *centroid, float *radius,
+                              float *quant, float *alpha, int64_t ppm_c, int64_t ppm_r, float scale,
+                              int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace, unsigned *done,
+                              int32_t *status, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point.
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,

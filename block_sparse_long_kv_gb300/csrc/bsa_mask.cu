@@ -8,7 +8,7 @@
 // selection paths, OR-combined.  The build reads every token a fixed number of
 // times, so it is linear in the sequence length.
 //
-// Five launches:
+// Kernels:
 //   meta_kernel     one CTA per (b, g, j): centroid and radius of key block j
 //                   (streams K once, the block held in registers)
 //   quant_kernel    one CTA per (b, g): bitonic sort of the nb radii in
@@ -17,11 +17,15 @@
 //                   norm of block i (streams Q once: the dominant HBM bytes),
 //                   written as tf32 hi / lo splits; one more CTA row splits the
 //                   centroids the same way
+//   meta_pool_kernel  the three above in one grid (bsa_mask_build and the
+//                   layer call): meta CTAs, then pooling CTAs; each KV group's
+//                   last meta CTA takes the quantiles
 //   score_kernel    (bsa_score.cu) centroid / rescue scores of every causal key
 //                   block on tensor cores
-//   select_kernel   one warp per (b, g, i): per-path exact top-k (a linear
-//                   value histogram, then a radix threshold inside its
-//                   threshold bin), OR, ascending kept-list emission
+//   select_kernel   a team of 1 to 8 warps per (b, g, i) row, sized to the
+//                   row: per-path exact top-k (a linear value histogram, then a
+//                   radix threshold inside its threshold bin), OR, ascending
+//                   kept-list emission
 // Every reduction runs in a fixed order, so results are deterministic.
 
 #include <cuda_bf16.h>
@@ -30,6 +34,7 @@
 #include "bsa_fp8.cuh"
 #include "bsa_internal.h"
 #include "bsa_topk.cuh"
+#include "sm103_ptx.cuh"
 
 namespace bsa {
 namespace {
@@ -64,6 +69,11 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float f[8]) {
 
 // ---------------------------------------------------------------- block meta
 
+// tf32 split of an fp32 value: hi keeps the top 10 mantissa bits (exact in
+// tf32), lo = x - hi is exact in fp32.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+
 // One CTA per (b, g, j), the key block held in registers: thread t owns the
 // 8 dimensions v = t % (D/8) of the tokens u, u + TL, u + 2 TL, ... with
 // u = t / (D/8) and TL = 256 / (D/8) token lanes.  Pass 1 sums the tokens into
@@ -73,13 +83,17 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float f[8]) {
 // A partial last block (a packed sequence whose length is not a multiple of
 // BLK) averages over its own tokens; CTAs past a sequence's last block write
 // zeros.
+template <int D, int BLK>
+constexpr int meta_min_blocks() { return D * BLK > 128 * 128 ? 1 : 3; }
+
+// Centroid and radius of key block j of (b, g); with c_hi / c_lo (nullable) also
+// the centroid's tf32 hi / lo split (the score GEMM's A operand).
 template <int D, int BLK, bool F8>
-__global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_kernel(const unsigned char *__restrict__ k,
-                                                        float *__restrict__ centroid,
-                                                        float *__restrict__ radius,
-                                                        const int32_t *__restrict__ cu, int seq,
-                                                        int total, int hkv, int nbs, float scale,
-                                                        int32_t *status) {
+__device__ __forceinline__ void meta_block(int j, int g, int b, const unsigned char *__restrict__ k,
+                                           float *__restrict__ centroid, float *__restrict__ radius,
+                                           float *__restrict__ c_hi, float *__restrict__ c_lo,
+                                           const int32_t *__restrict__ cu, int seq, int total, int hkv,
+                                           int nbs, float scale, int32_t *status) {
   constexpr int EB = F8 ? 1 : 2;      // bytes per input element
   constexpr int VPR = D / 8;          // 16-byte vectors per key row
   constexpr int TL = kThreads / VPR;  // token lanes
@@ -90,14 +104,16 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
   __shared__ __align__(16) float sc[D];
   __shared__ float wmax[NW];
 
-  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int v = tid % VPR, u = tid / VPR;
   const SeqSpan sp = seq_span(cu, b, seq, total, status);
   const size_t ob = (static_cast<size_t>(b) * hkv + g) * nbs + j;
   const int cnt = min(BLK, sp.len - j * BLK);  // keys in this block
   if (cnt <= 0) {
-    if (tid < D) centroid[ob * D + tid] = 0.f;
+    if (tid < D) {
+      centroid[ob * D + tid] = 0.f;
+      if (c_hi != nullptr) c_hi[ob * D + tid] = c_lo[ob * D + tid] = 0.f;
+    }
     if (tid == 0) radius[ob] = 0.f;
     return;
   }
@@ -142,7 +158,13 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     for (int w = 0; w < NW; ++w) c += part[w][tid];
     c /= static_cast<float>(cnt);
     sc[tid] = c;
-    centroid[ob * D + tid] = c * scale;  // in the inputs' units (scale 1 for bf16)
+    const float cv = c * scale;  // in the inputs' units (scale 1 for bf16)
+    centroid[ob * D + tid] = cv;
+    if (c_hi != nullptr) {
+      const float h = tf32_hi(cv);
+      c_hi[ob * D + tid] = h;
+      c_lo[ob * D + tid] = cv - h;
+    }
   }
   __syncthreads();
 
@@ -179,6 +201,14 @@ __global__ void __launch_bounds__(kThreads, (D * BLK > 128 * 128 ? 1 : 3)) meta_
     for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
     radius[ob] = sqrtf(m) * scale;
   }
+}
+
+template <int D, int BLK, bool F8>
+__global__ void __launch_bounds__(kThreads, (meta_min_blocks<D, BLK>())) meta_kernel(
+    const unsigned char *__restrict__ k, float *__restrict__ centroid, float *__restrict__ radius,
+    const int32_t *__restrict__ cu, int seq, int total, int hkv, int nbs, float scale, int32_t *status) {
+  meta_block<D, BLK, F8>(blockIdx.x, blockIdx.y, blockIdx.z, k, centroid, radius, nullptr, nullptr, cu, seq,
+                         total, hkv, nbs, scale, status);
 }
 
 // ---------------------------------------------------------------- quantiles
@@ -280,35 +310,70 @@ __global__ void __launch_bounds__(1024) quant_kernel(const float *__restrict__ r
 
 // ---------------------------------------------------------------- query pooling
 
-// tf32 split of an fp32 value: hi keeps the top 10 mantissa bits (exact in
-// tf32), lo = x - hi is exact in fp32.
-__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+// Sixteen consecutive elements of one query token for one lane: bf16 (two
+// 16-byte loads) or e4m3 (one).
+template <bool F8>
+struct Vec16 {
+  uint4 u[F8 ? 1 : 2];
+};
 
-// Sums a full block's queries (8 dimensions per lane) and their norms, 8 (bf16)
-// or 16 (e4m3) loads in flight per thread.
+template <bool F8>
+__device__ __forceinline__ Vec16<F8> load16(const unsigned char *p) {
+  Vec16<F8> v;
+  v.u[0] = __ldcs(reinterpret_cast<const uint4 *>(p));
+  if constexpr (!F8) v.u[1] = __ldcs(reinterpret_cast<const uint4 *>(p + 16));
+  return v;
+}
+
+// The sixteen elements as eight packed fp32 pairs (elements 2 e, 2 e + 1).
+template <bool F8>
+__device__ __forceinline__ void unpack16(const Vec16<F8> &v, uint64_t p[8]) {
+  if constexpr (F8) {
+    float f[16];
+    e4m3x8_to_f32(make_uint2(v.u[0].x, v.u[0].y), f);
+    e4m3x8_to_f32(make_uint2(v.u[0].z, v.u[0].w), f + 8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] = ptx::f32x2(f[2 * e], f[2 * e + 1]);
+  } else {
+    const uint32_t w[8] = {v.u[0].x, v.u[0].y, v.u[0].z, v.u[0].w, v.u[1].x, v.u[1].y, v.u[1].z, v.u[1].w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] = ptx::f32x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+  }
+}
+
+// Adds one token's sixteen elements to the lane's pair sums and its L2 norm
+// (the head's D / 16 lanes combine their partial squares) to nsum.
+template <int D, bool F8>
+__device__ __forceinline__ void pool_token(const Vec16<F8> &v, unsigned wmask, uint64_t acc[8], float &nsum) {
+  constexpr int VH = D / 16;  // lanes per head
+  uint64_t f[8];
+  unpack16<F8>(v, f);
+  uint64_t sq2 = 0ull;  // (+0.0f, +0.0f)
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    acc[e] = ptx::add_f32x2(acc[e], f[e]);
+    sq2 = ptx::fma_f32x2(f[e], f[e], sq2);
+  }
+  float s0, s1;
+  ptx::f32x2_split(sq2, s0, s1);
+  float sq = s0 + s1;
+#pragma unroll
+  for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
+  nsum += sqrtf(sq);
+}
+
+// Sums a full block's queries (16 dimensions per lane, on packed fp32 pairs)
+// and their norms, 4 (bf16) or 8 (e4m3) tokens in flight per thread.
 template <int D, bool F8>
 __device__ __forceinline__ void pool_full(const unsigned char *__restrict__ base, size_t tok_stride,
-                                          int cnt, unsigned wmask, float acc[8], float &nsum) {
-  constexpr int VH = D / 8;        // lanes per head
-  constexpr int TB = F8 ? 16 : 8;  // tokens in flight per lane (8-byte e4m3 loads: twice as many)
+                                          int cnt, unsigned wmask, uint64_t acc[8], float &nsum) {
+  constexpr int TB = F8 ? 8 : 4;  // tokens in flight (32 or 16 bytes each per lane)
   for (int t0 = 0; t0 < cnt; t0 += TB) {
-    uint4 u[TB];
+    Vec16<F8> u[TB];
 #pragma unroll
-    for (int r = 0; r < TB; ++r) u[r] = load8<F8>(base + static_cast<size_t>(t0 + r) * tok_stride);
+    for (int r = 0; r < TB; ++r) u[r] = load16<F8>(base + static_cast<size_t>(t0 + r) * tok_stride);
 #pragma unroll
-    for (int r = 0; r < TB; ++r) {
-      float f[8];
-      unpack8<F8>(u[r], f);
-      float sq = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[e] += f[e];
-        sq = fmaf(f[e], f[e], sq);
-      }
-#pragma unroll
-      for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
-      nsum += sqrtf(sq);
-    }
+    for (int r = 0; r < TB; ++r) pool_token<D, F8>(u[r], wmask, acc, nsum);
   }
 }
 
@@ -316,30 +381,72 @@ __device__ __forceinline__ void pool_full(const unsigned char *__restrict__ base
 // block, one token at a time (one such block per sequence).
 template <int D, bool F8>
 __device__ __forceinline__ void pool_partial(const unsigned char *__restrict__ base, size_t tok_stride,
-                                             int cnt, unsigned wmask, float acc[8], float &nsum) {
-  constexpr int VH = D / 8;
+                                             int cnt, unsigned wmask, uint64_t acc[8], float &nsum) {
 #pragma unroll 1
-  for (int t = 0; t < cnt; ++t) {
-    float f[8];
-    unpack8<F8>(load8<F8>(base + static_cast<size_t>(t) * tok_stride), f);
-    float sq = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      acc[e] += f[e];
-      sq = fmaf(f[e], f[e], sq);
-    }
-#pragma unroll
-    for (int off = VH / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(wmask, sq, off);
-    nsum += sqrtf(sq);
-  }
+  for (int t = 0; t < cnt; ++t) pool_token<D, F8>(load16<F8>(base + static_cast<size_t>(t) * tok_stride), wmask, acc, nsum);
 }
 
-// One thread per (head, 8 dimensions); the token loop keeps 8 16-byte loads in
-// flight per thread.  Writes the mean query as tf32 hi / lo splits,
+// One thread per (head, 16 dimensions); the token loop keeps 4 (bf16) or 8
+// (e4m3) tokens of loads in flight per thread.  Writes the mean query as tf32 hi / lo splits,
 // q_hi/q_lo[b][g][i][hh][x] (one K-major row per (query block, head): the B
 // operand of the score GEMM), and nbar[b][g][i][hh].  The extra row of CTAs
 // (blockIdx.y == nhc) splits the centroids of key block blockIdx.x of every KV
 // head into c_hi / c_lo, the GEMM's A operand.
+template <int D, bool F8>
+__device__ __forceinline__ void qpool_block(int i, int hc, int b, int nthreads, const unsigned char *__restrict__ q,
+                                            float *__restrict__ q_hi, float *__restrict__ q_lo,
+                                            float *__restrict__ nbar, const int32_t *__restrict__ cu, int seq,
+                                            int total, int hq, int hkv, int block, int nbs, int hpc, float scale,
+                                            int32_t *status) {
+  constexpr int VH = D / 16;  // lanes per head
+  constexpr int EB = F8 ? 1 : 2;  // bytes per input element
+  const int tid = threadIdx.x;
+  const int hl = tid / VH, xv = tid - hl * VH;
+  const int h = hc * hpc + hl;
+  const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
+  const size_t row = (static_cast<size_t>(b) * hkv + g) * nbs + i;
+  const size_t qo = (row * grp + hh) * D + xv * 16;
+  float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
+  float4 *ql = reinterpret_cast<float4 *>(q_lo + qo);
+  const SeqSpan sp = seq_span(cu, b, seq, total, status);
+  const int cnt = min(block, sp.len - i * block);  // queries in this block
+  if (cnt <= 0) {  // past the sequence's last block: zero rows
+#pragma unroll
+    for (int x = 0; x < 4; ++x) qh[x] = ql[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (xv == 0) nbar[row * grp + hh] = 0.f;
+    return;
+  }
+  const size_t tok_stride = static_cast<size_t>(hq) * D * EB;  // bytes
+  const unsigned char *base = q + (static_cast<size_t>(sp.start) + static_cast<size_t>(i) * block) * tok_stride +
+                              (static_cast<size_t>(h) * D + xv * 16) * EB;
+  // lanes present in this warp (the last warp may be partial); a head's lanes never straddle warps
+  const int present = min(32, nthreads - (tid & ~31));
+  const unsigned wmask = present >= 32 ? 0xffffffffu : ((1u << present) - 1u);
+  uint64_t acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0ull;
+  float nsum = 0.f;
+  if (cnt == block) pool_full<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
+  else pool_partial<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
+  const float inv = scale / static_cast<float>(cnt);  // exact for a full bf16 block (scale 1, cnt 2^k)
+  float m[16], hi[16];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ptx::f32x2_split(acc[e], m[2 * e], m[2 * e + 1]);
+    m[2 * e] *= inv;
+    m[2 * e + 1] *= inv;
+    hi[2 * e] = tf32_hi(m[2 * e]);
+    hi[2 * e + 1] = tf32_hi(m[2 * e + 1]);
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    qh[x] = make_float4(hi[4 * x], hi[4 * x + 1], hi[4 * x + 2], hi[4 * x + 3]);
+    ql[x] = make_float4(m[4 * x] - hi[4 * x], m[4 * x + 1] - hi[4 * x + 1], m[4 * x + 2] - hi[4 * x + 2],
+                        m[4 * x + 3] - hi[4 * x + 3]);
+  }
+  if (xv == 0) nbar[row * grp + hh] = nsum * inv;
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads) qpool_kernel(const unsigned char *__restrict__ q,
                                                          float *__restrict__ q_hi,
@@ -352,12 +459,9 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const unsigned char *__
                                                          int total, int hq, int hkv, int block,
                                                          int nbs, int hpc, int nhc, float scale,
                                                          int32_t *status) {
-  constexpr int VH = D / 8;  // lanes per head
-  constexpr int EB = F8 ? 1 : 2;  // bytes per input element
   const int i = blockIdx.x, hc = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
   if (hc == nhc) {
-    for (int e = tid; e < hkv * D; e += blockDim.x) {
+    for (int e = threadIdx.x; e < hkv * D; e += blockDim.x) {
       const int g = e / D, x = e - g * D;
       const size_t o = ((static_cast<size_t>(b) * hkv + g) * nbs + i) * D + x;
       const float v = centroid[o], h = tf32_hi(v);
@@ -366,99 +470,197 @@ __global__ void __launch_bounds__(kThreads) qpool_kernel(const unsigned char *__
     }
     return;
   }
-  const int hl = tid / VH, xv = tid - hl * VH;
-  const int h = hc * hpc + hl;
-  const int grp = hq / hkv, g = h / grp, hh = h - g * grp;
-  const size_t row = (static_cast<size_t>(b) * hkv + g) * nbs + i;
-  const size_t qo = (row * grp + hh) * D + xv * 8;
-  const SeqSpan sp = seq_span(cu, b, seq, total, status);
-  const int cnt = min(block, sp.len - i * block);  // queries in this block
-  if (cnt <= 0) {  // past the sequence's last block: zero rows
-    float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
-    float4 *ql = reinterpret_cast<float4 *>(q_lo + qo);
-    qh[0] = qh[1] = ql[0] = ql[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (xv == 0) nbar[row * grp + hh] = 0.f;
+  qpool_block<D, F8>(i, hc, b, static_cast<int>(blockDim.x), q, q_hi, q_lo, nbar, cu, seq, total, hq, hkv, block,
+                     nbs, hpc, scale, status);
+}
+
+// ---------------------------------------------------------------- meta + pooling in one launch
+
+// Nearest-rank median / p90 of the nb radii of one (b, g) and every block's
+// alpha, by one CTA: the radii (read through L2: other CTAs wrote them) sorted
+// ascending in shared memory by a bitonic network over npow2 entries (+inf
+// padding).  Same values as quant_kernel: the sort is exact and alpha takes the
+// same operations.
+__device__ __forceinline__ void quant_smem(const float *radius, float *quant, float *alpha, float *buf, int nb,
+                                           int nbs, size_t base, size_t qo) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int j = nb + tid; j < nbs; j += nt) alpha[base + j] = 0.f;
+  if (nb == 0) {
+    if (tid == 0) quant[qo] = quant[qo + 1] = 0.f;
     return;
   }
-  const size_t tok_stride = static_cast<size_t>(hq) * D * EB;  // bytes
-  const unsigned char *base = q + (static_cast<size_t>(sp.start) + static_cast<size_t>(i) * block) * tok_stride +
-                              (static_cast<size_t>(h) * D + xv * 8) * EB;
-  // lanes present in this warp (the last warp may be partial); a head's lanes never straddle warps
-  const int present = min(32, static_cast<int>(blockDim.x) - (tid & ~31));
-  const unsigned wmask = present >= 32 ? 0xffffffffu : ((1u << present) - 1u);
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  float nsum = 0.f;
-  if (cnt == block) pool_full<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
-  else pool_partial<D, F8>(base, tok_stride, cnt, wmask, acc, nsum);
-  const float inv = scale / static_cast<float>(cnt);  // exact for a full bf16 block (scale 1, cnt 2^k)
-  float m[8], hi[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    m[e] = acc[e] * inv;
-    hi[e] = tf32_hi(m[e]);
+  int npow2 = 2;
+  while (npow2 < nb) npow2 <<= 1;
+  for (int x = tid; x < npow2; x += nt) buf[x] = x < nb ? __ldcg(radius + base + x) : INFINITY;
+  __syncthreads();
+  for (int kk = 2; kk <= npow2; kk <<= 1) {
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int x = tid; x < npow2; x += nt) {
+        const int p = x ^ jj;
+        if (p > x) {
+          const float a = buf[x], c = buf[p];
+          if ((a > c) == ((x & kk) == 0)) {  // ascending where bit kk of x is clear
+            buf[x] = c;
+            buf[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
   }
-  float4 *qh = reinterpret_cast<float4 *>(q_hi + qo);
-  float4 *ql = reinterpret_cast<float4 *>(q_lo + qo);
-  qh[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
-  qh[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
-  ql[0] = make_float4(m[0] - hi[0], m[1] - hi[1], m[2] - hi[2], m[3] - hi[3]);
-  ql[1] = make_float4(m[4] - hi[4], m[5] - hi[5], m[6] - hi[6], m[7] - hi[7]);
-  if (xv == 0) nbar[row * grp + hh] = nsum * inv;
+  const float med = buf[(nb + 1) / 2 - 1], p90 = buf[(9 * nb + 9) / 10 - 1];
+  const float span = p90 - med;
+  const bool degenerate = span <= 1e-12f * p90;
+  if (tid == 0) {
+    quant[qo] = med;
+    quant[qo + 1] = p90;
+  }
+  for (int j = tid; j < nb; j += nt) {
+    float a = 0.f;
+    if (!degenerate) a = fminf(fmaxf((__ldcg(radius + base + j) - med) / span, 0.f), 1.f);
+    alpha[base + j] = a;
+  }
+}
+
+// The layer path's first launch: the key-block meta CTAs (b, g, j) first, then
+// the query-pooling CTAs (b, head chunk, i), so K and Q stream in one grid with
+// no launch boundary between them.  Meta CTAs also write the centroids' tf32
+// splits; the last meta CTA of each (b, g) to finish (counted in done[b][g],
+// zero before the launch) takes that group's quantiles and alpha, so no launch
+// waits on the radii.
+template <int D, int BLK>
+__global__ void __launch_bounds__(kThreads, (meta_min_blocks<D, BLK>())) meta_pool_kernel(
+    const unsigned char *__restrict__ k, const unsigned char *__restrict__ q, float *__restrict__ centroid,
+    float *__restrict__ radius, float *__restrict__ quant, float *__restrict__ alpha, float *__restrict__ c_hi,
+    float *__restrict__ c_lo, float *__restrict__ q_hi, float *__restrict__ q_lo, float *__restrict__ nbar,
+    unsigned *__restrict__ done, const int32_t *__restrict__ cu, int batch, int seq, int total, int hq, int hkv,
+    int block, int nbs, int hpc, int nhc, int32_t *status) {
+  extern __shared__ float sort_buf[];
+  __shared__ unsigned last;
+  const int nmeta = nbs * hkv * batch;
+  const int x = static_cast<int>(blockIdx.x);
+  if (x < nmeta) {
+    const int j = x % nbs, g = (x / nbs) % hkv, b = x / (nbs * hkv);
+    meta_block<D, BLK, false>(j, g, b, k, centroid, radius, c_hi, c_lo, cu, seq, total, hkv, nbs, 1.f, status);
+    __threadfence();  // this CTA's radius before its count
+    __syncthreads();
+    const size_t bg = static_cast<size_t>(b) * hkv + g;
+    if (threadIdx.x == 0) last = atomicAdd(done + bg, 1u) == static_cast<unsigned>(nbs - 1);
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      const SeqSpan sp = seq_span(cu, b, seq, total, status);
+      quant_smem(radius, quant, alpha, sort_buf, (sp.len + block - 1) / block, nbs, bg * nbs, bg * 2);
+    }
+    return;
+  }
+  const int y = x - nmeta;
+  const int i = y % nbs, hc = (y / nbs) % nhc, b = y / (nbs * nhc);
+  const int nthreads = hpc * (D / 16);
+  if (static_cast<int>(threadIdx.x) < nthreads)
+    qpool_block<D, false>(i, hc, b, nthreads, q, q_hi, q_lo, nbar, cu, seq, total, hq, hkv, block, nbs, hpc, 1.f,
+                          status);
 }
 
 // ---------------------------------------------------------------- select
 
 using namespace topk;
 
-constexpr int kSelWarps = 8;   // rows per select CTA, one warp each
+// Rows of one (b, g) go to teams of W warps (topk::Team), W the smallest power of
+// two with 32 W P >= i + 1, packed kTeamMaxWarps / W teams to a CTA of
+// kTeamMaxWarps warps; the widest class comes first and, inside a class, the
+// longest row.  Class W holds the rows with 16 P W < i + 1 <= 32 P W (those
+// with i + 1 <= 32 P for W = 1).  Returns the CTAs of a row set of nbs rows;
+// with cta >= 0 also the class, the first (longest) row and the team count of
+// CTA `cta`.
+struct TeamPlan {
+  int w, first_row, teams;
+};
 
+template <int P>
+__host__ __device__ inline int team_plan(int nbs, int cta, TeamPlan *plan) {
+  int total = 0;
+  for (int w = kTeamMaxWarps; w >= 1; w >>= 1) {
+    const int hi_n = nbs < 32 * P * w ? nbs : 32 * P * w;
+    const int lo_n = w == 1 ? 1 : 16 * P * w + 1;
+    if (hi_n < lo_n) continue;
+    const int rows = hi_n - lo_n + 1, tpc = kTeamMaxWarps / w;
+    const int ctas = (rows + tpc - 1) / tpc;
+    if (cta >= total && cta < total + ctas) {
+      const int k = cta - total;
+      plan->w = w;
+      plan->first_row = hi_n - 1 - k * tpc;
+      plan->teams = rows - k * tpc < tpc ? rows - k * tpc : tpc;
+    }
+    total += ctas;
+  }
+  return total;
+}
 
-// One warp per (b, g, i) row, longest rows first; kSelWarps rows per CTA.
-// Loads the row's centroid-path keys (scores from the tensor-core score
-// kernel), selects the top kc, then the rescue-path keys of the candidates the
-// centroid path dropped and whose alpha is positive, selects the top kr, ORs in
-// the forced sink and diagonal blocks and writes the ascending kept list.
-// nbs is the row stride of alpha, kv_idx, kv_cnt and mask (the caller's arrays),
-// nbw the row stride of the score matrices and of the per-warp shared scratch.
-// When nbs is not a multiple of 4 (a fixed-length batch whose block count is
-// not), alpha and mask rows are not 16- / 4-byte aligned and are accessed
-// element by element.
-template <bool ALIGNED>
-__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
-    const float *__restrict__ s_c, const float *__restrict__ s_r, const float *__restrict__ alpha,
-    int32_t *__restrict__ kv_idx, int32_t *__restrict__ kv_cnt, uint8_t *__restrict__ mask,
-    const int32_t *__restrict__ cu, int seq, int total, int block, int hkv, int nbs, int nbw,
-    long long ppm_c, long long ppm_r, int32_t *status) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = nbs - 1 - (static_cast<int>(blockIdx.x) * kSelWarps + warp);
-  if (i < 0) return;
-  const int g = blockIdx.y, b = blockIdx.z;
+struct SelectArgs {
+  const float *s_c, *s_r, *alpha;
+  int32_t *kv_idx, *kv_cnt;
+  uint8_t *mask;
+  const int32_t *cu;
+  int seq, total, block, hkv, nbs, nbw;
+  long long ppm_c, ppm_r;
+  int32_t *status;
+};
+
+template <int W, int P, bool ALIGNED>
+__device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int i, int b, int g, const SelectArgs &a) {
+  Team<W> tm(sh, 1 + team, static_cast<int>(threadIdx.x) - team * 32 * W);
+  const size_t gb = static_cast<size_t>(b) * a.hkv + g;
+  const size_t row = gb * a.nbs + i;
   {
     // rows past the sequence's last block: empty list, zero mask row
-    const SeqSpan sp = seq_span(cu, b, seq, total, status);
-    if (i >= (sp.len + block - 1) / block) {
-      const size_t row = (static_cast<size_t>(b) * hkv + g) * nbs + i;
-      if (lane == 0) kv_cnt[row] = 0;
-      if (mask != nullptr) {
+    const SeqSpan sp = seq_span(a.cu, b, a.seq, a.total, a.status);
+    if (i >= (sp.len + a.block - 1) / a.block) {
+      if (tm.t == 0) a.kv_cnt[row] = 0;
+      if (a.mask != nullptr) {
+        uint8_t *mrow = a.mask + row * static_cast<size_t>(a.nbs);
         if constexpr (ALIGNED) {
-          uint32_t *mrow = reinterpret_cast<uint32_t *>(mask + row * static_cast<size_t>(nbs));
-          for (int j4 = lane * 4; j4 < nbs; j4 += 128) mrow[j4 >> 2] = 0u;
+          for (int j4 = tm.t * 4; j4 < a.nbs; j4 += 4 * Team<W>::T) reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = 0u;
         } else {
-          for (int j = lane; j < nbs; j += 32) mask[row * static_cast<size_t>(nbs) + j] = 0u;
+          for (int j = tm.t; j < a.nbs; j += Team<W>::T) mrow[j] = 0u;
         }
       }
       return;
     }
   }
-  const RowScratch w = row_scratch(smem + static_cast<size_t>(warp) * row_scratch_bytes(nbw), nbw);
-  const size_t gb = static_cast<size_t>(b) * hkv + g;
-  const size_t row = gb * nbs + i;
-  warp_select_row<ALIGNED>(s_c + row * nbw, s_r + row * nbw, alpha + gb * nbs, i, ppm_c, ppm_r, w);
-  warp_emit_row<ALIGNED>(w, i, kv_idx + row * static_cast<size_t>(nbs), kv_cnt + row,
-                         mask != nullptr ? mask + row * static_cast<size_t>(nbs) : nullptr, nbs);
+  tm.clear_hist();
+  tm.sync();
+  uint32_t fl[P / 4];
+  team_select_row<W, P, ALIGNED>(tm, a.s_c + row * a.nbw, a.s_r + row * a.nbw, a.alpha + gb * a.nbs, i, a.ppm_c,
+                                 a.ppm_r, fl);
+  team_emit_row<W, P, ALIGNED>(tm, fl, i, a.kv_idx + row * static_cast<size_t>(a.nbs), a.kv_cnt + row,
+                               a.mask != nullptr ? a.mask + row * static_cast<size_t>(a.nbs) : nullptr, a.nbs);
+}
+
+// Per-path exact top-k, OR and kept-list emission for every (b, g, i) row:
+// loads the row's centroid-path scores (from the tensor-core score kernel),
+// selects the top kc, then the rescue-path scores of the candidates the
+// centroid path dropped and whose alpha is positive, selects the top kr, ORs in
+// the forced sink and diagonal blocks and writes the ascending kept list.
+// P entries per lane (32 kTeamMaxWarps P >= nbw).  nbs is the row stride of
+// alpha, kv_idx, kv_cnt and mask (the caller's arrays), nbw the row stride of
+// the score matrices.  When nbs is not a multiple of 4 (a fixed-length batch
+// whose block count is not), alpha and mask rows are not 16- / 4-byte aligned
+// and are accessed element by element.
+template <int P, bool ALIGNED>
+__global__ void __launch_bounds__(kTeamMaxWarps * 32, (P <= 8 ? 4 : 2)) select_kernel(const __grid_constant__ SelectArgs a) {
+  __shared__ TeamScratch sh[kTeamMaxWarps];
+  TeamPlan plan{1, 0, 0};
+  team_plan<P>(a.nbs, static_cast<int>(blockIdx.x), &plan);
+  const int team = static_cast<int>(threadIdx.x >> 5) / plan.w;
+  if (team >= plan.teams) return;  // whole teams leave; barriers are per team
+  const int i = plan.first_row - team, g = blockIdx.y, b = blockIdx.z;
+  switch (plan.w) {
+    case 1: select_team_row<1, P, ALIGNED>(sh[team], team, i, b, g, a); break;
+    case 2: select_team_row<2, P, ALIGNED>(sh[team], team, i, b, g, a); break;
+    case 4: select_team_row<4, P, ALIGNED>(sh[team], team, i, b, g, a); break;
+    default: select_team_row<8, P, ALIGNED>(sh[team], team, i, b, g, a); break;
+  }
 }
 
 template <int D, int BLK>
@@ -486,11 +688,12 @@ cudaError_t launch_meta_d(const MaskShape &s, const void *k, float *centroid, fl
   }
 }
 
-// Heads per query-pooling CTA: the largest divisor of hq with <= 256 threads.
+// Heads per query-pooling CTA: the largest divisor of hq with <= 256 threads
+// (d / 16 of them per head).
 int qpool_heads(int hq, int d) {
   int best = 1;
   for (int h = 1; h <= hq; ++h)
-    if (hq % h == 0 && h * (d / 8) <= kThreads) best = h;
+    if (hq % h == 0 && h * (d / 16) <= kThreads) best = h;
   return best;
 }
 
@@ -503,11 +706,11 @@ cudaError_t launch_qpool_d(const MaskShape &s, const void *q, float *q_hi, float
   dim3 grid(s.nbs, nhc + 1, s.batch);
   const unsigned char *qb = static_cast<const unsigned char *>(q);
   if (s.fp8)
-    qpool_kernel<D, true><<<grid, hpc * (D / 8), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
+    qpool_kernel<D, true><<<grid, hpc * (D / 16), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
                                                               s.seq, s.total, s.hq, s.hkv, s.block, s.nbs, hpc,
                                                               nhc, s.q_scale, status);
   else
-    qpool_kernel<D, false><<<grid, hpc * (D / 8), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
+    qpool_kernel<D, false><<<grid, hpc * (D / 16), 0, stream>>>(qb, q_hi, q_lo, nbar, centroid, c_hi, c_lo, s.cu,
                                                                s.seq, s.total, s.hq, s.hkv, s.block, s.nbs, hpc,
                                                                nhc, 1.f, status);
   return cudaGetLastError();
@@ -570,39 +773,109 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
-                          const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
-                          float scale, bool token_max, int32_t *kv_idx, int32_t *kv_cnt,
-                          uint8_t *mask, void *workspace, int32_t *status, cudaStream_t stream) {
+namespace {
+
+template <int P>
+cudaError_t launch_select_p(const SelectArgs &a, bool aligned, int batch, cudaStream_t stream) {
+  dim3 grid(team_plan<P>(a.nbs, -1, nullptr) > 0 ? team_plan<P>(a.nbs, -1, nullptr) : 1, a.hkv, batch);
+  auto kern = aligned ? select_kernel<P, true> : select_kernel<P, false>;
+  kern<<<grid, kTeamMaxWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t select_rows(const MaskShape &s, const float *s_c, const float *s_r, const float *alpha, int64_t ppm_c,
+                        int64_t ppm_r, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, int32_t *status,
+                        cudaStream_t stream) {
+  const bool al = s.nbs % 4 == 0;
+  const SelectArgs a{s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq, s.total, s.block, s.hkv, s.nbs, s.nbw,
+                     static_cast<long long>(ppm_c), static_cast<long long>(ppm_r), status};
+  if (s.nbw <= 32 * kTeamMaxWarps * 8) return launch_select_p<8>(a, al, s.batch, stream);
+  if (s.nbw <= 32 * kTeamMaxWarps * 16) return launch_select_p<16>(a, al, s.batch, stream);
+  return cudaErrorInvalidValue;
+}
+
+struct Regions {
+  float *q_hi, *q_lo, *nbar, *c_hi, *c_lo, *s_c, *s_r;
+};
+
+Regions regions(const MaskShape &s, void *workspace) {
   const SelectRegions r = select_regions(s);
   char *ws = static_cast<char *>(workspace);
   float *reg[7];
   for (int x = 0; x < 7; ++x) reg[x] = reinterpret_cast<float *>(ws + r.off[x]);
-  float *q_hi = reg[0], *q_lo = reg[1], *nbar = reg[2], *c_hi = reg[3], *c_lo = reg[4];
-  float *s_c = reg[5], *s_r = reg[6];
+  return Regions{reg[0], reg[1], reg[2], reg[3], reg[4], reg[5], reg[6]};
+}
+
+template <int D, int BLK>
+cudaError_t launch_meta_pool_t(const MaskShape &s, const void *q, const void *k, float *centroid, float *radius,
+                               float *quant, float *alpha, const Regions &w, unsigned *done, int32_t *status,
+                               cudaStream_t stream) {
+  const int hpc = qpool_heads(s.hq, D);
+  const int nhc = s.hq / hpc;
+  const long long nmeta = static_cast<long long>(s.nbs) * s.hkv * s.batch;
+  const long long npool = static_cast<long long>(s.nbs) * nhc * s.batch;
+  int npow2 = 2;
+  while (npow2 < s.nbs) npow2 <<= 1;
+  const size_t smem = static_cast<size_t>(npow2) * 4;
+  meta_pool_kernel<D, BLK><<<static_cast<unsigned>(nmeta + npool), kThreads, smem, stream>>>(
+      static_cast<const unsigned char *>(k), static_cast<const unsigned char *>(q), centroid, radius, quant, alpha,
+      w.c_hi, w.c_lo, w.q_hi, w.q_lo, w.nbar, done, s.cu, s.batch, s.seq, s.total, s.hq, s.hkv, s.block, s.nbs, hpc,
+      nhc, status);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_meta_pool_d(const MaskShape &s, const void *q, const void *k, float *centroid, float *radius,
+                               float *quant, float *alpha, const Regions &w, unsigned *done, int32_t *status,
+                               cudaStream_t stream) {
+  switch (s.block) {
+    case 64: return launch_meta_pool_t<D, 64>(s, q, k, centroid, radius, quant, alpha, w, done, status, stream);
+    case 128: return launch_meta_pool_t<D, 128>(s, q, k, centroid, radius, quant, alpha, w, done, status, stream);
+    case 256: return launch_meta_pool_t<D, 256>(s, q, k, centroid, radius, quant, alpha, w, done, status, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_select(const MaskShape &s, const void *q, const float *centroid,
+                          const float *radius, const float *alpha, int64_t ppm_c, int64_t ppm_r,
+                          float scale, bool token_max, int32_t *kv_idx, int32_t *kv_cnt,
+                          uint8_t *mask, void *workspace, int32_t *status, cudaStream_t stream) {
+  const Regions w = regions(s, workspace);
   cudaError_t e;
   if (token_max) {
     // the bf16 centroid splits (2 bytes each, hi then lo) fit in the fp32 c_hi region
-    e = launch_token_scores(s, q, centroid, c_hi, radius, alpha, scale, s_c, s_r, status, stream);
+    e = launch_token_scores(s, q, centroid, w.c_hi, radius, alpha, scale, w.s_c, w.s_r, status, stream);
   } else {
-    if (s.d == 64) e = launch_qpool_d<64>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
-    else if (s.d == 128) e = launch_qpool_d<128>(s, q, q_hi, q_lo, nbar, centroid, c_hi, c_lo, status, stream);
+    if (s.d == 64) e = launch_qpool_d<64>(s, q, w.q_hi, w.q_lo, w.nbar, centroid, w.c_hi, w.c_lo, status, stream);
+    else if (s.d == 128) e = launch_qpool_d<128>(s, q, w.q_hi, w.q_lo, w.nbar, centroid, w.c_hi, w.c_lo, status, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
-    e = launch_scores(s, ScoreOperands{c_hi, c_lo, q_hi, q_lo, nbar, radius, alpha}, scale, s_c, s_r,
+    e = launch_scores(s, ScoreOperands{w.c_hi, w.c_lo, w.q_hi, w.q_lo, w.nbar, radius, alpha}, scale, w.s_c, w.s_r,
                       status, stream);
   }
   if (e != cudaSuccess) return e;
-  const size_t smem = kSelWarps * row_scratch_bytes(s.nbw);
-  const bool aligned = s.nbs % 4 == 0;
-  auto kern = aligned ? select_kernel<true> : select_kernel<false>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  return select_rows(s, w.s_c, w.s_r, alpha, ppm_c, ppm_r, kv_idx, kv_cnt, mask, status, stream);
+}
+
+size_t layer_mask_counter_bytes(const MaskShape &s) { return static_cast<size_t>(s.batch) * s.hkv * 4; }
+
+cudaError_t launch_layer_mask(const MaskShape &s, const void *q, const void *k, float *centroid, float *radius,
+                              float *quant, float *alpha, int64_t ppm_c, int64_t ppm_r, float scale,
+                              int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace, unsigned *done,
+                              int32_t *status, cudaStream_t stream) {
+  if (s.fp8 || (s.d != 64 && s.d != 128)) return cudaErrorInvalidValue;
+  const Regions w = regions(s, workspace);
+  cudaError_t e = cudaMemsetAsync(done, 0, layer_mask_counter_bytes(s), stream);
   if (e != cudaSuccess) return e;
-  dim3 grid((s.nbs + kSelWarps - 1) / kSelWarps, s.hkv, s.batch);
-  kern<<<grid, kSelWarps * 32, smem, stream>>>(s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq, s.total,
-                                               s.block, s.hkv, s.nbs, s.nbw, static_cast<long long>(ppm_c),
-                                               static_cast<long long>(ppm_r), status);
-  return cudaGetLastError();
+  e = s.d == 64 ? launch_meta_pool_d<64>(s, q, k, centroid, radius, quant, alpha, w, done, status, stream)
+                : launch_meta_pool_d<128>(s, q, k, centroid, radius, quant, alpha, w, done, status, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_scores(s, ScoreOperands{w.c_hi, w.c_lo, w.q_hi, w.q_lo, w.nbar, radius, alpha}, scale, w.s_c, w.s_r,
+                    status, stream);
+  if (e != cudaSuccess) return e;
+  return select_rows(s, w.s_c, w.s_r, alpha, ppm_c, ppm_r, kv_idx, kv_cnt, mask, status, stream);
 }
 
 }  // namespace bsa

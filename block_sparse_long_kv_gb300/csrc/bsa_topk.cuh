@@ -1,10 +1,11 @@
-// Warp-level exact top-k over 32-bit order-preserving score keys, shared by
-// the prefill select kernel and the decode select kernel.
+// Exact top-k over 32-bit order-preserving score keys: warp-level helpers (used
+// by the decode select kernel) and the team-of-warps row selection of the
+// prefill select kernel.
 //
-// A row's candidates are keys[0, n) with key 0 marking a non-candidate.  The
-// k best are found by a linear 256-bin histogram of the candidates' values
-// (bins above the threshold bin are in), then an 8-bit-digit radix select over
-// the threshold bin's keys; equal keys at the threshold are ranked by index.
+// A row's candidates carry a nonzero key (key 0 marks a non-candidate).  The k
+// best are found by a linear 256-bin histogram of the candidates' values (bins
+// above the threshold bin are in), then a radix select over the threshold
+// bin's keys; equal keys at the threshold are ranked by index.
 #pragma once
 
 #include <stdint.h>
@@ -13,8 +14,6 @@
 
 namespace bsa {
 namespace topk {
-
-constexpr int kCompact = 256;  // capacity of the per-warp list of threshold-bin keys
 
 // Order-preserving key of a float score: a higher score gives a larger key.
 // Every non-NaN score maps to a key >= 1, so key 0 marks "not a candidate".
@@ -78,173 +77,10 @@ __device__ __forceinline__ void warp_find_bin(const unsigned *hist, unsigned tak
   __syncwarp();
 }
 
-// Radix threshold of the k largest nonzero keys of keys[0, n) (1 <= k < number
-// of nonzero keys), one warp, 8-bit digits from the top.  The selection is:
-// every key with (key & pmask) > prefix, plus the first `take` in index order
-// of the `n_eq` nonzero keys with (key & pmask) == prefix.
-struct Threshold {
-  uint32_t prefix, pmask;
-  unsigned take, n_eq;
-};
-
-__device__ inline Threshold warp_radix_threshold(const uint32_t *keys, int n, unsigned k, unsigned *hist) {
-  const int lane = threadIdx.x & 31;
-  Threshold t{0u, 0u, k, 0u};
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    for (int j0 = 0; j0 < n; j0 += 32) {  // warp-uniform trip count: every lane reaches the match
-      const int j = j0 + lane;
-      const uint32_t key = j < n ? keys[j] : 0u;
-      const bool ok = key != 0u && (key & t.pmask) == t.prefix;
-      const unsigned digit = (key >> shift) & 255u;
-      const unsigned peers = __match_any_sync(0xffffffffu, ok ? digit : 256u);
-      if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-    }
-    __syncwarp();
-    unsigned digit, above, count;
-    warp_find_bin(hist, t.take, &digit, &above, &count);
-    t.take -= above;
-    t.n_eq = count;
-    t.prefix |= digit << shift;
-    t.pmask |= 0xFFu << shift;
-    if (t.n_eq == t.take) break;  // the whole bin is in: no finer digit needed
-  }
-  return t;
-}
-
-// The k best candidates of a row.  A linear 256-bin histogram of the
-// candidates' values over [lo, hi] finds the bin holding the threshold; bins
-// above it are in, and inside it the radix threshold t over the bin's keys
-// (gathered into a short list) decides, unless the whole bin is in.  The bin
-// map is monotone in the value, so this is the exact top-k of the keys.  With
-// no usable value range, or a threshold bin too crowded for the list, every
-// candidate falls in bin 0 and t is taken over the whole row.
-struct RowSelect {
-  float lo, inv;  // bin(v) = min(255, trunc((v - lo) * inv)); inv == 0 maps everything to bin 0
-  int bstar;
-  bool whole;
-  Threshold t;
-};
-
+// Linear value bin of a key over [lo, lo + 256 / inv] (0 .. 255; everything in bin 0 when
+// inv is 0): monotone in the key.
 __device__ __forceinline__ int value_bin(uint32_t key, float lo, float inv) {
   return min(255, static_cast<int>((key_value(key) - lo) * inv));
-}
-
-// keys[0, n) are readable 4 at a time: the entries from n up to the next
-// multiple of 4 are zero.
-__device__ inline RowSelect warp_select(const uint32_t *keys, int n, unsigned k, float lo, float hi,
-                                 unsigned *hist, uint32_t *ckeys) {
-  const int lane = threadIdx.x & 31;
-  RowSelect r;
-  r.lo = lo;
-  r.inv = 0.f;
-  r.bstar = 0;
-  r.whole = false;
-  if (hi > lo) {
-    const float inv = 256.f / (hi - lo);
-    if (inv <= 1.0e38f) r.inv = inv;
-  }
-  if (r.inv > 0.f) {
-    reinterpret_cast<uint4 *>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    for (int j = 4 * lane; j < n; j += 128) {
-      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (kv[e] != 0u) atomicAdd(&hist[value_bin(kv[e], r.lo, r.inv)], 1u);
-    }
-    __syncwarp();
-    unsigned bstar, above, count;
-    warp_find_bin(hist, k, &bstar, &above, &count);
-    r.bstar = static_cast<int>(bstar);
-    const unsigned take = k - above;
-    if (count == take) {
-      r.whole = true;
-      return r;
-    }
-    if (count <= static_cast<unsigned>(kCompact)) {
-      unsigned base = 0;
-      for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
-        const int j = j0 + 4 * lane;
-        uint32_t kv[4] = {0u, 0u, 0u, 0u};
-        unsigned m = 0;
-        if (j < n) {
-          const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-          kv[0] = kk.x; kv[1] = kk.y; kv[2] = kk.z; kv[3] = kk.w;
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (kv[e] != 0u && value_bin(kv[e], r.lo, r.inv) == r.bstar) m |= 1u << e;
-        }
-        unsigned tot;
-        unsigned pos = base + warp_exclusive_scan(__popc(m), &tot);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((m >> e) & 1u) ckeys[pos++] = kv[e];
-        base += tot;
-      }
-      __syncwarp();
-      r.t = warp_radix_threshold(ckeys, static_cast<int>(count), take, hist);
-      return r;
-    }
-  }
-  r.inv = 0.f;
-  r.bstar = 0;
-  r.t = warp_radix_threshold(keys, n, k, hist);
-  return r;
-}
-
-// flags[j] |= bit for the candidates RowSelect r keeps among keys[0, n).  Each
-// lane owns 4 consecutive entries (one flags word); equal keys at the
-// threshold are ranked in index order.
-__device__ inline void warp_mark(const uint32_t *keys, int n, const RowSelect &r, uint8_t *flags, uint8_t bit) {
-  const int lane = threadIdx.x & 31;
-  const bool ranked = !r.whole && r.t.n_eq != r.t.take;
-  unsigned taken = 0;
-  for (int j0 = 0; j0 < n; j0 += 128) {  // warp-uniform trip count for the scan
-    const int j = j0 + 4 * lane;
-    unsigned in = 0, eq = 0;  // bit e: entry j + e
-    if (j < n) {
-      const uint4 kk = reinterpret_cast<const uint4 *>(keys)[j >> 2];
-      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (kv[e] == 0u) continue;
-        const int bn = value_bin(kv[e], r.lo, r.inv);
-        if (bn > r.bstar || (bn == r.bstar && r.whole)) {
-          in |= 1u << e;
-        } else if (bn == r.bstar) {
-          const uint32_t top = kv[e] & r.t.pmask;
-          if (top > r.t.prefix) in |= 1u << e;
-          else if (top == r.t.prefix) eq |= 1u << e;
-        }
-      }
-    }
-    if (ranked) {
-      unsigned tot;
-      unsigned rank = taken + warp_exclusive_scan(__popc(eq), &tot);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((eq >> e) & 1u) {
-          if (rank < r.t.take) in |= 1u << e;
-          ++rank;
-        }
-      taken += tot;
-    } else {
-      in |= eq;
-    }
-    if (in != 0u) {
-      uint32_t *fw = reinterpret_cast<uint32_t *>(flags) + (j >> 2);
-      uint32_t w = *fw;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((in >> e) & 1u) w |= static_cast<uint32_t>(bit) << (8 * e);
-      *fw = w;
-    }
-  }
 }
 
 __device__ __forceinline__ void warp_minmax(float &lo, float &hi) {
@@ -256,98 +92,356 @@ __device__ __forceinline__ void warp_minmax(float &lo, float &hi) {
 }
 
 
-// Per-warp scratch of one row: keys [nbs] u32, hist [256] u32, ckeys [kCompact]
-// u32, flags [nbs] u8 (nbs % 4 == 0 keeps each 16-byte aligned).
-struct RowScratch {
-  uint32_t *keys;
-  unsigned *hist;
-  uint32_t *ckeys;
-  uint8_t *flags;
+// ------------------------------------------------------------------ one team of warps per row
+//
+// The selection of a prefill row, spread over a team of W warps (W a power of two, up to 8), the
+// row's entries held in registers: team thread t owns entries P t .. P t + P - 1, so index order
+// is thread order and every rank is a team-wide prefix sum.  Rows get the smallest team that
+// holds them (32 W P >= the row's length), so short rows cost one warp and long rows finish in
+// a few dozen team barriers instead of one warp walking every entry through each phase.
+// Within the threshold bin the radix digits start at the highest bit on which the bin's keys
+// differ (the bits above it are shared by all of them), so a bin of near-equal values needs
+// one or two passes, not four.  Value bins are computed once per path and kept in registers.
+
+constexpr int kTeamMaxWarps = 8;
+
+struct BinHit {
+  unsigned bin, above, count;
 };
 
-__host__ __device__ constexpr size_t row_scratch_bytes(int nbs) {
-  return static_cast<size_t>(nbs) * 4 + 1024 + kCompact * 4 +
-         ((static_cast<size_t>(nbs) + 15) & ~static_cast<size_t>(15));
+struct TeamScratch {
+  unsigned hist[2][256];                 // alternating histograms; each is zeroed after its search
+  unsigned wsum[2][kTeamMaxWarps];       // alternating per-warp partials of scans and reductions
+  float wlo[2][kTeamMaxWarps], whi[2][kTeamMaxWarps];
+  unsigned res[3];                       // bin search result: bin, entries above, its count
+};
+
+template <int W>
+struct Team {
+  static constexpr int T = 32 * W;       // threads
+  static constexpr int B = 256 / T;      // histogram bins per thread
+  static_assert(W >= 1 && W <= kTeamMaxWarps && (W & (W - 1)) == 0, "team of 1, 2, 4 or 8 warps");
+  TeamScratch &sh;
+  int bar_id;                            // named barrier of the team (W > 1)
+  int t, lane, warp;                     // team-local thread, lane, warp
+  int rot = 0, hrot = 0;                 // alternation of the scratch buffers (team-uniform)
+
+  __device__ Team(TeamScratch &s, int id, int tid) : sh(s), bar_id(id), t(tid), lane(tid & 31), warp(tid >> 5) {}
+
+  __device__ __forceinline__ void sync() const {
+    if constexpr (W == 1) __syncwarp();
+    else asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(T) : "memory");
+  }
+
+  // Exclusive prefix sum over the team in thread order; *total receives the sum.  One barrier;
+  // the alternating partial buffers make back-to-back calls safe.
+  __device__ __forceinline__ unsigned scan(unsigned v, unsigned *total) {
+    unsigned incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if constexpr (W == 1) {
+      *total = __shfl_sync(0xffffffffu, incl, 31);
+      return incl - v;
+    } else {
+      unsigned *wb = sh.wsum[rot];
+      rot ^= 1;
+      if (lane == 31) wb[warp] = incl;
+      sync();
+      unsigned pre = 0, tot = 0;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const unsigned x = wb[w];
+        pre += w < warp ? x : 0u;
+        tot += x;
+      }
+      *total = tot;
+      return pre + incl - v;
+    }
+  }
+
+  // Team-wide min / max of lo / hi and sum of n.
+  __device__ __forceinline__ void minmax_count(float &lo, float &hi, unsigned &n) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+      n += __shfl_xor_sync(0xffffffffu, n, off);
+    }
+    if constexpr (W > 1) {
+      const int r = rot;
+      rot ^= 1;
+      if (lane == 0) {
+        sh.wlo[r][warp] = lo;
+        sh.whi[r][warp] = hi;
+        sh.wsum[r][warp] = n;
+      }
+      sync();
+      lo = sh.wlo[r][0];
+      hi = sh.whi[r][0];
+      n = sh.wsum[r][0];
+#pragma unroll
+      for (int w = 1; w < W; ++w) {
+        lo = fminf(lo, sh.wlo[r][w]);
+        hi = fmaxf(hi, sh.whi[r][w]);
+        n += sh.wsum[r][w];
+      }
+    }
+  }
+
+  // Team-wide AND and OR.
+  __device__ __forceinline__ void and_or(uint32_t &a, uint32_t &o) {
+    a = __reduce_and_sync(0xffffffffu, a);
+    o = __reduce_or_sync(0xffffffffu, o);
+    if constexpr (W > 1) {
+      const int r = rot;
+      rot ^= 1;
+      if (lane == 0) {
+        sh.wsum[r][warp] = a;
+        reinterpret_cast<uint32_t *>(sh.wlo[r])[warp] = o;
+      }
+      sync();
+      a = 0xFFFFFFFFu;
+      o = 0u;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        a &= sh.wsum[r][w];
+        o |= reinterpret_cast<const uint32_t *>(sh.wlo[r])[w];
+      }
+    }
+  }
+
+  // In histogram h (256 bins), the bin holding the take-th largest entry counting down from the
+  // top bin, the entries in the bins above it and its own count (1 <= take <= total).  Thread t
+  // reads bins 255 - B t - e, e < B (thread order = descending bins); afterwards it zeroes them
+  // for the histogram's next use (every team thread has read its bins by then).
+  __device__ __forceinline__ BinHit find_bin(unsigned *h, unsigned take) {
+    unsigned c[B], sum = 0;
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      c[e] = h[255 - B * t - e];
+      sum += c[e];
+    }
+    unsigned tot;
+    unsigned before = scan(sum, &tot);
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      if (before < take && take <= before + c[e]) {
+        sh.res[0] = 255u - B * t - e;
+        sh.res[1] = before;
+        sh.res[2] = c[e];
+      }
+      before += c[e];
+    }
+    sync();
+    const BinHit r{sh.res[0], sh.res[1], sh.res[2]};
+#pragma unroll
+    for (int e = 0; e < B; ++e) h[255 - B * t - e] = 0u;
+    return r;
+  }
+
+  // Both histograms to zero (before the row's first barrier).
+  __device__ __forceinline__ void clear_hist() {
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      sh.hist[0][B * t + e] = 0u;
+      sh.hist[1][B * t + e] = 0u;
+    }
+  }
+};
+
+// Outcome of one path's selection: value bins above bstar are in (all of bstar when whole);
+// inside bstar a key is in when (key & pmask) > prefix, and of the keys with (key & pmask) ==
+// prefix the first `take` in index order.
+struct TeamSel {
+  int bstar;
+  bool whole;
+  uint32_t prefix, pmask;
+  unsigned take, n_eq;
+};
+
+// The k best of the nonzero keys among the team's registers (1 <= k < number of nonzero keys);
+// bin[x]: value bin of key x (monotone in the key).  Both histograms are zero on entry and exit.
+template <int W, int P>
+__device__ inline TeamSel team_select(Team<W> &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], unsigned k) {
+  TeamSel r;
+  r.whole = false;
+  r.prefix = 0u;
+  r.pmask = 0u;
+  {
+    unsigned *h = tm.sh.hist[tm.hrot];
+    tm.hrot ^= 1;
+#pragma unroll
+    for (int x = 0; x < P; ++x)
+      if (key[x] != 0u) atomicAdd(&h[bin[x]], 1u);
+    tm.sync();
+    const BinHit b = tm.find_bin(h, k);
+    r.bstar = static_cast<int>(b.bin);
+    r.take = k - b.above;
+    r.n_eq = b.count;
+    if (b.count == r.take) {
+      r.whole = true;
+      return r;
+    }
+  }
+  // the bits every key of the threshold bin shares need no pass
+  uint32_t a = 0xFFFFFFFFu, o = 0u;
+#pragma unroll
+  for (int x = 0; x < P; ++x)
+    if (key[x] != 0u && bin[x] == r.bstar) {
+      a &= key[x];
+      o |= key[x];
+    }
+  tm.and_or(a, o);
+  const uint32_t diff = a ^ o;
+  if (diff == 0u) {  // every key of the bin is equal: index order decides
+    r.prefix = a;
+    r.pmask = 0xFFFFFFFFu;
+    return r;
+  }
+  int top = 31 - __clz(diff);
+  r.pmask = ~((2u << top) - 1u);  // bits above top (none when top is 31)
+  r.prefix = a & r.pmask;
+  while (top >= 0) {
+    const int shift = top >= 7 ? top - 7 : 0;
+    const uint32_t dmask = (2u << (top - shift)) - 1u;  // digit width top - shift + 1 <= 8
+    unsigned *h = tm.sh.hist[tm.hrot];
+    tm.hrot ^= 1;
+#pragma unroll
+    for (int x = 0; x < P; ++x) {
+      const uint32_t kv = key[x];
+      const bool ok = kv != 0u && bin[x] == r.bstar && (kv & r.pmask) == r.prefix;
+      if (ok) atomicAdd(&h[(kv >> shift) & dmask], 1u);
+    }
+    tm.sync();
+    const BinHit d = tm.find_bin(h, r.take);
+    r.take -= d.above;
+    r.n_eq = d.count;
+    r.prefix |= d.bin << shift;
+    r.pmask |= dmask << shift;
+    if (r.n_eq == r.take) break;  // the whole digit bin is in
+    top = shift - 1;
+  }
+  return r;
 }
 
-__device__ __forceinline__ RowScratch row_scratch(unsigned char *base, int nbs) {
-  RowScratch w;
-  w.keys = reinterpret_cast<uint32_t *>(base);
-  w.hist = reinterpret_cast<unsigned *>(base + static_cast<size_t>(nbs) * 4);
-  w.ckeys = reinterpret_cast<uint32_t *>(base + static_cast<size_t>(nbs) * 4 + 1024);
-  w.flags = base + static_cast<size_t>(nbs) * 4 + 1024 + kCompact * 4;
-  return w;
+// Sets `bit` in the flag bytes of the entries TeamSel r keeps (entry x: byte x % 4 of
+// fl[x / 4]); equal keys at the threshold are ranked in index order.
+template <int W, int P>
+__device__ inline void team_mark(Team<W> &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], const TeamSel &r,
+                                 uint32_t (&fl)[P / 4], uint32_t bit) {
+  unsigned in = 0u, eq = 0u;  // bit x: entry x
+#pragma unroll
+  for (int x = 0; x < P; ++x) {
+    const uint32_t kv = key[x];
+    if (kv == 0u) continue;
+    const int bn = bin[x];
+    if (bn > r.bstar || (bn == r.bstar && r.whole)) {
+      in |= 1u << x;
+    } else if (bn == r.bstar) {
+      const uint32_t tp = kv & r.pmask;
+      if (tp > r.prefix) in |= 1u << x;
+      else if (tp == r.prefix) eq |= 1u << x;
+    }
+  }
+  if (!r.whole && r.n_eq != r.take) {  // team-uniform
+    unsigned tot;
+    unsigned rank = tm.scan(__popc(eq), &tot);
+#pragma unroll
+    for (int x = 0; x < P; ++x)
+      if ((eq >> x) & 1u) {
+        if (rank < r.take) in |= 1u << x;
+        ++rank;
+      }
+  } else {
+    in |= eq;
+  }
+#pragma unroll
+  for (int x = 0; x < P; ++x)
+    if ((in >> x) & 1u) fl[x / 4] |= bit << (8 * (x % 4));
 }
 
-// Selection of one row i by one warp: key blocks 0 and i forced, the top kc
-// of the candidates 1..i-1 by rc, then among the candidates the centroid path
-// dropped whose alpha is positive the top kr by rr; keep counts
-// ceil(ratio * (i + 1)) from ppm, clipped to the candidates.  rc and rr point
-// at 16-byte aligned rows readable for round_up(i + 1, 4) entries (shared or
-// global memory); so does ab (alpha) when AB_ALIGNED, otherwise ab is read one
-// entry at a time and only for j < i.  Leaves the BSA_MASK_* bits in
-// w.flags[0..i] and zeros up to round_up(i + 1, 4).
-template <bool AB_ALIGNED = true>
-__device__ inline void warp_select_row(const float *rc, const float *rr, const float *ab, int i,
-                                       long long ppm_c, long long ppm_r, const RowScratch &w) {
-  const int lane = threadIdx.x & 31;
-  uint32_t *keys = w.keys;
-  uint8_t *flags = w.flags;
-  const int n4 = (i + 4) & ~3;  // keys / flags [0, n4) cover 0..i; entries j >= i are never candidates
+// Value bins of the keys over [lo, hi] (256 linear bins; everything in bin 0 without a usable
+// range).  Monotone in the key, so the top-k of the keys is decided bin by bin.
+template <int P>
+__device__ __forceinline__ void value_bins(const uint32_t (&key)[P], float lo, float hi, uint8_t (&bin)[P]) {
+  float inv = 0.f;
+  if (hi > lo) {
+    const float x = 256.f / (hi - lo);
+    if (x <= 1.0e38f) inv = x;
+  }
+#pragma unroll
+  for (int x = 0; x < P; ++x) bin[x] = key[x] != 0u ? static_cast<uint8_t>(value_bin(key[x], lo, inv)) : 0;
+}
+
+// Selection of row i by a team: key blocks 0 and i forced, the top kc of candidates 1..i-1 by
+// rc, then the top kr by rr among the candidates the centroid path dropped whose alpha is
+// positive; keep counts ceil(ratio (i + 1)) from ppm, clipped to the candidates.  rc and rr:
+// 16-byte aligned rows readable for round_up(i + 1, 4) entries; ab (alpha) likewise when
+// AB_ALIGNED, else read one entry at a time for j < i.  32 W P >= i + 1.  Leaves the BSA_MASK_*
+// bits of entry P t + x in byte x % 4 of fl[x / 4] (zero past i).  Both histograms must be zero
+// and ordered before the team's first barrier.
+template <int W, int P, bool AB_ALIGNED>
+__device__ inline void team_select_row(Team<W> &tm, const float *rc, const float *rr, const float *ab, int i,
+                                       long long ppm_c, long long ppm_r, uint32_t (&fl)[P / 4]) {
+  static_assert(P % 4 == 0 && P <= 32, "whole 16-byte groups, one mask bit per entry");
+  const int j0 = P * tm.t;
+  const int n4 = (i + 4) & ~3;
+  uint32_t key[P];
+  uint8_t bin[P];
+#pragma unroll
+  for (int x = 0; x < P / 4; ++x) fl[x] = 0u;
 
   // ---- centroid path: top kc of candidates 1..i-1 by S_c
-  // (the row is read in batches of eight 16-byte loads per lane, all issued before any is used)
-  constexpr int LB = 4;
   float lo = INFINITY, hi = -INFINITY;
-  for (int jb = lane * 4; jb < n4; jb += 128 * LB) {
-    float4 v[LB];
+  {
+    float4 v[P / 4];
 #pragma unroll
-    for (int u = 0; u < LB; ++u) {
-      const int j4 = jb + u * 128;
+    for (int u = 0; u < P / 4; ++u) {
+      const int j4 = j0 + 4 * u;
       v[u] = j4 < n4 ? reinterpret_cast<const float4 *>(rc)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < LB; ++u) {
-      const int j4 = jb + u * 128;
-      if (j4 >= n4) continue;
-      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t kp[4];
+    for (int u = 0; u < P / 4; ++u) {
+      const float xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int j = j4 + e;
+        const int j = j0 + 4 * u + e;
         const bool cand = j >= 1 && j < i;
-        kp[e] = cand ? score_key(x[e]) : 0u;
+        key[4 * u + e] = cand ? score_key(xs[e]) : 0u;
         if (cand) {
-          lo = fminf(lo, x[e]);
-          hi = fmaxf(hi, x[e]);
+          lo = fminf(lo, xs[e]);
+          hi = fmaxf(hi, xs[e]);
         }
       }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
-      reinterpret_cast<uint32_t *>(flags)[j4 >> 2] = 0u;
     }
   }
-  warp_minmax(lo, hi);
-  __syncwarp();
   const int ncand = i > 1 ? i - 1 : 0;
   const long long kc_full = (ppm_c * (i + 1) + 999999LL) / 1000000LL;
   const int kc = static_cast<int>(kc_full < ncand ? kc_full : ncand);
   if (kc == ncand) {
-    for (int j = 1 + lane; j < i; j += 32) flags[j] = BSA_MASK_CENTROID;
+#pragma unroll
+    for (int x = 0; x < P; ++x)
+      if (key[x] != 0u) fl[x / 4] |= BSA_MASK_CENTROID << (8 * (x % 4));
   } else if (kc > 0) {
-    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kc), lo, hi, w.hist, w.ckeys);
-    warp_mark(keys, i, r, flags, BSA_MASK_CENTROID);
+    unsigned dummy = 0u;
+    tm.minmax_count(lo, hi, dummy);
+    value_bins<P>(key, lo, hi, bin);
+    const TeamSel r = team_select<W, P>(tm, key, bin, static_cast<unsigned>(kc));
+    team_mark<W, P>(tm, key, bin, r, fl, BSA_MASK_CENTROID);
   }
-  __syncwarp();
 
   // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
-  int nelig = 0;
+  unsigned nelig = 0u;
   lo = INFINITY;
   hi = -INFINITY;
-  for (int jb = lane * 4; jb < n4; jb += 128 * (LB / 2)) {
-    float4 v[LB / 2], a[LB / 2];
+  {
+    float4 v[P / 4], a[P / 4];
 #pragma unroll
-    for (int u = 0; u < LB / 2; ++u) {
-      const int j4 = jb + u * 128;
+    for (int u = 0; u < P / 4; ++u) {
+      const int j4 = j0 + 4 * u;
       const bool in = j4 < n4;
       v[u] = in ? reinterpret_cast<const float4 *>(rr)[j4 >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
       if constexpr (AB_ALIGNED) {
@@ -358,79 +452,77 @@ __device__ inline void warp_select_row(const float *rc, const float *rr, const f
       }
     }
 #pragma unroll
-    for (int u = 0; u < LB / 2; ++u) {
-      const int j4 = jb + u * 128;
-      if (j4 >= n4) continue;
-      const uint32_t f4 = reinterpret_cast<const uint32_t *>(flags)[j4 >> 2];
-      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w}, al[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-      uint32_t kp[4];
+    for (int u = 0; u < P / 4; ++u) {
+      const float xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w}, al[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int j = j4 + e;
-        const bool elig = j >= 1 && j < i && al[e] > 0.f && ((f4 >> (8 * e)) & BSA_MASK_CENTROID) == 0;
-        kp[e] = elig ? score_key(x[e]) : 0u;
-        nelig += elig ? 1 : 0;
+        const int x = 4 * u + e;
+        const int j = j0 + x;
+        const bool elig = j >= 1 && j < i && al[e] > 0.f && ((fl[u] >> (8 * e)) & BSA_MASK_CENTROID) == 0u;
+        key[x] = elig ? score_key(xs[e]) : 0u;
+        nelig += elig ? 1u : 0u;
         if (elig) {
-          lo = fminf(lo, x[e]);
-          hi = fmaxf(hi, x[e]);
+          lo = fminf(lo, xs[e]);
+          hi = fmaxf(hi, xs[e]);
         }
       }
-      reinterpret_cast<uint4 *>(keys)[j4 >> 2] = make_uint4(kp[0], kp[1], kp[2], kp[3]);
     }
+  }
+  tm.minmax_count(lo, hi, nelig);
+  const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
+  const int kr = static_cast<int>(kr_full < static_cast<long long>(nelig) ? kr_full : static_cast<long long>(nelig));
+  if (kr > 0 && kr == static_cast<int>(nelig)) {
+#pragma unroll
+    for (int x = 0; x < P; ++x)
+      if (key[x] != 0u) fl[x / 4] |= BSA_MASK_RESCUE << (8 * (x % 4));
+  } else if (kr > 0) {
+    value_bins<P>(key, lo, hi, bin);
+    const TeamSel r = team_select<W, P>(tm, key, bin, static_cast<unsigned>(kr));
+    team_mark<W, P>(tm, key, bin, r, fl, BSA_MASK_RESCUE);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) nelig += __shfl_xor_sync(0xffffffffu, nelig, off);
-  warp_minmax(lo, hi);
-  __syncwarp();
-  const long long kr_full = (ppm_r * (i + 1) + 999999LL) / 1000000LL;
-  const int kr = static_cast<int>(kr_full < nelig ? kr_full : nelig);
-  if (kr > 0 && kr == nelig) {
-    for (int j = lane; j < i; j += 32)
-      if (keys[j] != 0u) flags[j] |= BSA_MASK_RESCUE;
-  } else if (kr > 0) {
-    const RowSelect r = warp_select(keys, i, static_cast<unsigned>(kr), lo, hi, w.hist, w.ckeys);
-    warp_mark(keys, i, r, flags, BSA_MASK_RESCUE);
+  for (int x = 0; x < P; ++x) {
+    const int j = j0 + x;
+    if (j == 0 || j == i) fl[x / 4] |= BSA_MASK_FORCED << (8 * (x % 4));
   }
-  __syncwarp();
-  if (lane == 0) {
-    flags[0] |= BSA_MASK_FORCED;
-    flags[i] |= BSA_MASK_FORCED;
-  }
-  __syncwarp();
 }
 
-// Writes the ascending kept list of row i (w.flags[0..i]) to dst and its
-// length to *cnt; with mrow, also the row's mask bits (nbs bytes, zero past i),
-// four bytes per store when MROW_ALIGNED (mrow 4-byte aligned, nbs % 4 == 0),
-// else byte by byte.
-template <bool MROW_ALIGNED = true>
-__device__ inline void warp_emit_row(const RowScratch &w, int i, int32_t *dst, int32_t *cnt,
+// Writes row i's ascending kept list (entries whose flag byte is nonzero) to dst and its length
+// to *cnt; with mrow, also the mask bytes (nbs of them, zero past i), a word per store when
+// MROW_ALIGNED (mrow 4-byte aligned, nbs % 4 == 0), else byte by byte.  32 W P >= nbs is not
+// required: entries past the team's reach are zero-filled by the lanes that reach them.
+template <int W, int P, bool MROW_ALIGNED>
+__device__ inline void team_emit_row(Team<W> &tm, const uint32_t (&fl)[P / 4], int i, int32_t *dst, int32_t *cnt,
                                      uint8_t *mrow, int nbs) {
-  const int lane = threadIdx.x & 31;
-  const unsigned lt = (1u << lane) - 1u;
-  int kept = 0;
-  for (int j0 = 0; j0 <= i; j0 += 32) {
-    const int j = j0 + lane;
-    const bool keep = j <= i && w.flags[j] != 0;
-    const unsigned bl = __ballot_sync(0xffffffffu, keep);
-    if (keep) dst[kept + __popc(bl & lt)] = j;
-    kept += __popc(bl);
-  }
-  if (lane == 0) *cnt = kept;
-  if (!MROW_ALIGNED && mrow != nullptr) {
-    for (int j = lane; j < nbs; j += 32) mrow[j] = j <= i ? w.flags[j] : 0u;
-    return;
-  }
-  if (mrow != nullptr) {
-    uint32_t *m4 = reinterpret_cast<uint32_t *>(mrow);
-    for (int j4 = lane * 4; j4 < nbs; j4 += 128) {
-      uint32_t m = 0;
-      if (j4 <= i) {
-        m = reinterpret_cast<const uint32_t *>(w.flags)[j4 >> 2];
-        if (j4 + 3 > i) m &= 0xFFFFFFFFu >> (8 * (j4 + 3 - i));  // zero the bytes past i
-      }
-      m4[j4 >> 2] = m;
+  const int j0 = P * tm.t;
+  unsigned mine = 0u;
+#pragma unroll
+  for (int x = 0; x < P; ++x) mine += ((fl[x / 4] >> (8 * (x % 4))) & 0xFFu) != 0u ? 1u : 0u;
+  unsigned tot;
+  unsigned pos = tm.scan(mine, &tot);
+#pragma unroll
+  for (int x = 0; x < P; ++x)
+    if (((fl[x / 4] >> (8 * (x % 4))) & 0xFFu) != 0u) dst[pos++] = j0 + x;
+  if (tm.t == 0) *cnt = static_cast<int32_t>(tot);
+  if (mrow == nullptr) return;
+  // the row's mask: the team's own entries, then zeros up to nbs (past 32 W P)
+#pragma unroll
+  for (int u = 0; u < P / 4; ++u) {
+    const int j4 = j0 + 4 * u;
+    if (j4 >= nbs) continue;
+    if constexpr (MROW_ALIGNED) {
+      reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = fl[u];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j4 + e < nbs) mrow[j4 + e] = static_cast<uint8_t>(fl[u] >> (8 * e));
     }
+  }
+  if constexpr (MROW_ALIGNED) {
+    for (int j4 = Team<W>::T * P + 4 * tm.t; j4 < nbs; j4 += 4 * Team<W>::T)
+      reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = 0u;
+  } else {
+    for (int j = Team<W>::T * P + tm.t; j < nbs; j += Team<W>::T) mrow[j] = 0u;
   }
 }
 

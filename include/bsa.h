@@ -185,6 +185,32 @@ bsa_status bsa_select_mask_noalloc(const bsa_shape *shape, const bsa_select_para
                                    uint8_t *mask, int32_t *dev_status, bsa_stream_t stream);
 
 /*
+ * bsa_mask_build - bsa_block_meta followed by bsa_select_mask, in fewer launches.
+ *
+ * Rescue branch section, the whole mask construction of one layer: the same
+ * centroid, radius, quant, alpha, kv_idx, kv_cnt and (nullable) mask as the
+ * two calls made one after the other on `stream` with the same arguments, bit
+ * for bit.  The key-block summaries and the query-block means are computed in
+ * one launch that streams K and Q together, and the quantiles are taken inside
+ * it, so the build costs three kernels instead of five.
+ * params->flags must be 0 (block-mean queries; per-token aggregation goes
+ * through bsa_block_meta and bsa_select_mask).  q: bf16 [batch, seq, hq,
+ * head_dim]; k: bf16 [batch, seq, hkv, head_dim]; every output as documented
+ * for the two calls, caller-allocated, 16-byte aligned.  workspace: device
+ * scratch of at least bsa_mask_build_workspace_bytes(shape) bytes, 16-byte
+ * aligned, owned by the caller; its contents need no initialisation (the call
+ * zeroes the counters it keeps there) and are dead once the call's kernels
+ * finish.  Errors: shape errors, then parameter and pointer errors
+ * (BSA_ERR_INVALID_ARG), then BSA_ERR_WORKSPACE, all before any launch;
+ * BSA_ERR_CUDA if a launch fails.  dev_status as bsa_select_mask.
+ */
+size_t bsa_mask_build_workspace_bytes(const bsa_shape *shape);
+bsa_status bsa_mask_build(const bsa_shape *shape, const bsa_select_params *params, const void *q,
+                          const void *k, float *centroid, float *radius, float *quant, float *alpha,
+                          int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, void *workspace,
+                          size_t workspace_bytes, int32_t *dev_status, bsa_stream_t stream);
+
+/*
  * bsa_prefill_fwd - causal attention over the kept key blocks.
  *
  * Rescue branch section: the combined mask is consumed by an ordinary
@@ -210,10 +236,11 @@ bsa_status bsa_prefill_dense_fwd(const bsa_shape *shape, const void *q, const vo
 
 /*
  * bsa_prefill_layer - one whole layer of the hot path in one call:
- * bsa_block_meta, bsa_select_mask, then bsa_prefill_fwd, all on `stream`.
+ * bsa_mask_build (bsa_block_meta then bsa_select_mask when params->flags is
+ * BSA_SELECT_TOKEN_MAX), then bsa_prefill_fwd, all on `stream`.
  * The intermediate tensors live in `workspace` (device, 256-byte aligned, at
  * least bsa_prefill_layer_workspace_bytes(shape) bytes): centroid, radius,
- * quant, alpha, kv_idx, kv_cnt and the select scratch.  bsa_prefill_layer_views
+ * quant, alpha, kv_idx, kv_cnt and the mask build scratch.  bsa_prefill_layer_views
  * gives the offsets of the first six.
  */
 size_t bsa_prefill_layer_workspace_bytes(const bsa_shape *shape);

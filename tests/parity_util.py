@@ -45,7 +45,9 @@ def shape_of(w):
 
 
 def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda", flags=0):
-    """Run bsa_block_meta + bsa_select_mask; return numpy results."""
+    """Run bsa_block_meta + bsa_select_mask; return numpy results.  With block-mean queries
+    (flags 0) also run bsa_mask_build on the same inputs and require the same outputs bit for
+    bit (kv_idx up to each row's kv_cnt: entries past it are unspecified)."""
     import block_sparse_long_kv_gb300 as bsa
     s = shape_of(w)
     q, k = to_dev(lay["q"], device), to_dev(lay["k"], device)
@@ -60,7 +62,29 @@ def gpu_mask_build(w, lay, centroid_keep=None, rescue_keep=None, device="cuda", 
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     out = {kk: v.cpu().numpy() for kk, v in {**meta, **sel}.items()}
+    if flags == 0:
+        check_fused_build(s, prm, q, k, out, device)
     return out
+
+
+def check_fused_build(s, prm, q, k, want, device="cuda"):
+    """bsa_mask_build gives `want` (the two-call results) bit for bit."""
+    import block_sparse_long_kv_gb300 as bsa
+    meta = bsa.alloc_meta(s, device)
+    sel = bsa.alloc_select(s, device, with_mask=True)
+    for t in (*meta.values(), *sel.values()):
+        t.fill_(-7 if t.dtype != torch.uint8 else 0xA5)  # nothing may survive from before the call
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    bsa.mask_build(s, prm, q, k, meta["centroid"], meta["radius"], meta["quant"], meta["alpha"],
+                   sel["kv_idx"], sel["kv_cnt"], sel["mask"], dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = {kk: v.cpu().numpy() for kk, v in {**meta, **sel}.items()}
+    for x in ("centroid", "radius", "quant", "alpha", "kv_cnt", "mask"):
+        np.testing.assert_array_equal(got[x], want[x], err_msg=f"bsa_mask_build {x}")
+    cnt = want["kv_cnt"]
+    live = np.arange(want["kv_idx"].shape[-1]) < cnt[..., None]
+    np.testing.assert_array_equal(got["kv_idx"][live], want["kv_idx"][live], err_msg="bsa_mask_build kv_idx")
 
 
 def check_lists_match_mask(mask, kv_idx, kv_cnt):

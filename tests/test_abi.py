@@ -257,3 +257,39 @@ def test_noalloc_scratch_boundary(lib):
     prm = _lib.SelectParams(0.1, 0.02, 0)
     assert lib.bsa_select_mask_noalloc(ctypes.byref(bad), ctypes.byref(prm), f, f, f, f, f, f,
                                        None, None, None) == 2
+
+
+def test_mask_build_validation_and_workspace(lib):
+    """bsa_mask_build: shape, parameter, pointer and workspace errors before any launch; its
+    workspace is the select scratch plus one counter per (batch, KV head), 256-byte rounded."""
+    from block_sparse_long_kv_gb300 import _lib
+    s = shp(batch=2, seq=9 * 128, hq=32, hkv=4, head_dim=128, block=128)
+    sel = lib.bsa_select_workspace_bytes(ctypes.byref(s))
+    need = lib.bsa_mask_build_workspace_bytes(ctypes.byref(s))
+    assert need == (sel + 255) // 256 * 256 + 2 * 4 * 4
+    bad = shp(seq=1000)
+    assert lib.bsa_mask_build_workspace_bytes(ctypes.byref(bad)) == 0
+    f = ctypes.c_void_p(FAKE)
+    m = ctypes.c_void_p(MIS)
+    ok = _lib.SelectParams(0.1, 0.02, 0)
+
+    def call(shape=s, prm=ok, q=f, k=f, outs=(f,) * 6, mask=None, ws=f, nbytes=need):
+        return lib.bsa_mask_build(ctypes.byref(shape), None if prm is None else ctypes.byref(prm), q, k,
+                                  *outs, mask, ws, ctypes.c_size_t(nbytes), None, None)
+
+    assert call(shape=bad) == 2
+    assert call(prm=None) == 1
+    assert call(prm=_lib.SelectParams(0.1, 0.02, 1)) == 1      # per-token aggregation: two-call path
+    assert call(prm=_lib.SelectParams(1.5, 0.02, 0)) == 1
+    assert call(prm=_lib.SelectParams(float("nan"), 0.02, 0)) == 1
+    assert call(q=None) == 1 and call(k=None) == 1
+    assert call(q=m) == 1 and call(k=m) == 1
+    for x in range(6):
+        outs = [f] * 6
+        outs[x] = None
+        assert call(outs=tuple(outs)) == 1
+        outs[x] = m
+        assert call(outs=tuple(outs)) == 1
+    assert call(mask=m) == 1
+    assert call(ws=None) == 4 and call(ws=m) == 4
+    assert call(nbytes=need - 1) == 4
