@@ -799,16 +799,18 @@ def run_ours(args):
         "clocks": clk,
     }
     # the softmax's exponentials: one ex2 on the MUFU units per needed S element (the diagonal
-    # block's causal half counted), i.e. kept FLOPs / (4 d); MUFU peak = 16 per clock per SM
+    # block's causal half counted), i.e. kept FLOPs / (4 d).  MUFU peak: 32 ex2 results per
+    # clock per SM on this part (twice the 16 of earlier Blackwell SMs); ncu agrees: the XU pipe
+    # (sm__inst_executed_pipe_xu) runs at about 30 % of its peak when this rate is 0.29 of 32
     exps = fl / (4.0 * w.head_dim)
     sm_mhz = clk.get("sm_mhz") if isinstance(clk, dict) else None
-    mufu_peak = 16 * 152 * (sm_mhz or 2070.0) * 1e6 / 1e9
+    mufu_peak = 32 * 152 * (sm_mhz or 2070.0) * 1e6 / 1e9
     exp_rate = float((exps / (att_ms * 1e-3)).mean() / 1e9)
     result["roofline_exp"] = {
         "kernel": "attn_kernel softmax (ex2.approx on MUFU)", "bound": "alu", "achieved": exp_rate,
         "peak": mufu_peak, "unit": "Gexp/s", "frac": exp_rate / mufu_peak,
         "exps_per_launch": float(np.mean(exps)),
-        "peak_source": "16 MUFU ex2 results per clock per SM x 152 SMs x the median SM clock of the "
+        "peak_source": "32 MUFU ex2 results per clock per SM x 152 SMs x the median SM clock of the "
                        "timed region" + ("" if sm_mhz else " (not sampled: 2070 MHz maximum)")}
     if args.token_max:
         # per-token scores are a dense contraction: report the select call against the bf16 peak

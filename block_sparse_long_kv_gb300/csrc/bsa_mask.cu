@@ -566,33 +566,35 @@ __global__ void __launch_bounds__(kThreads, (meta_min_blocks<D, BLK>())) meta_po
 
 using namespace topk;
 
-// Rows of one (b, g) go to teams of W warps (topk::Team), W the smallest power of
-// two with 32 W P >= i + 1, packed kTeamMaxWarps / W teams to a CTA of
-// kTeamMaxWarps warps; the widest class comes first and, inside a class, the
-// longest row.  Class W holds the rows with 16 P W < i + 1 <= 32 P W (those
-// with i + 1 <= 32 P for W = 1).  Returns the CTAs of a row set of nbs rows;
-// with cta >= 0 also the class, the first (longest) row and the team count of
-// CTA `cta`.
+// Rows go to teams of W warps (topk::Team), W the smallest power of two with
+// 32 W P >= i + 1, packed kTeamMaxWarps / W teams to a CTA of kTeamMaxWarps
+// warps.  Class W holds the rows with 16 P W < i + 1 <= 32 P W (those with
+// i + 1 <= 32 P for W = 1).  The grid runs class by class, widest first, and
+// within a class group by group (b, g) and longest row first, so the CTAs
+// resident at one time mostly run one team width's code.  Returns the CTAs of
+// `groups` row sets of nbs rows each; with cta >= 0 also the class, the
+// group, the first (longest) row and the team count of CTA `cta`.
 struct TeamPlan {
-  int w, first_row, teams;
+  int w, group, first_row, teams;
 };
 
 template <int P>
-__host__ __device__ inline int team_plan(int nbs, int cta, TeamPlan *plan) {
+__host__ __device__ inline int team_plan(int nbs, int groups, int cta, TeamPlan *plan) {
   int total = 0;
   for (int w = kTeamMaxWarps; w >= 1; w >>= 1) {
     const int hi_n = nbs < 32 * P * w ? nbs : 32 * P * w;
     const int lo_n = w == 1 ? 1 : 16 * P * w + 1;
     if (hi_n < lo_n) continue;
     const int rows = hi_n - lo_n + 1, tpc = kTeamMaxWarps / w;
-    const int ctas = (rows + tpc - 1) / tpc;
-    if (cta >= total && cta < total + ctas) {
-      const int k = cta - total;
+    const int ctas = (rows + tpc - 1) / tpc;  // per group
+    if (cta >= total && cta < total + ctas * groups) {
+      const int k = (cta - total) % ctas;
       plan->w = w;
+      plan->group = (cta - total) / ctas;
       plan->first_row = hi_n - 1 - k * tpc;
       plan->teams = rows - k * tpc < tpc ? rows - k * tpc : tpc;
     }
-    total += ctas;
+    total += ctas * groups;
   }
   return total;
 }
@@ -602,7 +604,7 @@ struct SelectArgs {
   int32_t *kv_idx, *kv_cnt;
   uint8_t *mask;
   const int32_t *cu;
-  int seq, total, block, hkv, nbs, nbw;
+  int batch, seq, total, block, hkv, nbs, nbw;
   long long ppm_c, ppm_r;
   int32_t *status;
 };
@@ -650,11 +652,11 @@ __device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int i
 template <int P, bool ALIGNED>
 __global__ void __launch_bounds__(kTeamMaxWarps * 32, (P <= 8 ? 4 : 2)) select_kernel(const __grid_constant__ SelectArgs a) {
   __shared__ TeamScratch sh[kTeamMaxWarps];
-  TeamPlan plan{1, 0, 0};
-  team_plan<P>(a.nbs, static_cast<int>(blockIdx.x), &plan);
+  TeamPlan plan{1, 0, 0, 0};
+  team_plan<P>(a.nbs, a.batch * a.hkv, static_cast<int>(blockIdx.x), &plan);
   const int team = static_cast<int>(threadIdx.x >> 5) / plan.w;
   if (team >= plan.teams) return;  // whole teams leave; barriers are per team
-  const int i = plan.first_row - team, g = blockIdx.y, b = blockIdx.z;
+  const int i = plan.first_row - team, g = plan.group % a.hkv, b = plan.group / a.hkv;
   switch (plan.w) {
     case 1: select_team_row<1, P, ALIGNED>(sh[team], team, i, b, g, a); break;
     case 2: select_team_row<2, P, ALIGNED>(sh[team], team, i, b, g, a); break;
@@ -776,8 +778,9 @@ cudaError_t launch_quantiles(const MaskShape &s, const float *radius, float *qua
 namespace {
 
 template <int P>
-cudaError_t launch_select_p(const SelectArgs &a, bool aligned, int batch, cudaStream_t stream) {
-  dim3 grid(team_plan<P>(a.nbs, -1, nullptr) > 0 ? team_plan<P>(a.nbs, -1, nullptr) : 1, a.hkv, batch);
+cudaError_t launch_select_p(const SelectArgs &a, bool aligned, cudaStream_t stream) {
+  const int ctas = team_plan<P>(a.nbs, a.batch * a.hkv, -1, nullptr);
+  dim3 grid(ctas > 0 ? ctas : 1);
   auto kern = aligned ? select_kernel<P, true> : select_kernel<P, false>;
   kern<<<grid, kTeamMaxWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
@@ -787,10 +790,10 @@ cudaError_t select_rows(const MaskShape &s, const float *s_c, const float *s_r, 
                         int64_t ppm_r, int32_t *kv_idx, int32_t *kv_cnt, uint8_t *mask, int32_t *status,
                         cudaStream_t stream) {
   const bool al = s.nbs % 4 == 0;
-  const SelectArgs a{s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.seq, s.total, s.block, s.hkv, s.nbs, s.nbw,
+  const SelectArgs a{s_c, s_r, alpha, kv_idx, kv_cnt, mask, s.cu, s.batch, s.seq, s.total, s.block, s.hkv, s.nbs, s.nbw,
                      static_cast<long long>(ppm_c), static_cast<long long>(ppm_r), status};
-  if (s.nbw <= 32 * kTeamMaxWarps * 8) return launch_select_p<8>(a, al, s.batch, stream);
-  if (s.nbw <= 32 * kTeamMaxWarps * 16) return launch_select_p<16>(a, al, s.batch, stream);
+  if (s.nbw <= 32 * kTeamMaxWarps * 8) return launch_select_p<8>(a, al, stream);
+  if (s.nbw <= 32 * kTeamMaxWarps * 16) return launch_select_p<16>(a, al, stream);
   return cudaErrorInvalidValue;
 }
 

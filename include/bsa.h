@@ -107,12 +107,13 @@ typedef struct {
  * median and 90th percentile, taken per layer and per KV head.
  *
  *   centroid[b][g][j][x]  (fp32, [batch, hkv, nb, head_dim])
- *                         = mean over the block's keys of k[x]
- *   radius[b][g][j]       = max over the block's keys of |k - centroid|_2
+ *                         = mean over the block's keys of k[x]          (reading 1)
+ *   radius[b][g][j]       = max over the block's keys of |k - centroid|_2 (reading 2)
  *   quant[b][g][0..1]     = median and 90th percentile of radius[b][g][:],
  *                           nearest rank: r_(ceil(p * nb)) of the ascending sort
+ *                                                                       (reading 4)
  *   alpha[b][g][j]        = clamp((r_j - med) / (p90 - med), 0, 1), or 0 for
- *                           all j when p90 - med <= 1e-12 * p90
+ *                           all j when p90 - med <= 1e-12 * p90          (reading 5)
  * All outputs fp32, caller-allocated.  k: bf16 [batch, seq, hkv, head_dim].
  */
 bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid, float *radius,
@@ -127,10 +128,11 @@ bsa_status bsa_block_meta(const bsa_shape *shape, const void *k, float *centroid
  * for head h and nbar_{h,i} the mean of those queries' L2 norms:
  *   S_c[i][j] = max over the G heads of KV head g of s * qbar_{h,i}.c_j
  *   R[i][j]   = max over those heads of s * (qbar_{h,i}.c_j + alpha_j * nbar_{h,i} * r_j)
- * Row i keeps blocks 0 and i (forced, outside both rankings), the top
- * ceil(centroid_keep * (i+1)) of 1..i-1 by S_c, and the top
- * ceil(rescue_keep * (i+1)) by R of the candidates the centroid path dropped
- * whose alpha_j > 0.  Ties go to the lower block index.
+ * (readings 6 to 8).  Row i keeps blocks 0 and i (forced, outside both
+ * rankings; reading 9), the top ceil(centroid_keep * (i+1)) of 1..i-1 by S_c
+ * (readings 10, 11), and the top ceil(rescue_keep * (i+1)) by R of the
+ * candidates the centroid path dropped whose alpha_j > 0 (reading 12).  Ties
+ * go to the lower block index; the kept set is the union (reading 13).
  *
  * Outputs: kv_idx[b][g][i][0..kv_cnt-1] (int32, [batch, hkv, nb, nb]) holds the
  * kept key blocks of row i in ascending order; entries past kv_cnt are left

@@ -13,14 +13,15 @@ paths, one mask", and the FlashAttention description in
 softmax computed here.
 
 The article gives prose, not formulas.  Each function states the reading it
-implements; the same readings are listed in the design notes of the repository.
+implements and cites it by number (reading 1 .. 19 of the repository's
+specification), so that the oracle and the CUDA path follow one definition.
 All arithmetic is float64 on the bf16-rounded inputs.
 
 Layouts: q [b, N, Hq, d], k and v [b, N, Hkv, d]; per-block tensors are
 [b, H, nb, ...]; masks are [b, Hkv, nb_q, nb_k] uint8 with bit 0 = forced
 (first or diagonal block), bit 1 = kept by the centroid path, bit 2 = kept by
 the rescue path.  N need not be a multiple of the block size: nb = ceil(N / B)
-and the last block holds the N - (nb - 1) B remaining tokens (reading: a
+and the last block holds the N - (nb - 1) B remaining tokens (reading 3: a
 partial block is summarised, ranked and attended over its own tokens only).
 Packed ragged batches ("varlen") hold sequence b in tokens
 cu_seqlens[b] .. cu_seqlens[b+1] - 1 of q [T, Hq, d], k and v [T, Hkv, d];
@@ -42,8 +43,8 @@ def block_meta(k: np.ndarray, block: int):
 
     Rescue branch section: every key block is summarised by its centroid and
     by the largest distance from one of its keys to that centroid.  The
-    centroid is the mean of the block's keys (mean-dilution section); the
-    distance is read as plain Euclidean.
+    centroid is the mean of the block's keys (reading 1, mean-dilution
+    section); the distance is read as plain Euclidean (reading 2).
 
     k: [b, N, Hkv, d].  Returns centroid [b, Hkv, nb, d], radius [b, Hkv, nb].
     """
@@ -74,7 +75,7 @@ def radius_quantiles(radius: np.ndarray):
 
     Rescue branch section: the coefficient is anchored at the median and the
     90th percentile of the radii, taken per layer and per KV head over the
-    prompt's blocks.  Reading: nearest-rank
+    prompt's blocks.  Reading 4: nearest-rank
     quantiles over all nb blocks, q(p) = r_(ceil(p nb)) of the ascending sort
     (so the median is the lower median for even nb).
 
@@ -91,7 +92,7 @@ def rescue_coefficient(radius: np.ndarray, med: np.ndarray, p90: np.ndarray):
     """Radius-adaptive rescue coefficient alpha_j in [0, 1].
 
     Rescue branch section: the coefficient adapts to where a block's radius
-    falls between the median and the 90th percentile.  Reading: a block
+    falls between the median and the 90th percentile.  Reading 5: a block
     no wider than the median gets no bonus, a block at or beyond p90 the full
     bonus, linear in between:
         alpha_j = clamp((r_j - med) / (p90 - med), 0, 1),
@@ -110,7 +111,7 @@ def query_summary(q: np.ndarray, block: int):
     """Per query block: mean query and mean query norm.
 
     Rescue branch section: the centroid branch ranks blocks by how relevant
-    they are on average.  Reading: the query side of a block is summarised by the mean
+    they are on average.  Reading 6: the query side of a block is summarised by the mean
     of its queries (qbar) and the mean of their Euclidean norms (nbar).
 
     q: [b, N, Hq, d].  Returns qbar [b, Hq, nb, d], nbar [b, Hq, nb].
@@ -137,10 +138,10 @@ def block_scores(qbar, nbar, centroid, radius, alpha, scale: float, b: int, g: i
     scale * (qbar_{h,i} . c_j).
     Rescue path (the base score plus the radius term weighted by the
     coefficient):  R[i, j] = max_h scale * (qbar_{h,i} . c_j +
-    alpha_j * nbar_{h,i} * r_j).  Since |qbar| <= nbar, with alpha_j = 1 the
-    rescue score bounds every key of block j (Cauchy-Schwarz), so a single
-    outlier key cannot be diluted away.  Reading: the group's heads are
-    combined by a max, so one head is not diluted by the others (GQA sharing,
+    alpha_j * nbar_{h,i} * r_j) (reading 7).  Since |qbar| <= nbar, with
+    alpha_j = 1 the rescue score bounds every key of block j (Cauchy-Schwarz),
+    so a single outlier key cannot be diluted away.  Reading 8: the group's
+    heads are combined by a max, so one head is not diluted by the others (GQA sharing,
     32 query heads over 4 KV heads).
 
     Returns (S_c, R), each [nb, nb] float64 (row i = query block, column j =
@@ -168,7 +169,7 @@ def token_block_scores(q, centroid, radius, alpha, block: int, scale: float, b: 
         R[i, j]   = scale * max_{h,t} (q_{h,t} . c_j + alpha_j |q_{h,t}| r_j).
     With alpha_j = 1, R bounds scale * q_{h,t} . k for every key k of block j
     (Cauchy-Schwarz, |k - c_j| <= r_j), i.e. the block's largest logit.
-    Reading: the maximum over tokens is the plain reading of the article's
+    Reading 15: the maximum over tokens is the plain reading of the article's
     token-to-centroid comparison (section "The numbers, stated honestly").
 
     q: [b, N, Hq, d].  Returns (S_c, R), each [ceil(N / block), nb] (row i =
@@ -205,7 +206,7 @@ def ratio_ppm(ratio: float) -> int:
 def keep_count(ppm: int, i: int) -> int:
     """ceil(ratio * (i + 1)) in integer arithmetic (ratio = ppm / 1e6).
 
-    Reading of the independent per-path thresholds: each path keeps a fixed fraction
+    Reading 10, of the independent per-path thresholds: each path keeps a fixed fraction
     of the causal row (i + 1 blocks), rounded up.
     """
     return (ppm * (i + 1) + PPM - 1) // PPM
@@ -224,14 +225,14 @@ def select_row(s_c_row, r_row, alpha_row, i: int, ppm_c: int, ppm_r: int):
     """Blocks kept for query block i (one batch, one KV head).
 
     * Forced: key block 0 and the diagonal block i are always kept and take
-      part in neither ranking (reading; the article does not say).
-    * Centroid path: the top k_c = min(ceil(rho_c (i+1)), i-1) candidates
-      j in 1..i-1 by S_c.
-    * Rescue path: among the candidates the centroid path dropped and whose
+      part in neither ranking (reading 9; the article does not say).
+    * Centroid path (reading 11): the top k_c = min(ceil(rho_c (i+1)), i-1)
+      candidates j in 1..i-1 by S_c.
+    * Rescue path (reading 12): among the candidates the centroid path dropped and whose
       radius is above the median (alpha_j > 0), the top
       k_r = min(ceil(rho_r (i+1)), #eligible) by R (wide blocks come back
       even when their mean score alone would drop them).
-    * The two paths are thresholded independently and combined by OR.
+    * The two paths are thresholded independently and combined by OR (reading 13).
 
     Returns (centroid_kept, rescue_kept) as ascending int arrays.
     """
@@ -333,7 +334,8 @@ def sparse_attention_rows(q, k, v, mask, block: int, rows, scale: float | None =
     block-sparse FlashAttention.  For each query token t of block i and head
     h (KV head g = h // (Hq/Hkv)) the keys are the tokens s <= t of the key
     blocks kept in mask[b, g, i]; the output is the explicit softmax-weighted
-    sum of their values and lse the natural log of the softmax normaliser.
+    sum of their values and lse the natural log of the softmax normaliser
+    (reading 14).
 
     mask: boolean-like [b, Hkv, nb, nb].  rows: iterable of (b, h, i).
     Returns {(b, h, i): (o [block, d], lse [block])}.
@@ -460,7 +462,7 @@ def decode_select(q_tok, centroid, radius, alpha, n: int, block: int, centroid_k
 
     The new token sits at position n - 1 of a sequence whose cache (including
     the token's own key) holds n tokens, so its row is the block
-    i = (n - 1) // block.  Reading: the decode query is a query block of one
+    i = (n - 1) // block.  Reading 16: the decode query is a query block of one
     token, so its summary is the token itself (mean = q, mean norm = |q|) and
     the row is selected exactly like a prefill row: forced 0 and i, the top
     k_c of 1..i-1 by S_c, the top k_r of the dropped blocks with alpha > 0 by R.

@@ -90,7 +90,13 @@ WORKLOADS = {
 
 
 def workload(name: str) -> Workload:
-    return WORKLOADS[name]
+    """A named workload: one of WORKLOADS or a point of the 64K sweep."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    for w in sweep_workloads():
+        if w.name == name:
+            return w
+    raise KeyError(name)
 
 
 def sweep_workloads():
