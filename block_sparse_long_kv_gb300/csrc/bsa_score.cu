@@ -22,7 +22,10 @@
 // swizzle row) of the four operands; warp 1 owns 256 TMEM columns and issues
 // the MMAs; then all eight warps read the accumulator (one TMEM lane per key
 // block, each warp half of the columns) and write S_c and R.  Every wait is
-// bounded.
+// bounded.  One stage of shared memory (96 KB) per CTA, so two CTAs share an
+// SM (256 TMEM columns and 128 registers a thread each): one CTA's loads and
+// epilogue overlap the other's MMAs, which a second stage inside one CTA did
+// less well (29 against 35 us per 128K layer).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,7 +46,7 @@ struct ScoreCfg {
   static constexpr int NI = COLS / G;  // query blocks per tile
   static constexpr int KC = 32;        // fp32 elements per K-chunk
   static constexpr int NKC = D / KC;
-  static constexpr int NS = 2;
+  static constexpr int NS = 1;       // stages (see the note on occupancy above)
   static constexpr uint32_t A_BYTES = ROWS * KC * 4;  // 16 KB
   static constexpr uint32_t B_BYTES = COLS * KC * 4;  // 32 KB
   // stage layout: A_hi, A_lo, B_hi, B_lo
@@ -94,7 +97,7 @@ struct ScoreSeq {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     score_kernel(const __grid_constant__ ScoreMaps maps, const float *__restrict__ nbar,
                  const float *__restrict__ radius, const float *__restrict__ alpha,
                  float *__restrict__ s_c, float *__restrict__ s_r, int nb, int nbw, const ScoreSeq sq,
