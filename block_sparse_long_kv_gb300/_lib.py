@@ -82,6 +82,8 @@ SIGNATURES = {
                                          _P, _P]),
     "bsa_decode_fwd": (ctypes.c_int, [_VP, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                       ctypes.c_size_t, _P, _P]),
+    "bsa_decode_step": (ctypes.c_int, [_VP, _PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                       _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "bsa_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_uint64, ctypes.c_int32, _P]),
     "bsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bsa_version": (ctypes.c_int32, []),

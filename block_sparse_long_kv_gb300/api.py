@@ -22,7 +22,7 @@ __all__ = [
     "VarlenShape", "make_varlen_shape", "varlen_block_stride", "varlen_block_meta",
     "varlen_select_workspace_bytes", "varlen_select_mask", "varlen_prefill_fwd",
     "varlen_prefill_dense_fwd", "alloc_varlen_meta", "alloc_varlen_select",
-    "decode_workspace_bytes", "decode_select", "decode_fwd",
+    "decode_workspace_bytes", "decode_select", "decode_fwd", "decode_step",
     "block_meta_fp8", "select_mask_fp8", "prefill_fwd_fp8", "prefill_dense_fwd_fp8",
     "prefill_fp8_workspace_bytes",
 ]
@@ -421,6 +421,28 @@ def decode_fwd(shape: VarlenShape, cu_seqlens, q_new, k, v, kv_idx, kv_cnt, soft
         _ptr(k, "k", torch.bfloat16, t * hkv * d), _ptr(v, "v", torch.bfloat16, t * hkv * d),
         _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs),
         _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv), ctypes.c_float(softmax_scale),
+        _ptr(o, "o", torch.bfloat16, b * hq * d), _ptr(lse, "lse", torch.float32, b * hq),
+        _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))
+
+
+def decode_step(shape: VarlenShape, params: SelectParams, cu_seqlens, q_new, k, v, centroid, radius,
+                alpha, softmax_scale, kv_idx, kv_cnt, o, lse=None, workspace=None, dev_status=None,
+                stream=None):
+    """bsa_decode_step: decode_select then decode_fwd in one cooperative launch."""
+    b, t, hq, hkv, d, nbs = _vdims(shape)
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(shape), dtype=torch.uint8, device=q_new.device)
+    _lib.check("bsa_decode_step", lib.bsa_decode_step(
+        ctypes.byref(shape), ctypes.byref(params), _cu(cu_seqlens, b),
+        _ptr(q_new, "q_new", torch.bfloat16, b * hq * d),
+        _ptr(k, "k", torch.bfloat16, t * hkv * d), _ptr(v, "v", torch.bfloat16, t * hkv * d),
+        _ptr(centroid, "centroid", torch.float32, b * hkv * nbs * d),
+        _ptr(radius, "radius", torch.float32, b * hkv * nbs),
+        _ptr(alpha, "alpha", torch.float32, b * hkv * nbs), ctypes.c_float(softmax_scale),
+        _ptr(kv_idx, "kv_idx", torch.int32, b * hkv * nbs),
+        _ptr(kv_cnt, "kv_cnt", torch.int32, b * hkv),
         _ptr(o, "o", torch.bfloat16, b * hq * d), _ptr(lse, "lse", torch.float32, b * hq),
         _ptr(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _ptr(dev_status, "dev_status", torch.int32), _stream(stream)))

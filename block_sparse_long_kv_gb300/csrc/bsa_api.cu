@@ -497,4 +497,32 @@ bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqle
   return BSA_OK;
 }
 
+bsa_status bsa_decode_step(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                           const int32_t *cu_seqlens, const void *q_new, const void *k, const void *v,
+                           const float *centroid, const float *radius, const float *alpha,
+                           float softmax_scale, int32_t *kv_idx, int32_t *kv_cnt, void *o, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           bsa_stream_t stream) {
+  const bsa_status st = check_varlen(shape, cu_seqlens);
+  if (st != BSA_OK) return st;
+  if (!params || !q_new || !k || !v || !centroid || !radius || !alpha || !kv_idx || !kv_cnt || !o)
+    return BSA_ERR_INVALID_ARG;
+  if (!ratio_ok(params->centroid_keep) || !ratio_ok(params->rescue_keep) || params->flags != 0)
+    return BSA_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(k) || !aligned16(v) || !aligned16(centroid) || !aligned16(radius) ||
+      !aligned16(alpha) || !aligned16(kv_idx) || !aligned16(kv_cnt) || !aligned16(o) || (lse && !aligned16(lse)))
+    return BSA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  const bsa::MaskShape ms = mask_shape(shape, cu_seqlens);
+  if (static_cast<long long>(ms.batch) * ms.hkv > bsa::kMaxDecodeRows) return BSA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < bsa::decode_workspace_bytes(ms))
+    return BSA_ERR_WORKSPACE;
+  const float select_scale = static_cast<float>(1.0 / sqrt(static_cast<double>(ms.d)));
+  if (bsa::launch_decode_step(ms, q_new, k, v, centroid, radius, alpha, ratio_ppm(params->centroid_keep),
+                              ratio_ppm(params->rescue_keep), select_scale, softmax_scale, kv_idx, kv_cnt, o, lse,
+                              workspace, dev_status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
 }  // extern "C"

@@ -36,6 +36,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "bsa_internal.h"
 #include "bsa_topk.cuh"
@@ -57,29 +58,28 @@ constexpr int kScoreWarps = 8;
 constexpr int kScoreBlocksPerWarp = 4;  // key blocks per warp: 32 per CTA
 
 // S_c[j] and R[j] of the new token of (b, g) for the candidates 1 <= j < i, one
-// warp per key block (a coalesced centroid row per lane group), 32 key blocks
-// per CTA so every SM takes part even at batch 1.  Each warp issues the loads
-// of all its centroid rows before it reads the query, so a CTA waits for
-// memory about once.
-template <int D>
-__global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
-    const uint16_t *__restrict__ q_new, const float *__restrict__ centroid, const float *__restrict__ radius,
-    const float *__restrict__ alpha, float *__restrict__ s_c, float *__restrict__ s_r,
-    const int32_t *__restrict__ cu, int seq, int total, int block, int hq, int hkv, int nbs, float scale,
-    int32_t *status) {
+// warp per key block (a coalesced centroid row per lane group), NW * R key
+// blocks per chunk jt, so every SM takes part even at batch 1.  Each warp
+// issues the loads of all its centroid rows before it reads the query, so a
+// CTA waits for memory about once.  A key block's scores do not depend on NW.
+template <int D, int NW>
+__device__ __forceinline__ void decode_score_chunk(
+    int jt, int g, int b, const uint16_t *__restrict__ q_new, const float *__restrict__ centroid,
+    const float *__restrict__ radius, const float *__restrict__ alpha, float *__restrict__ s_c,
+    float *__restrict__ s_r, const int32_t *__restrict__ cu, int seq, int total, int block, int hq, int hkv,
+    int nbs, float scale, int32_t *status) {
   constexpr int DPL = D / 32;  // dimensions per lane
   constexpr int R = kScoreBlocksPerWarp;
   __shared__ __align__(16) float qs[16 * D];
   __shared__ float qn[16];
-  const int jt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int grp = hq / hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t gb = static_cast<size_t>(b) * hkv + g;
   const SeqSpan sp = seq_span(cu, b, seq, total, status);
   if (sp.len == 0) return;
   const int i = (sp.len - 1) / block;  // the new token's block
-  const int j0 = jt * kScoreWarps * R;
-  if (j0 >= i) return;
+  const int j0 = jt * NW * R;
+  if (j0 >= i) return;  // CTA-uniform
   const int jw = j0 + warp * R;
   float c[R][DPL];
   float bonus[R];
@@ -102,9 +102,9 @@ __global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
     }
   }
   const uint16_t *qrow = q_new + (static_cast<size_t>(b) * hq + static_cast<size_t>(g) * grp) * D;
-  for (int e = tid; e < grp * D; e += kScoreWarps * 32) qs[e] = bf16f(qrow[e]);
+  for (int e = tid; e < grp * D; e += NW * 32) qs[e] = bf16f(qrow[e]);
   __syncthreads();
-  for (int h = warp; h < grp; h += kScoreWarps) {
+  for (int h = warp; h < grp; h += NW) {
     float s2 = 0.f;
     for (int x = lane; x < D; x += 32) s2 = fmaf(qs[h * D + x], qs[h * D + x], s2);
 #pragma unroll
@@ -131,6 +131,17 @@ __global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
       s_r[gb * nbs + j] = rm * scale;
     }
   }
+  __syncthreads();  // qs / qn are reused by the next chunk
+}
+
+template <int D>
+__global__ void __launch_bounds__(kScoreWarps * 32) decode_score_kernel(
+    const uint16_t *__restrict__ q_new, const float *__restrict__ centroid, const float *__restrict__ radius,
+    const float *__restrict__ alpha, float *__restrict__ s_c, float *__restrict__ s_r,
+    const int32_t *__restrict__ cu, int seq, int total, int block, int hq, int hkv, int nbs, float scale,
+    int32_t *status) {
+  decode_score_chunk<D, kScoreWarps>(blockIdx.x, blockIdx.y, blockIdx.z, q_new, centroid, radius, alpha, s_c, s_r,
+                                     cu, seq, total, block, hq, hkv, nbs, scale, status);
 }
 
 // ---------------------------------------------------------------- CTA-wide selection
@@ -582,14 +593,13 @@ __device__ __forceinline__ DChunk walk_next(DecWalk &w, const int *pre, const in
 // to its slot (unnormalised O, max and sum in log2 units).  A slot whose
 // entries name no valid block keeps max -inf, which the combine skips.
 template <int D, int G>
-__global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
+__device__ __forceinline__ void decode_attn_run(
     const uint16_t *__restrict__ q_new, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const int32_t *__restrict__ kv_idx, const int32_t *__restrict__ kv_cnt, float *__restrict__ part_o,
     float *__restrict__ part_ml, int *__restrict__ plan, const int32_t *__restrict__ cu, int seq, int total,
-    int block, int hkv, int nbs, int rows, float scale_log2, int32_t *status) {
+    int block, int hkv, int nbs, int rows, float scale_log2, int32_t *status, unsigned char *smem) {
   using C = DecCfg<D, G>;
   constexpr int NW = kAttnThreads / 32;
-  extern __shared__ __align__(16) unsigned char smem[];
   float (*oacc)[G][D] = reinterpret_cast<float (*)[G][D]>(smem + C::OFF_O);
   float (*wm)[16] = reinterpret_cast<float (*)[16]>(smem + C::OFF_ML);  // [warp][head]: max
   float (*wl)[16] = wm + NW;                                             // [warp][head]: sum
@@ -833,21 +843,34 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
   if (arow >= 0) flush(arow);
 }
 
-constexpr int kCombineThreads = 256;
-constexpr int kCombineWarps = kCombineThreads / 32;
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(
+    const uint16_t *__restrict__ q_new, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
+    const int32_t *__restrict__ kv_idx, const int32_t *__restrict__ kv_cnt, float *__restrict__ part_o,
+    float *__restrict__ part_ml, int *__restrict__ plan, const int32_t *__restrict__ cu, int seq, int total,
+    int block, int hkv, int nbs, int rows, float scale_log2, int32_t *status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  decode_attn_run<D, G>(q_new, k, v, kv_idx, kv_cnt, part_o, part_ml, plan, cu, seq, total, block, hkv, nbs, rows,
+                        scale_log2, status, smem);
+}
 
-// One CTA per (b, h): O = sum_s w_s O_s / sum_s w_s l_s over the slots of the
-// head's row, w_s = 2^(m_s - max m) (slots with max -inf are empty).  Warp w
-// takes the slots w, w + 8, ... (every warp first finds max m itself), each
-// lane D/32 dimensions; the warps' sums meet in shared memory in a fixed order.
-template <int D>
-__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
-    const float *__restrict__ part_o, const float *__restrict__ part_ml, const int *__restrict__ plan,
-    uint16_t *__restrict__ o, float *__restrict__ lse, int hq, int hkv) {
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / 32;  // the merge order: 8 warp partials
+
+// O and LSE of head h of sequence b: O = sum_s w_s O_s / sum_s w_s l_s over the
+// slots of the head's row, w_s = 2^(m_s - max m) (slots with max -inf are
+// empty).  The merge runs in a fixed order of kCombineWarps partials: partial
+// w takes the slots w, w + 8, w + 16, ... (each lane D/32 dimensions), and the
+// partials are added in order 0..7.  A CTA of NWR warps computes the partials
+// w = warp, warp + NWR, ..., so the result does not depend on NWR.
+template <int D, int NWR>
+__device__ __forceinline__ void combine_head(int b, int h, const float *__restrict__ part_o,
+                                             const float *__restrict__ part_ml, const int *__restrict__ plan,
+                                             uint16_t *__restrict__ o, float *__restrict__ lse, int hq, int hkv) {
   constexpr int VL = D / 32;  // dimensions per lane
   __shared__ __align__(16) float red_o[kCombineWarps][D];
   __shared__ float red_l[kCombineWarps];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = hq / hkv;
   const int r = b * hkv + h / grp, hl = h % grp;
   const int s0 = plan[1 + r], ns = plan[2 + r] - s0;
@@ -855,58 +878,210 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   for (int s = lane; s < ns; s += 32) m = fmaxf(m, part_ml[(static_cast<size_t>(s0 + s) * grp + hl) * 2]);
 #pragma unroll
   for (int offs = 16; offs > 0; offs >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, offs));
-  float acc[VL];
+  for (int vw = warp; vw < kCombineWarps; vw += NWR) {
+    float acc[VL];
 #pragma unroll
-  for (int x = 0; x < VL; ++x) acc[x] = 0.f;
-  float l = 0.f;
-  for (int sb = warp; sb < ns; sb += 4 * kCombineWarps) {
-    float2 ml[4];
-    float pv[4][VL];
+    for (int x = 0; x < VL; ++x) acc[x] = 0.f;
+    float l = 0.f;
+    for (int sb = vw; sb < ns; sb += 4 * kCombineWarps) {
+      float2 ml[4];
+      float pv[4][VL];
 #pragma unroll
-    for (int uu = 0; uu < 4; ++uu) {
-      const int s = sb + uu * kCombineWarps;
-      ml[uu] = make_float2(-INFINITY, 0.f);
+      for (int uu = 0; uu < 4; ++uu) {
+        const int s = sb + uu * kCombineWarps;
+        ml[uu] = make_float2(-INFINITY, 0.f);
 #pragma unroll
-      for (int x = 0; x < VL; ++x) pv[uu][x] = 0.f;
-      if (s < ns) {
-        const size_t at = static_cast<size_t>(s0 + s) * grp + hl;
-        ml[uu] = *reinterpret_cast<const float2 *>(part_ml + at * 2);
-        const float *src = part_o + at * D + lane * VL;
-        if constexpr (VL == 4) {
-          const float4 t = *reinterpret_cast<const float4 *>(src);
-          pv[uu][0] = t.x; pv[uu][1] = t.y; pv[uu][2] = t.z; pv[uu][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2 *>(src);
-          pv[uu][0] = t.x; pv[uu][1] = t.y;
+        for (int x = 0; x < VL; ++x) pv[uu][x] = 0.f;
+        if (s < ns) {
+          const size_t at = static_cast<size_t>(s0 + s) * grp + hl;
+          ml[uu] = *reinterpret_cast<const float2 *>(part_ml + at * 2);
+          const float *src = part_o + at * D + lane * VL;
+          if constexpr (VL == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            pv[uu][0] = t.x; pv[uu][1] = t.y; pv[uu][2] = t.z; pv[uu][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            pv[uu][0] = t.x; pv[uu][1] = t.y;
+          }
         }
+      }
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu) {
+        if (ml[uu].x == -INFINITY) continue;  // an empty slot (or past ns)
+        const float wgt = exp2f(ml[uu].x - m);
+        l = fmaf(ml[uu].y, wgt, l);
+#pragma unroll
+        for (int x = 0; x < VL; ++x) acc[x] = fmaf(pv[uu][x], wgt, acc[x]);
       }
     }
 #pragma unroll
-    for (int uu = 0; uu < 4; ++uu) {
-      if (ml[uu].x == -INFINITY) continue;  // an empty slot (or past ns)
-      const float wgt = exp2f(ml[uu].x - m);
-      l = fmaf(ml[uu].y, wgt, l);
-#pragma unroll
-      for (int x = 0; x < VL; ++x) acc[x] = fmaf(pv[uu][x], wgt, acc[x]);
-    }
+    for (int x = 0; x < VL; ++x) red_o[vw][lane * VL + x] = acc[x];
+    if (lane == 0) red_l[vw] = l;
   }
-#pragma unroll
-  for (int x = 0; x < VL; ++x) red_o[warp][lane * VL + x] = acc[x];
-  if (lane == 0) red_l[warp] = l;
   __syncthreads();
-  if (tid < D) {
+  for (int d = tid; d < D; d += NWR * 32) {
     float a = 0.f, ls = 0.f;
 #pragma unroll
     for (int wi = 0; wi < kCombineWarps; ++wi) {
-      a += red_o[wi][tid];
+      a += red_o[wi][d];
       ls += red_l[wi];
     }
     const float rr = ls > 0.f ? a / ls : 0.f;
     const __nv_bfloat16 rb = __float2bfloat16_rn(rr);
-    o[(static_cast<size_t>(b) * hq + h) * D + tid] = *reinterpret_cast<const uint16_t *>(&rb);
-    if (lse != nullptr && tid == 0)
+    o[(static_cast<size_t>(b) * hq + h) * D + d] = *reinterpret_cast<const uint16_t *>(&rb);
+    if (lse != nullptr && d == 0)
       lse[static_cast<size_t>(b) * hq + h] = ls > 0.f ? (m + log2f(ls)) * 0.69314718055994531f : -INFINITY;
   }
+  __syncthreads();  // red_o / red_l are reused by the next head
+}
+
+// One CTA per (b, h).
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
+    const float *__restrict__ part_o, const float *__restrict__ part_ml, const int *__restrict__ plan,
+    uint16_t *__restrict__ o, float *__restrict__ lse, int hq, int hkv) {
+  combine_head<D, kCombineWarps>(blockIdx.y, blockIdx.x, part_o, part_ml, plan, o, lse, hq, hkv);
+}
+
+// ---------------------------------------------------------------- the whole step in one launch
+
+// Grid-wide barrier k (k = 1, 2, ...) of a cooperative launch (every CTA is
+// resident): each CTA adds 1 to bar[0] with release semantics and waits until
+// it reads k * gridDim.x with acquire semantics, so every write before the
+// barrier is visible to every CTA after it.  bar[0] is zero before the launch
+// and is never reset inside it (barrier k's target follows from k).  The wait is
+// bounded: after kGridWaitNs it records BSA_ERR_DEVICE_TIMEOUT and returns, so
+// no CTA hangs.
+constexpr uint64_t kGridWaitNs = 2000000000ull;
+
+__device__ __forceinline__ void grid_sync(unsigned *bar, unsigned k, int32_t *status) {
+  __threadfence();  // every thread's writes, before the CTA's arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+    const unsigned target = k * gridDim.x;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+      unsigned seen;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(bar) : "memory");
+      if (seen >= target) break;
+      __nanosleep(32);
+      if (ptx::globaltimer_ns() - t0 > kGridWaitNs) {
+        if (status != nullptr) atomicCAS(status, 0, BSA_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+struct DecStepArgs {
+  const uint16_t *q_new, *k, *v;
+  const float *centroid, *radius, *alpha;
+  int32_t *kv_idx, *kv_cnt;
+  float *s_c, *s_r, *part_o, *part_ml;
+  int *plan;
+  unsigned *bar;
+  uint16_t *o;
+  float *lse;
+  const int32_t *cu;
+  int batch, seq, total, block, hq, hkv, nbs;
+  long long ppm_c, ppm_r;
+  float scale, scale_log2;
+  int32_t *status;
+};
+
+// The selection of row r = (b, g) by the CTA as one team of warps (P row entries
+// per lane, 32 NW P >= nbs): topk::team_select_row, exactly the selection of a
+// prefill row i = (len - 1) / B.
+template <int NW, int P>
+__device__ __forceinline__ void decode_select_team(int r, const DecStepArgs &a) {
+  __shared__ __align__(16) TeamScratch tsh;
+  Team<NW> tm(tsh, 1, static_cast<int>(threadIdx.x));
+  const int b = r / a.hkv;
+  const size_t gb = static_cast<size_t>(r);
+  const SeqSpan sp = seq_span(a.cu, b, a.seq, a.total, a.status);
+  if (sp.len == 0) {
+    if (threadIdx.x == 0) a.kv_cnt[gb] = 0;
+    return;
+  }
+  const int i = (sp.len - 1) / a.block;
+  tm.clear_hist();
+  tm.sync();
+  uint32_t fl[P / 4];
+  team_select_row<NW, P, true>(tm, a.s_c + gb * a.nbs, a.s_r + gb * a.nbs, a.alpha + gb * a.nbs, i, a.ppm_c,
+                               a.ppm_r, fl);
+  team_emit_row<NW, P, true>(tm, fl, i, a.kv_idx + gb * a.nbs, a.kv_cnt + gb, nullptr, a.nbs);
+  tm.sync();  // the scratch is reused by the next row
+}
+
+// One decode step in one cooperative launch:
+//   scores     chunks of key blocks of every row (b, g) over every CTA; the CTA
+//              that finishes a row's last chunk with candidates (counted in
+//              bar[1 + r]) runs that row's selection, so no barrier separates
+//              the two
+//   | barrier 1 | split-KV attention (the even cut of decode_attn_run)
+//   | barrier 2 | merge (one head per CTA).
+// The same arithmetic as the four-launch path.  bar holds 1 + rows zeroed words.
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnThreads) decode_step_kernel(const __grid_constant__ DecStepArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int row_done;
+  constexpr int NW = kAttnThreads / 32;
+  const int rows = a.batch * a.hkv;
+  // the rows' chunks that hold candidates (j0 < i; always chunk 0), laid end to end: row r owns
+  // items pre[r] .. pre[r+1]-1, and CTA c takes items c, c + gridDim.x, ..., so the work of short
+  // and long rows spreads over all CTAs at once
+  int *pre = reinterpret_cast<int *>(smem);  // rows + 1 entries; the attention phase reuses it
+  __shared__ int wsum[NW];
+  {
+    const int per = (rows + kAttnThreads - 1) / kAttnThreads;
+    const int r0 = min(rows, static_cast<int>(threadIdx.x) * per), r1 = min(rows, r0 + per);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) {
+      const SeqSpan sp = seq_span(a.cu, r / a.hkv, a.seq, a.total, a.status);
+      const int i = sp.len > 0 ? (sp.len - 1) / a.block : -1;
+      pre[r] = max(1, (i + NW * kScoreBlocksPerWarp - 1) / (NW * kScoreBlocksPerWarp));
+      local += pre[r];
+    }
+    int n;
+    int run = block_exclusive_scan(local, &n, wsum);
+    for (int r = r0; r < r1; ++r) {
+      const int c = pre[r];
+      pre[r] = run;
+      run += c;
+    }
+    if (threadIdx.x == 0) pre[rows] = n;
+    __syncthreads();
+  }
+  for (int item = blockIdx.x; item < pre[rows]; item += gridDim.x) {
+    int lo = 0, hi = rows - 1;  // the row holding item: the last r with pre[r] <= item
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= item) lo = mid;
+      else hi = mid - 1;
+    }
+    const int r = lo, jt = item - pre[r], counted = pre[r + 1] - pre[r];
+    decode_score_chunk<D, NW>(jt, r % a.hkv, r / a.hkv, a.q_new, a.centroid, a.radius, a.alpha, a.s_c, a.s_r,
+                              a.cu, a.seq, a.total, a.block, a.hq, a.hkv, a.nbs, a.scale, a.status);
+    __threadfence();  // this chunk's scores before its count
+    __syncthreads();
+    if (threadIdx.x == 0) row_done = atomicAdd(a.bar + 1 + r, 1u) == static_cast<unsigned>(counted - 1);
+    __syncthreads();
+    if (row_done) {  // CTA-uniform
+      __threadfence();
+      if (a.nbs <= 32 * NW * 8) decode_select_team<NW, 8>(r, a);
+      else if (a.nbs <= 32 * NW * 16) decode_select_team<NW, 16>(r, a);
+      else decode_select_team<NW, 32>(r, a);
+    }
+  }
+  grid_sync(a.bar, 1, a.status);
+  decode_attn_run<D, G>(a.q_new, a.k, a.v, a.kv_idx, a.kv_cnt, a.part_o, a.part_ml, a.plan, a.cu, a.seq, a.total,
+                        a.block, a.hkv, a.nbs, rows, a.scale_log2, a.status, smem);
+  grid_sync(a.bar, 2, a.status);
+  for (int item = blockIdx.x; item < a.batch * a.hq; item += gridDim.x)
+    combine_head<D, NW>(item / a.hq, item % a.hq, a.part_o, a.part_ml, a.plan, a.o, a.lse, a.hq, a.hkv);
 }
 
 template <int D, int G>
@@ -950,7 +1125,7 @@ cudaError_t launch_attn_d(const MaskShape &s, const void *q_new, const void *k, 
 // slot to the CTA count), the plan [b * hkv + 2] int32, then the selection's S_c and R rows
 // [b, hkv, nbs].
 struct DecRegions {
-  size_t po, pml, plan, sc, sr, total;
+  size_t po, pml, plan, sc, sr, bar, total;
 };
 
 DecRegions decode_regions(const MaskShape &s) {
@@ -964,8 +1139,78 @@ DecRegions decode_regions(const MaskShape &s) {
   r.plan = r.pml + r256(slots * 2 * 4);
   r.sc = r.plan + r256((rows + 2) * 4);
   r.sr = r.sc + r256(srow);
-  r.total = r.sr + r256(srow);
+  r.bar = r.sr + r256(srow);  // the fused step's barrier and per-row counters
+  r.total = r.bar + r256((rows + 1) * 4);
   return r;
+}
+
+// The CTAs of one decode step: as many as are resident at once (a cooperative launch), at most
+// kMaxDecodeCtas.  The kernel's dynamic shared-memory limit is set once, to what the largest row
+// count needs (it is one setting per kernel, so it must cover every shape), and the occupancy is
+// looked up once per (device, rows) and kept, so a step costs the host one memset and one launch.
+template <int D, int G>
+cudaError_t step_ctas(const void *kern, size_t smem, int rows, int *ctas) {
+  using C = DecCfg<D, G>;
+  struct Entry {
+    int dev, rows, ctas;
+  };
+  static std::mutex mu;
+  static Entry cache[16] = {};
+  static int used = 0;
+  static bool limit_set[64] = {};  // per device (the setting belongs to the device's context)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int x = 0; x < used; ++x)
+    if (cache[x].dev == dev && cache[x].rows == rows) {
+      *ctas = cache[x].ctas;
+      return cudaSuccess;
+    }
+  if (dev < 0 || dev >= 64 || !limit_set[dev]) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(C::smem(kMaxDecodeRows)))) != cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < 64) limit_set[dev] = true;
+  }
+  int sms = 0, per_sm = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAttnThreads, smem)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  *ctas = std::max(1, std::min(kMaxDecodeCtas, sms * per_sm));
+  if (used < 16) cache[used++] = Entry{dev, rows, *ctas};
+  return cudaSuccess;
+}
+
+template <int D, int G>
+cudaError_t launch_step_g(const MaskShape &s, const DecStepArgs &a, cudaStream_t stream) {
+  using C = DecCfg<D, G>;
+  auto kern = decode_step_kernel<D, G>;
+  const int rows = s.batch * s.hkv;
+  const size_t smem = C::smem(rows);
+  int ctas = 0;
+  cudaError_t e = step_ctas<D, G>(reinterpret_cast<const void *>(kern), smem, rows, &ctas);
+  if (e != cudaSuccess) return e;
+  // the barrier counter and the per-row score counters start at zero
+  if ((e = cudaMemsetAsync(a.bar, 0, (static_cast<size_t>(rows) + 1) * sizeof(unsigned), stream)) != cudaSuccess)
+    return e;
+  DecStepArgs args = a;
+  void *params[] = {&args};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(ctas), dim3(kAttnThreads), params,
+                                     smem, stream);
+}
+
+template <int D>
+cudaError_t launch_step_d(const MaskShape &s, const DecStepArgs &a, cudaStream_t st) {
+  switch (s.group) {
+    case 1: return launch_step_g<D, 1>(s, a, st);
+    case 2: return launch_step_g<D, 2>(s, a, st);
+    case 4: return launch_step_g<D, 4>(s, a, st);
+    case 8: return launch_step_g<D, 8>(s, a, st);
+    case 16: return launch_step_g<D, 16>(s, a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -1030,6 +1275,49 @@ cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, 
     decode_combine_kernel<128><<<grid, kCombineThreads, 0, stream>>>(po, pml, plan, static_cast<uint16_t *>(o),
                                                                     lse, s.hq, s.hkv);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_step(const MaskShape &s, const void *q_new, const void *k, const void *v,
+                               const float *centroid, const float *radius, const float *alpha, int64_t ppm_c,
+                               int64_t ppm_r, float select_scale, float softmax_scale, int32_t *kv_idx,
+                               int32_t *kv_cnt, void *o, float *lse, void *workspace, int32_t *status,
+                               cudaStream_t stream) {
+  if (static_cast<long long>(s.batch) * s.hkv > kMaxDecodeRows) return cudaErrorInvalidValue;
+  const DecRegions r = decode_regions(s);
+  char *ws = static_cast<char *>(workspace);
+  DecStepArgs a;
+  a.q_new = static_cast<const uint16_t *>(q_new);
+  a.k = static_cast<const uint16_t *>(k);
+  a.v = static_cast<const uint16_t *>(v);
+  a.centroid = centroid;
+  a.radius = radius;
+  a.alpha = alpha;
+  a.kv_idx = kv_idx;
+  a.kv_cnt = kv_cnt;
+  a.s_c = reinterpret_cast<float *>(ws + r.sc);
+  a.s_r = reinterpret_cast<float *>(ws + r.sr);
+  a.part_o = reinterpret_cast<float *>(ws + r.po);
+  a.part_ml = reinterpret_cast<float *>(ws + r.pml);
+  a.plan = reinterpret_cast<int *>(ws + r.plan);
+  a.bar = reinterpret_cast<unsigned *>(ws + r.bar);
+  a.o = static_cast<uint16_t *>(o);
+  a.lse = lse;
+  a.cu = s.cu;
+  a.batch = s.batch;
+  a.seq = s.seq;
+  a.total = s.total;
+  a.block = s.block;
+  a.hq = s.hq;
+  a.hkv = s.hkv;
+  a.nbs = s.nbs;
+  a.ppm_c = static_cast<long long>(ppm_c);
+  a.ppm_r = static_cast<long long>(ppm_r);
+  a.scale = select_scale;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.status = status;
+  if (s.d == 64) return launch_step_d<64>(s, a, stream);
+  if (s.d == 128) return launch_step_d<128>(s, a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace bsa

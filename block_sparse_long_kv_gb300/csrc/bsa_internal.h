@@ -110,6 +110,13 @@ size_t decode_workspace_bytes(const MaskShape &s);
 cudaError_t launch_decode(const MaskShape &s, const void *q_new, const void *k, const void *v,
                           const int32_t *kv_idx, const int32_t *kv_cnt, float scale, void *o, float *lse,
                           void *workspace, int32_t *status, cudaStream_t stream);
+// bsa_decode_select then bsa_decode_fwd in one cooperative launch (grid barriers between the
+// phases; the barrier words in the decode workspace are zeroed here).
+cudaError_t launch_decode_step(const MaskShape &s, const void *q_new, const void *k, const void *v,
+                               const float *centroid, const float *radius, const float *alpha, int64_t ppm_c,
+                               int64_t ppm_r, float select_scale, float softmax_scale, int32_t *kv_idx,
+                               int32_t *kv_cnt, void *o, float *lse, void *workspace, int32_t *status,
+                               cudaStream_t stream);
 
 // e4m3 codes -> bf16 codes of the same values; n elements, a multiple of 16.
 cudaError_t launch_widen_e4m3(const void *src, void *dst, size_t n, cudaStream_t stream);

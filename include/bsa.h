@@ -406,6 +406,32 @@ bsa_status bsa_decode_fwd(const bsa_varlen_shape *shape, const int32_t *cu_seqle
                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
                           bsa_stream_t stream);
 
+/*
+ * bsa_decode_step - bsa_decode_select followed by bsa_decode_fwd, in one launch.
+ *
+ * The same selection (kv_idx, kv_cnt written as bsa_decode_select writes them)
+ * and the same attention of the new token (o, lse) as the two calls on one
+ * stream with the same arguments.  A decode step is a few microseconds of work
+ * per phase, so it runs as one cooperative launch whose CTAs are all resident:
+ * scores | selection | split-KV attention | merge of the partial results, with
+ * a grid-wide barrier between the phases (bounded: a barrier that does not
+ * complete within 2 s records BSA_ERR_DEVICE_TIMEOUT in dev_status).  The
+ * selection and the partial attention results are those of the two calls; the
+ * merge adds the partials in the same order, but the partials themselves
+ * depend on how many CTAs the launch has, so O may differ from the two calls
+ * in the last bits.  workspace: bsa_decode_workspace_bytes(shape) bytes,
+ * 16-byte aligned (it includes the barrier words, which the call zeroes).
+ * Errors: shape errors, then the parameter and pointer errors of the two calls
+ * (BSA_ERR_INVALID_ARG), BSA_ERR_UNSUPPORTED for batch * hkv above 4096, then
+ * BSA_ERR_WORKSPACE, all before any launch; BSA_ERR_CUDA if the launch fails.
+ */
+bsa_status bsa_decode_step(const bsa_varlen_shape *shape, const bsa_select_params *params,
+                           const int32_t *cu_seqlens, const void *q_new, const void *k, const void *v,
+                           const float *centroid, const float *radius, const float *alpha,
+                           float softmax_scale, int32_t *kv_idx, int32_t *kv_cnt, void *o, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           bsa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Self-test of the device wait limits (no compute).  Launches `ctas` CTAs
  * (1..8) whose first thread waits, through the bounded wait the attention

@@ -293,3 +293,43 @@ def test_mask_build_validation_and_workspace(lib):
     assert call(mask=m) == 1
     assert call(ws=None) == 4 and call(ws=m) == 4
     assert call(nbytes=need - 1) == 4
+
+
+def test_decode_step_validation(lib):
+    """bsa_decode_step: the argument checks of bsa_decode_select and bsa_decode_fwd together,
+    before any launch; its workspace is bsa_decode_workspace_bytes (which holds the barrier
+    words)."""
+    from block_sparse_long_kv_gb300 import _lib
+    s = vshape()
+    need = lib.bsa_decode_workspace_bytes(ctypes.byref(s))
+    assert need > 0
+    f = ctypes.c_void_p(FAKE)
+    m = ctypes.c_void_p(MIS)
+    ok = _lib.SelectParams(0.1, 0.02, 0)
+
+    def call(shape=s, prm=ok, cu=f, ptrs=(f,) * 6, scale=0.1, outs=(f, f, f), lse=None, ws=f, nbytes=need):
+        return lib.bsa_decode_step(ctypes.byref(shape), None if prm is None else ctypes.byref(prm), cu, *ptrs,
+                                   ctypes.c_float(scale), *outs, lse, ws, ctypes.c_size_t(nbytes), None, None)
+
+    assert call(shape=vshape(batch=0)) == 2
+    assert call(cu=None) == 1 and call(cu=ctypes.c_void_p(FAKE + 2)) == 1
+    assert call(prm=None) == 1
+    assert call(prm=_lib.SelectParams(0.1, 0.02, 1)) == 1
+    assert call(prm=_lib.SelectParams(-0.1, 0.02, 0)) == 1
+    for x in range(6):                       # q_new, k, v, centroid, radius, alpha
+        p = [f] * 6
+        p[x] = None
+        assert call(ptrs=tuple(p)) == 1
+        p[x] = m
+        assert call(ptrs=tuple(p)) == 1
+    for x in range(3):                       # kv_idx, kv_cnt, o
+        o = [f] * 3
+        o[x] = None
+        assert call(outs=tuple(o)) == 1
+        o[x] = m
+        assert call(outs=tuple(o)) == 1
+    assert call(lse=m) == 1
+    assert call(scale=0.0) == 1 and call(scale=float("inf")) == 1 and call(scale=float("nan")) == 1
+    assert call(shape=vshape(batch=4097, total_tokens=5000, max_seqlen=64)) == 3   # batch * hkv > 4096
+    assert call(ws=None) == 4 and call(ws=m) == 4
+    assert call(nbytes=need - 1) == 4

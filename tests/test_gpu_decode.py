@@ -60,8 +60,27 @@ def gpu_decode(vw, lay, q_new, rc=None, rr=None, lists=None):
     bsa.decode_fwd(s, cu, qn, k, v, kv_idx, kv_cnt, 1.0 / math.sqrt(vw.head_dim), o, lse, ws, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    return dict(kv_idx=kv_idx.cpu().numpy(), kv_cnt=kv_cnt.cpu().numpy(), o=o.float().cpu().numpy(),
-                lse=lse.cpu().numpy(), nbs=nbs, alpha=meta["alpha"].cpu().numpy())
+    out = dict(kv_idx=kv_idx.cpu().numpy(), kv_cnt=kv_cnt.cpu().numpy(), o=o.float().cpu().numpy(),
+               lse=lse.cpu().numpy(), nbs=nbs, alpha=meta["alpha"].cpu().numpy())
+    if lists is None:
+        # the one-launch step: the same lists bit for bit, and its own O / LSE (checked against
+        # the oracle beside the two calls' by check_outputs)
+        idx2 = torch.full_like(kv_idx, -7)
+        cnt2 = torch.full_like(kv_cnt, -7)
+        o2 = torch.full_like(o, float("nan"))
+        lse2 = torch.full_like(lse, float("nan"))
+        ws2 = torch.full_like(ws, 0xA5)
+        bsa.decode_step(s, prm, cu, qn, k, v, meta["centroid"], meta["radius"], meta["alpha"],
+                        1.0 / math.sqrt(vw.head_dim), idx2, cnt2, o2, lse2, ws2, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        cnt = out["kv_cnt"]
+        np.testing.assert_array_equal(cnt2.cpu().numpy(), cnt)
+        live = np.arange(nbs) < cnt[..., None]
+        np.testing.assert_array_equal(idx2.cpu().numpy()[live], out["kv_idx"][live])
+        out["o_step"] = o2.float().cpu().numpy()
+        out["lse_step"] = lse2.cpu().numpy()
+    return out
 
 
 def oracle_decode(vw, lay, q_new, rc=None, rr=None):
@@ -149,8 +168,12 @@ def check_outputs(vw, lay, q_new, got, kept_by_bg, bs=None):
             continue
         per_g = [kept_by_bg[(b, g)] for g in range(vw.hkv)]
         o, lse = O.decode_attention(qn[b], k[s0:s1], v[s0:s1], per_g, s1 - s0, vw.block)
-        errs.append(np.abs(got["o"][b] - o).reshape(-1))
-        lerr = max(lerr, float(np.abs(got["lse"][b] - lse).max()))
+        for key in ("o", "o_step"):  # the two calls, and the one-launch step when it ran
+            if key in got:
+                errs.append(np.abs(got[key][b] - o).reshape(-1))
+        for key in ("lse", "lse_step"):
+            if key in got:
+                lerr = max(lerr, float(np.abs(got[key][b] - lse).max()))
     e = np.concatenate(errs)
     assert e.max() <= 2e-2 and e.mean() <= 2e-3, (e.max(), e.mean())
     assert lerr <= 1e-3, lerr
@@ -176,10 +199,11 @@ def test_decode_select_and_attention(name):
         for g in range(vw.hkv))]
     assert same
     check_outputs(vw, lay, q_new, got, {bg: d["kept"] for bg, d in orc.items()}, bs=same)
-    # an empty sequence decodes to zeros
+    # an empty sequence decodes to zeros, in both paths
     for b, n in enumerate(vw.lengths):
         if n == 0:
             assert np.all(got["o"][b] == 0) and np.all(np.isneginf(got["lse"][b]))
+            assert np.all(got["o_step"][b] == 0) and np.all(np.isneginf(got["lse_step"][b]))
 
 
 def test_decode_keep_all_equals_dense():
@@ -263,6 +287,20 @@ def test_decode_select_long_rows_synthetic_meta(nb):
     assert excused <= max(4, compared // 1000), (compared, excused)
     for g in range(hkv):  # pure ties: bit-exact, lowest indices first
         np.testing.assert_array_equal(got["kv_idx"][1, g, :got["kv_cnt"][1, g]], orc[(1, g)]["kept"])
+    # the one-launch step selects with a team of warps (P = 8, 16 or 32 entries per lane at these
+    # row lengths): the same lists bit for bit (a zero cache: only the selection is compared)
+    kz = torch.zeros(vw.total, hkv, d, dtype=torch.bfloat16, device="cuda")
+    idx2 = torch.full_like(kv_idx, -7)
+    cnt2 = torch.full_like(kv_cnt, -7)
+    o2 = torch.empty(2, hq, d, dtype=torch.bfloat16, device="cuda")
+    bsa.decode_step(s, bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0), cu, to_dev(q_new), kz, kz,
+                    torch.from_numpy(cen).cuda(), torch.from_numpy(rad).cuda(), torch.from_numpy(alpha).cuda(),
+                    1.0 / math.sqrt(d), idx2, cnt2, o2, None, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(cnt2.cpu().numpy(), got["kv_cnt"])
+    live = np.arange(nbs) < got["kv_cnt"][..., None]
+    np.testing.assert_array_equal(idx2.cpu().numpy()[live], got["kv_idx"][live])
 
 
 def test_decode_many_rows_and_malformed_entries():
@@ -287,6 +325,13 @@ def test_decode_many_rows_and_malformed_entries():
     for b, n in enumerate(vw.lengths):
         if n == 0:
             assert np.all(got2["o"][b] == 0) and np.all(np.isneginf(got2["lse"][b]))
+            assert np.all(got["o_step"][b] == 0) and np.all(np.isneginf(got["lse_step"][b]))
+    # end to end, both paths, on the sequences whose GPU lists all equal the oracle's
+    same = [b for b in range(vw.batch) if vw.lengths[b] > 0 and all(
+        np.array_equal(got["kv_idx"][b, g, :got["kv_cnt"][b, g]], orc[(b, g)]["kept"])
+        for g in range(vw.hkv))]
+    assert len(same) >= sum(1 for n in vw.lengths if n > 0) // 2
+    check_outputs(vw, lay, q_new, got, kept, bs=same)
     # malformed entries after the valid ones: skipped by the attention
     idx, cnt = (x.cpu().numpy().copy() for x in lists)
     for (b, g), d in orc.items():
