@@ -522,9 +522,9 @@ __device__ __forceinline__ void quant_smem(const float *radius, float *quant, fl
   }
 }
 
-// The layer path's first launch: the key-block meta CTAs (b, g, j) first, then
-// the query-pooling CTAs (b, head chunk, i), so K and Q stream in one grid with
-// no launch boundary between them.  Meta CTAs also write the centroids' tf32
+// The layer path's first launch: the key-block meta CTAs (b, g, j) and the
+// query-pooling CTAs (b, head chunk, i) in one grid, so K and Q stream with no
+// launch boundary between them.  Meta CTAs also write the centroids' tf32
 // splits; the last meta CTA of each (b, g) to finish (counted in done[b][g],
 // zero before the launch) takes that group's quantiles and alpha, so no launch
 // waits on the radii.
@@ -537,10 +537,59 @@ __global__ void __launch_bounds__(kThreads, (meta_min_blocks<D, BLK>())) meta_po
     int block, int nbs, int hpc, int nhc, int32_t *status) {
   extern __shared__ float sort_buf[];
   __shared__ unsigned last;
-  const int nmeta = nbs * hkv * batch;
-  const int x = static_cast<int>(blockIdx.x);
-  if (x < nmeta) {
-    const int j = x % nbs, g = (x / nbs) % hkv, b = x / (nbs * hkv);
+  // Grid order: unit u < nbs / 2 holds the pooling CTAs of query block u and the meta CTAs of key
+  // blocks 2u and 2u + 1 (for every sequence); an odd nbs adds one unit with the last key block;
+  // the remaining units pool query blocks ceil(nbs / 2) .. nbs - 1.  K streams beside Q instead of
+  // ahead of it, and every key block is summarised by the middle of the Q stream, so the
+  // quantiles are taken while the pooling goes on.
+  int kind = 0, idx = 0, sub = 0, b = 0;  // kind 0: pooling (i, head chunk), 1: meta (j, g)
+  {
+    int x = static_cast<int>(blockIdx.x);
+    const int hf = nbs / 2, s2 = nhc + 2 * hkv;
+    const int l1 = hf * batch * s2;
+    if (x < l1) {
+      const int u = x / (batch * s2), rem = x - u * (batch * s2);
+      b = rem / s2;
+      const int o = rem - b * s2;
+      if (o < nhc) {
+        idx = u;
+        sub = o;
+      } else {
+        kind = 1;
+        idx = 2 * u + (o - nhc) / hkv;
+        sub = (o - nhc) % hkv;
+      }
+    } else {
+      x -= l1;
+      bool placed = false;
+      if (nbs & 1) {
+        const int s1 = nhc + hkv;
+        if (x < batch * s1) {
+          b = x / s1;
+          const int o = x - b * s1;
+          if (o < nhc) {
+            idx = hf;
+            sub = o;
+          } else {
+            kind = 1;
+            idx = 2 * hf;
+            sub = o - nhc;
+          }
+          placed = true;
+        } else {
+          x -= batch * s1;
+        }
+      }
+      if (!placed) {
+        const int q = x / (batch * nhc), rem = x - q * (batch * nhc);
+        idx = (nbs + 1) / 2 + q;
+        b = rem / nhc;
+        sub = rem - b * nhc;
+      }
+    }
+  }
+  if (kind == 1) {
+    const int j = idx, g = sub;
     meta_block<D, BLK, false>(j, g, b, k, centroid, radius, c_hi, c_lo, cu, seq, total, hkv, nbs, 1.f, status);
     __threadfence();  // this CTA's radius before its count
     __syncthreads();
@@ -554,8 +603,7 @@ __global__ void __launch_bounds__(kThreads, (meta_min_blocks<D, BLK>())) meta_po
     }
     return;
   }
-  const int y = x - nmeta;
-  const int i = y % nbs, hc = (y / nbs) % nhc, b = y / (nbs * nhc);
+  const int i = idx, hc = sub;
   const int nthreads = hpc * (D / 16);
   if (static_cast<int>(threadIdx.x) < nthreads)
     qpool_block<D, false>(i, hc, b, nthreads, q, q_hi, q_lo, nbar, cu, seq, total, hq, hkv, block, nbs, hpc, 1.f,
