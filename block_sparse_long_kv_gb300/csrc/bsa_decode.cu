@@ -1010,9 +1010,9 @@ __device__ __forceinline__ void decode_select_team(int r, const DecStepArgs &a) 
   tm.clear_hist();
   tm.sync();
   uint32_t fl[P / 4];
-  team_select_row<NW, P, true>(tm, a.s_c + gb * a.nbs, a.s_r + gb * a.nbs, a.alpha + gb * a.nbs, i, a.ppm_c,
+  team_select_row<Team<NW>, P, true>(tm, a.s_c + gb * a.nbs, a.s_r + gb * a.nbs, a.alpha + gb * a.nbs, i, a.ppm_c,
                                a.ppm_r, fl);
-  team_emit_row<NW, P, true>(tm, fl, i, a.kv_idx + gb * a.nbs, a.kv_cnt + gb, nullptr, a.nbs);
+  team_emit_row<Team<NW>, P, true>(tm, fl, i, a.kv_idx + gb * a.nbs, a.kv_cnt + gb, nullptr, a.nbs);
   tm.sync();  // the scratch is reused by the next row
 }
 

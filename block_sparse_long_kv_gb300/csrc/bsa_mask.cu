@@ -657,9 +657,10 @@ struct SelectArgs {
   int32_t *status;
 };
 
-template <int W, int P, bool ALIGNED>
-__device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int i, int b, int g, const SelectArgs &a) {
-  Team<W> tm(sh, 1 + team, static_cast<int>(threadIdx.x) - team * 32 * W);
+template <int P, bool ALIGNED>
+__device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int w, int i, int b, int g,
+                                                const SelectArgs &a) {
+  TeamRT tm(sh, w, 1 + team, static_cast<int>(threadIdx.x) - team * 32 * w);
   const size_t gb = static_cast<size_t>(b) * a.hkv + g;
   const size_t row = gb * a.nbs + i;
   {
@@ -670,9 +671,9 @@ __device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int i
       if (a.mask != nullptr) {
         uint8_t *mrow = a.mask + row * static_cast<size_t>(a.nbs);
         if constexpr (ALIGNED) {
-          for (int j4 = tm.t * 4; j4 < a.nbs; j4 += 4 * Team<W>::T) reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = 0u;
+          for (int j4 = tm.t * 4; j4 < a.nbs; j4 += 4 * tm.T) reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = 0u;
         } else {
-          for (int j = tm.t; j < a.nbs; j += Team<W>::T) mrow[j] = 0u;
+          for (int j = tm.t; j < a.nbs; j += tm.T) mrow[j] = 0u;
         }
       }
       return;
@@ -681,10 +682,10 @@ __device__ __forceinline__ void select_team_row(TeamScratch &sh, int team, int i
   tm.clear_hist();
   tm.sync();
   uint32_t fl[P / 4];
-  team_select_row<W, P, ALIGNED>(tm, a.s_c + row * a.nbw, a.s_r + row * a.nbw, a.alpha + gb * a.nbs, i, a.ppm_c,
-                                 a.ppm_r, fl);
-  team_emit_row<W, P, ALIGNED>(tm, fl, i, a.kv_idx + row * static_cast<size_t>(a.nbs), a.kv_cnt + row,
-                               a.mask != nullptr ? a.mask + row * static_cast<size_t>(a.nbs) : nullptr, a.nbs);
+  team_select_row<TeamRT, P, ALIGNED>(tm, a.s_c + row * a.nbw, a.s_r + row * a.nbw, a.alpha + gb * a.nbs, i,
+                                      a.ppm_c, a.ppm_r, fl);
+  team_emit_row<TeamRT, P, ALIGNED>(tm, fl, i, a.kv_idx + row * static_cast<size_t>(a.nbs), a.kv_cnt + row,
+                                    a.mask != nullptr ? a.mask + row * static_cast<size_t>(a.nbs) : nullptr, a.nbs);
 }
 
 // Per-path exact top-k, OR and kept-list emission for every (b, g, i) row:
@@ -705,12 +706,7 @@ __global__ void __launch_bounds__(kTeamMaxWarps * 32, (P <= 8 ? 4 : 2)) select_k
   const int team = static_cast<int>(threadIdx.x >> 5) / plan.w;
   if (team >= plan.teams) return;  // whole teams leave; barriers are per team
   const int i = plan.first_row - team, g = plan.group % a.hkv, b = plan.group / a.hkv;
-  switch (plan.w) {
-    case 1: select_team_row<1, P, ALIGNED>(sh[team], team, i, b, g, a); break;
-    case 2: select_team_row<2, P, ALIGNED>(sh[team], team, i, b, g, a); break;
-    case 4: select_team_row<4, P, ALIGNED>(sh[team], team, i, b, g, a); break;
-    default: select_team_row<8, P, ALIGNED>(sh[team], team, i, b, g, a); break;
-  }
+  select_team_row<P, ALIGNED>(sh[team], team, plan.w, i, b, g, a);  // one code path for every team width
 }
 
 template <int D, int BLK>

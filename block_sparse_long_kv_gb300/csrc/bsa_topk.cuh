@@ -252,6 +252,130 @@ struct Team {
   }
 };
 
+// The same team with its width w chosen at run time (1, 2, 4 or 8 warps): one code path
+// serves every row length, so a kernel whose resident CTAs run teams of different widths keeps
+// a single copy of the selection code in the instruction cache.
+struct TeamRT {
+  TeamScratch &sh;
+  int W, T, B;                           // warps, threads, histogram bins per thread
+  int bar_id;
+  int t, lane, warp;
+  int rot = 0, hrot = 0;
+
+  __device__ TeamRT(TeamScratch &s, int w, int id, int tid)
+      : sh(s), W(w), T(32 * w), B(256 / (32 * w)), bar_id(id), t(tid), lane(tid & 31), warp(tid >> 5) {}
+
+  __device__ __forceinline__ void sync() const {
+    if (W == 1) __syncwarp();
+    else asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(T) : "memory");
+  }
+
+  __device__ __forceinline__ unsigned scan(unsigned v, unsigned *total) {
+    unsigned incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (W == 1) {
+      *total = __shfl_sync(0xffffffffu, incl, 31);
+      return incl - v;
+    }
+    unsigned *wb = sh.wsum[rot];
+    rot ^= 1;
+    if (lane == 31) wb[warp] = incl;
+    sync();
+    unsigned pre = 0, tot = 0;
+    for (int w = 0; w < W; ++w) {
+      const unsigned x = wb[w];
+      pre += w < warp ? x : 0u;
+      tot += x;
+    }
+    *total = tot;
+    return pre + incl - v;
+  }
+
+  __device__ __forceinline__ void minmax_count(float &lo, float &hi, unsigned &n) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+      n += __shfl_xor_sync(0xffffffffu, n, off);
+    }
+    if (W == 1) return;
+    const int r = rot;
+    rot ^= 1;
+    if (lane == 0) {
+      sh.wlo[r][warp] = lo;
+      sh.whi[r][warp] = hi;
+      sh.wsum[r][warp] = n;
+    }
+    sync();
+    lo = sh.wlo[r][0];
+    hi = sh.whi[r][0];
+    n = sh.wsum[r][0];
+    for (int w = 1; w < W; ++w) {
+      lo = fminf(lo, sh.wlo[r][w]);
+      hi = fmaxf(hi, sh.whi[r][w]);
+      n += sh.wsum[r][w];
+    }
+  }
+
+  __device__ __forceinline__ void and_or(uint32_t &a, uint32_t &o) {
+    a = __reduce_and_sync(0xffffffffu, a);
+    o = __reduce_or_sync(0xffffffffu, o);
+    if (W == 1) return;
+    const int r = rot;
+    rot ^= 1;
+    if (lane == 0) {
+      sh.wsum[r][warp] = a;
+      reinterpret_cast<uint32_t *>(sh.wlo[r])[warp] = o;
+    }
+    sync();
+    a = 0xFFFFFFFFu;
+    o = 0u;
+    for (int w = 0; w < W; ++w) {
+      a &= sh.wsum[r][w];
+      o |= reinterpret_cast<const uint32_t *>(sh.wlo[r])[w];
+    }
+  }
+
+  __device__ __forceinline__ BinHit find_bin(unsigned *h, unsigned take) {
+    unsigned c[8], sum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = e < B ? h[255 - B * t - e] : 0u;
+      sum += c[e];
+    }
+    unsigned tot;
+    unsigned before = scan(sum, &tot);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e < B && before < take && take <= before + c[e]) {
+        sh.res[0] = 255u - B * t - e;
+        sh.res[1] = before;
+        sh.res[2] = c[e];
+      }
+      before += c[e];
+    }
+    sync();
+    const BinHit r{sh.res[0], sh.res[1], sh.res[2]};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < B) h[255 - B * t - e] = 0u;
+    return r;
+  }
+
+  __device__ __forceinline__ void clear_hist() {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < B) {
+        sh.hist[0][B * t + e] = 0u;
+        sh.hist[1][B * t + e] = 0u;
+      }
+  }
+};
+
 // Outcome of one path's selection: value bins above bstar are in (all of bstar when whole);
 // inside bstar a key is in when (key & pmask) > prefix, and of the keys with (key & pmask) ==
 // prefix the first `take` in index order.
@@ -264,8 +388,8 @@ struct TeamSel {
 
 // The k best of the nonzero keys among the team's registers (1 <= k < number of nonzero keys);
 // bin[x]: value bin of key x (monotone in the key).  Both histograms are zero on entry and exit.
-template <int W, int P>
-__device__ inline TeamSel team_select(Team<W> &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], unsigned k) {
+template <class TM, int P>
+__device__ inline TeamSel team_select(TM &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], unsigned k) {
   TeamSel r;
   r.whole = false;
   r.prefix = 0u;
@@ -329,8 +453,8 @@ __device__ inline TeamSel team_select(Team<W> &tm, const uint32_t (&key)[P], con
 
 // Sets `bit` in the flag bytes of the entries TeamSel r keeps (entry x: byte x % 4 of
 // fl[x / 4]); equal keys at the threshold are ranked in index order.
-template <int W, int P>
-__device__ inline void team_mark(Team<W> &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], const TeamSel &r,
+template <class TM, int P>
+__device__ inline void team_mark(TM &tm, const uint32_t (&key)[P], const uint8_t (&bin)[P], const TeamSel &r,
                                  uint32_t (&fl)[P / 4], uint32_t bit) {
   unsigned in = 0u, eq = 0u;  // bit x: entry x
 #pragma unroll
@@ -383,8 +507,8 @@ __device__ __forceinline__ void value_bins(const uint32_t (&key)[P], float lo, f
 // AB_ALIGNED, else read one entry at a time for j < i.  32 W P >= i + 1.  Leaves the BSA_MASK_*
 // bits of entry P t + x in byte x % 4 of fl[x / 4] (zero past i).  Both histograms must be zero
 // and ordered before the team's first barrier.
-template <int W, int P, bool AB_ALIGNED>
-__device__ inline void team_select_row(Team<W> &tm, const float *rc, const float *rr, const float *ab, int i,
+template <class TM, int P, bool AB_ALIGNED>
+__device__ inline void team_select_row(TM &tm, const float *rc, const float *rr, const float *ab, int i,
                                        long long ppm_c, long long ppm_r, uint32_t (&fl)[P / 4]) {
   static_assert(P % 4 == 0 && P <= 32, "whole 16-byte groups, one mask bit per entry");
   const int j0 = P * tm.t;
@@ -429,8 +553,8 @@ __device__ inline void team_select_row(Team<W> &tm, const float *rc, const float
     unsigned dummy = 0u;
     tm.minmax_count(lo, hi, dummy);
     value_bins<P>(key, lo, hi, bin);
-    const TeamSel r = team_select<W, P>(tm, key, bin, static_cast<unsigned>(kc));
-    team_mark<W, P>(tm, key, bin, r, fl, BSA_MASK_CENTROID);
+    const TeamSel r = team_select<TM, P>(tm, key, bin, static_cast<unsigned>(kc));
+    team_mark<TM, P>(tm, key, bin, r, fl, BSA_MASK_CENTROID);
   }
 
   // ---- rescue path: among the dropped candidates with alpha > 0, top kr by R
@@ -477,8 +601,8 @@ __device__ inline void team_select_row(Team<W> &tm, const float *rc, const float
       if (key[x] != 0u) fl[x / 4] |= BSA_MASK_RESCUE << (8 * (x % 4));
   } else if (kr > 0) {
     value_bins<P>(key, lo, hi, bin);
-    const TeamSel r = team_select<W, P>(tm, key, bin, static_cast<unsigned>(kr));
-    team_mark<W, P>(tm, key, bin, r, fl, BSA_MASK_RESCUE);
+    const TeamSel r = team_select<TM, P>(tm, key, bin, static_cast<unsigned>(kr));
+    team_mark<TM, P>(tm, key, bin, r, fl, BSA_MASK_RESCUE);
   }
 #pragma unroll
   for (int x = 0; x < P; ++x) {
@@ -491,8 +615,8 @@ __device__ inline void team_select_row(Team<W> &tm, const float *rc, const float
 // to *cnt; with mrow, also the mask bytes (nbs of them, zero past i), a word per store when
 // MROW_ALIGNED (mrow 4-byte aligned, nbs % 4 == 0), else byte by byte.  32 W P >= nbs is not
 // required: entries past the team's reach are zero-filled by the lanes that reach them.
-template <int W, int P, bool MROW_ALIGNED>
-__device__ inline void team_emit_row(Team<W> &tm, const uint32_t (&fl)[P / 4], int i, int32_t *dst, int32_t *cnt,
+template <class TM, int P, bool MROW_ALIGNED>
+__device__ inline void team_emit_row(TM &tm, const uint32_t (&fl)[P / 4], int i, int32_t *dst, int32_t *cnt,
                                      uint8_t *mrow, int nbs) {
   const int j0 = P * tm.t;
   unsigned mine = 0u;
@@ -519,10 +643,10 @@ __device__ inline void team_emit_row(Team<W> &tm, const uint32_t (&fl)[P / 4], i
     }
   }
   if constexpr (MROW_ALIGNED) {
-    for (int j4 = Team<W>::T * P + 4 * tm.t; j4 < nbs; j4 += 4 * Team<W>::T)
+    for (int j4 = tm.T * P + 4 * tm.t; j4 < nbs; j4 += 4 * tm.T)
       reinterpret_cast<uint32_t *>(mrow)[j4 >> 2] = 0u;
   } else {
-    for (int j = Team<W>::T * P + tm.t; j < nbs; j += Team<W>::T) mrow[j] = 0u;
+    for (int j = tm.T * P + tm.t; j < nbs; j += tm.T) mrow[j] = 0u;
   }
 }
 
