@@ -322,18 +322,21 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
         // operations issued by one thread execute in issue order, so S_0(n) is
         // queued right behind PV_0(n-1) without waiting for it to complete.
         issue_s(0, ks);
+        // V(n) is waited for here, while the tensor core still works on S_0(n) and the issue
+        // of this tile's MMAs is held back by it anyway, so no wait but P_0's stands between
+        // S_1(n) and PV_0(n)
+        const int vs = n % C::VS;
+        if (!(ok = wait_bar(bar(C::B_VF + vs), (n / C::VS) & 1, ctl))) break;
         if constexpr (NT == 2) {
           if (n > 0) {
             // PV_1(n-1) overlaps softmax_0(n); S_1(n) follows it in issue order
-            const int pv = n - 1, vs = pv % C::VS;
-            if (!(ok = issue_pv(1, vs, pv))) break;
-            ptx::mma_commit(bar(C::B_VE + vs));
+            const int pv = n - 1, pvs = pv % C::VS;
+            if (!(ok = issue_pv(1, pvs, pv))) break;
+            ptx::mma_commit(bar(C::B_VE + pvs));
           }
           issue_s(1, ks);
         }
         ptx::mma_commit(bar(C::B_KE + ks));
-        const int vs = n % C::VS;
-        if (!(ok = wait_bar(bar(C::B_VF + vs), (n / C::VS) & 1, ctl))) break;
         if (!(ok = issue_pv(0, vs, n))) break;
         if constexpr (NT == 1) ptx::mma_commit(bar(C::B_VE + vs));
       }
