@@ -336,8 +336,10 @@ __global__ void __launch_bounds__(Cfg<D, BLK, NT, F8>::THREADS, 1)
           }
           issue_s(1, ks);
         }
-        ptx::mma_commit(bar(C::B_KE + ks));
         if (!(ok = issue_pv(0, vs, n))) break;
+        // K(n)'s slot is released only now, so nothing but the wait for P_0 separates S_1(n)
+        // from PV_0(n); K(n + KS) still has a whole key tile to arrive
+        ptx::mma_commit(bar(C::B_KE + ks));
         if constexpr (NT == 1) ptx::mma_commit(bar(C::B_VE + vs));
       }
       if constexpr (NT == 2) {
