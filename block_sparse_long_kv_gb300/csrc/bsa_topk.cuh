@@ -114,6 +114,9 @@ struct TeamScratch {
   unsigned wsum[2][kTeamMaxWarps];       // alternating per-warp partials of scans and reductions
   float wlo[2][kTeamMaxWarps], whi[2][kTeamMaxWarps];
   unsigned res[3];                       // bin search result: bin, entries above, its count
+  uint32_t gkey[32];                     // the keys of a small threshold bin, gathered to be ranked
+  unsigned gcnt;                         // how many are gathered (zero outside a gather)
+  unsigned gres[3];                      // their ranking: threshold key, take among equals, equals
 };
 
 template <int W>
@@ -242,13 +245,14 @@ struct Team {
     return r;
   }
 
-  // Both histograms to zero (before the row's first barrier).
+  // Both histograms and the gather count to zero (before the row's first barrier).
   __device__ __forceinline__ void clear_hist() {
 #pragma unroll
     for (int e = 0; e < B; ++e) {
       sh.hist[0][B * t + e] = 0u;
       sh.hist[1][B * t + e] = 0u;
     }
+    if (t == 0) sh.gcnt = 0u;
   }
 };
 
@@ -373,6 +377,7 @@ struct TeamRT {
         sh.hist[0][B * t + e] = 0u;
         sh.hist[1][B * t + e] = 0u;
       }
+    if (t == 0) sh.gcnt = 0u;
   }
 };
 
@@ -409,6 +414,43 @@ __device__ inline TeamSel team_select(TM &tm, const uint32_t (&key)[P], const ui
       r.whole = true;
       return r;
     }
+  }
+  if (r.n_eq <= 32u) {
+    // A small threshold bin (the common case): its keys are gathered and one warp ranks them,
+    // instead of radix passes over every entry.  The threshold is the key K whose count of
+    // larger keys is below take and whose count of larger-or-equal keys reaches it; the keys
+    // equal to K are then ranked by index as after the radix passes.  Every thread has read the
+    // bin search's result before the barrier below.
+#pragma unroll
+    for (int x = 0; x < P; ++x)
+      if (key[x] != 0u && bin[x] == r.bstar) tm.sh.gkey[atomicAdd(&tm.sh.gcnt, 1u)] = key[x];
+    tm.sync();
+    if (tm.warp == 0) {
+      const int n = static_cast<int>(r.n_eq);
+      const uint32_t kl = tm.lane < n ? tm.sh.gkey[tm.lane] : 0u;
+      unsigned above = 0u, equal = 0u;
+      for (int c = 0; c < n; ++c) {
+        const uint32_t kc = tm.sh.gkey[c];
+        above += kc > kl ? 1u : 0u;
+        equal += kc == kl ? 1u : 0u;
+      }
+      const bool hit = tm.lane < n && above < r.take && r.take <= above + equal;
+      const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;  // some lane holds K
+      const uint32_t kt = __shfl_sync(0xffffffffu, kl, src);
+      const unsigned at = __shfl_sync(0xffffffffu, above, src), eq = __shfl_sync(0xffffffffu, equal, src);
+      if (tm.lane == 0) {
+        tm.sh.gres[0] = kt;
+        tm.sh.gres[1] = r.take - at;
+        tm.sh.gres[2] = eq;
+        tm.sh.gcnt = 0u;
+      }
+    }
+    tm.sync();
+    r.prefix = tm.sh.gres[0];
+    r.pmask = 0xFFFFFFFFu;
+    r.take = tm.sh.gres[1];
+    r.n_eq = tm.sh.gres[2];
+    return r;
   }
   // the bits every key of the threshold bin shares need no pass
   uint32_t a = 0xFFFFFFFFu, o = 0u;
