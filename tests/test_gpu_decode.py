@@ -343,3 +343,52 @@ def test_decode_many_rows_and_malformed_entries():
         cnt[b, g] = c + room
     got3 = gpu_decode(vw, lay, q_new, lists=(torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda()))
     check_outputs(vw, lay, q_new, got3, kept)
+
+
+@pytest.mark.parametrize("nb", [500, 1024])
+def test_decode_step_tied_templates_exact(nb):
+    """Exact ties inside small threshold bins (ranked directly by one warp): block j's summary is
+    template j % 48, centroid (m + 1) / 64 along dimension 0, radius 0.5 with alpha 1 on every
+    fourth template and 0.125 with alpha 0 elsewhere, and the new token is e_0 in every head.  All
+    scores are exact in fp32 and fp64, so the one-launch step's lists equal the oracle's bit for
+    bit: of equal scores the lowest block indices are kept, in both paths."""
+    import block_sparse_long_kv_gb300 as bsa
+    block, hq, hkv, d, templates = 64, 8, 2, 64, 48
+    lengths = (nb * block,)
+    vw = synth.VarlenWorkload("dec_ties", lengths, hq, hkv, d, block, 0.1, 0.05)
+    s = bsa.make_varlen_shape(vw.batch, vw.total, vw.max_seqlen, hq, hkv, d, block)
+    nbs = bsa.varlen_block_stride(s)
+    m = np.arange(nbs) % templates
+    cen = np.zeros((1, hkv, nbs, d), dtype=np.float32)
+    cen[..., 0] = ((m + 1) / 64.0)[None, None, :]
+    wide = m % 4 == 0
+    rad = np.broadcast_to(np.where(wide, 0.5, 0.125).astype(np.float32), (1, hkv, nbs)).copy()
+    alpha = np.broadcast_to(np.where(wide, 1.0, 0.0).astype(np.float32), (1, hkv, nbs)).copy()
+    qf = np.zeros((1, hq, d), dtype=np.float32)
+    qf[..., 0] = 1.0
+    q_new = synth.bf16_bits(qf)
+    cu = torch.tensor(vw.cu_seqlens(), dtype=torch.int32, device="cuda")
+    kz = torch.zeros(vw.total, hkv, d, dtype=torch.bfloat16, device="cuda")
+    kv_idx = torch.full((1, hkv, nbs), -7, dtype=torch.int32, device="cuda")
+    kv_cnt = torch.full((1, hkv), -7, dtype=torch.int32, device="cuda")
+    o = torch.empty(1, hq, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(bsa.decode_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsa.decode_step(s, bsa.SelectParams(vw.centroid_keep, vw.rescue_keep, 0), cu, to_dev(q_new), kz, kz,
+                    torch.from_numpy(cen).cuda(), torch.from_numpy(rad).cuda(), torch.from_numpy(alpha).cuda(),
+                    1.0 / math.sqrt(d), kv_idx, kv_cnt, o, None, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    n = lengths[0]
+    i = (n - 1) // block
+    qn = synth.bf16_to_f64(q_new)
+    c64, r64, a64 = (x[0, :, :nb].astype(np.float64) for x in (cen, rad, alpha))
+    for g in range(hkv):
+        kept, _, _ = O.decode_select(qn[0], c64, r64, a64, n, block, vw.centroid_keep, vw.rescue_keep, g)
+        cnt = int(kv_cnt[0, g].item())
+        np.testing.assert_array_equal(kv_idx[0, g, :cnt].cpu().numpy(), kept, err_msg=f"g {g}")
+    # the rows do split tie groups: some template is only partly kept
+    kept_set = set(kept.tolist())
+    cands = [[j for j in range(1, i) if j % templates == t] for t in range(templates)]
+    split = [t for t in range(templates) if 0 < sum(j in kept_set for j in cands[t]) < len(cands[t])]
+    assert split, "no tie group is split at the thresholds"

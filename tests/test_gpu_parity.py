@@ -304,3 +304,46 @@ def test_token_max_long_rows_sampled():
     orc = oracle_rows(w, lay, rows, token_max=True)
     compared, excused = compare_mask_rows(got["mask"], orc)
     assert excused <= max(4, compared // 1000), (compared, excused)
+
+
+def _tied_layer(nb, block, d, hq, templates):
+    """K blocks copied from `templates` template blocks (block j is template j % templates), each
+    an exactly representable centroid (m + 1) / 64 along dimension 0 plus a zero-mean +-a pattern
+    on dimension 1 (a = 0.5 on every fourth template, else 0.125); every query token is e_0 plus a
+    zero-mean +-1/16 pattern.  Every score is then exact in bf16, tf32 and fp64, the templates'
+    scores are at least 2 % apart, and the copies of one template tie exactly."""
+    n = nb * block
+    t = np.arange(block)
+    sign = np.where(t < block // 2, 1.0, -1.0).astype(np.float32)  # zero mean over a block
+    k = np.zeros((1, n, 1, d), dtype=np.float32)
+    for j in range(nb):
+        m = j % templates
+        a = 0.5 if m % 4 == 0 else 0.125
+        k[0, j * block:(j + 1) * block, 0, 0] = (m + 1) / 64.0
+        k[0, j * block:(j + 1) * block, 0, 1] = a * sign
+    q = np.zeros((1, n, hq, d), dtype=np.float32)
+    q[..., 0] = 1.0
+    qs = np.where((np.arange(n) // 2) % 2 == 0, 1.0, -1.0).astype(np.float32)  # zero mean per block
+    q[..., 2] = (qs / 16.0)[:, None]
+    v = np.zeros((1, n, 1, d), dtype=np.float32)
+    return {"q": synth.bf16_bits(q), "k": synth.bf16_bits(k), "v": synth.bf16_bits(v)}
+
+
+@pytest.mark.parametrize("nb", [300, 1024])
+def test_tied_blocks_exact(nb):
+    """Exact ties at the selection thresholds of both paths: rows of up to 1024 blocks whose
+    threshold bin holds up to 22 copies of one template (ranked directly by one warp, not by
+    radix passes).  Masks and lists equal the oracle's bit for bit, no excuse: of equal scores
+    the lowest block indices are kept."""
+    block, d, hq, templates = 64, 64, 2, 48
+    w = synth.Workload("tied", 1, nb * block, hq, 1, d, block, 0.10, 0.02)
+    lay = _tied_layer(nb, block, d, hq, templates)
+    got = gpu_mask_build(w, lay)
+    check_lists_match_mask(got["mask"], got["kv_idx"], got["kv_cnt"])
+    q64, k64 = synth.bf16_to_f64(lay["q"]), synth.bf16_to_f64(lay["k"])
+    orc = O.select_blocks(q64, k64, block, w.centroid_keep, w.rescue_keep)
+    assert float(orc["alpha"].max()) == 1.0 and float(orc["alpha"].min()) == 0.0  # both paths select
+    rescued = int(((orc["mask"] & O.RESCUE) != 0).sum())
+    assert rescued > 0
+    bad = np.argwhere(got["mask"] != orc["mask"])
+    assert bad.size == 0, f"{len(bad)} mask entries differ, first (b, g, i, j) {bad[:4].tolist()}"
